@@ -1,0 +1,414 @@
+"""Benchmark: GDN tree-verify nodes/s per layer on one GB300, with the
+roofline fraction of the dominant kernel and the fp64 CPU oracle as a
+reported baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch: gdn_tree_verify for
+every node of every tree, then gdn_tree_commit of every accepted path.  The
+workload is the serving-scale case: 32 sequences x 32 v-heads (16 q/k heads),
+dk = dv = 128, bf16 q/k/v, fp32 S0, 128-node random trees (branching 1-4,
+depth <= 24), accepted paths of up to 24 nodes.  L2 is flushed (a 256 MiB
+write) before every timed step, outside the timed events.  Under torchrun
+each rank runs its own independent batch (weak scaling, no collective on the
+data path) and rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "GDN tree-verify nodes/sec per layer on 1 GB300; % of HBM/tensor roofline"
+UNIT = "nodes/s"
+WORKLOAD_CFG = 3
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "gated_deltanet_tree_gdn_gb300", "csrc", f)
+                  for f in ("verify_generic.cu", "verify_tc.cu", "common.cuh")]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# byte / FLOP model (per launch)
+# ---------------------------------------------------------------------------
+
+def verify_bytes(w: W.Workload) -> int:
+    es = 2 if w.dtype == W.BF16 else 4
+    B, N, Hqk, Hv, dk, dv = w.B, w.N, w.Hqk, w.Hv, w.dk, w.dv
+    return (B * Hv * dk * dv * 4            # S0 read
+            + 2 * B * N * Hqk * dk * es     # q, k read (once per q/k head)
+            + B * N * Hv * dv * es          # v read
+            + 2 * B * N * Hv * 4            # log_alpha, beta read
+            + B * N * 4                     # parent read
+            + B * N * Hv * dv * es          # o write
+            + B * Hv * N * dv * 4)          # U write
+
+
+def commit_bytes(w: W.Workload) -> int:
+    es = 2 if w.dtype == W.BF16 else 4
+    Lsum = int(w.path_len.sum())
+    return (2 * w.B * w.Hv * w.dk * w.dv * 4   # S0 read + S1 write
+            + Lsum * w.Hv * w.dv * 4           # U rows of the accepted paths
+            + Lsum * w.Hqk * w.dk * es         # k rows (once per q/k head)
+            + Lsum * w.Hv * 4                  # log_alpha along the paths
+            + w.B * (w.Lmax + 1) * 4)          # path + path_len
+
+
+def verify_flops(w: W.Workload) -> int:
+    B, N, Hqk, Hv, d = w.B, w.N, w.Hqk, w.Hv, w.dk
+    return (B * Hv * (2 * 2 * N * d * d        # Q S0 and K S0
+                      + N * N * d              # solve (dense lower-triangular)
+                      + N * N * d)             # Y U
+            + B * Hqk * (2 * N * N * d + N * N * d))  # Q K^T, K K^T (symmetric)
+
+
+def commit_flops(w: W.Workload) -> int:
+    return int(w.path_len.sum()) * w.Hv * 2 * w.dk * w.dv
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """dram read+write bytes per launch from the committed ncu summary, or None
+    when it was taken on a different kernel source."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel") != kernel or rec.get("source_sha") != kernel_source_sha():
+        return None
+    return rec.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def workload_config(w: W.Workload) -> dict:
+    return {"workload": f"{w.name}: B={w.B} seqs x Hv={w.Hv} v-heads (Hqk={w.Hqk}), "
+                        f"dk=dv={w.dk}, {w.dtype} q/k/v, fp32 S0, N={w.N}-node random trees "
+                        "(branching 1-4, depth<=24), accepted paths <=24",
+            "B": w.B, "N": w.N, "Hqk": w.Hqk, "Hv": w.Hv, "dk": w.dk, "dv": w.dv,
+            "l2": "flushed before every timed step (256 MiB write, outside the events)"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank: int) -> None:
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = W.make_config(WORKLOAD_CFG)
+    cores = cpu_cores()
+    per_step = max(8, cores)
+    units_all = w.B * w.Hv
+    rng = np.random.default_rng(0)
+
+    def step():
+        units = rng.choice(units_all, per_step, replace=False).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.verify_workload(w, mode="memo", units=units, threads=cores)
+        oracle.commit_workload(w, units=units, threads=cores)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    ts = [step() for _ in range(args.steps)]
+    t_unit = sum(ts) / (len(ts) * per_step)        # seconds per (b, h) unit
+    t_layer = t_unit * units_all                    # a whole layer's step
+    value = w.B * w.N / t_layer
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_layer, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {per_step} random (sequence, head) units of "
+                                       f"the {units_all}, memoised fp64 recurrence + commit, "
+                                       "scaled to the whole layer"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w: W.Workload) -> dict:
+    """The oracle as it stands on all host cores, on the whole workload."""
+    import oracle
+    oracle.build()
+    cores = cpu_cores()
+    t0 = time.perf_counter()
+    oracle.verify_workload(w, mode="memo", threads=cores)
+    oracle.commit_workload(w, threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": w.B * w.N / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the whole workload ({w.B * w.Hv} (sequence, head) units), memoised "
+                      f"fp64 recurrence + commit, {dt:.2f} s wall"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    from gated_deltanet_tree_gdn_gb300 import build as gbuild
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    gbuild.build_library()
+    gt.load()
+    dev = torch.device("cuda", local_rank)
+
+    w = W.make_config(WORKLOAD_CFG, seed=1000 + WORKLOAD_CFG + rank)
+    dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
+
+    def host(x, dtype=None):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dtype=dtype).pin_memory()
+
+    hin = dict(q=host(w.q, dt), k=host(w.k, dt), v=host(w.v, dt), log_alpha=host(w.log_alpha),
+               beta=host(w.beta), parent=host(w.parent), S0=host(w.S0), path=host(w.path),
+               path_len=host(w.path_len))
+    x = {kk: t.to(dev) for kk, t in hin.items()}
+    o = torch.empty((w.B, w.N, w.Hv, w.dv), dtype=dt, device=dev)
+    U = torch.empty((w.B, w.Hv, w.N, w.dv), dtype=torch.float32, device=dev)
+    S1 = torch.empty_like(x["S0"])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(xx, oo, UU, SS):
+        gt.verify(xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["beta"], xx["parent"],
+                  xx["S0"], o=oo, U=UU)
+        gt.commit(xx["path"], xx["path_len"], UU, xx["k"], xx["log_alpha"], xx["S0"], S1=SS,
+                  parent=xx["parent"])
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(x, o, U, S1)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
+                      o=o, U=U)
+            ev[i][1].record(stream)
+            gt.commit(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["S0"], S1=S1,
+                      parent=x["parent"])
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_ver = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]   # ms
+    t_com = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = float(sum(t_ver) + sum(t_com))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * w.B * w.N / (ms_per_step * 1e-3)
+
+    # end to end through the public API: pinned host inputs -> device -> verify
+    # + commit -> o and S1 back to pinned host memory, every step
+    h_o = torch.empty(o.shape, dtype=dt).pin_memory()
+    h_S1 = torch.empty(S1.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = h_o.numel() * h_o.element_size() + h_S1.numel() * h_S1.element_size()
+    Ke = max(3, min(K, 50))
+    xe = {kk: torch.empty_like(t) for kk, t in x.items()}
+
+    def e2e_step():
+        for kk in hin:
+            xe[kk].copy_(hin[kk], non_blocking=True)
+        step(xe, o, U, S1)
+        h_o.copy_(o, non_blocking=True)
+        h_S1.copy_(S1, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank == 0:
+        peaks, peak_kind = measured_peaks()
+        vb, cb = verify_bytes(w), commit_bytes(w)
+        vf, cf = verify_flops(w), commit_flops(w)
+        ver_ms = statistics.mean(t_ver)
+        com_ms = statistics.mean(t_com)
+        hbm = float(peaks["hbm_gbs"])
+        tflops = float(peaks["bf16_tflops"])
+        kernel = "verify_generic_kernel"
+        achieved = vb / (ver_ms * 1e-3) / 1e9
+        traffic = profiled_traffic(kernel)
+        t_roof = max((vb + cb) / (hbm * 1e9), (vf + cf) / (tflops * 1e12))
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(w), parallelism=f"dp{world}"),
+            "clocks": clk.summary(),
+            "e2e": {"value": world * w.B * w.N / (e2e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * K,
+            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
+                         "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": vb, "peak_source": peak_kind},
+            "step": {"verify_us": 1e3 * ver_ms, "commit_us": 1e3 * com_ms,
+                     "verify_bytes": vb, "commit_bytes": cb, "verify_flops": vf,
+                     "commit_flops": cf, "roofline_us": 1e6 * t_roof,
+                     "roofline_frac": t_roof / (ms_per_step * 1e-3),
+                     "wall_s_timed_loop": wall},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

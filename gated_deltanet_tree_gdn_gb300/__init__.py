@@ -1,0 +1,18 @@
+"""GB300-native rollback-free tree verification for Gated DeltaNet layers.
+
+Python face of libgdntree (C ABI in include/gdn_tree.h):
+
+    o, U = verify(q, k, v, log_alpha, beta, parent, S0)
+    S1   = commit(path, path_len, U, k, log_alpha, S0, parent=parent)
+
+Build the library first with ``python -m gated_deltanet_tree_gdn_gb300.build``.
+"""
+
+from ._binding import (  # noqa: F401
+    BF16, F32, OK, EINVAL, EUNSUPPORTED, ECUDA, STATUS_OK, STATUS_BAD_TREE,
+    STATUS_BAD_PATH, SYMBOLS, Dims, GdnTreeError, commit, library_path, load, strerror,
+    verify,
+)
+from .build import build_library  # noqa: F401
+
+__version__ = "0.1.0"

@@ -1,0 +1,98 @@
+// gdn_tree_api.cu -- the extern "C" entry points of libgdntree.
+//
+// Every shape, dtype, pointer and alignment check happens here, on the host,
+// before anything is enqueued; the kernels only check what depends on device
+// data (tree and path validity) and report it through dev_status.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn_tree.h"
+#include "kernels.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_head_dim(int d) { return d >= 16 && d <= gdn::kMaxDHost && d % 16 == 0; }
+
+int check_dims(const gdn_tree_dims& d) {
+  if (d.B < 0 || d.N < 0 || d.Hqk <= 0 || d.Hv <= 0 || d.dk <= 0 || d.dv <= 0)
+    return GDN_TREE_EINVAL;
+  if (d.Hv % d.Hqk != 0) return GDN_TREE_EINVAL;
+  if (d.dtype != GDN_TREE_BF16 && d.dtype != GDN_TREE_F32) return GDN_TREE_EUNSUPPORTED;
+  if (d.N > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (!supported_head_dim(d.dk) || !supported_head_dim(d.dv)) return GDN_TREE_EUNSUPPORTED;
+  // every flat index must fit comfortably in the kernels' size_t arithmetic and
+  // the grid's y dimension
+  if (d.B > 65535) return GDN_TREE_EUNSUPPORTED;
+  return GDN_TREE_OK;
+}
+
+}  // namespace
+
+namespace gdn {
+
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
+  return launch_verify_generic(a, stream);
+}
+
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_tree_verify(const void* q, const void* k, const void* v, const float* log_alpha,
+                    const float* beta, const int32_t* parent, const float* S0, void* o,
+                    float* U, gdn_tree_dims dims, int32_t* dev_status, void* stream) {
+  const int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  if (dims.B == 0 || dims.N == 0) return GDN_TREE_OK;  // nothing to do
+  const void* ptrs[] = {q, k, v, log_alpha, beta, parent, S0, o, U};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return GDN_TREE_EINVAL;
+  gdn::VerifyArgs a{q, k, v, log_alpha, beta, parent, S0, o, U, dims, dev_status};
+  const cudaError_t err = gdn::launch_verify(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
+int gdn_tree_commit(const int32_t* path, const int32_t* path_len, const int32_t* parent,
+                    const float* U, const void* k, const float* log_alpha, const float* S0,
+                    float* S1, gdn_tree_dims dims, int32_t Lmax, int32_t* dev_status,
+                    void* stream) {
+  const int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  if (Lmax < 0) return GDN_TREE_EINVAL;
+  if (dims.B == 0) return GDN_TREE_OK;
+  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  const void* ptrs[] = {path_len, U, k, log_alpha, S0, S1};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (Lmax > 0 && (path == nullptr || (reinterpret_cast<uintptr_t>(path) & 3u)))
+    return GDN_TREE_EINVAL;
+  if (parent && (reinterpret_cast<uintptr_t>(parent) & 3u)) return GDN_TREE_EINVAL;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return GDN_TREE_EINVAL;
+  // S1 may be S0 exactly; a partial overlap would race between CTAs
+  const size_t bytes = (size_t)dims.B * dims.Hv * dims.dk * dims.dv * sizeof(float);
+  const char* a0 = reinterpret_cast<const char*>(S0);
+  const char* a1 = reinterpret_cast<const char*>(S1);
+  if (a0 != a1 && a0 < a1 + bytes && a1 < a0 + bytes) return GDN_TREE_EINVAL;
+  gdn::CommitArgs a{path, path_len, parent, U, k, log_alpha, S0, S1, dims, Lmax, dev_status};
+  const cudaError_t err = gdn::launch_commit(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
+const char* gdn_tree_strerror(int code) {
+  switch (code) {
+    case GDN_TREE_OK: return "ok";
+    case GDN_TREE_EINVAL: return "invalid argument (NULL or misaligned pointer, bad dims)";
+    case GDN_TREE_EUNSUPPORTED: return "unsupported shape or dtype";
+    case GDN_TREE_ECUDA: return "CUDA launch failed";
+    case GDN_TREE_STATUS_BAD_TREE: return "device status: parent[] is not topologically ordered";
+    case GDN_TREE_STATUS_BAD_PATH: return "device status: accepted path is invalid";
+    default: return "unknown code";
+  }
+}
+
+int gdn_tree_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// kernels.h -- internal launch interface between the C-ABI layer and the
+// kernels of libgdntree (not installed, not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gdn_tree.h"
+
+namespace gdn {
+
+constexpr int kMaxNHost = 256;  // largest tree the kernels take
+constexpr int kMaxDHost = 128;  // largest dk / dv
+
+struct VerifyArgs {
+  const void *q, *k, *v;
+  const float *log_alpha, *beta;
+  const int32_t* parent;
+  const float* S0;
+  void* o;
+  float* U;
+  gdn_tree_dims d;
+  int32_t* dev_status;
+};
+
+struct CommitArgs {
+  const int32_t *path, *path_len, *parent;
+  const float* U;
+  const void* k;
+  const float *log_alpha, *S0;
+  float* S1;
+  gdn_tree_dims d;
+  int32_t Lmax;
+  int32_t* dev_status;
+};
+
+// picks the kernel for the shape and dtype
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);
+
+size_t verify_generic_smem_bytes(int N, int dk, int dv);
+cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream);
+
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,134 @@
+/*
+ * gdn_tree.h -- C ABI of libgdntree: rollback-free tree verification and
+ * delayed state commitment for Gated DeltaNet (GDN) layers, on sm_103a.
+ *
+ * The method is the one of "DFlash-TfM: Trees from Marginals"
+ * (gist.science/it/paper/2607.06763), section 3 "Verifica dell'Albero Senza
+ * Rollback per GDN":
+ *
+ *   - GDN recurrence ("Sfida"):
+ *       S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+ *     S in R^{dk x dv}; the output of a step is o_t = S_t^T q_t.
+ *   - The draft tree is topologically ordered; every node's output is the
+ *     recurrence run along its own root-to-node path from the committed state
+ *     S0, computed in one chunked pass as a masked triangular solve with
+ *     ancestor interaction matrices X and Y ("Soluzione").
+ *   - The state is committed only at the next decoding iteration, once the
+ *     accepted branch is known, so no state is ever rolled back.
+ *
+ * Closed form used by the kernels (the page prints the system only as
+ * "(I+X)U = beta V", its S0 = 0 case): with g_t the sum of log alpha over the
+ * root-to-t path P(t) and gamma_t = exp(g_t),
+ *     X[t,s] = beta_t exp(g_t - g_s) (k_t . k_s)   for s a strict ancestor of t,
+ *     Y[t,s] =        exp(g_t - g_s) (q_t . k_s)   for s in P(t),
+ *     (I + X) U = diag(beta) (V - diag(gamma) K S0),
+ *     O = diag(gamma) Q S0 + Y U,
+ *     S1 = gamma_{p_L} S0 + sum_j exp(g_{p_L} - g_{p_j}) k_{p_j} u_{p_j}^T.
+ * Row t of U is u_t = beta_t (v_t - alpha_t S_parent(t)^T k_t): one row per
+ * node, shared by every branch through it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    keeps no pointer after the call returns and allocates no device memory.
+ *  - Every tensor is dense, row-major (C-contiguous) and 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  A return of GDN_TREE_OK means the work was enqueued.
+ *  - Shape/pointer problems are reported by the return value BEFORE any
+ *    launch.  Problems that depend on device data (an invalid tree or path)
+ *    are reported per sequence in `dev_status` (int32[B], device memory,
+ *    may be NULL); the outputs of such a sequence are left unwritten.
+ *  - The library is thread-safe and holds no global mutable state.
+ *
+ * Shapes (B sequences, Hqk query/key heads, Hv value heads, Hv % Hqk == 0,
+ * v-head h reads q/k head h / (Hv / Hqk)):
+ *    q, k        [B, N, Hqk, dk]   bf16 or fp32 (dims.dtype)
+ *    v           [B, N, Hv,  dv]   same dtype as q, k
+ *    log_alpha   [B, N, Hv]        fp32, log of the decay alpha (<= 0 typical)
+ *    beta        [B, N, Hv]        fp32
+ *    parent      [B, N]            int32, -1 <= parent[b][i] < i (-1: child of S0)
+ *    S0, S1      [B, Hv, dk, dv]   fp32, dv contiguous
+ *    o           [B, N, Hv, dv]    same dtype as q
+ *    U           [B, Hv, N, dv]    fp32
+ *    path        [B, Lmax]         int32 accepted root-to-node path, -1 padded
+ *    path_len    [B]               int32, 0 <= path_len[b] <= min(N, Lmax)
+ *
+ * Limits: 1 <= N <= 256; dk, dv in {16, 32, 48, ..., 128}; B, Hv >= 1.
+ * B == 0 or N == 0 is a valid empty call that enqueues nothing.
+ */
+#ifndef GDN_TREE_H
+#define GDN_TREE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* return codes */
+#define GDN_TREE_OK 0
+#define GDN_TREE_EINVAL (-1)      /* NULL or misaligned pointer, bad dims       */
+#define GDN_TREE_EUNSUPPORTED (-2) /* N > 256, dk/dv outside the list, dtype   */
+#define GDN_TREE_ECUDA (-3)       /* a CUDA call (launch, attribute) failed     */
+
+/* per-sequence device status codes written to dev_status[b] */
+#define GDN_TREE_STATUS_OK 0
+#define GDN_TREE_STATUS_BAD_TREE 1 /* some parent[b][i] outside [-1, i-1]       */
+#define GDN_TREE_STATUS_BAD_PATH 2 /* path_len or a path entry out of range, or
+                                      (with parent given) not a root chain     */
+
+/* element type of q, k, v and o */
+#define GDN_TREE_BF16 0
+#define GDN_TREE_F32 1
+
+typedef struct {
+  int32_t B, N, Hqk, Hv, dk, dv;
+  int32_t dtype; /* GDN_TREE_BF16 or GDN_TREE_F32 */
+} gdn_tree_dims;
+
+/*
+ * gdn_tree_verify -- outputs of every tree node, without touching S0.
+ *
+ * Defined by the DFlash-TfM page, section 3 "Soluzione": o[b, t, h, :] is
+ * S_t^T q_t where S_t is the GDN recurrence run along t's root-to-node path
+ * from S0[b, h]; U[b, h, t, :] is the node's write vector u_t (see above).
+ * Reads q, k, v, log_alpha, beta, parent, S0; writes o and U.  S0 is never
+ * written (the "rollback-free" property).  dev_status[b] (if non-NULL) is set
+ * to GDN_TREE_STATUS_OK or GDN_TREE_STATUS_BAD_TREE for every b.
+ */
+int gdn_tree_verify(const void *q, const void *k, const void *v,
+                    const float *log_alpha, const float *beta,
+                    const int32_t *parent, const float *S0, void *o, float *U,
+                    gdn_tree_dims dims, int32_t *dev_status, void *stream);
+
+/*
+ * gdn_tree_commit -- delayed state commitment of the accepted branch.
+ *
+ * Defined by the DFlash-TfM page, section 3 (state commitment deferred to the
+ * next decoding iteration): S1[b, h] is the state reached by running the GDN
+ * recurrence from S0[b, h] along path[b, 0 .. path_len[b]-1], evaluated as
+ * gamma_{p_L} S0 + sum_j exp(g_{p_L} - g_{p_j}) k_{p_j} u_{p_j}^T from the U
+ * rows a previous gdn_tree_verify wrote for the same tree.  `k` and
+ * `log_alpha` must be the arrays that verify saw.  `parent` may be NULL; when
+ * given, the path must start at a node with parent -1 and follow parent
+ * links, else the sequence gets GDN_TREE_STATUS_BAD_PATH.  path_len[b] == 0
+ * gives S1 = S0.  S1 may alias S0 exactly (in-place commit); any other
+ * overlap is undefined.  dev_status[b] (if non-NULL) is set for every b.
+ */
+int gdn_tree_commit(const int32_t *path, const int32_t *path_len,
+                    const int32_t *parent, const float *U, const void *k,
+                    const float *log_alpha, const float *S0, float *S1,
+                    gdn_tree_dims dims, int32_t Lmax, int32_t *dev_status,
+                    void *stream);
+
+/* Human-readable text for a return code or a device status code. */
+const char *gdn_tree_strerror(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int gdn_tree_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_TREE_H */

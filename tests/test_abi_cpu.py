@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/*.h; host-side argument checks answer before any CUDA call (these
+tests make no compute call and need no GPU)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import gated_deltanet_tree_gdn_gb300 as gt
+from gated_deltanet_tree_gdn_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return _binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_strerror", "gdn_tree_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_version_and_strerror(lib):
+    assert lib.gdn_tree_version() >= 100
+    assert b"invalid" in lib.gdn_tree_strerror(gt.EINVAL)
+    assert b"path" in lib.gdn_tree_strerror(gt.STATUS_BAD_PATH)
+
+
+def _dims(**kw):
+    d = dict(B=2, N=16, Hqk=2, Hv=4, dk=64, dv=64, dtype=gt.BF16)
+    d.update(kw)
+    return gt.Dims(**d)
+
+
+def _verify(lib, dims, ptr=16):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return lib.gdn_tree_verify(p, p, p, p, p, p, p, p, p, dims, None, None)
+
+
+def _commit(lib, dims, ptr=16, Lmax=4):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return lib.gdn_tree_commit(p, p, None, p, p, p, p, ctypes.c_void_p(1 << 40), dims, Lmax,
+                               None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=257), gt.EUNSUPPORTED),
+    (dict(dk=24), gt.EUNSUPPORTED),
+    (dict(dv=256), gt.EUNSUPPORTED),
+    (dict(dtype=7), gt.EUNSUPPORTED),
+    (dict(Hv=3), gt.EINVAL),
+    (dict(Hqk=0), gt.EINVAL),
+    (dict(B=-1), gt.EINVAL),
+])
+def test_bad_dims_rejected_before_launch(lib, kw, code):
+    assert _verify(lib, _dims(**kw)) == code
+    assert _commit(lib, _dims(**kw)) == code
+
+
+def test_null_or_misaligned_pointers_rejected(lib):
+    assert _verify(lib, _dims(), ptr=0) == gt.EINVAL
+    assert _verify(lib, _dims(), ptr=24) == gt.EINVAL  # 8-byte aligned only
+    assert _commit(lib, _dims(), ptr=0) == gt.EINVAL
+    assert _commit(lib, _dims(), Lmax=-1) == gt.EINVAL
+    assert _commit(lib, _dims(), Lmax=300) == gt.EUNSUPPORTED
+
+
+def test_partial_overlap_of_S0_and_S1_rejected(lib):
+    d = _dims()
+    p = ctypes.c_void_p(1 << 20)
+    q = ctypes.c_void_p((1 << 20) + 256)  # overlaps S0 but is not S0
+    assert lib.gdn_tree_commit(p, p, None, p, p, p, p, q, d, 4, None, None) == gt.EINVAL
+
+
+def test_empty_calls_are_noops(lib):
+    assert _verify(lib, _dims(B=0), ptr=0) == gt.OK
+    assert _verify(lib, _dims(N=0), ptr=0) == gt.OK
+    assert _commit(lib, _dims(B=0), ptr=0) == gt.OK

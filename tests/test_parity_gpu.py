@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on
+the same seeded inputs, element by element.
+
+The five workloads of the tree-verification setting run at full size
+(the stress workload on a sample of (sequence, head) units that covers every
+tree family and the beta = 0.99 sequence); smaller shapes span several tiles
+and ragged tails; edge cases cover single nodes, forests, stars, chains,
+invalid trees/paths, empty paths and in-place commits."""
+
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    import gated_deltanet_tree_gdn_gb300 as gt
+    gt.build_library()
+    gt.load()
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_config_full(cfg):
+    w = H.ensure_state(W.make_config(cfg))
+    gpu = H.run_gpu(w)
+    assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
+    errs = H.compare(w, gpu, H.run_oracle(w))
+    H.assert_parity(w, errs)
+
+
+def test_config4_sampled_units():
+    w = W.make_config(4)
+    gpu = H.run_gpu(w)
+    assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
+    rng = np.random.default_rng(4)
+    seqs = sorted(set([0, 1, 2, 3, 4, 5, w.B - 1]) | set(rng.choice(w.B, 8, replace=False)))
+    units = [b * w.Hv + h for b in seqs for h in rng.choice(w.Hv, 6, replace=False)]
+    units += [(w.B - 1) * w.Hv + h for h in range(w.Hv)]  # the beta = 0.99 sequence
+    units = sorted(set(units))
+    errs = H.compare(w, gpu, H.run_oracle(w, units=units), units=units)
+    H.assert_parity(w, errs)
+    assert np.isfinite(gpu["o"]).all() and np.isfinite(gpu["S1"]).all()
+
+
+SHAPES = [
+    # (B, N, Hqk, Hv, dk, dv, dtype, tree)
+    (2, 37, 1, 2, 32, 32, W.F32, "uniform"),
+    (2, 100, 2, 4, 64, 64, W.BF16, "mixed"),
+    (3, 129, 1, 1, 128, 128, W.BF16, "mixed"),
+    (1, 200, 2, 2, 128, 64, W.F32, "random"),
+    (2, 256, 1, 4, 128, 128, W.BF16, "chain"),
+    (2, 256, 1, 2, 64, 128, W.BF16, "flatstar"),
+    (6, 61, 2, 8, 128, 128, W.BF16, "mixed"),
+    (1, 5, 1, 1, 16, 48, W.F32, "uniform"),
+    (1, 1, 1, 1, 128, 128, W.BF16, "chain"),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SHAPES)), ids=["x".join(map(str, s)) for s in SHAPES])
+def test_shapes_elementwise(idx):
+    B, N, Hqk, Hv, dk, dv, dt, tree = SHAPES[idx]
+    w = W.make_custom(seed=100 + idx, B=B, N=N, Hqk=Hqk, Hv=Hv, dk=dk, dv=dv,
+                      dtype=dt, tree=tree, max_depth=40)
+    H.assert_parity(w, H.compare(w, H.run_gpu(w), H.run_oracle(w)))
+
+
+def test_strong_decay_and_high_beta():
+    w = W.make_custom(seed=5, B=6, N=160, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="mixed", max_depth=160, la_range=(0.01, 4.0), beta_kind="uniform")
+    w.beta[:] = np.float32(0.99)
+    H.assert_parity(w, H.compare(w, H.run_gpu(w), H.run_oracle(w)))
+
+
+def test_inplace_commit_and_no_parent_check():
+    w = W.make_custom(seed=6, B=3, N=48, Hqk=2, Hv=4, dk=64, dv=64, dtype=W.BF16)
+    ref = H.run_oracle(w)
+    gpu = H.run_gpu(w, inplace=True, with_parent=False)
+    H.assert_parity(w, H.compare(w, gpu, ref))
+
+
+def test_empty_path_commits_S0():
+    w = W.make_custom(seed=7, B=2, N=20, Hqk=1, Hv=2, dk=32, dv=32, dtype=W.F32)
+    w.path[:] = -1
+    w.path_len[:] = 0
+    gpu = H.run_gpu(w)
+    assert np.array_equal(gpu["S1"], w.S0)
+
+
+def test_invalid_tree_and_path_reported_per_sequence():
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    w = W.make_custom(seed=8, B=3, N=16, Hqk=1, Hv=2, dk=32, dv=32, dtype=W.BF16)
+    w.parent[1, 5] = 9          # not topologically ordered
+    w.path[2, :] = -1           # sequence 2: path 0 -> 2 where 2's parent may differ
+    w.path[2, 0], w.path[2, 1] = 0, 3
+    w.path_len[2] = 2
+    ok_chain = w.parent[2, 3] == 0
+    x = H.to_device(w)
+    st = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    o = torch.full((3, 16, 2, 32), 123.0, dtype=torch.bfloat16, device="cuda")
+    o, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"],
+                     x["S0"], o=o, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [gt.STATUS_OK, gt.STATUS_BAD_TREE, gt.STATUS_OK]
+    assert (o[1].float() == 123.0).all()  # invalid sequence left unwritten
+    w.parent[1, 5] = 4
+    x = H.to_device(w)
+    o, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"])
+    x["path_len"][1] = 99       # longer than the tree
+    S1 = torch.full_like(x["S0"], 5.0)
+    gt.commit(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["S0"], S1=S1,
+              parent=x["parent"], dev_status=st)
+    torch.cuda.synchronize()
+    want2 = gt.STATUS_OK if ok_chain else gt.STATUS_BAD_PATH
+    assert st.cpu().tolist() == [gt.STATUS_OK, gt.STATUS_BAD_PATH, want2]
+    assert (S1[1] == 5.0).all()
+
+
+def test_sibling_permutation_on_gpu():
+    from tests.pins import random_topological_relabel
+    w = W.make_custom(seed=9, B=1, N=90, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="random", max_depth=12)
+    a = H.run_gpu(w)
+    perm, newp = random_topological_relabel(np.random.default_rng(1), w.parent[0])
+    for name in ("q", "k", "v", "log_alpha", "beta"):
+        setattr(w, name, np.ascontiguousarray(getattr(w, name)[:, perm]))
+    w.parent = newp[None].astype(np.int32)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    w.path[0, : w.path_len[0]] = inv[w.path[0, : w.path_len[0]]]
+    b = H.run_gpu(w)
+    assert H.rel_err(b["o"][0], a["o"][0, perm]) <= 1e-2
+    assert H.rel_err(b["U"][0], a["U"][0][:, perm]) <= 1e-4
+    assert H.rel_err(b["S1"], a["S1"]) <= 1e-4
