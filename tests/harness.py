@@ -3,6 +3,9 @@ results, and compare with the fp64 oracle under the stated tolerances."""
 
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -91,7 +94,16 @@ def compare(w: W.Workload, gpu, ref, units=None):
     return dict(o=rel_err(o_g, o_r), U=rel_err(U_g, U_r), S1=rel_err(S_g, S_r))
 
 
+def report(w: W.Workload, errs, tag: str = "") -> None:
+    """Append the errors to $GDN_PARITY_REPORT (JSON lines) when set."""
+    path = os.environ.get("GDN_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(workload=w.name, tag=tag, dtype=w.dtype, **errs)) + "\n")
+
+
 def assert_parity(w: W.Workload, errs):
+    report(w, errs)
     assert errs["o"] <= TOL_O[w.dtype], f"{w.name}: o rel err {errs['o']:.3e}"
     assert errs["U"] <= TOL_U, f"{w.name}: U rel err {errs['U']:.3e}"
     assert errs["S1"] <= TOL_S1, f"{w.name}: S1 rel err {errs['S1']:.3e}"

@@ -93,7 +93,7 @@ def test_empty_path_commits_S0():
 def test_invalid_tree_and_path_reported_per_sequence():
     import torch
     import gated_deltanet_tree_gdn_gb300 as gt
-    w = W.make_custom(seed=8, B=3, N=16, Hqk=1, Hv=2, dk=32, dv=32, dtype=W.BF16)
+    w = W.make_custom(seed=8, B=3, N=16, Hqk=1, Hv=2, dk=32, dv=32, dtype=W.BF16, lmax=16)
     w.parent[1, 5] = 9          # not topologically ordered
     w.path[2, :] = -1           # sequence 2: path 0 -> 2 where 2's parent may differ
     w.path[2, 0], w.path[2, 1] = 0, 3
