@@ -10,7 +10,7 @@ Build the library first with ``python -m gated_deltanet_tree_gdn_gb300.build``.
 
 from ._binding import (  # noqa: F401
     BF16, F32, OK, EINVAL, EUNSUPPORTED, ECUDA, STATUS_OK, STATUS_BAD_TREE,
-    STATUS_BAD_PATH, SYMBOLS, Dims, GdnTreeError, commit, library_path, load, strerror,
+    STATUS_BAD_PATH, STATUS_TIMEOUT, SYMBOLS, Dims, GdnTreeError, commit, library_path, load, strerror,
     verify,
 )
 from .build import build_library  # noqa: F401

@@ -17,7 +17,7 @@ from . import build as _build
 
 BF16, F32 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECUDA = 0, -1, -2, -3
-STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH = 0, 1, 2
+STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TIMEOUT = 0, 1, 2, 3
 
 SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_strerror", "gdn_tree_version")
 

@@ -5,6 +5,8 @@
 // data (tree and path validity) and report it through dev_status.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "../../include/gdn_tree.h"
 #include "kernels.h"
@@ -32,7 +34,16 @@ int check_dims(const gdn_tree_dims& d) {
 
 namespace gdn {
 
+// GDN_TREE_KERNEL=generic forces the CUDA-core kernel (used by the tests to
+// cover both kernels on the same shapes); the default picks the tensor-core
+// kernel whenever it takes the shape.
+static bool force_generic() {
+  const char* e = getenv("GDN_TREE_KERNEL");
+  return e && strcmp(e, "generic") == 0;
+}
+
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
+  if (!force_generic() && verify_tc_supported(a.d)) return launch_verify_tc(a, stream);
   return launch_verify_generic(a, stream);
 }
 
@@ -89,6 +100,7 @@ const char* gdn_tree_strerror(int code) {
     case GDN_TREE_ECUDA: return "CUDA launch failed";
     case GDN_TREE_STATUS_BAD_TREE: return "device status: parent[] is not topologically ordered";
     case GDN_TREE_STATUS_BAD_PATH: return "device status: accepted path is invalid";
+    case GDN_TREE_STATUS_TIMEOUT: return "device status: an on-device wait timed out";
     default: return "unknown code";
   }
 }

@@ -41,6 +41,9 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);
 size_t verify_generic_smem_bytes(int N, int dk, int dv);
 cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream);
 
+bool verify_tc_supported(const gdn_tree_dims& d);
+cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
+
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
 
 }  // namespace gdn

@@ -76,6 +76,8 @@ extern "C" {
 #define GDN_TREE_STATUS_BAD_TREE 1 /* some parent[b][i] outside [-1, i-1]       */
 #define GDN_TREE_STATUS_BAD_PATH 2 /* path_len or a path entry out of range, or
                                       (with parent given) not a root chain     */
+#define GDN_TREE_STATUS_TIMEOUT 3  /* a bounded on-device wait (TMA or tensor-core
+                                      completion) ran out; outputs incomplete   */
 
 /* element type of q, k, v and o */
 #define GDN_TREE_BF16 0

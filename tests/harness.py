@@ -99,7 +99,9 @@ def report(w: W.Workload, errs, tag: str = "") -> None:
     path = os.environ.get("GDN_PARITY_REPORT")
     if path:
         with open(path, "a") as f:
-            f.write(json.dumps(dict(workload=w.name, tag=tag, dtype=w.dtype, **errs)) + "\n")
+            f.write(json.dumps(dict(workload=w.name, tag=tag, dtype=w.dtype,
+                                    kernel=os.environ.get("GDN_TREE_KERNEL", "auto"),
+                                    **errs)) + "\n")
 
 
 def assert_parity(w: W.Workload, errs):

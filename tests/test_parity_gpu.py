@@ -23,8 +23,19 @@ def built_library():
     gt.load()
 
 
+@pytest.fixture(params=["auto", "generic"])
+def kernel(request, monkeypatch):
+    """Runs a test with the default kernel choice (the tensor-core kernel where
+    it takes the shape) and again with the CUDA-core kernel forced."""
+    if request.param == "generic":
+        monkeypatch.setenv("GDN_TREE_KERNEL", "generic")
+    else:
+        monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3])
-def test_config_full(cfg):
+def test_config_full(cfg, kernel):
     w = H.ensure_state(W.make_config(cfg))
     gpu = H.run_gpu(w)
     assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
@@ -57,25 +68,30 @@ SHAPES = [
     (6, 61, 2, 8, 128, 128, W.BF16, "mixed"),
     (1, 5, 1, 1, 16, 48, W.F32, "uniform"),
     (1, 1, 1, 1, 128, 128, W.BF16, "chain"),
+    (4, 128, 2, 4, 128, 128, W.BF16, "mixed"),
+    (3, 97, 1, 3, 128, 128, W.BF16, "chain"),
+    (5, 33, 4, 8, 128, 128, W.BF16, "flatstar"),
+    (2, 128, 1, 2, 128, 128, W.BF16, "chain"),
 ]
 
 
 @pytest.mark.parametrize("idx", range(len(SHAPES)), ids=["x".join(map(str, s)) for s in SHAPES])
-def test_shapes_elementwise(idx):
+def test_shapes_elementwise(idx, kernel):
     B, N, Hqk, Hv, dk, dv, dt, tree = SHAPES[idx]
     w = W.make_custom(seed=100 + idx, B=B, N=N, Hqk=Hqk, Hv=Hv, dk=dk, dv=dv,
                       dtype=dt, tree=tree, max_depth=40)
     H.assert_parity(w, H.compare(w, H.run_gpu(w), H.run_oracle(w)))
 
 
-def test_strong_decay_and_high_beta():
-    w = W.make_custom(seed=5, B=6, N=160, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+@pytest.mark.parametrize("N", [128, 160])
+def test_strong_decay_and_high_beta(kernel, N):
+    w = W.make_custom(seed=5, B=6, N=N, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
                       tree="mixed", max_depth=160, la_range=(0.01, 4.0), beta_kind="uniform")
     w.beta[:] = np.float32(0.99)
     H.assert_parity(w, H.compare(w, H.run_gpu(w), H.run_oracle(w)))
 
 
-def test_inplace_commit_and_no_parent_check():
+def test_inplace_commit_and_no_parent_check(kernel):
     w = W.make_custom(seed=6, B=3, N=48, Hqk=2, Hv=4, dk=64, dv=64, dtype=W.BF16)
     ref = H.run_oracle(w)
     gpu = H.run_gpu(w, inplace=True, with_parent=False)
@@ -90,7 +106,7 @@ def test_empty_path_commits_S0():
     assert np.array_equal(gpu["S1"], w.S0)
 
 
-def test_invalid_tree_and_path_reported_per_sequence():
+def test_invalid_tree_and_path_reported_per_sequence(kernel):
     import torch
     import gated_deltanet_tree_gdn_gb300 as gt
     w = W.make_custom(seed=8, B=3, N=16, Hqk=1, Hv=2, dk=32, dv=32, dtype=W.BF16, lmax=16)
@@ -120,7 +136,7 @@ def test_invalid_tree_and_path_reported_per_sequence():
     assert (S1[1] == 5.0).all()
 
 
-def test_sibling_permutation_on_gpu():
+def test_sibling_permutation_on_gpu(kernel):
     from tests.pins import random_topological_relabel
     w = W.make_custom(seed=9, B=1, N=90, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
                       tree="random", max_depth=12)
