@@ -69,17 +69,32 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // ---- tree preparation --------------------------------------------------------
+
+// block-wide barrier (the default for tree_prepare)
+struct BlockSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// barrier over the first `count` threads of the block (named barrier `id`)
+template <int kId, int kCount>
+struct NamedSync {
+  __device__ __forceinline__ void operator()() const {
+    asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
+  }
+};
+
 //
 // For the tree of one sequence (parent[] already in shared memory and
 // validated), computes with pointer jumping (ceil(log2 N) rounds):
 //   anc[t*W .. t*W+W-1] : bitset of the strict ancestors of t (W = ceil(N/32))
 //   g[t]                : double-float sum of log_alpha over the path P(t)
-// `jump` is an int scratch of N entries.  Must be called by all threads of
-// the block; node t is handled by thread t (requires blockDim.x >= N).
+// `jump` is an int scratch of N entries.  Must be called by every thread that
+// `sync` synchronises; node t is handled by thread t (needs N such threads).
+template <typename Sync = BlockSync>
 __device__ __forceinline__ void tree_prepare(const int* s_parent, int N, int W,
                                              const float* s_log_alpha,
                                              int* s_jump, uint32_t* s_anc,
-                                             df* s_g) {
+                                             df* s_g, Sync sync = Sync()) {
   const int t = threadIdx.x;
   if (t < N) {
     const int p = s_parent[t];
@@ -88,7 +103,7 @@ __device__ __forceinline__ void tree_prepare(const int* s_parent, int N, int W,
     for (int i = 0; i < W; ++i) s_anc[t * W + i] = 0u;
     if (p >= 0) s_anc[t * W + (p >> 5)] = 1u << (p & 31);
   }
-  __syncthreads();
+  sync();
   for (int span = 1; span < N; span <<= 1) {
     int j = -1, jj = -1;
     df gj = {0.f, 0.f};
@@ -102,7 +117,7 @@ __device__ __forceinline__ void tree_prepare(const int* s_parent, int N, int W,
         for (int i = 0; i < kMaxN / 32; ++i) w[i] = i < W ? s_anc[j * W + i] : 0u;
       }
     }
-    __syncthreads();
+    sync();
     if (t < N && j >= 0) {
       s_g[t] = df_add(s_g[t], gj);
 #pragma unroll
@@ -110,7 +125,7 @@ __device__ __forceinline__ void tree_prepare(const int* s_parent, int N, int W,
         if (i < W) s_anc[t * W + i] |= w[i];
       s_jump[t] = jj;
     }
-    __syncthreads();
+    sync();
   }
 }
 

@@ -45,31 +45,46 @@ using namespace sm100;
 
 constexpr int kTile = 128;         // padded node count = MMA M
 constexpr int kD = 128;            // dk = dv
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kW = kTile / 32;     // ancestor bitset words per node
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384, kColYU = 0;
-constexpr int kXStride = kTile + 1;  // padded fp32 row of X
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kIssuer = 128;  // the one thread that issues every MMA (warp 4, lane 0)
+
+#ifdef GDN_TC_PROFILE
+// per-CTA phase timestamps for a profiling build (never in the product build)
+__device__ unsigned long long g_tc_phase[4096][16];
+#define TC_MARK(i)                                                                   \
+  do {                                                                               \
+    if (threadIdx.x == 0 && blockIdx.y * gridDim.x + blockIdx.x < 4096)              \
+      g_tc_phase[blockIdx.y * gridDim.x + blockIdx.x][i] = globaltimer_ns();         \
+  } while (0)
+#else
+#define TC_MARK(i) \
+  do {             \
+  } while (0)
+#endif
 
 // shared memory map (byte offsets from a 1024-aligned base)
-constexpr uint32_t kTileBytes = kTile * 128 * 2 / 2;  // one 64-wide K block: 128 rows x 128 B
+constexpr uint32_t kTileBytes = 128 * 128;            // one 64-wide K block: 128 rows x 128 B
 constexpr uint32_t kOpBytes = 2 * kTileBytes;         // a 128 x 128 bf16 operand (2 K blocks)
-constexpr uint32_t OFF_K = 0;                 // phase A
+constexpr uint32_t OFF_K = 0;                 // K, Q, S0^T: live until the K S0 / Q S0 MMAs end
 constexpr uint32_t OFF_Q = 1 * kOpBytes;
 constexpr uint32_t OFF_S0H = 2 * kOpBytes;
 constexpr uint32_t OFF_S0L = 3 * kOpBytes;
-constexpr uint32_t OFF_X = 0;                 // phase B (solve), aliases phase A
-constexpr uint32_t OFF_YH = 0;                // phase C (output), aliases A and B
+constexpr uint32_t OFF_X = 0;                 // X (packed lower triangle, fp32): the solve
+constexpr uint32_t OFF_YH = 0;                // Y and U^T operands of Y U
 constexpr uint32_t OFF_YL = 1 * kOpBytes;
 constexpr uint32_t OFF_UTH = 2 * kOpBytes;
 constexpr uint32_t OFF_UTL = 3 * kOpBytes;
-constexpr uint32_t OFF_U = 4 * kOpBytes;      // R / U, fp32, 64 KB
+constexpr uint32_t OFF_U = 4 * kOpBytes;      // raw S0 (TMA), then R / U, fp32, 64 KB
 constexpr uint32_t OFF_SMALL = OFF_U + kTile * kD * 4;
-constexpr uint32_t kSmallBytes = 8192;
+constexpr uint32_t kSmallBytes = 10240;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
-static_assert(kTile * kXStride * 4 <= 4 * kOpBytes, "X must fit in the operand region");
+static_assert(kTile * (kTile - 1) / 2 * 4 <= OFF_UTH, "X must not reach U^T");
 static_assert(OFF_U % 1024 == 0, "alignment");
 
 struct Small {
@@ -79,22 +94,22 @@ struct Small {
   float beta[kTile];
   float la[kTile];
   uint32_t anc[kTile * kW];
-  int depth[kTile];
   int order[kTile];
+  int depth[kTile];
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
-  uint64_t bar_tma;
-  uint64_t bar_mma;
+  uint32_t level_bits[(kTile + 2) * kW];
+  uint64_t bar_kq, bar_s0, bar_g, bar_ks, bar_yu;
   uint32_t tmem_base;
   int max_depth;
   int err;
+  int issued;  // bit 0: Gram MMAs, bit 1: K S0 / Q S0 MMAs, bit 2: Y U MMAs
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
 
-// byte offset of element (row, k) inside a 128-row, 128-wide K-major
-// bf16 tile with the 128-byte swizzle (two 64-wide K blocks)
+// byte offset of 16-byte chunk k8 (K elements 8*k8 .. 8*k8+7) of `row` in a
+// 128-row, 128-wide K-major bf16 tile stored with the 128-byte swizzle
 __device__ __forceinline__ uint32_t sw128_chunk(int row, int k8) {
-  // k8 = index of the 8-element (16-byte) chunk along K, 0..15
   const int kb = k8 >> 3, j = k8 & 7;
   return (uint32_t)(kb * kTileBytes + row * 128 + ((j ^ (row & 7)) << 4));
 }
@@ -102,6 +117,9 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int k8) {
 // fp32 R/U tile: row t, 4-float chunk c4 (0..31), chunk index xor-swizzled by
 // the row so that row-per-thread float4 accesses are bank-conflict free
 __device__ __forceinline__ int u_index(int t, int c4) { return t * kD + ((c4 ^ (t & 7)) << 2); }
+
+// packed strictly-lower triangle of X
+__device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
 
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);
@@ -124,12 +142,22 @@ __device__ __forceinline__ void umma_128x128x128(uint32_t d_tmem, uint32_t a_bas
   }
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmS,
                  const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
                  const float* __restrict__ beta, const int32_t* __restrict__ parent,
-                 const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                 float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status) {
+                 __nv_bfloat16* __restrict__ o, float* __restrict__ U, gdn_tree_dims d,
+                 int32_t* dev_status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -142,111 +170,151 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int h = blockIdx.x, b = blockIdx.y;
   const int hq = h / (Hv / Hqk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // epilogue mapping: thread <-> (tree row t, 32-column quarter cq); warp w
+  // may only touch TMEM lanes 32*(w%4) .. 32*(w%4)+31
+  const int q4 = warp & 3, cq = warp >> 2;
+  const int t = q4 * 32 + lane;
+  const bool live = t < N;
 
-  // ---- 1. tree: load + validate (nothing issued yet) ----------------------
-  int bad = 0;
-  for (int t = tid; t < kTile; t += kThreads) {
-    int p = -1;
-    float be = 0.f, la = 0.f;
-    if (t < N) {
-      p = parent[(size_t)b * N + t];
-      bad |= (p < -1 || p >= t);
-      be = beta[((size_t)b * N + t) * Hv + h];
-      la = log_alpha[((size_t)b * N + t) * Hv + h];
+  // ---- 0. tree loads first (their latency hides the set-up), then TMEM,
+  //         barriers and every bulk load ------------------------------------------
+  TC_MARK(0);
+  int p_in = -1;
+  float be_in = 0.f, la_in = 0.f;
+  if (tid < N) {
+    p_in = parent[(size_t)b * N + tid];
+    be_in = beta[((size_t)b * N + tid) * Hv + h];
+    la_in = log_alpha[((size_t)b * N + tid) * Hv + h];
+  }
+  // this thread's 32 values of v (row t, columns 32 cq ..), kept in registers
+  uint4 vreg[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                   make_uint4(0, 0, 0, 0)};
+  if (live) {
+    const uint4* vrow = reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    if (lane == 0) {
+      mbar_init(&S.bar_kq, 1);
+      mbar_init(&S.bar_s0, 1);
+      mbar_init(&S.bar_g, 1);
+      mbar_init(&S.bar_ks, 1);
+      mbar_init(&S.bar_yu, 1);
+      S.err = 0;
+      S.issued = 0;
+      S.max_depth = 0;
+      mbar_fence_init();
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmS);
+      mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
+      tma_load_4d(smem + OFF_K, &tmK, &S.bar_kq, 0, hq, 0, b);
+      tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_kq, 64, hq, 0, b);
+      tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
+      tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
+      mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
+      tma_load_3d(smem + OFF_U, &tmS, &S.bar_s0, 0, 0, b * Hv + h);
     }
-    S.parent[t] = p;
-    S.beta[t] = be;
-    S.la[t] = la;
   }
-  if (tid == 0) {
-    S.err = 0;
-    S.max_depth = 0;
-  }
-  bad = __syncthreads_or(bad);
-  if (h == 0 && tid == 0 && dev_status)
-    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
-  if (bad) return;
 
-  // ---- 2. TMEM, barriers, TMA of K and Q --------------------------------------
-  if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
-  if (tid == 32) {
-    mbar_init(&S.bar_tma, 1);
-    mbar_init(&S.bar_mma, 1);
-    mbar_fence_init();
+  // ---- 1. tree: validate ------------------------------------------------------------
+  TC_MARK(1);
+  int bad = 0;
+  if (tid < kTile) {
+    S.parent[tid] = p_in;
+    S.beta[tid] = be_in;
+    S.la[tid] = la_in;
+    bad = tid < N && (p_in < -1 || p_in >= tid);
+  }
+  if (tid < kTile + 2) {
+    S.level_start[tid] = 0;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) S.level_bits[tid * kW + w] = 0u;
   }
   tc_fence_before_sync();
-  __syncthreads();
+  bad = __syncthreads_or(bad);
   tc_fence_after_sync();
   const uint32_t tmem = S.tmem_base;
-  if (tid == 0) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmQ);
-    mbar_arrive_expect_tx(&S.bar_tma, 4 * kTileBytes);
-    tma_load_4d(smem + OFF_K, &tmK, &S.bar_tma, 0, hq, 0, b);
-    tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_tma, 64, hq, 0, b);
-    tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_tma, 0, hq, 0, b);
-    tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_tma, 64, hq, 0, b);
+  if (h == 0 && tid == 0 && dev_status)
+    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
+  if (bad) {
+    if (tid == 0) {  // let the bulk loads land before the CTA exits
+      mbar_wait(&S.bar_kq, 0, kWaitLimitNs);
+      mbar_wait(&S.bar_s0, 0, kWaitLimitNs);
+    }
+    goto release;
   }
 
-  // ---- 3. ancestor bitsets, path log-decays, depth levels -----------------------
-  tree_prepare(S.parent, kTile, kW, S.la, S.jump, S.anc, S.g);
-  int my_depth = 0;
-  if (tid < kTile + 2) S.level_start[tid] = 0;
-  if (tid < N) {
+  // ---- 2. warps 0-3: ancestor bitsets, path log-decays, depth levels;
+  //         warp 4 lane 0: Gram MMAs once K and Q have landed;
+  //         warps 4-15: S0^T = hi + lo (bf16, K-major, 128-byte swizzle) --------------
+  TC_MARK(2);
+  if (warp < 4) {
+    using TreeSync = NamedSync<1, 128>;
+    tree_prepare(S.parent, kTile, kW, S.la, S.jump, S.anc, S.g, TreeSync());
+    int dep = 0;
+    if (tid < N) {
 #pragma unroll
-    for (int w = 0; w < kW; ++w) my_depth += __popc(S.anc[tid * kW + w]);
-    my_depth += 1;
-    S.depth[tid] = my_depth;
-  }
-  __syncthreads();
-  if (tid < N) {
-    atomicAdd(&S.level_start[my_depth], 1);
-    atomicMax(&S.max_depth, my_depth);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
-    int cnt[5], run = 0;
-#pragma unroll
-    for (int e = 0; e < 5; ++e) {
-      const int l = lane * 5 + e;
-      cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
-      run += cnt[e];
+      for (int w = 0; w < kW; ++w) dep += __popc(S.anc[tid * kW + w]);
+      dep += 1;
+      S.depth[tid] = dep;
+      atomicAdd(&S.level_start[dep], 1);
+      atomicOr(&S.level_bits[dep * kW + (tid >> 5)], 1u << (tid & 31));
+      atomicMax(&S.max_depth, dep);
     }
-    int incl = run;
+    TreeSync()();
+    if (warp == 0) {
+      // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
+      int cnt[5], run = 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int up = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += up;
-    }
-    int excl = incl - run;
-#pragma unroll
-    for (int e = 0; e < 5; ++e) {
-      const int l = lane * 5 + e;
-      if (l < kTile + 2) {
-        S.level_start[l] = excl;
-        S.level_cursor[l] = excl;
+      for (int e = 0; e < 5; ++e) {
+        const int l = lane * 5 + e;
+        cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
+        run += cnt[e];
       }
-      excl += cnt[e];
-    }
-  }
-  __syncthreads();
-  if (tid < N) S.order[atomicAdd(&S.level_cursor[my_depth], 1)] = tid;
-
-  // ---- S0^T = hi + lo (bf16, K-major, 128-byte swizzle) --------------------------
-  {
-    const float* S0bh = S0 + ((size_t)b * Hv + h) * kD * kD;
-    for (int item = tid; item < kD * 16; item += kThreads) {
-      const int n = item & (kD - 1), k8 = item >> 7;
-      float x[8];
+      int incl = run;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = __ldg(S0bh + (size_t)(k8 * 8 + i) * kD + n);
+      for (int off = 1; off < 32; off <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += up;
+      }
+      int excl = incl - run;
+#pragma unroll
+      for (int e = 0; e < 5; ++e) {
+        const int l = lane * 5 + e;
+        if (l < kTile + 2) {
+          S.level_start[l] = excl;
+          S.level_cursor[l] = excl;
+        }
+        excl += cnt[e];
+      }
+    }
+    TreeSync()();
+    if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
+  } else {
+    if (tid == kIssuer) {
+      if (!mbar_wait(&S.bar_kq, 0, kWaitLimitNs)) {
+        S.err = 1;
+      } else {
+        tc_fence_after_sync();
+        umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
+        umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
+        umma_commit(&S.bar_g);
+        S.issued |= 1;
+      }
+    }
+    if (!mbar_wait(&S.bar_s0, 0, kWaitLimitNs)) S.err = 1;
+    const float* raw = sU;  // S0 [dk][dv], row-major, landed by TMA
+    for (int item = tid - 128; item < kD * 16; item += kThreads - 128) {
+      const int n = item & (kD - 1), k8 = item >> 7;
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         __nv_bfloat16 h0, l0, h1, l1;
-        split_bf16(x[2 * i], h0, l0);
-        split_bf16(x[2 * i + 1], h1, l1);
+        split_bf16(raw[(k8 * 8 + 2 * i) * kD + n], h0, l0);
+        split_bf16(raw[(k8 * 8 + 2 * i + 1) * kD + n], h1, l1);
         hi[i] = pack2(h0, h1);
         lo[i] = pack2(l0, l1);
       }
@@ -254,81 +322,61 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       *reinterpret_cast<uint4*>(smem + OFF_S0H + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(smem + OFF_S0L + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
+    fence_proxy_async_smem();
   }
-  fence_proxy_async_smem();
-  __syncthreads();
-
-  // ---- 4. Gram, K S0, Q S0 on the tensor cores --------------------------------
-  if (tid == 0) {
-    if (!mbar_wait(&S.bar_tma, 0, kWaitLimitNs)) {
-      S.err = 1;
-    } else {
-      tc_fence_after_sync();
-      umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
-      umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
-      umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
-      umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
-      umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-      umma_commit(&S.bar_mma);
-    }
-  }
-  __syncthreads();
-  if (S.err) goto fail;
-  if (!mbar_wait(&S.bar_mma, 0, kWaitLimitNs)) S.err = 2;
-  tc_fence_after_sync();
+  TC_MARK(3);
+  TC_MARK(4);
   if (__syncthreads_or(S.err)) goto fail;
 
+  // ---- 5. K S0 (hi + lo) and Q S0 (hi) -----------------------------------------------
+  if (tid == kIssuer) {
+    tc_fence_after_sync();
+    umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+    umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+    umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+    umma_commit(&S.bar_ks);
+    S.issued |= 2;
+  }
+
   {
-    // thread <-> (tree row t, column half): warp w reads TMEM lanes 32*(w%4)..
-    const int q4 = warp & 3, half = warp >> 2;
-    const int t = q4 * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    const bool live = t < N;
+    const int col0 = cq * 32;
     const float bt = live ? S.beta[t] : 0.f;
     const df gt = live ? S.g[t] : df{0.f, 0.f};
-    const float gam = expf(df_value(gt));
-    uint32_t anc[kW];
-#pragma unroll
-    for (int w = 0; w < kW; ++w) anc[w] = live ? S.anc[t * kW + w] : 0u;
+    const float gam = __expf(df_value(gt));
+    const uint32_t abits = live ? S.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
 
-    // ---- 5. X (masked, decay-weighted K K^T) and R ----------------------------
+    // ---- 6. X row segment (registers) while K S0 / Q S0 run ------------------------
+    TC_MARK(5);
+    if (!mbar_wait(&S.bar_g, 0, kWaitLimitNs)) S.err = 2;
+    tc_fence_after_sync();
+    float xr[32];
+    tmem_ld_32cols(trow + kColGkk + col0, xr);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int col0 = half * 64 + c * 32;
-      float gk[32];
-      tmem_ld_32cols(trow + kColGkk + col0, gk);
-      const uint32_t bits = anc[col0 >> 5];
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if ((bits >> j) & 1u) {
-            const int s = col0 + j;
-            sX[t * kXStride + s] = bt * expf(df_diff(gt, S.g[s])) * gk[j];
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int col0 = half * 64 + c * 32;
+    for (int j = 0; j < 32; ++j)
+      xr[j] = ((abits >> j) & 1u) ? bt * __expf(df_diff(gt, S.g[col0 + j])) * xr[j] : 0.f;
+
+    // ---- 7. R = beta (V - gamma K S0); X and R to shared memory -------------------
+    if (!mbar_wait(&S.bar_ks, 0, kWaitLimitNs)) S.err = 2;
+    tc_fence_after_sync();
+    if (__syncthreads_or(S.err)) goto fail;  // K, Q, S0^T are dead from here on
+    {
       float ks[32];
       tmem_ld_32cols(trow + kColKS + col0, ks);
       if (live) {
-        const uint4* vrow = reinterpret_cast<const uint4*>(
-            v + (((size_t)b * N + t) * Hv + h) * kD + col0);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((abits >> j) & 1u) sX[x_index(t, col0 + j)] = xr[j];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 raw = __ldg(vrow + q);
-          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+          const uint32_t w4[4] = {vreg[q].x, vreg[q].y, vreg[q].z, vreg[q].w};
           float r[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float v0 = __uint_as_float(w4[e] << 16);
-            const float v1 = __uint_as_float(w4[e] & 0xffff0000u);
-            r[2 * e] = bt * (v0 - gam * ks[q * 8 + 2 * e]);
-            r[2 * e + 1] = bt * (v1 - gam * ks[q * 8 + 2 * e + 1]);
+            r[2 * e] = bt * (__uint_as_float(w4[e] << 16) - gam * ks[q * 8 + 2 * e]);
+            r[2 * e + 1] = bt * (__uint_as_float(w4[e] & 0xffff0000u) - gam * ks[q * 8 + 2 * e + 1]);
           }
-          const int c4 = (col0 >> 2) + q * 2;
+          const int c4 = cq * 8 + q * 2;
           *reinterpret_cast<float4*>(sU + u_index(t, c4)) = make_float4(r[0], r[1], r[2], r[3]);
           *reinterpret_cast<float4*>(sU + u_index(t, c4 + 1)) =
               make_float4(r[4], r[5], r[6], r[7]);
@@ -338,38 +386,59 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc_fence_before_sync();
     __syncthreads();
 
-    // ---- 6. forward substitution, level by level -------------------------------
-    const int max_depth = S.max_depth;
-    for (int lvl = 2; lvl <= max_depth; ++lvl) {
-      const int beg = S.level_start[lvl], end = S.level_start[lvl + 1];
-      for (int i = beg + warp; i < end; i += kThreads / 32) {
-        const int tn = S.order[i];
-        float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
+    // ---- 8. forward substitution, right-looking over depth levels -------------------
+    // once every node of depth <= l is final, each deeper node t subtracts the
+    // term of its unique ancestor a at depth l: u_t -= X[t,a] u_a.  Warp w owns
+    // the nodes at positions w, w + 16, ... of the depth order and keeps their
+    // partial sums in registers (lane = 4 value columns); a node is written to
+    // shared memory (and to U) the moment it is final.
+    TC_MARK(6);
+    {
+      constexpr int kSlots = kTile / kWarps;
+      int tn[kSlots], dp[kSlots];
+      float4 acc[kSlots];
+      float* Ubh = U + ((size_t)b * Hv + h) * N * kD;
 #pragma unroll
-        for (int w = 0; w < kW; ++w) {
-          uint32_t bits = S.anc[tn * kW + w];
-          while (bits) {
-            const int s = w * 32 + __ffs(bits) - 1;
-            bits &= bits - 1;
-            const float x = sX[tn * kXStride + s];
-            const float4 us = *reinterpret_cast<const float4*>(sU + u_index(s, lane));
-            acc.x = fmaf(-x, us.x, acc.x);
-            acc.y = fmaf(-x, us.y, acc.y);
-            acc.z = fmaf(-x, us.z, acc.z);
-            acc.w = fmaf(-x, us.w, acc.w);
+      for (int k = 0; k < kSlots; ++k) {
+        const int i = warp + k * kWarps;
+        tn[k] = i < N ? S.order[i] : 0;
+        dp[k] = i < N ? S.depth[tn[k]] : 0;
+        acc[k] = *reinterpret_cast<const float4*>(sU + u_index(tn[k], lane));
+        if (dp[k] == 1) *reinterpret_cast<float4*>(Ubh + (size_t)tn[k] * kD + lane * 4) = acc[k];
+      }
+      const int max_depth = S.max_depth;
+      for (int lvl = 1; lvl < max_depth; ++lvl) {
+        const uint32_t lb0 = S.level_bits[lvl * kW + 0], lb1 = S.level_bits[lvl * kW + 1];
+        const uint32_t lb2 = S.level_bits[lvl * kW + 2], lb3 = S.level_bits[lvl * kW + 3];
+#pragma unroll
+        for (int k = 0; k < kSlots; ++k) {
+          if (dp[k] > lvl) {
+            const int tk = tn[k];
+            const uint32_t m0 = S.anc[tk * kW + 0] & lb0, m1 = S.anc[tk * kW + 1] & lb1;
+            const uint32_t m2 = S.anc[tk * kW + 2] & lb2, m3 = S.anc[tk * kW + 3] & lb3;
+            const int a = m0 ? __ffs(m0) - 1
+                             : m1 ? 31 + __ffs(m1) : m2 ? 63 + __ffs(m2) : 95 + __ffs(m3);
+            const float x = sX[x_index(tk, a)];
+            const float4 ua = *reinterpret_cast<const float4*>(sU + u_index(a, lane));
+            acc[k].x = fmaf(-x, ua.x, acc[k].x);
+            acc[k].y = fmaf(-x, ua.y, acc[k].y);
+            acc[k].z = fmaf(-x, ua.z, acc[k].z);
+            acc[k].w = fmaf(-x, ua.w, acc[k].w);
+            if (dp[k] == lvl + 1) {
+              *reinterpret_cast<float4*>(sU + u_index(tk, lane)) = acc[k];
+              *reinterpret_cast<float4*>(Ubh + (size_t)tk * kD + lane * 4) = acc[k];
+            }
           }
         }
-        *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
+        __syncthreads();
       }
-      __syncthreads();
     }
 
-    // ---- 7. U out; U^T and Y to shared memory as bf16 hi + lo -------------------
-    for (int tn = warp; tn < N; tn += kThreads / 32) {
-      const float4 u = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
-      *reinterpret_cast<float4*>(U + (((size_t)b * Hv + h) * N + tn) * kD + lane * 4) = u;
-    }
-    for (int item = tid; item < kD * 16; item += kThreads) {
+    // ---- 9. U out; U^T and Y to shared memory as bf16 hi + lo ----------------------
+    TC_MARK(7);
+#pragma unroll
+    for (int r = 0; r < (kD * 16) / kThreads; ++r) {
+      const int item = tid + r * kThreads;
       const int n = item & (kD - 1), t8 = item >> 7;
       uint32_t hi[4], lo[4];
 #pragma unroll
@@ -388,12 +457,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       *reinterpret_cast<uint4*>(smem + OFF_UTH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(smem + OFF_UTL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int col0 = half * 64 + c * 32;
+    {
       float gq[32];
       tmem_ld_32cols(trow + kColGqk + col0, gq);
-      const uint32_t bits = anc[col0 >> 5];
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
         uint32_t hi[4], lo[4];
@@ -404,9 +470,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int e = 0; e < 2; ++e) {
             const int j = g8 * 8 + 2 * i + e;
             const int s = col0 + j;
-            y[e] = 0.f;
-            if (live && (((bits >> j) & 1u) || s == t))
-              y[e] = (s == t ? 1.f : expf(df_diff(gt, S.g[s]))) * gq[j];
+            const bool on_path = live && (((abits >> j) & 1u) || s == t);
+            y[e] = on_path ? (s == t ? gq[j] : __expf(df_diff(gt, S.g[s])) * gq[j]) : 0.f;
           }
           __nv_bfloat16 h0, l0, h1, l1;
           split_bf16(y[0], h0, l0);
@@ -414,7 +479,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           hi[i] = pack2(h0, h1);
           lo[i] = pack2(l0, l1);
         }
-        const uint32_t off = sw128_chunk(t, (col0 >> 3) + g8);
+        const uint32_t off = sw128_chunk(t, cq * 4 + g8);
         *reinterpret_cast<uint4*>(smem + OFF_YH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(smem + OFF_YL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
@@ -423,22 +488,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc_fence_before_sync();
     __syncthreads();
 
-    // ---- 8. Y U on the tensor cores (three bf16 passes) ---------------------------
-    if (tid == 0) {
+    // ---- 10. Y U on the tensor cores (three bf16 passes) -------------------------------
+    TC_MARK(8);
+    if (tid == kIssuer) {
       tc_fence_after_sync();
       umma_128x128x128(tmem + kColYU, sbase + OFF_YH, sbase + OFF_UTH, false);
       umma_128x128x128(tmem + kColYU, sbase + OFF_YH, sbase + OFF_UTL, true);
       umma_128x128x128(tmem + kColYU, sbase + OFF_YL, sbase + OFF_UTH, true);
-      umma_commit(&S.bar_mma);
+      umma_commit(&S.bar_yu);
+      S.issued |= 4;
     }
-    if (!mbar_wait(&S.bar_mma, 1, kWaitLimitNs)) S.err = 3;
+    if (!mbar_wait(&S.bar_yu, 0, kWaitLimitNs)) S.err = 3;
     tc_fence_after_sync();
     if (__syncthreads_or(S.err)) goto fail;
 
-    // ---- 9. O = gamma QS + Y U -------------------------------------------------------
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int col0 = half * 64 + c * 32;
+    // ---- 11. O = gamma QS + Y U --------------------------------------------------------
+    TC_MARK(9);
+    {
       float yu[32], qs[32];
       tmem_ld_32cols(trow + kColYU + col0, yu);
       tmem_ld_32cols(trow + kColQS + col0, qs);
@@ -458,18 +524,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
     }
   }
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-  return;
+  TC_MARK(10);
+  goto release;
 
 fail:
-  // a wait ran out: report, let in-flight copies / MMAs drain (bounded), free TMEM
+  // a bounded wait ran out: report it, let in-flight copies and MMAs drain
+  // (again bounded), then free TMEM
   if (tid == 0) {
     if (dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
-    if (S.err == 1) mbar_wait(&S.bar_tma, 0, kWaitLimitNs);          // TMA still in flight
-    if (S.err >= 2) mbar_wait(&S.bar_mma, S.err == 3 ? 1 : 0, kWaitLimitNs);  // MMAs
+    mbar_wait(&S.bar_kq, 0, kWaitLimitNs);
+    mbar_wait(&S.bar_s0, 0, kWaitLimitNs);
+    if (S.issued & 1) mbar_wait(&S.bar_g, 0, kWaitLimitNs);
+    if (S.issued & 2) mbar_wait(&S.bar_ks, 0, kWaitLimitNs);
+    if (S.issued & 4) mbar_wait(&S.bar_yu, 0, kWaitLimitNs);
   }
+
+release:
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
@@ -506,6 +576,19 @@ bool encode_qk_map(CUtensorMap* map, const void* base, const gdn_tree_dims& d) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// S0 [B*Hv, dk, dv] fp32 -> one 128 x 128 box per (b, h), unswizzled
+bool encode_state_map(CUtensorMap* map, const float* base, const gdn_tree_dims& d) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kD, (cuuint64_t)d.B * d.Hv};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)kD * kD * 4};
+  const cuuint32_t box[3] = {kD, kD, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool verify_tc_supported(const gdn_tree_dims& d) {
@@ -514,16 +597,24 @@ bool verify_tc_supported(const gdn_tree_dims& d) {
 }
 
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
-  CUtensorMap tmQ, tmK;
-  if (!encode_qk_map(&tmQ, a.q, a.d) || !encode_qk_map(&tmK, a.k, a.d))
+  CUtensorMap tmQ, tmK, tmS;
+  if (!encode_qk_map(&tmQ, a.q, a.d) || !encode_qk_map(&tmK, a.k, a.d) ||
+      !encode_state_map(&tmS, a.S0, a.d))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
   verify_tc_kernel<<<dim3(a.d.Hv, a.d.B), kThreads, kSmemBytes, stream>>>(
-      tmQ, tmK, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
+      tmQ, tmK, tmS, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent,
       static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status);
   return cudaGetLastError();
 }
 
 }  // namespace gdn
+
+#ifdef GDN_TC_PROFILE
+extern "C" int gdn_tree_debug_tc_phases(unsigned long long* host, int n_ctas) {
+  return (int)cudaMemcpyFromSymbol(host, gdn::g_tc_phase,
+                                   sizeof(unsigned long long) * 16 * (n_ctas < 4096 ? n_ctas : 4096));
+}
+#endif
