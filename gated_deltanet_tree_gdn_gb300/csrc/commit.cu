@@ -11,9 +11,11 @@
 //
 // Grid: (Hv, B, dk / kRows).  Each CTA owns kRows rows of one (b, h) state and
 // all dv columns; thread (r, c4) keeps a 4x4 register tile: rows r*4..r*4+3,
-// columns c4*4..c4*4+3.  The path's k rows (restricted to the CTA's rows) and
-// the scaled U rows w_j u_{p_j} are staged through shared memory in chunks of
-// kChunk path entries.
+// columns c4*4..c4*4+3.  Its S0 tile is loaded first, so that the state stream
+// overlaps the path-dependent loads; those come in one round (path and its
+// length together, then parent links, log alpha, k rows and U rows), and the
+// path's k rows (restricted to the CTA's rows) and U rows are staged through
+// shared memory in chunks of kChunk path entries.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -23,7 +25,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kRows = 32;    // state rows per CTA
-constexpr int kChunk = 64;   // path entries staged per round
+constexpr int kChunk = 32;   // path entries staged per round
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
@@ -35,10 +37,10 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   // S0 and S1 may alias (in-place commit): every element is read and then
   // written by the same thread, so they are not __restrict__.
   __shared__ int sPath[kMaxN];
+  __shared__ float sLa[kMaxN];         // log alpha along the path
   __shared__ float sW[kMaxN];          // w_j
-  __shared__ df sScan[kMaxN];          // prefix sums G_j
   __shared__ __align__(16) float sK[kChunk][kRows];     // k_{p_j}[row0 + r]
-  __shared__ __align__(16) float sWU[kChunk][kMaxD];    // w_j u_{p_j}
+  __shared__ __align__(16) float sU[kChunk][kMaxD];     // u_{p_j}
   __shared__ float sGamma;
 
   const int N = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
@@ -47,32 +49,42 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = min(kRows, dk - row0);
 
-  // ---- path: load + validate ---------------------------------------------
+  // ---- S0 tile prefetch: thread (r4, c4) owns rows r4*4.., columns c4*4.. ----
+  const int r4 = tid / 32, c4 = tid % 32;
+  const bool active = (r4 * 4 < rows) && (c4 < dv / 4);
+  const size_t sbase = ((size_t)b * Hv + h) * dk * dv;
+  float4 s0v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    s0v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active)
+      s0v[i] = *reinterpret_cast<const float4*>(S0 + sbase + (size_t)(row0 + r4 * 4 + i) * dv + c4 * 4);
+  }
+
+  // ---- path length and entries, loaded together ------------------------------
   const int L = path_len[b];
+  int pj = -1;
+  if (tid < Lmax) pj = path[(size_t)b * Lmax + tid];
   int bad = (L < 0 || L > N || L > Lmax);
-  const int Lc = bad ? 0 : L;
-  for (int j = tid; j < Lc; j += kThreads) {
-    const int p = path[(size_t)b * Lmax + j];
-    sPath[j] = p;
-    bad |= (p < 0 || p >= N);
+  if (!bad && tid < L) {
+    bad |= (pj < 0 || pj >= N);
+    sPath[tid] = pj;
   }
   bad = __syncthreads_or(bad);
-  if (!bad) {
-    for (int j = tid; j < Lc; j += kThreads) {
-      const int p = sPath[j];
-      const int prev = j == 0 ? -1 : sPath[j - 1];
-      // a root-to-node path is strictly increasing in a topological order;
-      // with the tree given it must also follow the parent links
-      bad |= (j > 0 && p <= prev);
-      if (parent) bad |= (parent[(size_t)b * N + p] != prev);
-    }
+  if (!bad && tid < L) {
+    // a root-to-node path is strictly increasing in a topological order; with
+    // the tree given it must also follow the parent links
+    const int prev = tid == 0 ? -1 : sPath[tid - 1];
+    bad |= (tid > 0 && pj <= prev);
+    if (parent) bad |= (parent[(size_t)b * N + pj] != prev);
+    sLa[tid] = log_alpha[((size_t)b * N + pj) * Hv + h];
   }
   bad = __syncthreads_or(bad);
   if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
     dev_status[b] = bad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
   if (bad) return;
 
-  // ---- G_j: inclusive double-float prefix sums of log alpha along the path
+  // ---- G_j: inclusive double-float prefix sums of log alpha along the path ------
   if (warp == 0) {
     // lane l owns entries l*8 .. l*8+7 (L <= 256)
     df loc[8];
@@ -80,11 +92,9 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int j = lane * 8 + e;
-      const float x = j < L ? log_alpha[((size_t)b * N + sPath[j]) * Hv + h] : 0.f;
-      run = df_add(run, df{x, 0.f});
+      run = df_add(run, df{j < L ? sLa[j] : 0.f, 0.f});
       loc[e] = run;
     }
-    // exclusive scan of the lane totals
     df pre = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -97,29 +107,28 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     excl.hi = __shfl_up_sync(0xffffffffu, pre.hi, 1);
     excl.lo = __shfl_up_sync(0xffffffffu, pre.lo, 1);
     if (lane == 0) excl = df{0.f, 0.f};
+    df G[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) G[e] = df_add(excl, loc[e]);
+    // G_L lives in the lane that owns entry L-1
+    const int owner = L > 0 ? (L - 1) >> 3 : 0, slot = L > 0 ? (L - 1) & 7 : 0;
+    df mine = G[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e)
+      if (e == slot) mine = G[e];
+    df GL;
+    GL.hi = __shfl_sync(0xffffffffu, mine.hi, owner);
+    GL.lo = __shfl_sync(0xffffffffu, mine.lo, owner);
+    if (L == 0) GL = df{0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int j = lane * 8 + e;
-      if (j < L) sScan[j] = df_add(excl, loc[e]);
+      if (j < L) sW[j] = expf(df_diff(GL, G[e]));
     }
+    if (lane == 0) sGamma = expf(df_value(GL));
   }
-  __syncthreads();
-  if (L > 0) {
-    const df GL = sScan[L - 1];
-    for (int j = tid; j < L; j += kThreads) sW[j] = expf(df_diff(GL, sScan[j]));
-    if (tid == 0) sGamma = expf(df_value(GL));
-  } else if (tid == 0) {
-    sGamma = 1.f;
-  }
-  __syncthreads();
-  const float gamma = sGamma;
 
-  // ---- S1 = gamma S0 + K_P^T diag(w) U_P over this CTA's rows -------------
-  const int r4 = tid / 32;           // row group: rows r4*4 .. r4*4+3
-  const int c4 = tid % 32;           // column group: cols c4*4 .. c4*4+3
-  const int ncg = dv / 4;            // active column groups
-  const bool active = (r4 * 4 < rows) && (c4 < ncg);
-  const size_t sbase = ((size_t)b * Hv + h) * dk * dv;
+  // ---- S1 = gamma S0 + K_P^T diag(w) U_P over this CTA's rows ---------------------
   float acc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -128,43 +137,42 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 
   for (int j0 = 0; j0 < L; j0 += kChunk) {
     const int nj = min(kChunk, L - j0);
-    __syncthreads();
+    if (j0 > 0) __syncthreads();
     for (int e = tid; e < nj * rows; e += kThreads) {
       const int jj = e / rows, r = e % rows;
       sK[jj][r] = to_f32(k[(((size_t)b * N + sPath[j0 + jj]) * Hqk + hq) * dk + row0 + r]);
     }
     for (int e = tid; e < nj * (dv / 4); e += kThreads) {
       const int jj = e / (dv / 4), c = (e % (dv / 4)) * 4;
-      const float w = sW[j0 + jj];
-      float4 u = *reinterpret_cast<const float4*>(
+      *reinterpret_cast<float4*>(&sU[jj][c]) = *reinterpret_cast<const float4*>(
           U + (((size_t)b * Hv + h) * N + sPath[j0 + jj]) * dv + c);
-      u.x *= w; u.y *= w; u.z *= w; u.w *= w;
-      *reinterpret_cast<float4*>(&sWU[jj][c]) = u;
     }
     __syncthreads();
     if (active) {
       for (int jj = 0; jj < nj; ++jj) {
+        const float w = sW[j0 + jj];
         const float4 kr = *reinterpret_cast<const float4*>(&sK[jj][r4 * 4]);
-        const float4 wu = *reinterpret_cast<const float4*>(&sWU[jj][c4 * 4]);
-        const float kk[4] = {kr.x, kr.y, kr.z, kr.w};
-        const float uu[4] = {wu.x, wu.y, wu.z, wu.w};
+        const float4 uu = *reinterpret_cast<const float4*>(&sU[jj][c4 * 4]);
+        const float kk[4] = {w * kr.x, w * kr.y, w * kr.z, w * kr.w};
+        const float ul[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(kk[i], uu[j], acc[i][j]);
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(kk[i], ul[j], acc[i][j]);
       }
     }
   }
+  __syncthreads();  // sGamma (L == 0 skips the chunk loop)
+  const float gamma = sGamma;
   if (active) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const size_t off = sbase + (size_t)(row0 + r4 * 4 + i) * dv + c4 * 4;
-      const float4 s0 = *reinterpret_cast<const float4*>(S0 + off);
       float4 s1;
-      s1.x = fmaf(gamma, s0.x, acc[i][0]);
-      s1.y = fmaf(gamma, s0.y, acc[i][1]);
-      s1.z = fmaf(gamma, s0.z, acc[i][2]);
-      s1.w = fmaf(gamma, s0.w, acc[i][3]);
+      s1.x = fmaf(gamma, s0v[i].x, acc[i][0]);
+      s1.y = fmaf(gamma, s0v[i].y, acc[i][1]);
+      s1.z = fmaf(gamma, s0v[i].z, acc[i][2]);
+      s1.w = fmaf(gamma, s0v[i].w, acc[i][3]);
       *reinterpret_cast<float4*>(S1 + off) = s1;
     }
   }

@@ -74,18 +74,20 @@ constexpr uint32_t OFF_K = 0;                 // K, Q, S0^T: live until the K S0
 constexpr uint32_t OFF_Q = 1 * kOpBytes;
 constexpr uint32_t OFF_S0H = 2 * kOpBytes;
 constexpr uint32_t OFF_S0L = 3 * kOpBytes;
-constexpr uint32_t OFF_X = 0;                 // X (packed lower triangle, fp32): the solve
-constexpr uint32_t OFF_YH = 0;                // Y and U^T operands of Y U
+constexpr uint32_t OFF_YH = 0;                // then Y (hi, lo) over K, Q ...
 constexpr uint32_t OFF_YL = 1 * kOpBytes;
-constexpr uint32_t OFF_UTH = 2 * kOpBytes;
+constexpr uint32_t OFF_X = 2 * kOpBytes;      // ... X (packed lower triangle, fp32) over S0^T
+constexpr uint32_t OFF_UTH = 2 * kOpBytes;    // ... and, after the solve, U^T (hi, lo) over X
 constexpr uint32_t OFF_UTL = 3 * kOpBytes;
 constexpr uint32_t OFF_U = 4 * kOpBytes;      // raw S0 (TMA), then R / U, fp32, 64 KB
-constexpr uint32_t OFF_SMALL = OFF_U + kTile * kD * 4;
-constexpr uint32_t kSmallBytes = 10240;
+constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth] -> ancestor
+constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
+constexpr uint32_t kSmallBytes = 8192;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
-static_assert(kTile * (kTile - 1) / 2 * 4 <= OFF_UTH, "X must not reach U^T");
-static_assert(OFF_U % 1024 == 0, "alignment");
+static_assert(kTile * (kTile - 1) / 2 * 4 <= 2 * kOpBytes, "X must fit in the S0^T region");
+static_assert(OFF_U % 1024 == 0 && OFF_SMALL % 16 == 0, "alignment");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Small {
   int parent[kTile];
@@ -98,7 +100,6 @@ struct Small {
   int depth[kTile];
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
-  uint32_t level_bits[(kTile + 2) * kW];
   uint64_t bar_kq, bar_s0, bar_g, bar_ks, bar_yu;
   uint32_t tmem_base;
   int max_depth;
@@ -121,13 +122,18 @@ __device__ __forceinline__ int u_index(int t, int c4) { return t * kD + ((c4 ^ (
 // packed strictly-lower triangle of X
 __device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
 
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-  hi = __float2bfloat16_rn(x);
-  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+// (a, b) -> bf16x2 hi parts and bf16x2 lo parts (x = hi + lo to ~2^-17)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
-  return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+__device__ __forceinline__ uint32_t pack2f(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // issue the 8 K-steps (K = 128) of D (+)= A B^T for two 128x128 K-major tiles
@@ -165,6 +171,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   Small& S = *reinterpret_cast<Small*>(smem + OFF_SMALL);
   float* sU = reinterpret_cast<float*>(smem + OFF_U);
   float* sX = reinterpret_cast<float*>(smem + OFF_X);
+  uint8_t* sPath = smem + OFF_PATH;
 
   const int N = d.N, Hv = d.Hv, Hqk = d.Hqk;
   const int h = blockIdx.x, b = blockIdx.y;
@@ -176,9 +183,27 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int t = q4 * 32 + lane;
   const bool live = t < N;
 
-  // ---- 0. tree loads first (their latency hides the set-up), then TMEM,
-  //         barriers and every bulk load ------------------------------------------
+  // ---- 0. barriers and every bulk load first; tree loads and v meanwhile ------------
   TC_MARK(0);
+  if (tid == 0) {
+    mbar_init(&S.bar_kq, 1);
+    mbar_init(&S.bar_s0, 1);
+    mbar_init(&S.bar_g, 1);
+    mbar_init(&S.bar_ks, 1);
+    mbar_init(&S.bar_yu, 1);
+    S.err = 0;
+    S.issued = 0;
+    S.max_depth = 0;
+    mbar_fence_init();
+    mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
+    tma_load_4d(smem + OFF_K, &tmK, &S.bar_kq, 0, hq, 0, b);
+    tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_kq, 64, hq, 0, b);
+    tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
+    tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
+    mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
+    tma_load_3d(smem + OFF_U, &tmS, &S.bar_s0, 0, 0, b * Hv + h);
+  }
+  if (warp == 1) tmem_alloc(&S.tmem_base, kTmemCols);
   int p_in = -1;
   float be_in = 0.f, la_in = 0.f;
   if (tid < N) {
@@ -190,33 +215,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint4 vreg[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                    make_uint4(0, 0, 0, 0)};
   if (live) {
-    const uint4* vrow = reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
+    const uint4* vrow =
+        reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
-  }
-  if (warp == 0) {
-    tmem_alloc(&S.tmem_base, kTmemCols);
-    if (lane == 0) {
-      mbar_init(&S.bar_kq, 1);
-      mbar_init(&S.bar_s0, 1);
-      mbar_init(&S.bar_g, 1);
-      mbar_init(&S.bar_ks, 1);
-      mbar_init(&S.bar_yu, 1);
-      S.err = 0;
-      S.issued = 0;
-      S.max_depth = 0;
-      mbar_fence_init();
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmS);
-      mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
-      tma_load_4d(smem + OFF_K, &tmK, &S.bar_kq, 0, hq, 0, b);
-      tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_kq, 64, hq, 0, b);
-      tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
-      tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
-      mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
-      tma_load_3d(smem + OFF_U, &tmS, &S.bar_s0, 0, 0, b * Hv + h);
-    }
   }
 
   // ---- 1. tree: validate ------------------------------------------------------------
@@ -228,11 +230,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     S.la[tid] = la_in;
     bad = tid < N && (p_in < -1 || p_in >= tid);
   }
-  if (tid < kTile + 2) {
-    S.level_start[tid] = 0;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) S.level_bits[tid * kW + w] = 0u;
-  }
+  if (tid < kTile + 2) S.level_start[tid] = 0;
   tc_fence_before_sync();
   bad = __syncthreads_or(bad);
   tc_fence_after_sync();
@@ -247,7 +245,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     goto release;
   }
 
-  // ---- 2. warps 0-3: ancestor bitsets, path log-decays, depth levels;
+  // ---- 2. warps 0-3: ancestor bitsets, path log-decays, depth order, path table;
   //         warp 4 lane 0: Gram MMAs once K and Q have landed;
   //         warps 4-15: S0^T = hi + lo (bf16, K-major, 128-byte swizzle) --------------
   TC_MARK(2);
@@ -261,8 +259,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       dep += 1;
       S.depth[tid] = dep;
       atomicAdd(&S.level_start[dep], 1);
-      atomicOr(&S.level_bits[dep * kW + (tid >> 5)], 1u << (tid & 31));
       atomicMax(&S.max_depth, dep);
+      // path table: sPath[t * 128 + depth(s)] = s for every s on t's path
+      int s = tid, ds = dep;
+      while (s >= 0) {
+        sPath[tid * kTile + ds] = (uint8_t)s;
+        s = S.parent[s];
+        --ds;
+      }
     }
     TreeSync()();
     if (warp == 0) {
@@ -309,15 +313,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const float* raw = sU;  // S0 [dk][dv], row-major, landed by TMA
     for (int item = tid - 128; item < kD * 16; item += kThreads - 128) {
       const int n = item & (kD - 1), k8 = item >> 7;
+      const float* col = raw + (k8 * 8) * kD + n;
       uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        split_bf16(raw[(k8 * 8 + 2 * i) * kD + n], h0, l0);
-        split_bf16(raw[(k8 * 8 + 2 * i + 1) * kD + n], h1, l1);
-        hi[i] = pack2(h0, h1);
-        lo[i] = pack2(l0, l1);
-      }
+      for (int i = 0; i < 4; ++i) split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi[i], lo[i]);
       const uint32_t off = sw128_chunk(n, k8);
       *reinterpret_cast<uint4*>(smem + OFF_S0H + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(smem + OFF_S0L + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -325,10 +324,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     fence_proxy_async_smem();
   }
   TC_MARK(3);
-  TC_MARK(4);
   if (__syncthreads_or(S.err)) goto fail;
 
-  // ---- 5. K S0 (hi + lo) and Q S0 (hi) -----------------------------------------------
+  // ---- 3. K S0 (hi + lo) and Q S0 (hi) -----------------------------------------------
   if (tid == kIssuer) {
     tc_fence_after_sync();
     umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
@@ -346,8 +344,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const float gam = __expf(df_value(gt));
     const uint32_t abits = live ? S.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
 
-    // ---- 6. X row segment (registers) while K S0 / Q S0 run ------------------------
-    TC_MARK(5);
+    // ---- 4. X row segment (registers) while K S0 / Q S0 run ------------------------
+    TC_MARK(4);
     if (!mbar_wait(&S.bar_g, 0, kWaitLimitNs)) S.err = 2;
     tc_fence_after_sync();
     float xr[32];
@@ -356,10 +354,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     for (int j = 0; j < 32; ++j)
       xr[j] = ((abits >> j) & 1u) ? bt * __expf(df_diff(gt, S.g[col0 + j])) * xr[j] : 0.f;
 
-    // ---- 7. R = beta (V - gamma K S0); X and R to shared memory -------------------
+    // ---- 5. once K S0 / Q S0 are done (K, Q, S0^T dead): X, R = beta (V - gamma K S0)
+    //         and Y (hi, lo) to shared memory -------------------------------------------
     if (!mbar_wait(&S.bar_ks, 0, kWaitLimitNs)) S.err = 2;
     tc_fence_after_sync();
-    if (__syncthreads_or(S.err)) goto fail;  // K, Q, S0^T are dead from here on
+    if (__syncthreads_or(S.err)) goto fail;
+    TC_MARK(5);
     {
       float ks[32];
       tmem_ld_32cols(trow + kColKS + col0, ks);
@@ -383,80 +383,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    tc_fence_before_sync();
-    __syncthreads();
-
-    // ---- 8. forward substitution, right-looking over depth levels -------------------
-    // once every node of depth <= l is final, each deeper node t subtracts the
-    // term of its unique ancestor a at depth l: u_t -= X[t,a] u_a.  Warp w owns
-    // the nodes at positions w, w + 16, ... of the depth order and keeps their
-    // partial sums in registers (lane = 4 value columns); a node is written to
-    // shared memory (and to U) the moment it is final.
-    TC_MARK(6);
-    {
-      constexpr int kSlots = kTile / kWarps;
-      int tn[kSlots], dp[kSlots];
-      float4 acc[kSlots];
-      float* Ubh = U + ((size_t)b * Hv + h) * N * kD;
-#pragma unroll
-      for (int k = 0; k < kSlots; ++k) {
-        const int i = warp + k * kWarps;
-        tn[k] = i < N ? S.order[i] : 0;
-        dp[k] = i < N ? S.depth[tn[k]] : 0;
-        acc[k] = *reinterpret_cast<const float4*>(sU + u_index(tn[k], lane));
-        if (dp[k] == 1) *reinterpret_cast<float4*>(Ubh + (size_t)tn[k] * kD + lane * 4) = acc[k];
-      }
-      const int max_depth = S.max_depth;
-      for (int lvl = 1; lvl < max_depth; ++lvl) {
-        const uint32_t lb0 = S.level_bits[lvl * kW + 0], lb1 = S.level_bits[lvl * kW + 1];
-        const uint32_t lb2 = S.level_bits[lvl * kW + 2], lb3 = S.level_bits[lvl * kW + 3];
-#pragma unroll
-        for (int k = 0; k < kSlots; ++k) {
-          if (dp[k] > lvl) {
-            const int tk = tn[k];
-            const uint32_t m0 = S.anc[tk * kW + 0] & lb0, m1 = S.anc[tk * kW + 1] & lb1;
-            const uint32_t m2 = S.anc[tk * kW + 2] & lb2, m3 = S.anc[tk * kW + 3] & lb3;
-            const int a = m0 ? __ffs(m0) - 1
-                             : m1 ? 31 + __ffs(m1) : m2 ? 63 + __ffs(m2) : 95 + __ffs(m3);
-            const float x = sX[x_index(tk, a)];
-            const float4 ua = *reinterpret_cast<const float4*>(sU + u_index(a, lane));
-            acc[k].x = fmaf(-x, ua.x, acc[k].x);
-            acc[k].y = fmaf(-x, ua.y, acc[k].y);
-            acc[k].z = fmaf(-x, ua.z, acc[k].z);
-            acc[k].w = fmaf(-x, ua.w, acc[k].w);
-            if (dp[k] == lvl + 1) {
-              *reinterpret_cast<float4*>(sU + u_index(tk, lane)) = acc[k];
-              *reinterpret_cast<float4*>(Ubh + (size_t)tk * kD + lane * 4) = acc[k];
-            }
-          }
-        }
-        __syncthreads();
-      }
-    }
-
-    // ---- 9. U out; U^T and Y to shared memory as bf16 hi + lo ----------------------
-    TC_MARK(7);
-#pragma unroll
-    for (int r = 0; r < (kD * 16) / kThreads; ++r) {
-      const int item = tid + r * kThreads;
-      const int n = item & (kD - 1), t8 = item >> 7;
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float x0 = 0.f, x1 = 0.f;
-        const int ta = t8 * 8 + 2 * i, tb = ta + 1;
-        if (ta < N) x0 = sU[u_index(ta, n >> 2) + (n & 3)];
-        if (tb < N) x1 = sU[u_index(tb, n >> 2) + (n & 3)];
-        __nv_bfloat16 h0, l0, h1, l1;
-        split_bf16(x0, h0, l0);
-        split_bf16(x1, h1, l1);
-        hi[i] = pack2(h0, h1);
-        lo[i] = pack2(l0, l1);
-      }
-      const uint32_t off = sw128_chunk(n, t8);
-      *reinterpret_cast<uint4*>(smem + OFF_UTH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + OFF_UTL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
     {
       float gq[32];
       tmem_ld_32cols(trow + kColGqk + col0, gq);
@@ -473,22 +399,95 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const bool on_path = live && (((abits >> j) & 1u) || s == t);
             y[e] = on_path ? (s == t ? gq[j] : __expf(df_diff(gt, S.g[s])) * gq[j]) : 0.f;
           }
-          __nv_bfloat16 h0, l0, h1, l1;
-          split_bf16(y[0], h0, l0);
-          split_bf16(y[1], h1, l1);
-          hi[i] = pack2(h0, h1);
-          lo[i] = pack2(l0, l1);
+          split2(y[0], y[1], hi[i], lo[i]);
         }
         const uint32_t off = sw128_chunk(t, cq * 4 + g8);
         *reinterpret_cast<uint4*>(smem + OFF_YH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(smem + OFF_YL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
+    tc_fence_before_sync();
+    __syncthreads();
+
+    // ---- 6. forward substitution, level by level ---------------------------------------
+    // nodes of one depth are independent: a warp takes a node t and subtracts
+    // X[t,a] u_a for all its ancestors a (listed root-first in the path table),
+    // four at a time so that their loads overlap; lane = 4 value columns.
+    TC_MARK(6);
+    {
+      float* Ubh = U + ((size_t)b * Hv + h) * N * kD;
+      for (int i = S.level_start[1] + warp; i < S.level_start[2]; i += kWarps) {
+        const int tn = S.order[i];  // roots: u = r
+        *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) =
+            *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
+      }
+      const int max_depth = S.max_depth;
+      for (int lvl = 2; lvl <= max_depth; ++lvl) {
+        const int end = S.level_start[lvl + 1];
+        for (int i = S.level_start[lvl] + warp; i < end; i += kWarps) {
+          const int tn = S.order[i];
+          const uint8_t* pth = sPath + tn * kTile;
+          const float* xrow = sX + x_index(tn, 0);
+          float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
+          int j = 1;
+          for (; j + 4 <= lvl; j += 4) {
+            int aa[4];
+            float xx[4];
+            float4 uu[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) aa[e] = pth[j + e];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              xx[e] = xrow[aa[e]];
+              uu[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], lane));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc.x = fmaf(-xx[e], uu[e].x, acc.x);
+              acc.y = fmaf(-xx[e], uu[e].y, acc.y);
+              acc.z = fmaf(-xx[e], uu[e].z, acc.z);
+              acc.w = fmaf(-xx[e], uu[e].w, acc.w);
+            }
+          }
+          for (; j < lvl; ++j) {
+            const int a1 = pth[j];
+            const float x1 = xrow[a1];
+            const float4 u1 = *reinterpret_cast<const float4*>(sU + u_index(a1, lane));
+            acc.x = fmaf(-x1, u1.x, acc.x);
+            acc.y = fmaf(-x1, u1.y, acc.y);
+            acc.z = fmaf(-x1, u1.z, acc.z);
+            acc.w = fmaf(-x1, u1.w, acc.w);
+          }
+          *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
+          *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
+        }
+        __syncthreads();
+      }
+    }
+
+    // ---- 7. U^T (hi, lo) over X ----------------------------------------------------------
+    TC_MARK(7);
+#pragma unroll
+    for (int r = 0; r < (kD * 16) / kThreads; ++r) {
+      const int item = tid + r * kThreads;
+      const int n = item & (kD - 1), t8 = item >> 7;
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ta = t8 * 8 + 2 * i, tb = ta + 1;
+        const float x0 = ta < N ? sU[u_index(ta, n >> 2) + (n & 3)] : 0.f;
+        const float x1 = tb < N ? sU[u_index(tb, n >> 2) + (n & 3)] : 0.f;
+        split2(x0, x1, hi[i], lo[i]);
+      }
+      const uint32_t off = sw128_chunk(n, t8);
+      *reinterpret_cast<uint4*>(smem + OFF_UTH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + OFF_UTL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
 
-    // ---- 10. Y U on the tensor cores (three bf16 passes) -------------------------------
+    // ---- 8. Y U on the tensor cores (three bf16 passes) -------------------------------
     TC_MARK(8);
     if (tid == kIssuer) {
       tc_fence_after_sync();
@@ -502,7 +501,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc_fence_after_sync();
     if (__syncthreads_or(S.err)) goto fail;
 
-    // ---- 11. O = gamma QS + Y U --------------------------------------------------------
+    // ---- 9. O = gamma QS + Y U ----------------------------------------------------------
     TC_MARK(9);
     {
       float yu[32], qs[32];
@@ -516,8 +515,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = q * 8 + 2 * e;
-            w4[e] = pack2(__float2bfloat16_rn(fmaf(gam, qs[j], yu[j])),
-                          __float2bfloat16_rn(fmaf(gam, qs[j + 1], yu[j + 1])));
+            w4[e] = pack2f(fmaf(gam, qs[j], yu[j]), fmaf(gam, qs[j + 1], yu[j + 1]));
           }
           orow[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
@@ -542,7 +540,7 @@ fail:
 release:
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---- host side -------------------------------------------------------------------
