@@ -9,59 +9,63 @@
 //     w_j = exp(G_L - G_j),  gamma_L = exp(G_L),  G_j = sum_{i<=j} log alpha_{p_i},
 // a rank-L update of S0 that streams S0 in and S1 out once (HBM-bound).
 //
-// Grid: (Hv, B, dk / kRows).  Each CTA owns kRows rows of one (b, h) state and
-// all dv columns; thread (r, c4) keeps a 4x4 register tile: rows r*4..r*4+3,
-// columns c4*4..c4*4+3.  Its S0 tile is loaded first, so that the state stream
-// overlaps the path-dependent loads; those come in one round (path and its
-// length together, then parent links, log alpha, k rows and U rows), and the
-// path's k rows (restricted to the CTA's rows) and U rows are staged through
-// shared memory in chunks of kChunk path entries.
+// Grid: (Hv, B), 512 threads.  Each CTA owns one (b, h) state.  The state is
+// bulk-copied into shared memory the moment the CTA starts, so the state
+// stream overlaps the path-dependent gathers, which take two rounds: the path
+// and its length together, then (with indices range-checked) the parent-link
+// check, log alpha and the k and U rows of the path all at once.  Thread
+// (r8, c4) keeps an 8x4 register tile (rows r8*8.., columns c4*4..); k and U
+// rows are staged through shared memory in chunks of kChunk path entries.
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRows = 32;    // state rows per CTA
+constexpr int kThreads = 512;
 constexpr int kChunk = 32;   // path entries staged per round
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on the S0 copy wait
+
+// dynamic shared memory: S0 (dk x dv fp32) | k rows [kChunk][dk] | u rows [kChunk][dv]
+constexpr size_t kSmemBytes = (size_t)(kMaxD * kMaxD + 2 * kChunk * kMaxD) * sizeof(float);
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path_len,
               const int32_t* __restrict__ parent, const float* __restrict__ U,
               const T* __restrict__ k, const float* __restrict__ log_alpha,
               const float* S0, float* S1, gdn_tree_dims d, int32_t Lmax,
               int32_t* dev_status) {
-  // S0 and S1 may alias (in-place commit): every element is read and then
-  // written by the same thread, so they are not __restrict__.
+  // S0 and S1 may alias (in-place commit): the whole state is copied into
+  // shared memory before any element of S1 is written.
+  extern __shared__ __align__(128) float smem_f[];
+  float* sS0 = smem_f;                            // [dk][dv]
+  float* sK = sS0 + kMaxD * kMaxD;                // [kChunk][dk]
+  float* sU = sK + kChunk * kMaxD;                // [kChunk][dv]
   __shared__ int sPath[kMaxN];
-  __shared__ float sLa[kMaxN];         // log alpha along the path
-  __shared__ float sW[kMaxN];          // w_j
-  __shared__ __align__(16) float sK[kChunk][kRows];     // k_{p_j}[row0 + r]
-  __shared__ __align__(16) float sU[kChunk][kMaxD];     // u_{p_j}
+  __shared__ float sLa[kMaxN];                    // log alpha along the path
+  __shared__ float sW[kMaxN];                     // w_j
+  __shared__ uint64_t sBar;
   __shared__ float sGamma;
 
   const int N = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
-  const int h = blockIdx.x, b = blockIdx.y, row0 = blockIdx.z * kRows;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int hq = h / (Hv / Hqk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rows = min(kRows, dk - row0);
-
-  // ---- S0 tile prefetch: thread (r4, c4) owns rows r4*4.., columns c4*4.. ----
-  const int r4 = tid / 32, c4 = tid % 32;
-  const bool active = (r4 * 4 < rows) && (c4 < dv / 4);
   const size_t sbase = ((size_t)b * Hv + h) * dk * dv;
-  float4 s0v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    s0v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active)
-      s0v[i] = *reinterpret_cast<const float4*>(S0 + sbase + (size_t)(row0 + r4 * 4 + i) * dv + c4 * 4);
+
+  // ---- the whole (b, h) state starts streaming into shared memory at once ----
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)(dk * dv * sizeof(float));
+    sm100::mbar_init(&sBar, 1);
+    sm100::mbar_fence_init();
+    sm100::mbar_arrive_expect_tx(&sBar, bytes);
+    sm100::bulk_load(sS0, S0 + sbase, bytes, &sBar);
   }
 
-  // ---- path length and entries, loaded together ------------------------------
+  // ---- round 1: path length and entries (range-checked) ----------------------
   const int L = path_len[b];
   int pj = -1;
   if (tid < Lmax) pj = path[(size_t)b * Lmax + tid];
@@ -71,6 +75,9 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     sPath[tid] = pj;
   }
   bad = __syncthreads_or(bad);
+
+  // ---- round 2: chain check, log alpha, and the first chunk of k / u rows,
+  //      all issued together (indices are in range from here on) ----------------
   if (!bad && tid < L) {
     // a root-to-node path is strictly increasing in a topological order; with
     // the tree given it must also follow the parent links
@@ -79,10 +86,27 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     if (parent) bad |= (parent[(size_t)b * N + pj] != prev);
     sLa[tid] = log_alpha[((size_t)b * N + pj) * Hv + h];
   }
+  auto stage = [&](int j0, int nj) {
+    for (int e = tid; e < nj * (dk / 4); e += kThreads) {
+      const int jj = e / (dk / 4), c = (e % (dk / 4)) * 4;
+      const T* kr = k + (((size_t)b * N + sPath[j0 + jj]) * Hqk + hq) * dk + c;
+      *reinterpret_cast<float4*>(sK + jj * dk + c) =
+          make_float4(to_f32(kr[0]), to_f32(kr[1]), to_f32(kr[2]), to_f32(kr[3]));
+    }
+    for (int e = tid; e < nj * (dv / 4); e += kThreads) {
+      const int jj = e / (dv / 4), c = (e % (dv / 4)) * 4;
+      *reinterpret_cast<float4*>(sU + jj * dv + c) = *reinterpret_cast<const float4*>(
+          U + (((size_t)b * Hv + h) * N + sPath[j0 + jj]) * dv + c);
+    }
+  };
+  if (!bad) stage(0, min(kChunk, L));
   bad = __syncthreads_or(bad);
-  if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
+  if (h == 0 && tid == 0 && dev_status)
     dev_status[b] = bad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
-  if (bad) return;
+  if (bad) {
+    if (tid == 0) sm100::mbar_wait(&sBar, 0, kWaitLimitNs);  // drain the copy
+    return;
+  }
 
   // ---- G_j: inclusive double-float prefix sums of log alpha along the path ------
   if (warp == 0) {
@@ -127,53 +151,57 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     }
     if (lane == 0) sGamma = expf(df_value(GL));
   }
+  __syncthreads();
 
-  // ---- S1 = gamma S0 + K_P^T diag(w) U_P over this CTA's rows ---------------------
-  float acc[4][4];
+  // ---- S1 = gamma S0 + K_P^T diag(w) U_P ------------------------------------------
+  // thread (r8, c4): rows r8*8 .. r8*8+7, columns c4*4 .. c4*4+3
+  const int r8 = tid / 32, c4 = tid % 32;
+  const bool active = (r8 * 8 < dk) && (c4 * 4 < dv);
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
   for (int j0 = 0; j0 < L; j0 += kChunk) {
     const int nj = min(kChunk, L - j0);
-    if (j0 > 0) __syncthreads();
-    for (int e = tid; e < nj * rows; e += kThreads) {
-      const int jj = e / rows, r = e % rows;
-      sK[jj][r] = to_f32(k[(((size_t)b * N + sPath[j0 + jj]) * Hqk + hq) * dk + row0 + r]);
+    if (j0 > 0) {
+      __syncthreads();
+      stage(j0, nj);
+      __syncthreads();
     }
-    for (int e = tid; e < nj * (dv / 4); e += kThreads) {
-      const int jj = e / (dv / 4), c = (e % (dv / 4)) * 4;
-      *reinterpret_cast<float4*>(&sU[jj][c]) = *reinterpret_cast<const float4*>(
-          U + (((size_t)b * Hv + h) * N + sPath[j0 + jj]) * dv + c);
-    }
-    __syncthreads();
     if (active) {
       for (int jj = 0; jj < nj; ++jj) {
         const float w = sW[j0 + jj];
-        const float4 kr = *reinterpret_cast<const float4*>(&sK[jj][r4 * 4]);
-        const float4 uu = *reinterpret_cast<const float4*>(&sU[jj][c4 * 4]);
-        const float kk[4] = {w * kr.x, w * kr.y, w * kr.z, w * kr.w};
+        const float4 k0 = *reinterpret_cast<const float4*>(sK + jj * dk + r8 * 8);
+        const float4 k1 = *reinterpret_cast<const float4*>(sK + jj * dk + r8 * 8 + 4);
+        const float4 uu = *reinterpret_cast<const float4*>(sU + jj * dv + c4 * 4);
+        const float kk[8] = {w * k0.x, w * k0.y, w * k0.z, w * k0.w,
+                             w * k1.x, w * k1.y, w * k1.z, w * k1.w};
         const float ul[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(kk[i], ul[j], acc[i][j]);
       }
     }
   }
-  __syncthreads();  // sGamma (L == 0 skips the chunk loop)
   const float gamma = sGamma;
+  const bool landed = sm100::mbar_wait(&sBar, 0, kWaitLimitNs);
+  if (!landed) {
+    if (tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
+    return;  // S1 left unwritten
+  }
   if (active) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const size_t off = sbase + (size_t)(row0 + r4 * 4 + i) * dv + c4 * 4;
+    for (int i = 0; i < 8; ++i) {
+      const int row = r8 * 8 + i;
+      const float4 s0 = *reinterpret_cast<const float4*>(sS0 + row * dv + c4 * 4);
       float4 s1;
-      s1.x = fmaf(gamma, s0v[i].x, acc[i][0]);
-      s1.y = fmaf(gamma, s0v[i].y, acc[i][1]);
-      s1.z = fmaf(gamma, s0v[i].z, acc[i][2]);
-      s1.w = fmaf(gamma, s0v[i].w, acc[i][3]);
-      *reinterpret_cast<float4*>(S1 + off) = s1;
+      s1.x = fmaf(gamma, s0.x, acc[i][0]);
+      s1.y = fmaf(gamma, s0.y, acc[i][1]);
+      s1.z = fmaf(gamma, s0.z, acc[i][2]);
+      s1.w = fmaf(gamma, s0.w, acc[i][3]);
+      *reinterpret_cast<float4*>(S1 + sbase + (size_t)row * dv + c4 * 4) = s1;
     }
   }
 }
@@ -181,13 +209,20 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 }  // namespace
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
-  const dim3 grid(a.d.Hv, a.d.B, (a.d.dk + kRows - 1) / kRows);
+  const dim3 grid(a.d.Hv, a.d.B);
+  cudaError_t err;
   if (a.d.dtype == GDN_TREE_BF16) {
-    commit_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+    err = cudaFuncSetAttribute(commit_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    commit_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const __nv_bfloat16*>(a.k),
         a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status);
   } else {
-    commit_kernel<float><<<grid, kThreads, 0, stream>>>(
+    err = cudaFuncSetAttribute(commit_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemBytes);
+    if (err != cudaSuccess) return err;
+    commit_kernel<float><<<grid, kThreads, kSmemBytes, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const float*>(a.k),
         a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status);
   }

@@ -52,6 +52,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384, kColYU = 0;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kIssuer = 128;  // the one thread that issues every MMA (warp 4, lane 0)
+constexpr uint32_t kSpinLimit = 1u << 24;  // bounded wait on a solve ready flag
 
 #ifdef GDN_TC_PROFILE
 // per-CTA phase timestamps for a profiling build (never in the product build)
@@ -100,6 +101,7 @@ struct Small {
   int depth[kTile];
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
+  int ready[kTile];  // solve: node's u is final
   uint64_t bar_kq, bar_s0, bar_g, bar_ks, bar_yu;
   uint32_t tmem_base;
   int max_depth;
@@ -363,6 +365,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     {
       float ks[32];
       tmem_ld_32cols(trow + kColKS + col0, ks);
+      if (cq == 0) S.ready[t] = 0;
       if (live) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -409,28 +412,37 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc_fence_before_sync();
     __syncthreads();
 
-    // ---- 6. forward substitution, level by level ---------------------------------------
-    // nodes of one depth are independent: a warp takes a node t and subtracts
-    // X[t,a] u_a for all its ancestors a (listed root-first in the path table),
-    // four at a time so that their loads overlap; lane = 4 value columns.
+    // ---- 6. forward substitution as a dataflow over the tree ------------------------
+    // u_t = r_t - sum over ancestors a of X[t,a] u_a.  Warp w takes the nodes at
+    // positions w, w + 16, ... of the depth order; for node t it waits for the
+    // ready flag of t's parent only (every other ancestor was final before the
+    // parent was), then sums all ancestor terms, four at a time so that their
+    // loads overlap (lane = 4 value columns), publishes u_t and raises t's
+    // flag.  No cycle of waits can form: the unfinished node of lowest depth
+    // order never waits (its parent comes earlier in that order).
     TC_MARK(6);
     {
+      volatile int* ready = S.ready;
       float* Ubh = U + ((size_t)b * Hv + h) * N * kD;
-      for (int i = S.level_start[1] + warp; i < S.level_start[2]; i += kWarps) {
-        const int tn = S.order[i];  // roots: u = r
-        *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) =
-            *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
-      }
-      const int max_depth = S.max_depth;
-      for (int lvl = 2; lvl <= max_depth; ++lvl) {
-        const int end = S.level_start[lvl + 1];
-        for (int i = S.level_start[lvl] + warp; i < end; i += kWarps) {
-          const int tn = S.order[i];
-          const uint8_t* pth = sPath + tn * kTile;
-          const float* xrow = sX + x_index(tn, 0);
-          float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
+      bool timed_out = false;
+      for (int i = warp; i < N; i += kWarps) {
+        const int tn = S.order[i];
+        const int dep = S.depth[tn];
+        const uint8_t* pth = sPath + tn * kTile;
+        const float* xrow = sX + x_index(tn, 0);
+        float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
+        if (dep > 1) {
+          const int par = pth[dep - 1];
+          uint32_t spins = 0;
+          while (ready[par] == 0) {
+            if (++spins > kSpinLimit) {
+              timed_out = true;
+              break;
+            }
+          }
+          __threadfence_block();
           int j = 1;
-          for (; j + 4 <= lvl; j += 4) {
+          for (; j + 4 <= dep; j += 4) {
             int aa[4];
             float xx[4];
             float4 uu[4];
@@ -449,7 +461,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               acc.w = fmaf(-xx[e], uu[e].w, acc.w);
             }
           }
-          for (; j < lvl; ++j) {
+          for (; j < dep; ++j) {
             const int a1 = pth[j];
             const float x1 = xrow[a1];
             const float4 u1 = *reinterpret_cast<const float4*>(sU + u_index(a1, lane));
@@ -459,11 +471,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             acc.w = fmaf(-x1, u1.w, acc.w);
           }
           *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
-          *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
+          __threadfence_block();
         }
-        __syncthreads();
+        __syncwarp();
+        if (lane == 0) ready[tn] = 1;
+        *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
       }
+      if (timed_out) S.err = 4;
     }
+    if (__syncthreads_or(S.err)) goto fail;
 
     // ---- 7. U^T (hi, lo) over X ----------------------------------------------------------
     TC_MARK(7);
