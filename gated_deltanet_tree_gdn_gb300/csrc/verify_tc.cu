@@ -106,6 +106,7 @@ struct Small {
   uint32_t tmem_base;
   int max_depth;
   int err;
+  int bad;  // the tree failed validation
   int issued;  // bit 0: Gram MMAs, bit 1: K S0 / Q S0 MMAs, bit 2: Y U MMAs
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
@@ -185,34 +186,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int t = q4 * 32 + lane;
   const bool live = t < N;
 
-  // ---- 0. barriers and every bulk load first; tree loads and v meanwhile ------------
+  // ---- 0. two groups run side by side until the tensor cores need both:
+  //   tree group (warps 0-3): tree loads, validation, one upward walk per node
+  //     (depth, path log-decay, ancestor bitset, path table), depth order;
+  //   operand group (warps 4-15): bulk loads, TMEM, Gram MMAs, S0^T split, and
+  //     the K S0 / Q S0 MMAs as soon as S0^T is in place.
   TC_MARK(0);
-  if (tid == 0) {
-    mbar_init(&S.bar_kq, 1);
-    mbar_init(&S.bar_s0, 1);
-    mbar_init(&S.bar_g, 1);
-    mbar_init(&S.bar_ks, 1);
-    mbar_init(&S.bar_yu, 1);
-    S.err = 0;
-    S.issued = 0;
-    S.max_depth = 0;
-    mbar_fence_init();
-    mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
-    tma_load_4d(smem + OFF_K, &tmK, &S.bar_kq, 0, hq, 0, b);
-    tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_kq, 64, hq, 0, b);
-    tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
-    tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
-    mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
-    tma_load_3d(smem + OFF_U, &tmS, &S.bar_s0, 0, 0, b * Hv + h);
-  }
-  if (warp == 1) tmem_alloc(&S.tmem_base, kTmemCols);
-  int p_in = -1;
-  float be_in = 0.f, la_in = 0.f;
-  if (tid < N) {
-    p_in = parent[(size_t)b * N + tid];
-    be_in = beta[((size_t)b * N + tid) * Hv + h];
-    la_in = log_alpha[((size_t)b * N + tid) * Hv + h];
-  }
   // this thread's 32 values of v (row t, columns 32 cq ..), kept in registers
   uint4 vreg[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                    make_uint4(0, 0, 0, 0)};
@@ -222,91 +201,121 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
     for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
   }
-
-  // ---- 1. tree: validate ------------------------------------------------------------
-  TC_MARK(1);
-  int bad = 0;
-  if (tid < kTile) {
+  if (warp < 4) {
+    using TreeSync = NamedSync<1, 128>;
+    int p_in = -1;
+    float be_in = 0.f, la_in = 0.f;
+    if (tid < N) {
+      p_in = parent[(size_t)b * N + tid];
+      be_in = beta[((size_t)b * N + tid) * Hv + h];
+      la_in = log_alpha[((size_t)b * N + tid) * Hv + h];
+    }
     S.parent[tid] = p_in;
     S.beta[tid] = be_in;
     S.la[tid] = la_in;
-    bad = tid < N && (p_in < -1 || p_in >= tid);
-  }
-  if (tid < kTile + 2) S.level_start[tid] = 0;
-  tc_fence_before_sync();
-  bad = __syncthreads_or(bad);
-  tc_fence_after_sync();
-  const uint32_t tmem = S.tmem_base;
-  if (h == 0 && tid == 0 && dev_status)
-    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
-  if (bad) {
-    if (tid == 0) {  // let the bulk loads land before the CTA exits
-      mbar_wait(&S.bar_kq, 0, kWaitLimitNs);
-      mbar_wait(&S.bar_s0, 0, kWaitLimitNs);
-    }
-    goto release;
-  }
-
-  // ---- 2. warps 0-3: ancestor bitsets, path log-decays, depth order, path table;
-  //         warp 4 lane 0: Gram MMAs once K and Q have landed;
-  //         warps 4-15: S0^T = hi + lo (bf16, K-major, 128-byte swizzle) --------------
-  TC_MARK(2);
-  if (warp < 4) {
-    using TreeSync = NamedSync<1, 128>;
-    tree_prepare(S.parent, kTile, kW, S.la, S.jump, S.anc, S.g, TreeSync());
-    int dep = 0;
-    if (tid < N) {
-#pragma unroll
-      for (int w = 0; w < kW; ++w) dep += __popc(S.anc[tid * kW + w]);
-      dep += 1;
-      S.depth[tid] = dep;
-      atomicAdd(&S.level_start[dep], 1);
-      atomicMax(&S.max_depth, dep);
-      // path table: sPath[t * 128 + depth(s)] = s for every s on t's path
-      int s = tid, ds = dep;
-      while (s >= 0) {
-        sPath[tid * kTile + ds] = (uint8_t)s;
-        s = S.parent[s];
-        --ds;
-      }
-    }
-    TreeSync()();
-    if (warp == 0) {
-      // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
-      int cnt[5], run = 0;
-#pragma unroll
-      for (int e = 0; e < 5; ++e) {
-        const int l = lane * 5 + e;
-        cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
-        run += cnt[e];
-      }
-      int incl = run;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int up = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += up;
-      }
-      int excl = incl - run;
-#pragma unroll
-      for (int e = 0; e < 5; ++e) {
-        const int l = lane * 5 + e;
-        if (l < kTile + 2) {
-          S.level_start[l] = excl;
-          S.level_cursor[l] = excl;
+    S.level_start[tid] = 0;
+    if (tid < 2) S.level_start[kTile + tid] = 0;
+    if (tid == 0) S.max_depth = 0;
+    const int bad_me = tid < N && (p_in < -1 || p_in >= tid);
+    int bad_any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.b32 %0, 1, 0, q;\n\t}"
+        : "=r"(bad_any)
+        : "r"(bad_me)
+        : "memory");
+    if (tid == 0) S.bad = bad_any;
+    if (!bad_any) {
+      // walk t -> root once: depth, g_t (double-float), ancestor bits
+      int dep = 0;
+      if (tid < N) {
+        df g = {0.f, 0.f};
+        uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
+        for (int s = tid; s >= 0; s = S.parent[s]) {
+          g = df_add(g, df{S.la[s], 0.f});
+          const uint32_t bit = (s != tid) ? 1u << (s & 31) : 0u;
+          const int w = s >> 5;
+          a0 |= w == 0 ? bit : 0u;
+          a1 |= w == 1 ? bit : 0u;
+          a2 |= w == 2 ? bit : 0u;
+          a3 |= w == 3 ? bit : 0u;
+          ++dep;
         }
-        excl += cnt[e];
+        S.g[tid] = g;
+        S.anc[tid * kW + 0] = a0;
+        S.anc[tid * kW + 1] = a1;
+        S.anc[tid * kW + 2] = a2;
+        S.anc[tid * kW + 3] = a3;
+        S.depth[tid] = dep;
+        // path table: sPath[t * 128 + depth(s)] = s for every s on t's path
+        int ds = dep;
+        for (int s = tid; s >= 0; s = S.parent[s]) sPath[tid * kTile + ds--] = (uint8_t)s;
+        atomicAdd(&S.level_start[dep], 1);
+        atomicMax(&S.max_depth, dep);
       }
+      TreeSync()();
+      if (warp == 0) {
+        // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
+        int cnt[5], run = 0;
+#pragma unroll
+        for (int e = 0; e < 5; ++e) {
+          const int l = lane * 5 + e;
+          cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
+          run += cnt[e];
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int up = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += up;
+        }
+        int excl = incl - run;
+#pragma unroll
+        for (int e = 0; e < 5; ++e) {
+          const int l = lane * 5 + e;
+          if (l < kTile + 2) {
+            S.level_start[l] = excl;
+            S.level_cursor[l] = excl;
+          }
+          excl += cnt[e];
+        }
+      }
+      TreeSync()();
+      if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
     }
-    TreeSync()();
-    if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
   } else {
+    using OperandSync = NamedSync<2, kThreads - 128>;
+    if (tid == kIssuer) {
+      mbar_init(&S.bar_kq, 1);
+      mbar_init(&S.bar_s0, 1);
+      mbar_init(&S.bar_g, 1);
+      mbar_init(&S.bar_ks, 1);
+      mbar_init(&S.bar_yu, 1);
+      S.err = 0;
+      S.issued = 0;
+      mbar_fence_init();
+      mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
+      tma_load_4d(smem + OFF_K, &tmK, &S.bar_kq, 0, hq, 0, b);
+      tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_kq, 64, hq, 0, b);
+      tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
+      tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
+      mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
+      tma_load_3d(smem + OFF_U, &tmS, &S.bar_s0, 0, 0, b * Hv + h);
+    }
+    if (warp == 5) tmem_alloc(&S.tmem_base, kTmemCols);
+    tc_fence_before_sync();
+    OperandSync()();
+    tc_fence_after_sync();
+    const uint32_t tm = S.tmem_base;
     if (tid == kIssuer) {
       if (!mbar_wait(&S.bar_kq, 0, kWaitLimitNs)) {
         S.err = 1;
       } else {
         tc_fence_after_sync();
-        umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
-        umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
+        umma_128x128x128(tm + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
+        umma_128x128x128(tm + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
         umma_commit(&S.bar_g);
         S.issued |= 1;
       }
@@ -324,19 +333,27 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       *reinterpret_cast<uint4*>(smem + OFF_S0L + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     fence_proxy_async_smem();
+    OperandSync()();
+    if (tid == kIssuer && S.err == 0) {
+      tc_fence_after_sync();
+      umma_128x128x128(tm + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+      umma_128x128x128(tm + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+      umma_128x128x128(tm + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+      umma_commit(&S.bar_ks);
+      S.issued |= 2;
+    }
   }
+  TC_MARK(1);
+  TC_MARK(2);
   TC_MARK(3);
-  if (__syncthreads_or(S.err)) goto fail;
-
-  // ---- 3. K S0 (hi + lo) and Q S0 (hi) -----------------------------------------------
-  if (tid == kIssuer) {
-    tc_fence_after_sync();
-    umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
-    umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
-    umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-    umma_commit(&S.bar_ks);
-    S.issued |= 2;
-  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = S.tmem_base;
+  if (h == 0 && tid == 0 && dev_status)
+    dev_status[b] = S.bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
+  if (S.bad) goto drain;
+  if (S.err) goto fail;
 
   {
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -353,8 +370,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     float xr[32];
     tmem_ld_32cols(trow + kColGkk + col0, xr);
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      xr[j] = ((abits >> j) & 1u) ? bt * __expf(df_diff(gt, S.g[col0 + j])) * xr[j] : 0.f;
+    for (int j = 0; j < 32; ++j) {
+      const bool need = (abits >> j) & 1u;
+      float xv = 0.f;
+      if (__any_sync(0xffffffffu, need)) {  // skip columns no lane of the warp needs
+        const float e = __expf(df_diff(gt, S.g[col0 + j]));
+        xv = need ? bt * e * xr[j] : 0.f;
+      }
+      xr[j] = xv;
+    }
 
     // ---- 5. once K S0 / Q S0 are done (K, Q, S0^T dead): X, R = beta (V - gamma K S0)
     //         and Y (hi, lo) to shared memory -------------------------------------------
@@ -399,8 +423,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           for (int e = 0; e < 2; ++e) {
             const int j = g8 * 8 + 2 * i + e;
             const int s = col0 + j;
-            const bool on_path = live && (((abits >> j) & 1u) || s == t);
-            y[e] = on_path ? (s == t ? gq[j] : __expf(df_diff(gt, S.g[s])) * gq[j]) : 0.f;
+            const bool anc_s = live && ((abits >> j) & 1u);
+            float yv = (live && s == t) ? gq[j] : 0.f;
+            if (__any_sync(0xffffffffu, anc_s)) {
+              const float dec = __expf(df_diff(gt, S.g[s]));
+              if (anc_s) yv = dec * gq[j];
+            }
+            y[e] = yv;
           }
           split2(y[0], y[1], hi[i], lo[i]);
         }
@@ -414,17 +443,27 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
     // ---- 6. forward substitution as a dataflow over the tree ------------------------
     // u_t = r_t - sum over ancestors a of X[t,a] u_a.  Warp w takes the nodes at
-    // positions w, w + 16, ... of the depth order; for node t it waits for the
-    // ready flag of t's parent only (every other ancestor was final before the
-    // parent was), then sums all ancestor terms, four at a time so that their
-    // loads overlap (lane = 4 value columns), publishes u_t and raises t's
-    // flag.  No cycle of waits can form: the unfinished node of lowest depth
-    // order never waits (its parent comes earlier in that order).
+    // positions w, w + 16, ... of the depth order.  For node t it waits (acquire)
+    // on the ready flag of t's grandparent -- every ancestor but the parent is
+    // then final -- sums those terms four at a time (lane = 4 value columns),
+    // then waits on the parent and adds its term, publishes u_t and raises t's
+    // flag (release).  So a link of the dependency chain costs one term, not the
+    // whole ancestor sum.  No cycle of waits can form: the unfinished node of
+    // lowest depth order never waits (its ancestors come earlier in that order).
     TC_MARK(6);
     {
-      volatile int* ready = S.ready;
+      int* ready = S.ready;
       float* Ubh = U + ((size_t)b * Hv + h) * N * kD;
       bool timed_out = false;
+      auto wait_ready = [&](int node) {
+        uint32_t spins = 0;
+        while (ld_acquire_shared(ready + node) == 0) {
+          if (++spins > kSpinLimit) {
+            timed_out = true;
+            break;
+          }
+        }
+      };
       for (int i = warp; i < N; i += kWarps) {
         const int tn = S.order[i];
         const int dep = S.depth[tn];
@@ -432,17 +471,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const float* xrow = sX + x_index(tn, 0);
         float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
         if (dep > 1) {
-          const int par = pth[dep - 1];
-          uint32_t spins = 0;
-          while (ready[par] == 0) {
-            if (++spins > kSpinLimit) {
-              timed_out = true;
-              break;
-            }
-          }
-          __threadfence_block();
+          if (dep > 2) wait_ready(pth[dep - 2]);
           int j = 1;
-          for (; j + 4 <= dep; j += 4) {
+          for (; j + 4 <= dep - 1; j += 4) {
             int aa[4];
             float xx[4];
             float4 uu[4];
@@ -461,7 +492,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               acc.w = fmaf(-xx[e], uu[e].w, acc.w);
             }
           }
-          for (; j < dep; ++j) {
+          for (; j < dep - 1; ++j) {
             const int a1 = pth[j];
             const float x1 = xrow[a1];
             const float4 u1 = *reinterpret_cast<const float4*>(sU + u_index(a1, lane));
@@ -470,11 +501,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             acc.z = fmaf(-x1, u1.z, acc.z);
             acc.w = fmaf(-x1, u1.w, acc.w);
           }
+          const int par = pth[dep - 1];
+          const float xp = xrow[par];
+          wait_ready(par);
+          const float4 up = *reinterpret_cast<const float4*>(sU + u_index(par, lane));
+          acc.x = fmaf(-xp, up.x, acc.x);
+          acc.y = fmaf(-xp, up.y, acc.y);
+          acc.z = fmaf(-xp, up.z, acc.z);
+          acc.w = fmaf(-xp, up.w, acc.w);
           *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
-          __threadfence_block();
         }
         __syncwarp();
-        if (lane == 0) ready[tn] = 1;
+        if (lane == 0) st_release_shared(ready + tn, 1);
         *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
       }
       if (timed_out) S.err = 4;
@@ -544,8 +582,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 fail:
   // a bounded wait ran out: report it, let in-flight copies and MMAs drain
   // (again bounded), then free TMEM
+  if (tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
+drain:
   if (tid == 0) {
-    if (dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
     mbar_wait(&S.bar_kq, 0, kWaitLimitNs);
     mbar_wait(&S.bar_s0, 0, kWaitLimitNs);
     if (S.issued & 1) mbar_wait(&S.bar_g, 0, kWaitLimitNs);
@@ -556,7 +595,7 @@ fail:
 release:
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---- host side -------------------------------------------------------------------
