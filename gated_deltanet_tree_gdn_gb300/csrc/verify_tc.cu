@@ -52,6 +52,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384, kColYU = 0;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kIssuer = 128;  // the one thread that issues every MMA (warp 4, lane 0)
+constexpr int kS0BoxRows = 32;  // S0 arrives as four 32-row boxes
 constexpr uint32_t kSpinLimit = 1u << 24;  // bounded wait on a solve ready flag
 
 #ifdef GDN_TC_PROFILE
@@ -192,14 +193,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   //   operand group (warps 4-15): bulk loads, TMEM, Gram MMAs, S0^T split, and
   //     the K S0 / Q S0 MMAs as soon as S0^T is in place.
   TC_MARK(0);
-  // this thread's 32 values of v (row t, columns 32 cq ..), kept in registers
-  uint4 vreg[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                   make_uint4(0, 0, 0, 0)};
-  if (live) {
-    const uint4* vrow =
-        reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
+  if (tid == kIssuer) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmS);
   }
   if (warp < 4) {
     using TreeSync = NamedSync<1, 128>;
@@ -302,7 +299,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
       tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
       mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
-      tma_load_3d(smem + OFF_U, &tmS, &S.bar_s0, 0, 0, b * Hv + h);
+#pragma unroll
+      for (int r = 0; r < kD; r += kS0BoxRows)  // four boxes land in parallel
+        tma_load_3d(smem + OFF_U + r * kD * 4, &tmS, &S.bar_s0, 0, r, b * Hv + h);
     }
     if (warp == 5) tmem_alloc(&S.tmem_base, kTmemCols);
     tc_fence_before_sync();
@@ -320,40 +319,63 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         S.issued |= 1;
       }
     }
-    if (!mbar_wait(&S.bar_s0, 0, kWaitLimitNs)) S.err = 1;
-    const float* raw = sU;  // S0 [dk][dv], row-major, landed by TMA
-    for (int item = tid - 128; item < kD * 16; item += kThreads - 128) {
-      const int n = item & (kD - 1), k8 = item >> 7;
-      const float* col = raw + (k8 * 8) * kD + n;
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi[i], lo[i]);
-      const uint32_t off = sw128_chunk(n, k8);
-      *reinterpret_cast<uint4*>(smem + OFF_S0H + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + OFF_S0L + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    fence_proxy_async_smem();
-    OperandSync()();
-    if (tid == kIssuer && S.err == 0) {
-      tc_fence_after_sync();
-      umma_128x128x128(tm + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
-      umma_128x128x128(tm + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
-      umma_128x128x128(tm + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-      umma_commit(&S.bar_ks);
-      S.issued |= 2;
-    }
   }
+  // ---- 1. both groups: S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the
+  //         raw S0 tile; the hi half first, so that K S0_hi and Q S0_hi can run on
+  //         the tensor cores while the lo half is written --------------------------
   TC_MARK(1);
-  TC_MARK(2);
-  TC_MARK(3);
   tc_fence_before_sync();
-  __syncthreads();
+  __syncthreads();  // barriers initialised, TMEM allocated, tree group done
   tc_fence_after_sync();
   const uint32_t tmem = S.tmem_base;
+  if (!mbar_wait(&S.bar_s0, 0, kWaitLimitNs)) S.err = 1;
+  TC_MARK(2);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const float* raw = sU;  // S0 [dk][dv], row-major, landed by TMA
+#pragma unroll
+    for (int r = 0; r < (kD * 16) / kThreads; ++r) {
+      const int item = tid + r * kThreads;
+      const int n = item & (kD - 1), k8 = item >> 7;
+      const float* col = raw + (k8 * 8) * kD + n;
+      uint32_t part[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t hi, lo;
+        split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi, lo);
+        part[i] = half == 0 ? hi : lo;
+      }
+      *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + sw128_chunk(n, k8)) =
+          make_uint4(part[0], part[1], part[2], part[3]);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == kIssuer && S.err == 0) {
+      tc_fence_after_sync();
+      if (half == 0) {
+        umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+      } else {
+        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+        umma_commit(&S.bar_ks);
+        S.issued |= 2;
+      }
+    }
+  }
+  // this thread's 32 values of v (row t, columns 32 cq ..), kept in registers
+  uint4 vreg[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                   make_uint4(0, 0, 0, 0)};
+  if (live) {
+    const uint4* vrow =
+        reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
+  }
+  TC_MARK(3);
   if (h == 0 && tid == 0 && dev_status)
     dev_status[b] = S.bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
   if (S.bad) goto drain;
-  if (S.err) goto fail;
+  if (__syncthreads_or(S.err)) goto fail;
 
   {
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -629,13 +651,13 @@ bool encode_qk_map(CUtensorMap* map, const void* base, const gdn_tree_dims& d) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// S0 [B*Hv, dk, dv] fp32 -> one 128 x 128 box per (b, h), unswizzled
+// S0 [B*Hv, dk, dv] fp32 -> 32-row boxes of one (b, h) state, unswizzled
 bool encode_state_map(CUtensorMap* map, const float* base, const gdn_tree_dims& d) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kD, (cuuint64_t)d.B * d.Hv};
   const cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)kD * kD * 4};
-  const cuuint32_t box[3] = {kD, kD, 1};
+  const cuuint32_t box[3] = {kD, kS0BoxRows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
