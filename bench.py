@@ -103,6 +103,21 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def verify_kernel_name(w: W.Workload) -> str:
+    """The verify kernel the library dispatches for this shape (mirrors the
+    C-ABI's rule: tensor-core kernel for bf16, dk = dv = 128, N <= 128)."""
+    if (w.dtype == W.BF16 and w.dk == 128 and w.dv == 128 and w.N <= 128
+            and os.environ.get("GDN_TREE_KERNEL", "auto") != "generic"):
+        return "verify_tc_kernel"
+    return "verify_generic_kernel"
+
+
+def arithmetic_dtype(kernel: str) -> str:
+    # tensor-core kernel: bf16 products (fp32 accumulate, split-bf16 where the
+    # state needs fp32 accuracy) and an fp32 solve; CUDA-core kernel: fp32
+    return "bf16" if kernel == "verify_tc_kernel" else "f32"
+
+
 def profiled_traffic(kernel: str):
     """dram read+write bytes per launch from the committed ncu summary, or None
     when it was taken on a different kernel source."""
@@ -117,7 +132,7 @@ def profiled_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -134,7 +149,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-i", str(self.gpu), "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -170,6 +185,22 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Largest value of x over all ranks (identity when not distributed)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, B: int, N: int, ms_per_step: float) -> float:
+    """Whole-job nodes/s: every rank verifies its own B x N nodes per step and
+    the step time is the slowest rank's."""
+    return world * B * N / (ms_per_step * 1e-3)
 
 
 def cpu_cores() -> int:
@@ -312,13 +343,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     torch.cuda.synchronize()
     t_ver = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]   # ms
     t_com = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    total_ms = float(sum(t_ver) + sum(t_com))
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(t_ver) + sum(t_com)), dist, dev)
     ms_per_step = total_ms / K
-    value = world * w.B * w.N / (ms_per_step * 1e-3)
+    value = job_throughput(world, w.B, w.N, ms_per_step)
 
     # end to end through the public API: pinned host inputs -> device -> verify
     # + commit -> o and S1 back to pinned host memory, every step
@@ -348,11 +375,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, dist, dev)
 
     if rank == 0:
         peaks, peak_kind = measured_peaks()
@@ -362,17 +385,18 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         com_ms = statistics.mean(t_com)
         hbm = float(peaks["hbm_gbs"])
         tflops = float(peaks["bf16_tflops"])
-        kernel = "verify_generic_kernel"
+        kernel = verify_kernel_name(w)
         achieved = vb / (ver_ms * 1e-3) / 1e9
         traffic = profiled_traffic(kernel)
         t_roof = max((vb + cb) / (hbm * 1e9), (vf + cf) / (tflops * 1e12))
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": arithmetic_dtype(kernel),
+            "data": "synthetic",
             "config": dict(workload_config(w), parallelism=f"dp{world}"),
             "clocks": clk.summary(),
-            "e2e": {"value": world * w.B * w.N / (e2e_ms * 1e-3), "unit": UNIT,
+            "e2e": {"value": job_throughput(world, w.B, w.N, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * K,
             "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
@@ -394,7 +418,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

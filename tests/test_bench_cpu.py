@@ -1,0 +1,64 @@
+"""Host-side logic of bench.py: the byte model, the multi-rank aggregation
+(world size 2 over gloo on the CPU), and the reference arm's JSON line."""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_byte_model_serving_workload():
+    w = W.make_config(3)
+    # S0 64 MiB + q,k 32 MiB + v 32 MiB + gates 1 MiB + parent + o 32 MiB + U 64 MiB
+    assert bench.verify_bytes(w) == 235945984
+    L = int(w.path_len.sum())
+    assert bench.commit_bytes(w) == (2 * 64 * 2**20 + L * 32 * 512 + L * 16 * 256
+                                     + L * 32 * 4 + 32 * 25 * 4)
+    assert bench.verify_kernel_name(w) == "verify_tc_kernel"
+    assert bench.verify_kernel_name(W.make_config(0)) == "verify_generic_kernel"
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [2.0, 3.0][rank]  # rank 1 is the slow one
+    m = bench.max_over_ranks(ms, dist)
+    out[rank] = (m, bench.job_throughput(world, 32, 128, m))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_over_gloo():
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = 29500 + os.getpid() % 1000
+    ps = [ctx.Process(target=_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0][0] == out[1][0] == 3.0
+    assert out[0][1] == pytest.approx(2 * 32 * 128 / 3e-3)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "nodes/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
