@@ -37,7 +37,7 @@ UNIT = "nodes/s"
 WORKLOAD_CFG = 3
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "gated_deltanet_tree_gdn_gb300", "csrc", f)
-                  for f in ("verify_generic.cu", "verify_tc.cu", "common.cuh")]
+                  for f in ("verify_generic.cu", "verify_tc.cu", "common.cuh", "sm100.cuh")]
 
 
 def log(*a):
