@@ -9,8 +9,9 @@
 //     w_j = exp(G_L - G_j),  gamma_L = exp(G_L),  G_j = sum_{i<=j} log alpha_{p_i},
 // a rank-L update of S0 that streams S0 in and S1 out once (HBM-bound).
 //
-// Grid: (Hv, B), 512 threads.  Each CTA owns one (b, h) state.  The state is
-// bulk-copied into shared memory the moment the CTA starts, so the state
+// Grid: (Hv, B, dk / 64), 256 threads, four CTAs per SM.  Each CTA owns 64 rows
+// of one (b, h) state, bulk-copied into shared memory the moment the CTA
+// starts, so that the state
 // stream overlaps the path-dependent gathers, which take two rounds: the path
 // and its length together, then (with indices range-checked) the parent-link
 // check, log alpha and the k and U rows of the path all at once.  Thread
@@ -24,15 +25,18 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
+constexpr int kRowsPerCta = 64;  // each CTA owns half of a (b, h) state's rows
 constexpr int kChunk = 32;   // path entries staged per round
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on the S0 copy wait
 
-// dynamic shared memory: S0 (dk x dv fp32) | k rows [kChunk][dk] | u rows [kChunk][dv]
-constexpr size_t kSmemBytes = (size_t)(kMaxD * kMaxD + 2 * kChunk * kMaxD) * sizeof(float);
+// dynamic shared memory: S0 rows (kRowsPerCta x dv fp32) | k rows [kChunk][kRowsPerCta] |
+// u rows [kChunk][dv]
+constexpr size_t kSmemBytes =
+    (size_t)(kRowsPerCta * kMaxD + kChunk * kRowsPerCta + kChunk * kMaxD) * sizeof(float);
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 4)
 commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path_len,
               const int32_t* __restrict__ parent, const float* __restrict__ U,
               const T* __restrict__ k, const float* __restrict__ log_alpha,
@@ -41,9 +45,9 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   // S0 and S1 may alias (in-place commit): the whole state is copied into
   // shared memory before any element of S1 is written.
   extern __shared__ __align__(128) float smem_f[];
-  float* sS0 = smem_f;                            // [dk][dv]
-  float* sK = sS0 + kMaxD * kMaxD;                // [kChunk][dk]
-  float* sU = sK + kChunk * kMaxD;                // [kChunk][dv]
+  float* sS0 = smem_f;                            // [rows][dv]
+  float* sK = sS0 + kRowsPerCta * kMaxD;          // [kChunk][rows]
+  float* sU = sK + kChunk * kRowsPerCta;          // [kChunk][dv]
   __shared__ int sPath[kMaxN];
   __shared__ float sLa[kMaxN];                    // log alpha along the path
   __shared__ float sW[kMaxN];                     // w_j
@@ -51,18 +55,19 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   __shared__ float sGamma;
 
   const int N = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int h = blockIdx.x, b = blockIdx.y, row0 = blockIdx.z * kRowsPerCta;
   const int hq = h / (Hv / Hqk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rows = min(kRowsPerCta, dk - row0);
   const size_t sbase = ((size_t)b * Hv + h) * dk * dv;
 
-  // ---- the whole (b, h) state starts streaming into shared memory at once ----
+  // ---- this CTA's rows of the (b, h) state start streaming in at once ----------
   if (tid == 0) {
-    const uint32_t bytes = (uint32_t)(dk * dv * sizeof(float));
+    const uint32_t bytes = (uint32_t)(rows * dv * sizeof(float));
     sm100::mbar_init(&sBar, 1);
     sm100::mbar_fence_init();
     sm100::mbar_arrive_expect_tx(&sBar, bytes);
-    sm100::bulk_load(sS0, S0 + sbase, bytes, &sBar);
+    sm100::bulk_load(sS0, S0 + sbase + (size_t)row0 * dv, bytes, &sBar);
   }
 
   // ---- round 1: path length and entries (range-checked) ----------------------
@@ -87,10 +92,10 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     sLa[tid] = log_alpha[((size_t)b * N + pj) * Hv + h];
   }
   auto stage = [&](int j0, int nj) {
-    for (int e = tid; e < nj * (dk / 4); e += kThreads) {
-      const int jj = e / (dk / 4), c = (e % (dk / 4)) * 4;
-      const T* kr = k + (((size_t)b * N + sPath[j0 + jj]) * Hqk + hq) * dk + c;
-      *reinterpret_cast<float4*>(sK + jj * dk + c) =
+    for (int e = tid; e < nj * (rows / 4); e += kThreads) {
+      const int jj = e / (rows / 4), c = (e % (rows / 4)) * 4;
+      const T* kr = k + (((size_t)b * N + sPath[j0 + jj]) * Hqk + hq) * dk + row0 + c;
+      *reinterpret_cast<float4*>(sK + jj * kRowsPerCta + c) =
           make_float4(to_f32(kr[0]), to_f32(kr[1]), to_f32(kr[2]), to_f32(kr[3]));
     }
     for (int e = tid; e < nj * (dv / 4); e += kThreads) {
@@ -101,7 +106,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   };
   if (!bad) stage(0, min(kChunk, L));
   bad = __syncthreads_or(bad);
-  if (h == 0 && tid == 0 && dev_status)
+  if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
     dev_status[b] = bad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
   if (bad) {
     if (tid == 0) sm100::mbar_wait(&sBar, 0, kWaitLimitNs);  // drain the copy
@@ -156,7 +161,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   // ---- S1 = gamma S0 + K_P^T diag(w) U_P ------------------------------------------
   // thread (r8, c4): rows r8*8 .. r8*8+7, columns c4*4 .. c4*4+3
   const int r8 = tid / 32, c4 = tid % 32;
-  const bool active = (r8 * 8 < dk) && (c4 * 4 < dv);
+  const bool active = (r8 * 8 < rows) && (c4 * 4 < dv);
   float acc[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -172,8 +177,8 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     if (active) {
       for (int jj = 0; jj < nj; ++jj) {
         const float w = sW[j0 + jj];
-        const float4 k0 = *reinterpret_cast<const float4*>(sK + jj * dk + r8 * 8);
-        const float4 k1 = *reinterpret_cast<const float4*>(sK + jj * dk + r8 * 8 + 4);
+        const float4 k0 = *reinterpret_cast<const float4*>(sK + jj * kRowsPerCta + r8 * 8);
+        const float4 k1 = *reinterpret_cast<const float4*>(sK + jj * kRowsPerCta + r8 * 8 + 4);
         const float4 uu = *reinterpret_cast<const float4*>(sU + jj * dv + c4 * 4);
         const float kk[8] = {w * k0.x, w * k0.y, w * k0.z, w * k0.w,
                              w * k1.x, w * k1.y, w * k1.z, w * k1.w};
@@ -201,7 +206,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
       s1.y = fmaf(gamma, s0.y, acc[i][1]);
       s1.z = fmaf(gamma, s0.z, acc[i][2]);
       s1.w = fmaf(gamma, s0.w, acc[i][3]);
-      *reinterpret_cast<float4*>(S1 + sbase + (size_t)row * dv + c4 * 4) = s1;
+      *reinterpret_cast<float4*>(S1 + sbase + (size_t)(row0 + row) * dv + c4 * 4) = s1;
     }
   }
 }
@@ -209,7 +214,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 }  // namespace
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
-  const dim3 grid(a.d.Hv, a.d.B);
+  const dim3 grid(a.d.Hv, a.d.B, (a.d.dk + kRowsPerCta - 1) / kRowsPerCta);
   cudaError_t err;
   if (a.d.dtype == GDN_TREE_BF16) {
     err = cudaFuncSetAttribute(commit_kernel<__nv_bfloat16>,
