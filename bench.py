@@ -4,14 +4,17 @@ reported baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-A step is one pass of the whole path over one batch: gdn_tree_verify for
-every node of every tree, then gdn_tree_commit of every accepted path.  The
-workload is the serving-scale case: 32 sequences x 32 v-heads (16 q/k heads),
-dk = dv = 128, bf16 q/k/v, fp32 S0, 128-node random trees (branching 1-4,
-depth <= 24), accepted paths of up to 24 nodes.  L2 is flushed (a 256 MiB
-write) before every timed step, outside the timed events.  Under torchrun
-each rank runs its own independent batch (weak scaling, no collective on the
-data path) and rank 0 prints one JSON line.
+A step is one decoding iteration of the whole path over one batch: the
+delayed commitment of the previous tree's accepted path and the verification
+of every node of the next tree, as one gdn_tree_commit_verify call (state
+buffers and U buffers ping-pong between steps).  The same work done as the two
+separate calls (gdn_tree_verify, then gdn_tree_commit) is timed as well and
+reported under "separate_calls".  The workload is the serving-scale case: 32
+sequences x 32 v-heads (16 q/k heads), dk = dv = 128, bf16 q/k/v, fp32 state,
+128-node random trees (branching 1-4, depth <= 24), accepted paths of up to 24
+nodes.  L2 is flushed (a 256 MiB write) before every timed step, outside the
+timed events.  Under torchrun each rank runs its own independent batch (weak
+scaling, no collective on the data path) and rank 0 prints one JSON line.
 """
 
 from __future__ import annotations
@@ -70,6 +73,21 @@ def commit_bytes(w: W.Workload) -> int:
             + w.B * (w.Lmax + 1) * 4)          # path + path_len
 
 
+def iteration_bytes(w: W.Workload) -> int:
+    """One fused decoding iteration: the verify's traffic (the previous state is
+    read once), the committed state written once, and the previous accepted
+    path's rows (U, k, log alpha, parent links)."""
+    es = 2 if w.dtype == W.BF16 else 4
+    Lsum = int(w.path_len.sum())
+    return (verify_bytes(w)
+            + w.B * w.Hv * w.dk * w.dv * 4           # S1 write
+            + Lsum * w.Hv * w.dv * 4                 # U rows of the accepted paths
+            + Lsum * w.Hqk * w.dk * es               # k rows (once per q/k head)
+            + Lsum * w.Hv * 4                        # log_alpha along the paths
+            + Lsum * 4                               # parent links checked
+            + w.B * (w.Lmax + 1) * 4)                # path + path_len
+
+
 def verify_flops(w: W.Workload) -> int:
     B, N, Hqk, Hv, d = w.B, w.N, w.Hqk, w.Hv, w.dk
     return (B * Hv * (2 * 2 * N * d * d        # Q S0 and K S0
@@ -112,10 +130,18 @@ def verify_kernel_name(w: W.Workload) -> str:
     return "verify_generic_kernel"
 
 
+def iteration_kernel_name(w: W.Workload) -> str:
+    """The kernel one fused decoding iteration runs on (the tensor-core kernel
+    with the delayed commitment fused in, where it takes the shape)."""
+    if verify_kernel_name(w) == "verify_tc_kernel":
+        return "verify_tc_kernel<fused commit>"
+    return "commit_kernel + verify_generic_kernel"
+
+
 def arithmetic_dtype(kernel: str) -> str:
     # tensor-core kernel: bf16 products (fp32 accumulate, split-bf16 where the
     # state needs fp32 accuracy) and an fp32 solve; CUDA-core kernel: fp32
-    return "bf16" if kernel == "verify_tc_kernel" else "f32"
+    return "bf16" if kernel.startswith("verify_tc_kernel") else "f32"
 
 
 def profiled_traffic(kernel: str):
@@ -315,13 +341,30 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         gt.commit(xx["path"], xx["path_len"], UU, xx["k"], xx["log_alpha"], xx["S0"], S1=SS,
                   parent=xx["parent"])
 
-    for _ in range(args.warmup):
+    # ping-pong buffers of a decoding loop: step i commits the accepted path of
+    # the tree verified at step i-1 (its U rows) and verifies the next tree
+    Sbuf = [x["S0"].clone(), torch.empty_like(x["S0"])]
+    Ubuf = [torch.empty_like(U), torch.empty_like(U)]
+    gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], Sbuf[0],
+              o=o, U=Ubuf[0])
+
+    def iteration(i, xx=None):
+        xx = xx or x
+        cur, nxt = i & 1, (i + 1) & 1
+        gt.commit_verify(xx["path"], xx["path_len"], Ubuf[cur], xx["k"], xx["log_alpha"],
+                         Sbuf[cur], xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["beta"],
+                         xx["parent"], S1=Sbuf[nxt], o=o, U=Ubuf[nxt],
+                         prev_parent=xx["parent"])
+
+    for i in range(args.warmup):
+        flush.zero_()
+        iteration(i)
         flush.zero_()
         step(x, o, U, S1)
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -330,83 +373,107 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         for i in range(K):
             flush.zero_()
             ev[i][0].record(stream)
-            gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
-                      o=o, U=U)
+            iteration(i)
             ev[i][1].record(stream)
-            gt.commit(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["S0"], S1=S1,
-                      parent=x["parent"])
-            ev[i][2].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    t_ver = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]   # ms
-    t_com = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    total_ms = max_over_ranks(float(sum(t_ver) + sum(t_com)), dist, dev)
-    ms_per_step = total_ms / K
+    t_it = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ms_per_step = max_over_ranks(float(sum(t_it)), dist, dev) / K
     value = job_throughput(world, w.B, w.N, ms_per_step)
 
-    # end to end through the public API: pinned host inputs -> device -> verify
-    # + commit -> o and S1 back to pinned host memory, every step
+    # the same work as two separate calls (verify, then commit)
+    Ks = min(K, 1000)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Ks)]
+    for i in range(Ks):
+        flush.zero_()
+        evs[i][0].record(stream)
+        gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
+                  o=o, U=U)
+        evs[i][1].record(stream)
+        gt.commit(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["S0"], S1=S1,
+                  parent=x["parent"])
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_ver = [evs[i][0].elapsed_time(evs[i][1]) for i in range(Ks)]   # ms
+    t_com = [evs[i][1].elapsed_time(evs[i][2]) for i in range(Ks)]
+    sep_ms = max_over_ranks(float(sum(t_ver) + sum(t_com)), dist, dev) / Ks
+
+    # end to end through the public API: every step copies the tree's inputs and
+    # the accepted path from pinned host memory (the recurrent state stays
+    # resident on the device, as in a decoding loop), runs one decoding
+    # iteration, and reads o and the committed state back into pinned memory
     h_o = torch.empty(o.shape, dtype=dt).pin_memory()
     h_S1 = torch.empty(S1.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    per_step_inputs = [kk for kk in hin if kk != "S0"]
+    h2d = sum(hin[kk].numel() * hin[kk].element_size() for kk in per_step_inputs)
     d2h = h_o.numel() * h_o.element_size() + h_S1.numel() * h_S1.element_size()
     Ke = max(3, min(K, 50))
     xe = {kk: torch.empty_like(t) for kk, t in x.items()}
 
-    def e2e_step():
-        for kk in hin:
+    def e2e_step(i):
+        for kk in per_step_inputs:
             xe[kk].copy_(hin[kk], non_blocking=True)
-        step(xe, o, U, S1)
+        iteration(i, xe)
         h_o.copy_(o, non_blocking=True)
-        h_S1.copy_(S1, non_blocking=True)
+        h_S1.copy_(Sbuf[(i + 1) & 1], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(Ke):
-        e2e_step()
+    for i in range(Ke):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, dist, dev)
 
     if rank == 0:
         peaks, peak_kind = measured_peaks()
-        vb, cb = verify_bytes(w), commit_bytes(w)
+        vb, cb, ib = verify_bytes(w), commit_bytes(w), iteration_bytes(w)
         vf, cf = verify_flops(w), commit_flops(w)
-        ver_ms = statistics.mean(t_ver)
-        com_ms = statistics.mean(t_com)
+        it_ms = ms_per_step
         hbm = float(peaks["hbm_gbs"])
         tflops = float(peaks["bf16_tflops"])
-        kernel = verify_kernel_name(w)
-        achieved = vb / (ver_ms * 1e-3) / 1e9
+        kernel = iteration_kernel_name(w)
+        achieved = ib / (statistics.mean(t_it) * 1e-3) / 1e9
         traffic = profiled_traffic(kernel)
-        t_roof = max((vb + cb) / (hbm * 1e9), (vf + cf) / (tflops * 1e12))
+        t_roof = max(ib / (hbm * 1e9), (vf + cf) / (tflops * 1e12))
+        t_roof_sep = max((vb + cb) / (hbm * 1e9), (vf + cf) / (tflops * 1e12))
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": arithmetic_dtype(kernel),
             "data": "synthetic",
-            "config": dict(workload_config(w), parallelism=f"dp{world}"),
+            "config": dict(workload_config(w), parallelism=f"dp{world}",
+                           step="one decoding iteration: commit of the previous accepted "
+                                "path fused with verification of the next tree"),
             "clocks": clk.summary(),
             "e2e": {"value": job_throughput(world, w.B, w.N, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * K,
+            "gpu_launches": K,
             "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
                          "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": vb, "peak_source": peak_kind},
-            "step": {"verify_us": 1e3 * ver_ms, "commit_us": 1e3 * com_ms,
-                     "verify_bytes": vb, "commit_bytes": cb, "verify_flops": vf,
-                     "commit_flops": cf, "roofline_us": 1e6 * t_roof,
-                     "roofline_frac": t_roof / (ms_per_step * 1e-3),
+                         "algorithmic_bytes_per_launch": ib, "peak_source": peak_kind},
+            "step": {"iteration_us": 1e3 * it_ms, "iteration_bytes": ib,
+                     "roofline_us": 1e6 * t_roof, "roofline_frac": t_roof / (it_ms * 1e-3),
                      "wall_s_timed_loop": wall},
+            "separate_calls": {"value": job_throughput(world, w.B, w.N, sep_ms),
+                               "ms_per_step": sep_ms,
+                               "verify_us": 1e3 * statistics.mean(t_ver),
+                               "commit_us": 1e3 * statistics.mean(t_com),
+                               "verify_bytes": vb, "commit_bytes": cb,
+                               "verify_roofline_frac": vb / (statistics.mean(t_ver) * 1e-3)
+                               / (hbm * 1e9),
+                               "roofline_frac": t_roof_sep / (sep_ms * 1e-3),
+                               "verify_flops": vf, "commit_flops": cf,
+                               "verify_kernel": verify_kernel_name(w)},
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)

@@ -19,7 +19,8 @@ BF16, F32 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECUDA = 0, -1, -2, -3
 STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TIMEOUT = 0, 1, 2, 3
 
-SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_strerror", "gdn_tree_version")
+SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_commit_verify", "gdn_tree_strerror",
+           "gdn_tree_version")
 
 
 class Dims(ctypes.Structure):
@@ -55,6 +56,10 @@ def load(path: str | None = None):
     lib.gdn_tree_verify.restype = ctypes.c_int
     lib.gdn_tree_commit.argtypes = [ip, ip, ip, fp, vp, fp, fp, fp, Dims, ctypes.c_int32, ip, vp]
     lib.gdn_tree_commit.restype = ctypes.c_int
+    lib.gdn_tree_commit_verify.argtypes = [ip, ip, ip, fp, vp, fp, ctypes.c_int32, ctypes.c_int32,
+                                           fp, fp, vp, vp, vp, fp, fp, ip, vp, fp, Dims, ip, ip,
+                                           vp]
+    lib.gdn_tree_commit_verify.restype = ctypes.c_int
     lib.gdn_tree_strerror.argtypes = [ctypes.c_int]
     lib.gdn_tree_strerror.restype = ctypes.c_char_p
     lib.gdn_tree_version.argtypes = []
@@ -175,3 +180,50 @@ def commit(path, path_len, U, k, log_alpha, S0, *, S1=None, parent=None, dev_sta
     if rc != OK:
         raise GdnTreeError(rc, "gdn_tree_commit")
     return S1
+
+
+def commit_verify(prev_path, prev_path_len, prev_U, prev_k, prev_log_alpha, S_prev, q, k, v,
+                  log_alpha, beta, parent, *, S1=None, prev_parent=None, o=None, U=None,
+                  commit_status=None, verify_status=None, stream=None):
+    """One decoding iteration (C ABI gdn_tree_commit_verify): commit the previous
+    tree's accepted path into S1, then verify the next tree from S1.
+    Returns (S1, o, U).  S1=S_prev commits in place; U=prev_U reuses the buffer."""
+    B, N, Hqk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    dt = q.dtype
+    Np = prev_k.shape[1]
+    _check(prev_path, "prev_path", torch.int32)
+    Lmax = prev_path.shape[1]
+    _check(prev_path_len, "prev_path_len", torch.int32, (B,))
+    _check(prev_U, "prev_U", torch.float32, (B, Hv, Np, dv))
+    _check(prev_k, "prev_k", dt, (B, Np, Hqk, dk))
+    _check(prev_log_alpha, "prev_log_alpha", torch.float32, (B, Np, Hv))
+    _check(S_prev, "S_prev", torch.float32, (B, Hv, dk, dv))
+    _check(q, "q", dt)
+    _check(k, "k", dt, (B, N, Hqk, dk))
+    _check(v, "v", dt, (B, N, Hv, dv))
+    _check(log_alpha, "log_alpha", torch.float32, (B, N, Hv))
+    _check(beta, "beta", torch.float32, (B, N, Hv))
+    _check(parent, "parent", torch.int32, (B, N))
+    if S1 is None:
+        S1 = torch.empty_like(S_prev)
+    if o is None:
+        o = torch.empty((B, N, Hv, dv), dtype=dt, device=q.device)
+    if U is None:
+        U = torch.empty((B, Hv, N, dv), dtype=torch.float32, device=q.device)
+    _check(S1, "S1", torch.float32, (B, Hv, dk, dv))
+    _check(o, "o", dt, (B, N, Hv, dv))
+    _check(U, "U", torch.float32, (B, Hv, N, dv))
+    if prev_parent is not None:
+        _check(prev_parent, "prev_parent", torch.int32, (B, Np))
+    for name, st in (("commit_status", commit_status), ("verify_status", verify_status)):
+        if st is not None:
+            _check(st, name, torch.int32, (B,))
+    rc = load().gdn_tree_commit_verify(
+        _ptr(prev_path), _ptr(prev_path_len), _ptr(prev_parent), _ptr(prev_U), _ptr(prev_k),
+        _ptr(prev_log_alpha), Np, Lmax, _ptr(S_prev), _ptr(S1), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(log_alpha), _ptr(beta), _ptr(parent), _ptr(o), _ptr(U), dims_of(q, v),
+        _ptr(commit_status), _ptr(verify_status), _stream(stream))
+    if rc != OK:
+        raise GdnTreeError(rc, "gdn_tree_commit_verify")
+    return S1, o, U

@@ -47,6 +47,21 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   return launch_verify_generic(a, stream);
 }
 
+cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream) {
+  if (!force_generic() && commit_verify_tc_supported(a.verify.d, a.prev_N))
+    return launch_commit_verify_tc(a, stream);
+  // two launches on the same stream: commit S_prev -> S1, then verify from S1
+  gdn_tree_dims dp = a.verify.d;
+  dp.N = a.prev_N;
+  const CommitArgs c{a.prev_path, a.prev_path_len, a.prev_parent, a.prev_U, a.prev_k,
+                     a.prev_log_alpha, a.S_prev, a.S1, dp, a.Lmax, a.commit_status};
+  cudaError_t err = launch_commit(c, stream);
+  if (err != cudaSuccess) return err;
+  VerifyArgs v = a.verify;
+  v.S0 = a.S1;
+  return launch_verify(v, stream);
+}
+
 }  // namespace gdn
 
 extern "C" {
@@ -89,6 +104,44 @@ int gdn_tree_commit(const int32_t* path, const int32_t* path_len, const int32_t*
   if (a0 != a1 && a0 < a1 + bytes && a1 < a0 + bytes) return GDN_TREE_EINVAL;
   gdn::CommitArgs a{path, path_len, parent, U, k, log_alpha, S0, S1, dims, Lmax, dev_status};
   const cudaError_t err = gdn::launch_commit(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
+int gdn_tree_commit_verify(const int32_t* prev_path, const int32_t* prev_path_len,
+                           const int32_t* prev_parent, const float* prev_U, const void* prev_k,
+                           const float* prev_log_alpha, int32_t prev_N, int32_t Lmax,
+                           const float* S_prev, float* S1, const void* q, const void* k,
+                           const void* v, const float* log_alpha, const float* beta,
+                           const int32_t* parent, void* o, float* U, gdn_tree_dims dims,
+                           int32_t* commit_status, int32_t* verify_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  gdn_tree_dims dp = dims;
+  dp.N = prev_N;
+  if (prev_N < 0 || Lmax < 0) return GDN_TREE_EINVAL;
+  rc = check_dims(dp);
+  if (rc != GDN_TREE_OK) return rc;
+  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (dims.B == 0) return GDN_TREE_OK;
+  if (prev_N == 0 || dims.N == 0) return GDN_TREE_EUNSUPPORTED;
+  const void* ptrs[] = {prev_path_len, prev_U, prev_k, prev_log_alpha, S_prev, S1,
+                        q, k, v, log_alpha, beta, parent, o, U};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (Lmax > 0 && (prev_path == nullptr || (reinterpret_cast<uintptr_t>(prev_path) & 3u)))
+    return GDN_TREE_EINVAL;
+  const void* small[] = {prev_parent, commit_status, verify_status};
+  for (const void* p : small)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u)) return GDN_TREE_EINVAL;
+  const size_t sbytes = (size_t)dims.B * dims.Hv * dims.dk * dims.dv * sizeof(float);
+  const char* a0 = reinterpret_cast<const char*>(S_prev);
+  const char* a1 = reinterpret_cast<const char*>(S1);
+  if (a0 != a1 && a0 < a1 + sbytes && a1 < a0 + sbytes) return GDN_TREE_EINVAL;
+  gdn::CommitVerifyArgs a{prev_path, prev_path_len, prev_parent, prev_U, prev_k, prev_log_alpha,
+                          prev_N, Lmax, S_prev, S1, commit_status,
+                          gdn::VerifyArgs{q, k, v, log_alpha, beta, parent, S1, o, U, dims,
+                                          verify_status}};
+  const cudaError_t err = gdn::launch_commit_verify(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
 

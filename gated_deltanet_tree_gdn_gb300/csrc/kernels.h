@@ -35,6 +35,20 @@ struct CommitArgs {
   int32_t* dev_status;
 };
 
+// delayed commitment of the previous tree's accepted path fused with the
+// verification of the next tree (the next tree is verified from S1)
+struct CommitVerifyArgs {
+  const int32_t *prev_path, *prev_path_len, *prev_parent;
+  const float* prev_U;
+  const void* prev_k;
+  const float* prev_log_alpha;
+  int32_t prev_N, Lmax;
+  const float* S_prev;
+  float* S1;
+  int32_t* commit_status;
+  VerifyArgs verify;  // verify.S0 is ignored (the state is S1)
+};
+
 // picks the kernel for the shape and dtype
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);
 
@@ -45,5 +59,9 @@ bool verify_tc_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+
+bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N);
+cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stream);
+cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream);
 
 }  // namespace gdn

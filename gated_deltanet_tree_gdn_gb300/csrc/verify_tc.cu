@@ -53,6 +53,7 @@ constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384, kColY
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kIssuer = 128;  // the one thread that issues every MMA (warp 4, lane 0)
 constexpr int kS0BoxRows = 32;  // S0 arrives as four 32-row boxes
+constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
 constexpr uint32_t kSpinLimit = 1u << 24;  // bounded wait on a solve ready flag
 
 #ifdef GDN_TC_PROFILE
@@ -82,9 +83,11 @@ constexpr uint32_t OFF_X = 2 * kOpBytes;      // ... X (packed lower triangle, f
 constexpr uint32_t OFF_UTH = 2 * kOpBytes;    // ... and, after the solve, U^T (hi, lo) over X
 constexpr uint32_t OFF_UTL = 3 * kOpBytes;
 constexpr uint32_t OFF_U = 4 * kOpBytes;      // raw S0 (TMA), then R / U, fp32, 64 KB
+constexpr uint32_t OFF_CK = 2 * kOpBytes;     // fused commit: k rows of the path, before S0^T
+constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;  // ... and their U rows
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth] -> ancestor
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
-constexpr uint32_t kSmallBytes = 8192;
+constexpr uint32_t kSmallBytes = 11264;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 4 <= 2 * kOpBytes, "X must fit in the S0^T region");
@@ -108,7 +111,14 @@ struct Small {
   int max_depth;
   int err;
   int bad;  // the tree failed validation
-  int issued;  // bit 0: Gram MMAs, bit 1: K S0 / Q S0 MMAs, bit 2: Y U MMAs
+  int issued;
+  // fused delayed commitment of the previous tree's accepted path
+  int cpath[kMaxN];
+  float cla[kMaxN];
+  float cw[kMaxN];
+  float cgamma;
+  int cL;
+  int cbad;  // bit 0: Gram MMAs, bit 1: K S0 / Q S0 MMAs, bit 2: Y U MMAs
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
 
@@ -161,13 +171,178 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// previous tree's accepted path for the fused delayed commitment
+struct FusedCommit {
+  const int32_t* path;      // [B, Lmax]
+  const int32_t* path_len;  // [B]
+  const int32_t* parent;    // [B, N] or NULL
+  const float* U;           // [B, Hv, N, dv]
+  const __nv_bfloat16* k;   // [B, N, Hqk, dk]
+  const float* log_alpha;   // [B, N, Hv]
+  int32_t N, Lmax;
+  float* S1;                // [B, Hv, dk, dv] committed state (may alias the input state)
+  int32_t* status;          // [B] or NULL
+};
+
+
+// reduction barrier over the first kCount threads (named barrier kId): OR of v
+template <int kId, int kCount>
+__device__ __forceinline__ int bar_or(int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.b32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v), "n"(kId), "n"(kCount)
+      : "memory");
+  return r;
+}
+
+// k and U rows of path entries j0 .. j0+nj-1 of the previous tree into the
+// staging area as fp32; items i0, i0 + stride, ... of the calling group
+__device__ __forceinline__ void commit_stage_rows(const FusedCommit& fc, const Small& S,
+                                                  uint8_t* smem, int b, int h, int hq, int Hqk,
+                                                  int Hv, int j0, int nj, int i0, int stride) {
+  float* sk = reinterpret_cast<float*>(smem + OFF_CK);  // [kCommitChunk][kD]
+  float* su = reinterpret_cast<float*>(smem + OFF_CU);  // [kCommitChunk][kD]
+  for (int e = i0; e < nj * (kD / 8); e += stride) {
+    const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
+    const uint4 raw = *reinterpret_cast<const uint4*>(
+        fc.k + (((size_t)b * fc.N + S.cpath[j0 + jj]) * Hqk + hq) * kD + c);
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    float* dst = sk + jj * kD + c;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      dst[2 * q] = __uint_as_float(w4[q] << 16);
+      dst[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+    }
+  }
+  for (int e = i0; e < nj * (kD / 4); e += stride) {
+    const int jj = e / (kD / 4), c = (e % (kD / 4)) * 4;
+    *reinterpret_cast<float4*>(su + jj * kD + c) = *reinterpret_cast<const float4*>(
+        fc.U + (((size_t)b * Hv + h) * fc.N + S.cpath[j0 + jj]) * kD + c);
+  }
+}
+
+// w_j = exp(G_L - G_j) and gamma_L = exp(G_L) along the committed path, with
+// G_j the inclusive double-float prefix sums of log alpha; one warp
+__device__ __forceinline__ void commit_weights(Small& S, int L, int lane) {
+  df loc[8];
+  df run = {0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int j = lane * 8 + e;
+    run = df_add(run, df{j < L ? S.cla[j] : 0.f, 0.f});
+    loc[e] = run;
+  }
+  df pre = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    df up;
+    up.hi = __shfl_up_sync(0xffffffffu, pre.hi, o);
+    up.lo = __shfl_up_sync(0xffffffffu, pre.lo, o);
+    if (lane >= o) pre = df_add(pre, up);
+  }
+  df excl;
+  excl.hi = __shfl_up_sync(0xffffffffu, pre.hi, 1);
+  excl.lo = __shfl_up_sync(0xffffffffu, pre.lo, 1);
+  if (lane == 0) excl = df{0.f, 0.f};
+  df G[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) G[e] = df_add(excl, loc[e]);
+  const int owner = L > 0 ? (L - 1) >> 3 : 0, slot = L > 0 ? (L - 1) & 7 : 0;
+  df mine = G[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e)
+    if (e == slot) mine = G[e];
+  df GL;
+  GL.hi = __shfl_sync(0xffffffffu, mine.hi, owner);
+  GL.lo = __shfl_sync(0xffffffffu, mine.lo, owner);
+  if (L == 0) GL = df{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int j = lane * 8 + e;
+    if (j < L) S.cw[j] = expf(df_diff(GL, G[e]));
+  }
+  if (lane == 0) S.cgamma = expf(df_value(GL));
+}
+
+// K_P^T diag(w) U_P for this thread's 8x4 tile of the state (rows r8*8 .., columns
+// c4*4 ..); needs no state, so it runs while the state is still in flight
+__device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const Small& S,
+                                                  uint8_t* smem, int b, int h, int hq, int Hqk,
+                                                  int Hv, int tid, float (&acc)[8][4]) {
+  const int L = S.cL;
+  const int r8 = tid / 32, c4 = tid % 32;
+  const float* sk = reinterpret_cast<const float*>(smem + OFF_CK);
+  const float* su = reinterpret_cast<const float*>(smem + OFF_CU);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int j0 = 0; j0 < L; j0 += kCommitChunk) {
+    const int nj = min(kCommitChunk, L - j0);
+    if (j0 > 0) {  // the first chunk was staged while the state was in flight
+      __syncthreads();
+      commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, j0, nj, tid, kThreads);
+      __syncthreads();
+    }
+    for (int jj = 0; jj < nj; ++jj) {
+      const float w = S.cw[j0 + jj];
+      const float4 k0 = *reinterpret_cast<const float4*>(sk + jj * kD + r8 * 8);
+      const float4 k1 = *reinterpret_cast<const float4*>(sk + jj * kD + r8 * 8 + 4);
+      const float4 uu = *reinterpret_cast<const float4*>(su + jj * kD + c4 * 4);
+      const float kk[8] = {w * k0.x, w * k0.y, w * k0.z, w * k0.w,
+                           w * k1.x, w * k1.y, w * k1.z, w * k1.w};
+      const float ul[4] = {uu.x, uu.y, uu.z, uu.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(kk[i], ul[j], acc[i][j]);
+    }
+  }
+}
+
+// S1 = gamma S0 + acc on the raw fp32 state tile in shared memory (updated in
+// place: it is the state the next tree is verified from), then stored to fc.S1
+// as one bulk copy; all threads of the CTA
+__device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S, float* tile,
+                                              int b, int h, int Hv, int tid,
+                                              const float (&acc)[8][4]) {
+  const int r8 = tid / 32, c4 = tid % 32;
+  const float gamma = S.cgamma;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = r8 * 8 + i;
+    float4* cell = reinterpret_cast<float4*>(tile + row * kD + c4 * 4);
+    const float4 s0 = *cell;
+    float4 s1;
+    s1.x = fmaf(gamma, s0.x, acc[i][0]);
+    s1.y = fmaf(gamma, s0.y, acc[i][1]);
+    s1.z = fmaf(gamma, s0.z, acc[i][2]);
+    s1.w = fmaf(gamma, s0.w, acc[i][3]);
+    *cell = s1;
+  }
+  fence_proxy_async_smem();
+  __syncthreads();  // the committed state is in place before S0^T is formed from it
+  // the tile goes back to S1 as one bulk store; thread 0 waits for it to finish
+  // reading the tile before that region is reused
+  if (tid == 0) {
+    bulk_store(fc.S1 + ((size_t)b * Hv + h) * kD * kD, tile, kD * kD * 4);
+    bulk_commit_group();
+  }
+}
+
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmS,
                  const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
                  const float* __restrict__ beta, const int32_t* __restrict__ parent,
                  __nv_bfloat16* __restrict__ o, float* __restrict__ U, gdn_tree_dims d,
-                 int32_t* dev_status) {
+                 int32_t* dev_status, FusedCommit fc) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -319,6 +494,34 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         S.issued |= 1;
       }
     }
+    if constexpr (kFused) {
+      // previous tree's accepted path: range check, chain check, log alpha, and the
+      // first chunk of its k / U rows, staged where S0^T will go (still free)
+      const int ot = tid - 128;
+      const int L = fc.path_len[b];
+      int pj = -1;
+      if (ot < fc.Lmax) pj = fc.path[(size_t)b * fc.Lmax + ot];
+      int cbad = (L < 0 || L > fc.N || L > fc.Lmax);
+      if (!cbad && ot < L) {
+        cbad |= (pj < 0 || pj >= fc.N);
+        S.cpath[ot] = pj;
+      }
+      cbad = bar_or<2, kThreads - 128>(cbad);
+      if (!cbad && ot < L) {
+        const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
+        cbad |= (ot > 0 && pj <= prev);
+        if (fc.parent) cbad |= (fc.parent[(size_t)b * fc.N + pj] != prev);
+        S.cla[ot] = fc.log_alpha[((size_t)b * fc.N + pj) * Hv + h];
+      }
+      if (!cbad)
+        commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 128);
+      cbad = bar_or<2, kThreads - 128>(cbad);
+      if (ot == 0) {
+        S.cbad = cbad;
+        S.cL = L;
+      }
+      if (!cbad && warp == 4) commit_weights(S, L, lane);
+    }
   }
   // ---- 1. both groups: S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the
   //         raw S0 tile; the hi half first, so that K S0_hi and Q S0_hi can run on
@@ -328,7 +531,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   __syncthreads();  // barriers initialised, TMEM allocated, tree group done
   tc_fence_after_sync();
   const uint32_t tmem = S.tmem_base;
+  uint4 vreg[4];  // this thread's 32 values of v (row t, columns 32 cq ..), loaded below
+  float cacc[8][4];  // fused commit: this thread's part of K_P^T diag(w) U_P
+  if constexpr (kFused) {
+    if (!S.cbad) commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, cacc);
+  }
   if (!mbar_wait(&S.bar_s0, 0, kWaitLimitNs)) S.err = 1;
+  if constexpr (kFused) {
+    // delayed commitment: S1 = gamma S0 + K_P^T diag(w) U_P over the raw state tile,
+    // written back in place (it is the state this tree is verified from) and to S1
+    if (h == 0 && tid == 0 && fc.status)
+      fc.status[b] = S.cbad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
+    if (S.cbad) {
+      if (h == 0 && tid == 0 && dev_status) dev_status[b] = GDN_TREE_STATUS_BAD_PATH;
+      goto drain;
+    }
+    if (!S.err) commit_finish(fc, S, sU, b, h, Hv, tid, cacc);
+  }
   TC_MARK(2);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
@@ -362,9 +581,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
     }
   }
-  // this thread's 32 values of v (row t, columns 32 cq ..), kept in registers
-  uint4 vreg[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                   make_uint4(0, 0, 0, 0)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vreg[i] = make_uint4(0, 0, 0, 0);
   if (live) {
     const uint4* vrow =
         reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
@@ -406,6 +624,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     //         and Y (hi, lo) to shared memory -------------------------------------------
     if (!mbar_wait(&S.bar_ks, 0, kWaitLimitNs)) S.err = 2;
     tc_fence_after_sync();
+    if constexpr (kFused) {
+      if (tid == 0) bulk_wait_read_all();  // the S1 store has read the tile R goes into
+    }
     if (__syncthreads_or(S.err)) goto fail;
     TC_MARK(5);
     {
@@ -615,6 +836,9 @@ drain:
   }
 
 release:
+  if constexpr (kFused) {
+    if (tid == 0) bulk_wait_all();  // the S1 store is complete before the CTA leaves
+  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
@@ -671,18 +895,40 @@ bool verify_tc_supported(const gdn_tree_dims& d) {
          tensor_map_encoder() != nullptr;
 }
 
-cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
+namespace {
+
+template <bool kFused>
+cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
   CUtensorMap tmQ, tmK, tmS;
   if (!encode_qk_map(&tmQ, a.q, a.d) || !encode_qk_map(&tmK, a.k, a.d) ||
       !encode_state_map(&tmS, a.S0, a.d))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel,
+  cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-  verify_tc_kernel<<<dim3(a.d.Hv, a.d.B), kThreads, kSmemBytes, stream>>>(
+  verify_tc_kernel<kFused><<<dim3(a.d.Hv, a.d.B), kThreads, kSmemBytes, stream>>>(
       tmQ, tmK, tmS, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status);
+      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, fc);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
+  return launch_tc<false>(a, FusedCommit{}, stream);
+}
+
+bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N) {
+  return verify_tc_supported(d) && prev_N >= 1 && prev_N <= kMaxN;
+}
+
+cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stream) {
+  FusedCommit fc{a.prev_path, a.prev_path_len, a.prev_parent, a.prev_U,
+                 static_cast<const __nv_bfloat16*>(a.prev_k), a.prev_log_alpha, a.prev_N,
+                 a.Lmax, a.S1, a.commit_status};
+  VerifyArgs v = a.verify;
+  v.S0 = a.S_prev;  // the kernel loads the previous state and commits it on chip
+  return launch_tc<true>(v, fc, stream);
 }
 
 }  // namespace gdn

@@ -123,6 +123,42 @@ int gdn_tree_commit(const int32_t *path, const int32_t *path_len,
                     gdn_tree_dims dims, int32_t Lmax, int32_t *dev_status,
                     void *stream);
 
+/*
+ * gdn_tree_commit_verify -- one decoding iteration: the delayed commitment of
+ * the previous tree's accepted path, fused with the verification of the next
+ * tree from the state it produces.
+ *
+ * The DFlash-TfM page, section 3, commits the state "at the next decoding
+ * iteration, once the accepted branch is known"; this call is that iteration.
+ * It equals gdn_tree_commit(prev_path, prev_path_len, prev_parent, prev_U,
+ * prev_k, prev_log_alpha, S_prev -> S1) followed by gdn_tree_verify(q, k, v,
+ * log_alpha, beta, parent, S1 -> o, U), but the state is read once and
+ * written once (the tensor-core path commits it on chip).
+ *
+ *   prev_*          the previous tree (prev_N nodes): its accepted path
+ *                   [B, Lmax] / [B], optional parent [B, prev_N], the U rows
+ *                   verify wrote [B, Hv, prev_N, dv], its k [B, prev_N, Hqk, dk]
+ *                   and log_alpha [B, prev_N, Hv]
+ *   S_prev -> S1    [B, Hv, dk, dv] fp32; S1 may alias S_prev exactly
+ *   q .. parent     the next tree, shapes as for gdn_tree_verify (dims.N nodes)
+ *   o, U            its outputs; U may alias prev_U exactly (each (b, h) slice
+ *                   is read before it is written)
+ *   commit_status   [B] or NULL: as gdn_tree_commit's dev_status
+ *   verify_status   [B] or NULL: as gdn_tree_verify's dev_status (the fused
+ *                   path also sets GDN_TREE_STATUS_BAD_PATH when the commit of
+ *                   that sequence failed).  Whenever commit_status reports an
+ *                   error, that sequence's S1, o and U are unspecified.
+ * Limits as for the two calls; 1 <= prev_N <= 256; prev_k has the dtype of q.
+ */
+int gdn_tree_commit_verify(const int32_t *prev_path, const int32_t *prev_path_len,
+                           const int32_t *prev_parent, const float *prev_U,
+                           const void *prev_k, const float *prev_log_alpha,
+                           int32_t prev_N, int32_t Lmax, const float *S_prev, float *S1,
+                           const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta,
+                           const int32_t *parent, void *o, float *U, gdn_tree_dims dims,
+                           int32_t *commit_status, int32_t *verify_status, void *stream);
+
 /* Human-readable text for a return code or a device status code. */
 const char *gdn_tree_strerror(int code);
 

@@ -1,0 +1,113 @@
+"""GPU parity of one decoding iteration, gdn_tree_commit_verify: the delayed
+commitment of the previous tree's accepted path fused with the verification
+of the next tree.  Checked against the oracle (commit of the previous path by
+the recurrence, then verification of the next tree from that state) and
+against the two separate calls, on the tensor-core path and the two-launch
+fallback."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    import gated_deltanet_tree_gdn_gb300 as gt
+    gt.build_library()
+    gt.load()
+
+
+def _pair(seed, B, Np, N, Hqk, Hv, d, dtype, tree="random"):
+    prev = W.make_custom(seed=seed, B=B, N=Np, Hqk=Hqk, Hv=Hv, dk=d, dv=d, dtype=dtype,
+                         tree=tree, max_depth=24)
+    nxt = W.make_custom(seed=seed + 1, B=B, N=N, Hqk=Hqk, Hv=Hv, dk=d, dv=d, dtype=dtype,
+                        tree="mixed", max_depth=24)
+    return prev, nxt
+
+
+def _run(prev, nxt, inplace=False):
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    xp, xn = H.to_device(prev), H.to_device(nxt)
+    _, U_prev = gt.verify(xp["q"], xp["k"], xp["v"], xp["log_alpha"], xp["beta"], xp["parent"],
+                          xp["S0"])
+    # separate calls
+    S1_sep = gt.commit(xp["path"], xp["path_len"], U_prev, xp["k"], xp["log_alpha"], xp["S0"],
+                       parent=xp["parent"])
+    o_sep, U_sep = gt.verify(xn["q"], xn["k"], xn["v"], xn["log_alpha"], xn["beta"],
+                             xn["parent"], S1_sep)
+    # fused
+    cs = torch.full((prev.B,), -7, dtype=torch.int32, device="cuda")
+    vs = torch.full((prev.B,), -7, dtype=torch.int32, device="cuda")
+    S_prev = xp["S0"].clone()
+    U_buf = U_prev.clone() if inplace and prev.N == nxt.N else None
+    S1, o, U = gt.commit_verify(xp["path"], xp["path_len"], U_prev if U_buf is None else U_buf,
+                                xp["k"], xp["log_alpha"], S_prev, xn["q"], xn["k"], xn["v"],
+                                xn["log_alpha"], xn["beta"], xn["parent"],
+                                S1=S_prev if inplace else None, prev_parent=xp["parent"],
+                                U=U_buf, commit_status=cs, verify_status=vs)
+    torch.cuda.synchronize()
+    return dict(S1=S1.cpu().numpy(), o=o.float().cpu().numpy(), U=U.cpu().numpy(),
+                cs=cs.cpu().numpy(), vs=vs.cpu().numpy(), S1_sep=S1_sep.cpu().numpy(),
+                o_sep=o_sep.float().cpu().numpy(), U_sep=U_sep.cpu().numpy())
+
+
+def _oracle(prev, nxt):
+    S1 = oracle.commit_workload(prev)
+    o, U = oracle.verify(nxt.q, nxt.k, nxt.v, nxt.log_alpha, nxt.beta, nxt.parent, S1)
+    return S1, o, U
+
+
+CASES = [
+    # (B, prev N, next N, Hqk, Hv, d, dtype, prev tree)
+    (4, 128, 128, 2, 4, 128, W.BF16, "random"),   # tensor-core fused path
+    (3, 100, 64, 1, 2, 128, W.BF16, "chain"),     # long paths (> one staging chunk)
+    (2, 200, 90, 1, 2, 128, W.BF16, "random"),    # previous tree larger than a tile
+    (2, 48, 40, 1, 2, 64, W.BF16, "mixed"),       # fallback: two launches
+    (2, 20, 24, 1, 1, 32, W.F32, "uniform"),      # fallback, fp32
+]
+
+
+@pytest.mark.parametrize("idx", range(len(CASES)), ids=["x".join(map(str, c)) for c in CASES])
+def test_commit_verify_matches_oracle_and_separate_calls(idx):
+    B, Np, N, Hqk, Hv, d, dt, tree = CASES[idx]
+    prev, nxt = _pair(300 + idx, B, Np, N, Hqk, Hv, d, dt, tree)
+    g = _run(prev, nxt)
+    assert (g["cs"] == 0).all() and (g["vs"] == 0).all()
+    S1_ref, o_ref, U_ref = _oracle(prev, nxt)
+    assert H.rel_err(g["S1"], S1_ref) <= H.TOL_S1
+    assert H.rel_err(g["U"], U_ref) <= H.TOL_U
+    assert H.rel_err(g["o"], o_ref) <= H.TOL_O[dt]
+    # and it is the same computation as the two calls
+    assert H.rel_err(g["S1"], g["S1_sep"]) <= 1e-6
+    assert H.rel_err(g["U"], g["U_sep"]) <= 1e-5
+    assert H.rel_err(g["o"], g["o_sep"]) <= 1e-2
+
+
+def test_commit_verify_in_place_buffers():
+    prev, nxt = _pair(400, 3, 96, 96, 1, 2, 128, W.BF16)
+    g = _run(prev, nxt, inplace=True)
+    S1_ref, o_ref, U_ref = _oracle(prev, nxt)
+    assert H.rel_err(g["S1"], S1_ref) <= H.TOL_S1
+    assert H.rel_err(g["U"], U_ref) <= H.TOL_U
+
+
+def test_commit_verify_empty_and_invalid_paths():
+    prev, nxt = _pair(500, 3, 64, 64, 1, 2, 128, W.BF16)
+    prev.path_len[0] = 0                      # empty: S1 = S_prev
+    prev.path[1, :] = -1                      # invalid: not a root chain
+    prev.path[1, 0], prev.path[1, 1] = 5, 3
+    prev.path_len[1] = 2
+    g = _run(prev, nxt)
+    assert g["cs"].tolist()[0] == 0 and g["cs"].tolist()[1] == 2 and g["cs"].tolist()[2] == 0
+    assert g["vs"].tolist()[1] == 2
+    assert np.array_equal(g["S1"][0], prev.S0[0])
+    S1_ref = oracle.commit(prev.path[[0, 2]], prev.path_len[[0, 2]], prev.k[[0, 2]],
+                           prev.v[[0, 2]], prev.log_alpha[[0, 2]], prev.beta[[0, 2]],
+                           prev.S0[[0, 2]])
+    assert H.rel_err(g["S1"][[0, 2]], S1_ref) <= H.TOL_S1
