@@ -11,26 +11,29 @@
 // substitution and applies the output stage in one pass; this kernel does the
 // same in one launch, laid out for Blackwell:
 //
-//   one CTA (256 threads) per (sequence b, v-head h); 512 TMEM columns.
-//   1. TMA (128-byte swizzle) brings K and Q of the q/k head into shared
-//      memory; threads turn S0 (fp32) into S0^T = hi + lo, two bf16 K-major
-//      tiles, so K S0 keeps fp32 accuracy (K is exact in bf16).
+//   a persistent grid, one CTA (512 threads, 512 TMEM columns) per SM, walks the
+//   (sequence b, v-head h) units; the next unit's operands are already being
+//   loaded while the current unit finishes.  Per unit:
+//   1. TMA (128-byte swizzle) brings K and Q of the q/k head and the fp32 state;
+//      threads turn S0 into S0^T = hi + lo, two bf16 K-major tiles, so K S0
+//      keeps fp32 accuracy (K is exact in bf16).
 //   2. tcgen05.mma, accumulators in TMEM:  G_kk = K K^T, G_qk = Q K^T,
 //      KS = K S0_hi + K S0_lo, QS = Q S0_hi.
-//   3. TMEM -> registers (thread = tree node): X (masked, decay-weighted,
-//      fp32) and R = beta (V - gamma KS) to shared memory.
-//   4. forward substitution over tree depth levels (nodes of one depth are
-//      independent): fp32 FMA, warp per node, lane per 4 value columns.
-//   5. Y (from G_qk) and U^T go to shared memory as bf16 hi + lo pairs;
-//      tcgen05.mma computes Y U in three passes (hi*hi + hi*lo + lo*hi).
-//   6. O = gamma QS + Y U from TMEM, stored as bf16; U stored as fp32.
+//   3. TMEM -> registers (thread = tree node): the X and Y entries of the node's
+//      ancestors (masked, decay-weighted, fp32), R = beta (V - gamma KS) and the
+//      output seed gamma QS go to shared memory.
+//   4. forward substitution as a dataflow over the tree, a warp per node and a
+//      lane per 4 value columns: u_t = r_t - sum_a X[t,a] u_a, and in the same
+//      walk over t's path o_t = gamma_t (Q S0)_t + sum_s Y[t,s] u_s, both fp32;
+//      u_t and o_t are stored straight from the solve.
 //
-// Precision: K S0 and the solve are fp32-accurate (U feeds the commit's 1e-4
-// bound); Q S0 uses S0_hi only and Y U the three-pass split, both ample for
-// the bf16 output.  Waits are bounded; a timeout reports a device status.
+// Precision: K S0, the solve and Y U are fp32-accurate (U feeds the commit's
+// 1e-4 bound); Q S0 uses S0_hi only, ample for the bf16 output.  Waits are
+// bounded; a timeout reports a device status.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -49,20 +52,19 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kW = kTile / 32;     // ancestor bitset words per node
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384, kColYU = 0;
+constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kIssuer = 128;  // the one thread that issues every MMA (warp 4, lane 0)
-constexpr int kS0BoxRows = 32;  // S0 arrives as four 32-row boxes
+constexpr int kIssuer = 128;  // the one thread that issues every copy and MMA (warp 4, lane 0)
+constexpr int kS0BoxRows = 32;  // the state arrives as four 32-row boxes
 constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
 constexpr uint32_t kSpinLimit = 1u << 24;  // bounded wait on a solve ready flag
 
 #ifdef GDN_TC_PROFILE
-// per-CTA phase timestamps for a profiling build (never in the product build)
+// per-unit phase timestamps for a profiling build (never in the product build)
 __device__ unsigned long long g_tc_phase[4096][16];
-#define TC_MARK(i)                                                                   \
-  do {                                                                               \
-    if (threadIdx.x == 0 && blockIdx.y * gridDim.x + blockIdx.x < 4096)              \
-      g_tc_phase[blockIdx.y * gridDim.x + blockIdx.x][i] = globaltimer_ns();         \
+#define TC_MARK(i)                                                               \
+  do {                                                                           \
+    if (threadIdx.x == 0 && unit < 4096) g_tc_phase[unit][i] = globaltimer_ns(); \
   } while (0)
 #else
 #define TC_MARK(i) \
@@ -70,55 +72,57 @@ __device__ unsigned long long g_tc_phase[4096][16];
   } while (0)
 #endif
 
-// shared memory map (byte offsets from a 1024-aligned base)
+// shared memory map (byte offsets from a 1024-aligned base); three 64 KB regions
+// change roles within a unit
 constexpr uint32_t kTileBytes = 128 * 128;            // one 64-wide K block: 128 rows x 128 B
 constexpr uint32_t kOpBytes = 2 * kTileBytes;         // a 128 x 128 bf16 operand (2 K blocks)
-constexpr uint32_t OFF_K = 0;                 // K, Q, S0^T: live until the K S0 / Q S0 MMAs end
+// region 1: K, Q (TMA) until the MMAs that read them end; then X, Y
+constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = 1 * kOpBytes;
+constexpr uint32_t OFF_XY = 0;
+// region 2: the fused commit's staged path rows; S0^T hi, lo until the K S0 / Q S0
+// MMAs end; then the output rows (seeded with gamma Q S0, finished by the solve)
+constexpr uint32_t OFF_CK = 2 * kOpBytes;
+constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;
 constexpr uint32_t OFF_S0H = 2 * kOpBytes;
 constexpr uint32_t OFF_S0L = 3 * kOpBytes;
-constexpr uint32_t OFF_YH = 0;                // then Y (hi, lo) over K, Q ...
-constexpr uint32_t OFF_YL = 1 * kOpBytes;
-constexpr uint32_t OFF_X = 2 * kOpBytes;      // ... X (packed lower triangle, fp32) over S0^T
-constexpr uint32_t OFF_UTH = 2 * kOpBytes;    // ... and, after the solve, U^T (hi, lo) over X
-constexpr uint32_t OFF_UTL = 3 * kOpBytes;
-constexpr uint32_t OFF_U = 4 * kOpBytes;      // raw S0 (TMA), then R / U, fp32, 64 KB
-constexpr uint32_t OFF_CK = 2 * kOpBytes;     // fused commit: k rows of the path, before S0^T
-constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;  // ... and their U rows
-constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth] -> ancestor
+constexpr uint32_t OFF_P = 2 * kOpBytes;
+// region 3: the raw fp32 state (TMA) until S0^T is formed; then R / U
+constexpr uint32_t OFF_U = 4 * kOpBytes;
+constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
 constexpr uint32_t kSmallBytes = 11264;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
-static_assert(kTile * (kTile - 1) / 2 * 4 <= 2 * kOpBytes, "X must fit in the S0^T region");
+static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
+static_assert(2 * kCommitChunk * kD * 4 <= 2 * kOpBytes, "commit staging must fit in region 2");
 static_assert(OFF_U % 1024 == 0 && OFF_SMALL % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Small {
   int parent[kTile];
-  int jump[kTile];
   df g[kTile];
   float beta[kTile];
   float la[kTile];
+  float ydiag[kTile];  // Y[t,t] = q_t . k_t
   uint32_t anc[kTile * kW];
   int order[kTile];
   int depth[kTile];
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
   int ready[kTile];  // solve: node's u is final
-  uint64_t bar_kq, bar_s0, bar_g, bar_ks, bar_yu;
+  uint64_t bar_kq, bar_s0, bar_g, bar_ks;
   uint32_t tmem_base;
-  int max_depth;
   int err;
   int bad;  // the tree failed validation
-  int issued;
+  int n_loads, n_g, n_ks;  // phases issued on bar_kq / bar_s0, bar_g, bar_ks
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
   float cla[kMaxN];
   float cw[kMaxN];
   float cgamma;
   int cL;
-  int cbad;  // bit 0: Gram MMAs, bit 1: K S0 / Q S0 MMAs, bit 2: Y U MMAs
+  int cbad;
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
 
@@ -129,11 +133,12 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int k8) {
   return (uint32_t)(kb * kTileBytes + row * 128 + ((j ^ (row & 7)) << 4));
 }
 
-// fp32 R/U tile: row t, 4-float chunk c4 (0..31), chunk index xor-swizzled by
-// the row so that row-per-thread float4 accesses are bank-conflict free
+// fp32 128 x 128 row tiles (R / U, output rows): row t, 4-float chunk c4 (0..31),
+// chunk index xor-swizzled by the row so that row-per-thread float4 accesses
+// are bank-conflict free
 __device__ __forceinline__ int u_index(int t, int c4) { return t * kD + ((c4 ^ (t & 7)) << 2); }
 
-// packed strictly-lower triangle of X
+// packed strictly-lower triangle of X and Y
 __device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
 
 // (a, b) -> bf16x2 hi parts and bf16x2 lo parts (x = hi + lo to ~2^-17)
@@ -148,6 +153,14 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 __device__ __forceinline__ uint32_t pack2f(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
+  acc.x = fmaf(a, x.x, acc.x);
+  acc.y = fmaf(a, x.y, acc.y);
+  acc.z = fmaf(a, x.z, acc.z);
+  acc.w = fmaf(a, x.w, acc.w);
+  return acc;
 }
 
 // issue the 8 K-steps (K = 128) of D (+)= A B^T for two 128x128 K-major tiles
@@ -184,7 +197,6 @@ struct FusedCommit {
   int32_t* status;          // [B] or NULL
 };
 
-
 // reduction barrier over the first kCount threads (named barrier kId): OR of v
 template <int kId, int kCount>
 __device__ __forceinline__ int bar_or(int v) {
@@ -198,6 +210,104 @@ __device__ __forceinline__ int bar_or(int v) {
       : "r"(v), "n"(kId), "n"(kCount)
       : "memory");
   return r;
+}
+
+// K and Q of the unit's q/k head into region 1 (bar_kq), its fp32 state into
+// region 3 (bar_s0); issuing thread only
+__device__ __forceinline__ void issue_loads(Small& S, uint8_t* smem, const CUtensorMap* tmK,
+                                            const CUtensorMap* tmQ, const CUtensorMap* tmS,
+                                            int unit, int Hv, int Hqk) {
+  const int b = unit / Hv, h = unit - b * Hv, hq = h / (Hv / Hqk);
+  mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
+  tma_load_4d(smem + OFF_K, tmK, &S.bar_kq, 0, hq, 0, b);
+  tma_load_4d(smem + OFF_K + kTileBytes, tmK, &S.bar_kq, 64, hq, 0, b);
+  tma_load_4d(smem + OFF_Q, tmQ, &S.bar_kq, 0, hq, 0, b);
+  tma_load_4d(smem + OFF_Q + kTileBytes, tmQ, &S.bar_kq, 64, hq, 0, b);
+  mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
+#pragma unroll
+  for (int r = 0; r < kD; r += kS0BoxRows)  // four boxes land in parallel
+    tma_load_3d(smem + OFF_U + r * kD * 4, tmS, &S.bar_s0, 0, r, unit);
+  ++S.n_loads;
+}
+
+// Tree group (threads 0..127): loads the unit's tree and gates, validates the
+// tree, then one upward walk per node gives its depth, its path log-decay g_t
+// (double-float), its strict-ancestor bitset and its path (sPath row, root
+// first); finally the nodes are ordered by depth.  An invalid tree is replaced
+// by all-roots (nothing of it is stored).
+__device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_t* parent,
+                                          const float* beta, const float* log_alpha, int b,
+                                          int h, int N, int Hv, int tid, int lane, int warp) {
+  using TreeSync = NamedSync<1, 128>;
+  int p_in = -1;
+  float be_in = 0.f, la_in = 0.f;
+  if (tid < N) {
+    p_in = parent[(size_t)b * N + tid];
+    be_in = beta[((size_t)b * N + tid) * Hv + h];
+    la_in = log_alpha[((size_t)b * N + tid) * Hv + h];
+  }
+  S.beta[tid] = be_in;
+  S.la[tid] = la_in;
+  S.level_start[tid] = 0;
+  if (tid < 2) S.level_start[kTile + tid] = 0;
+  const int bad_any = bar_or<1, 128>(tid < N && (p_in < -1 || p_in >= tid));
+  S.parent[tid] = bad_any ? -1 : p_in;
+  if (tid == 0) S.bad = bad_any;
+  TreeSync()();
+  int dep = 0;
+  if (tid < N) {
+    df g = {0.f, 0.f};
+    uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
+    for (int s = tid; s >= 0; s = S.parent[s]) {
+      g = df_add(g, df{S.la[s], 0.f});
+      const uint32_t bit = (s != tid) ? 1u << (s & 31) : 0u;
+      const int w = s >> 5;
+      a0 |= w == 0 ? bit : 0u;
+      a1 |= w == 1 ? bit : 0u;
+      a2 |= w == 2 ? bit : 0u;
+      a3 |= w == 3 ? bit : 0u;
+      ++dep;
+    }
+    S.g[tid] = g;
+    S.anc[tid * kW + 0] = a0;
+    S.anc[tid * kW + 1] = a1;
+    S.anc[tid * kW + 2] = a2;
+    S.anc[tid * kW + 3] = a3;
+    S.depth[tid] = dep;
+    // path: sPath[t * 128 + depth(s) - 1] = s for every s on t's path
+    int ds = dep - 1;
+    for (int s = tid; s >= 0; s = S.parent[s]) sPath[tid * kTile + ds--] = (uint8_t)s;
+    atomicAdd(&S.level_start[dep], 1);
+  }
+  TreeSync()();
+  if (warp == 0) {
+    // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
+    int cnt[5], run = 0;
+#pragma unroll
+    for (int e = 0; e < 5; ++e) {
+      const int l = lane * 5 + e;
+      cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
+      run += cnt[e];
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += up;
+    }
+    int excl = incl - run;
+#pragma unroll
+    for (int e = 0; e < 5; ++e) {
+      const int l = lane * 5 + e;
+      if (l < kTile + 2) {
+        S.level_start[l] = excl;
+        S.level_cursor[l] = excl;
+      }
+      excl += cnt[e];
+    }
+  }
+  TreeSync()();
+  if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
 }
 
 // k and U rows of path entries j0 .. j0+nj-1 of the previous tree into the
@@ -269,6 +379,38 @@ __device__ __forceinline__ void commit_weights(Small& S, int L, int lane) {
   if (lane == 0) S.cgamma = expf(df_value(GL));
 }
 
+// Operand group (threads 128..511, ot = tid - 128): checks the previous tree's
+// accepted path of sequence b (range, chain order, parent links), gathers its
+// log alpha, stages the first chunk of its k / U rows into region 2 and forms
+// the path weights.  Sets S.cbad, S.cL.
+__device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S, uint8_t* smem,
+                                                int b, int h, int hq, int Hqk, int Hv, int ot,
+                                                int warp, int lane) {
+  const int L = fc.path_len[b];
+  int pj = -1;
+  if (ot < fc.Lmax) pj = fc.path[(size_t)b * fc.Lmax + ot];
+  int cbad = (L < 0 || L > fc.N || L > fc.Lmax);
+  if (!cbad && ot < L) {
+    cbad |= (pj < 0 || pj >= fc.N);
+    S.cpath[ot] = pj;
+  }
+  cbad = bar_or<2, kThreads - 128>(cbad);
+  if (!cbad && ot < L) {
+    const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
+    cbad |= (ot > 0 && pj <= prev);
+    if (fc.parent) cbad |= (fc.parent[(size_t)b * fc.N + pj] != prev);
+    S.cla[ot] = fc.log_alpha[((size_t)b * fc.N + pj) * Hv + h];
+  }
+  if (!cbad)
+    commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 128);
+  cbad = bar_or<2, kThreads - 128>(cbad);
+  if (ot == 0) {
+    S.cbad = cbad;
+    S.cL = L;
+  }
+  if (!cbad && warp == 4) commit_weights(S, L, lane);
+}
+
 // K_P^T diag(w) U_P for this thread's 8x4 tile of the state (rows r8*8 .., columns
 // c4*4 ..); needs no state, so it runs while the state is still in flight
 __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const Small& S,
@@ -284,7 +426,7 @@ __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const S
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int j0 = 0; j0 < L; j0 += kCommitChunk) {
     const int nj = min(kCommitChunk, L - j0);
-    if (j0 > 0) {  // the first chunk was staged while the state was in flight
+    if (j0 > 0) {  // the first chunk was staged by the operand group
       __syncthreads();
       commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, j0, nj, tid, kThreads);
       __syncthreads();
@@ -309,8 +451,7 @@ __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const S
 // place: it is the state the next tree is verified from), then stored to fc.S1
 // as one bulk copy; all threads of the CTA
 __device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S, float* tile,
-                                              int b, int h, int Hv, int tid,
-                                              const float (&acc)[8][4]) {
+                                              int unit, int tid, const float (&acc)[8][4]) {
   const int r8 = tid / 32, c4 = tid % 32;
   const float gamma = S.cgamma;
 #pragma unroll
@@ -330,7 +471,7 @@ __device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small
   // the tile goes back to S1 as one bulk store; thread 0 waits for it to finish
   // reading the tile before that region is reused
   if (tid == 0) {
-    bulk_store(fc.S1 + ((size_t)b * Hv + h) * kD * kD, tile, kD * kD * 4);
+    bulk_store(fc.S1 + (size_t)unit * kD * kD, tile, kD * kD * 4);
     bulk_commit_group();
   }
 }
@@ -349,354 +490,235 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t sbase = smem_addr(smem);
   Small& S = *reinterpret_cast<Small*>(smem + OFF_SMALL);
   float* sU = reinterpret_cast<float*>(smem + OFF_U);
-  float* sX = reinterpret_cast<float*>(smem + OFF_X);
+  float* sP = reinterpret_cast<float*>(smem + OFF_P);
+  float2* sXY = reinterpret_cast<float2*>(smem + OFF_XY);
   uint8_t* sPath = smem + OFF_PATH;
 
   const int N = d.N, Hv = d.Hv, Hqk = d.Hqk;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int hq = h / (Hv / Hqk);
+  const int n_units = d.B * Hv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // epilogue mapping: thread <-> (tree row t, 32-column quarter cq); warp w
-  // may only touch TMEM lanes 32*(w%4) .. 32*(w%4)+31
+  // row mapping: thread <-> (tree row t, 32-column quarter cq); warp w may only
+  // touch TMEM lanes 32*(w%4) .. 32*(w%4)+31
   const int q4 = warp & 3, cq = warp >> 2;
   const int t = q4 * 32 + lane;
+  const int col0 = cq * 32;
   const bool live = t < N;
+  const uint32_t trow_off = (uint32_t)(q4 * 32) << 16;
+  int unit = blockIdx.x;
 
-  // ---- 0. two groups run side by side until the tensor cores need both:
-  //   tree group (warps 0-3): tree loads, validation, one upward walk per node
-  //     (depth, path log-decay, ancestor bitset, path table), depth order;
-  //   operand group (warps 4-15): bulk loads, TMEM, Gram MMAs, S0^T split, and
-  //     the K S0 / Q S0 MMAs as soon as S0^T is in place.
-  TC_MARK(0);
   if (tid == kIssuer) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmS);
+    mbar_init(&S.bar_kq, 1);
+    mbar_init(&S.bar_s0, 1);
+    mbar_init(&S.bar_g, 1);
+    mbar_init(&S.bar_ks, 1);
+    S.err = 0;
+    S.n_loads = 0;
+    S.n_g = 0;
+    S.n_ks = 0;
+    S.cbad = 0;
+    mbar_fence_init();
+    if (unit < n_units) issue_loads(S, smem, &tmK, &tmQ, &tmS, unit, Hv, Hqk);
   }
-  if (warp < 4) {
-    using TreeSync = NamedSync<1, 128>;
-    int p_in = -1;
-    float be_in = 0.f, la_in = 0.f;
-    if (tid < N) {
-      p_in = parent[(size_t)b * N + tid];
-      be_in = beta[((size_t)b * N + tid) * Hv + h];
-      la_in = log_alpha[((size_t)b * N + tid) * Hv + h];
-    }
-    S.parent[tid] = p_in;
-    S.beta[tid] = be_in;
-    S.la[tid] = la_in;
-    S.level_start[tid] = 0;
-    if (tid < 2) S.level_start[kTile + tid] = 0;
-    if (tid == 0) S.max_depth = 0;
-    const int bad_me = tid < N && (p_in < -1 || p_in >= tid);
-    int bad_any;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\t"
-        "selp.b32 %0, 1, 0, q;\n\t}"
-        : "=r"(bad_any)
-        : "r"(bad_me)
-        : "memory");
-    if (tid == 0) S.bad = bad_any;
-    if (!bad_any) {
-      // walk t -> root once: depth, g_t (double-float), ancestor bits
-      int dep = 0;
-      if (tid < N) {
-        df g = {0.f, 0.f};
-        uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
-        for (int s = tid; s >= 0; s = S.parent[s]) {
-          g = df_add(g, df{S.la[s], 0.f});
-          const uint32_t bit = (s != tid) ? 1u << (s & 31) : 0u;
-          const int w = s >> 5;
-          a0 |= w == 0 ? bit : 0u;
-          a1 |= w == 1 ? bit : 0u;
-          a2 |= w == 2 ? bit : 0u;
-          a3 |= w == 3 ? bit : 0u;
-          ++dep;
-        }
-        S.g[tid] = g;
-        S.anc[tid * kW + 0] = a0;
-        S.anc[tid * kW + 1] = a1;
-        S.anc[tid * kW + 2] = a2;
-        S.anc[tid * kW + 3] = a3;
-        S.depth[tid] = dep;
-        // path table: sPath[t * 128 + depth(s)] = s for every s on t's path
-        int ds = dep;
-        for (int s = tid; s >= 0; s = S.parent[s]) sPath[tid * kTile + ds--] = (uint8_t)s;
-        atomicAdd(&S.level_start[dep], 1);
-        atomicMax(&S.max_depth, dep);
-      }
-      TreeSync()();
-      if (warp == 0) {
-        // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
-        int cnt[5], run = 0;
-#pragma unroll
-        for (int e = 0; e < 5; ++e) {
-          const int l = lane * 5 + e;
-          cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
-          run += cnt[e];
-        }
-        int incl = run;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int up = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += up;
-        }
-        int excl = incl - run;
-#pragma unroll
-        for (int e = 0; e < 5; ++e) {
-          const int l = lane * 5 + e;
-          if (l < kTile + 2) {
-            S.level_start[l] = excl;
-            S.level_cursor[l] = excl;
-          }
-          excl += cnt[e];
-        }
-      }
-      TreeSync()();
-      if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
-    }
-  } else {
-    using OperandSync = NamedSync<2, kThreads - 128>;
-    if (tid == kIssuer) {
-      mbar_init(&S.bar_kq, 1);
-      mbar_init(&S.bar_s0, 1);
-      mbar_init(&S.bar_g, 1);
-      mbar_init(&S.bar_ks, 1);
-      mbar_init(&S.bar_yu, 1);
-      S.err = 0;
-      S.issued = 0;
-      mbar_fence_init();
-      mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
-      tma_load_4d(smem + OFF_K, &tmK, &S.bar_kq, 0, hq, 0, b);
-      tma_load_4d(smem + OFF_K + kTileBytes, &tmK, &S.bar_kq, 64, hq, 0, b);
-      tma_load_4d(smem + OFF_Q, &tmQ, &S.bar_kq, 0, hq, 0, b);
-      tma_load_4d(smem + OFF_Q + kTileBytes, &tmQ, &S.bar_kq, 64, hq, 0, b);
-      mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
-#pragma unroll
-      for (int r = 0; r < kD; r += kS0BoxRows)  // four boxes land in parallel
-        tma_load_3d(smem + OFF_U + r * kD * 4, &tmS, &S.bar_s0, 0, r, b * Hv + h);
-    }
-    if (warp == 5) tmem_alloc(&S.tmem_base, kTmemCols);
-    tc_fence_before_sync();
-    OperandSync()();
-    tc_fence_after_sync();
-    const uint32_t tm = S.tmem_base;
-    if (tid == kIssuer) {
-      if (!mbar_wait(&S.bar_kq, 0, kWaitLimitNs)) {
-        S.err = 1;
-      } else {
-        tc_fence_after_sync();
-        umma_128x128x128(tm + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
-        umma_128x128x128(tm + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
-        umma_commit(&S.bar_g);
-        S.issued |= 1;
-      }
-    }
-    if constexpr (kFused) {
-      // previous tree's accepted path: range check, chain check, log alpha, and the
-      // first chunk of its k / U rows, staged where S0^T will go (still free)
-      const int ot = tid - 128;
-      const int L = fc.path_len[b];
-      int pj = -1;
-      if (ot < fc.Lmax) pj = fc.path[(size_t)b * fc.Lmax + ot];
-      int cbad = (L < 0 || L > fc.N || L > fc.Lmax);
-      if (!cbad && ot < L) {
-        cbad |= (pj < 0 || pj >= fc.N);
-        S.cpath[ot] = pj;
-      }
-      cbad = bar_or<2, kThreads - 128>(cbad);
-      if (!cbad && ot < L) {
-        const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
-        cbad |= (ot > 0 && pj <= prev);
-        if (fc.parent) cbad |= (fc.parent[(size_t)b * fc.N + pj] != prev);
-        S.cla[ot] = fc.log_alpha[((size_t)b * fc.N + pj) * Hv + h];
-      }
-      if (!cbad)
-        commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 128);
-      cbad = bar_or<2, kThreads - 128>(cbad);
-      if (ot == 0) {
-        S.cbad = cbad;
-        S.cL = L;
-      }
-      if (!cbad && warp == 4) commit_weights(S, L, lane);
-    }
-  }
-  // ---- 1. both groups: S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the
-  //         raw S0 tile; the hi half first, so that K S0_hi and Q S0_hi can run on
-  //         the tensor cores while the lo half is written --------------------------
-  TC_MARK(1);
+  if (warp == 5) tmem_alloc(&S.tmem_base, kTmemCols);
   tc_fence_before_sync();
-  __syncthreads();  // barriers initialised, TMEM allocated, tree group done
+  __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = S.tmem_base;
-  uint4 vreg[4];  // this thread's 32 values of v (row t, columns 32 cq ..), loaded below
-  float cacc[8][4];  // fused commit: this thread's part of K_P^T diag(w) U_P
-  if constexpr (kFused) {
-    if (!S.cbad) commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, cacc);
-  }
-  if (!mbar_wait(&S.bar_s0, 0, kWaitLimitNs)) S.err = 1;
-  if constexpr (kFused) {
-    // delayed commitment: S1 = gamma S0 + K_P^T diag(w) U_P over the raw state tile,
-    // written back in place (it is the state this tree is verified from) and to S1
-    if (h == 0 && tid == 0 && fc.status)
-      fc.status[b] = S.cbad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
-    if (S.cbad) {
-      if (h == 0 && tid == 0 && dev_status) dev_status[b] = GDN_TREE_STATUS_BAD_PATH;
-      goto drain;
-    }
-    if (!S.err) commit_finish(fc, S, sU, b, h, Hv, tid, cacc);
-  }
-  TC_MARK(2);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const float* raw = sU;  // S0 [dk][dv], row-major, landed by TMA
-#pragma unroll
-    for (int r = 0; r < (kD * 16) / kThreads; ++r) {
-      const int item = tid + r * kThreads;
-      const int n = item & (kD - 1), k8 = item >> 7;
-      const float* col = raw + (k8 * 8) * kD + n;
-      uint32_t part[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t hi, lo;
-        split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi, lo);
-        part[i] = half == 0 ? hi : lo;
+
+  for (uint32_t it = 0; unit < n_units; unit += gridDim.x, ++it) {
+    const uint32_t ph = it & 1u;
+    const int b = unit / Hv, h = unit - b * Hv;
+    const int hq = h / (Hv / Hqk);
+
+    // ---- 0. tree group (warps 0-3): the unit's tree; operand group (warps 4-15):
+    //         the fused commit's path, then the Gram MMAs once K and Q have landed
+    TC_MARK(0);
+    if (warp < 4) {
+      tree_prep(S, sPath, parent, beta, log_alpha, b, h, N, Hv, tid, lane, warp);
+    } else {
+      if constexpr (kFused) commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 128, warp, lane);
+      if (tid == kIssuer) {
+        if (!mbar_wait(&S.bar_kq, ph, kWaitLimitNs)) {
+          S.err = 1;
+        } else {
+          tc_fence_after_sync();
+          umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
+          umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
+          umma_commit(&S.bar_g);
+          ++S.n_g;
+        }
       }
-      *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + sw128_chunk(n, k8)) =
-          make_uint4(part[0], part[1], part[2], part[3]);
     }
-    fence_proxy_async_smem();
+    tc_fence_before_sync();
     __syncthreads();
-    if (tid == kIssuer && S.err == 0) {
-      tc_fence_after_sync();
-      if (half == 0) {
-        umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
-      } else {
-        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
-        umma_commit(&S.bar_ks);
-        S.issued |= 2;
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) vreg[i] = make_uint4(0, 0, 0, 0);
-  if (live) {
-    const uint4* vrow =
-        reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + cq * 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
-  }
-  TC_MARK(3);
-  if (h == 0 && tid == 0 && dev_status)
-    dev_status[b] = S.bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
-  if (S.bad) goto drain;
-  if (__syncthreads_or(S.err)) goto fail;
-
-  {
-    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    const int col0 = cq * 32;
-    const float bt = live ? S.beta[t] : 0.f;
-    const df gt = live ? S.g[t] : df{0.f, 0.f};
-    const float gam = __expf(df_value(gt));
-    const uint32_t abits = live ? S.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
-
-    // ---- 4. X row segment (registers) while K S0 / Q S0 run ------------------------
-    TC_MARK(4);
-    if (!mbar_wait(&S.bar_g, 0, kWaitLimitNs)) S.err = 2;
     tc_fence_after_sync();
-    float xr[32];
-    tmem_ld_32cols(trow + kColGkk + col0, xr);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const bool need = (abits >> j) & 1u;
-      float xv = 0.f;
-      if (__any_sync(0xffffffffu, need)) {  // skip columns no lane of the warp needs
-        const float e = __expf(df_diff(gt, S.g[col0 + j]));
-        xv = need ? bt * e * xr[j] : 0.f;
-      }
-      xr[j] = xv;
-    }
+    if (S.err) goto fail;
+    TC_MARK(1);
 
-    // ---- 5. once K S0 / Q S0 are done (K, Q, S0^T dead): X, R = beta (V - gamma K S0)
-    //         and Y (hi, lo) to shared memory -------------------------------------------
-    if (!mbar_wait(&S.bar_ks, 0, kWaitLimitNs)) S.err = 2;
-    tc_fence_after_sync();
-    if constexpr (kFused) {
-      if (tid == 0) bulk_wait_read_all();  // the S1 store has read the tile R goes into
-    }
-    if (__syncthreads_or(S.err)) goto fail;
-    TC_MARK(5);
+    // ---- 1. fused: S1 = gamma S0 + K_P^T diag(w) U_P on the landed state tile
+    //         (the product is formed while the state is still in flight)
     {
-      float ks[32];
-      tmem_ld_32cols(trow + kColKS + col0, ks);
-      if (cq == 0) S.ready[t] = 0;
+      float cacc[8][4];
+      if constexpr (kFused) {
+        if (!S.cbad) commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, cacc);
+      }
+      if (__syncthreads_or(!mbar_wait(&S.bar_s0, ph, kWaitLimitNs))) goto fail;
+      if constexpr (kFused) {
+        if (!S.cbad) commit_finish(fc, S, sU, unit, tid, cacc);
+      }
+    }
+    TC_MARK(2);
+
+    // ---- 2. S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the raw tile;
+    //         the hi half first, so that K S0_hi and Q S0_hi run on the tensor
+    //         cores while the lo half is written
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int r = 0; r < (kD * 16) / kThreads; ++r) {
+        const int item = tid + r * kThreads;
+        const int n = item & (kD - 1), k8 = item >> 7;
+        const float* col = sU + (k8 * 8) * kD + n;
+        uint32_t part[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t hi, lo;
+          split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi, lo);
+          part[i] = half == 0 ? hi : lo;
+        }
+        *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + sw128_chunk(n, k8)) =
+            make_uint4(part[0], part[1], part[2], part[3]);
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == kIssuer) {
+        tc_fence_after_sync();
+        if (half == 0) {
+          umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+          umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+        } else {
+          umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+          umma_commit(&S.bar_ks);
+          ++S.n_ks;
+        }
+      }
+    }
+    uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vreg[i] = make_uint4(0, 0, 0, 0);
+    if (live) {
+      const uint4* vrow =
+          reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + col0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
+    }
+    TC_MARK(3);
+    const bool cbad = kFused && S.cbad;
+    if (h == 0 && tid == 0) {
+      if (dev_status)
+        dev_status[b] = cbad ? GDN_TREE_STATUS_BAD_PATH
+                             : (S.bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK);
+      if (kFused && fc.status) fc.status[b] = cbad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
+    }
+    // an invalid tree (verified as all-roots) or path leaves the unit's outputs unwritten
+    const bool write_out = !S.bad && !cbad;
+
+    {
+      const uint32_t trow = tmem + trow_off;
+      const float bt = live ? S.beta[t] : 0.f;
+      const df gt = live ? S.g[t] : df{0.f, 0.f};
+      const float gam = __expf(df_value(gt));
+      const uint32_t abits = live ? S.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
+
+      // ---- 3. X and Y entries of t's ancestors in registers while K S0 / Q S0 run
+      if (!mbar_wait(&S.bar_g, ph, kWaitLimitNs)) S.err = 2;
+      tc_fence_after_sync();
+      float xr[32], yr[32];
+      tmem_ld_32cols(trow + kColGkk + col0, xr);
+      tmem_ld_32cols(trow + kColGqk + col0, yr);
+      float ydiag = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (col0 + j == t) ydiag = yr[j];
+        const bool need = (abits >> j) & 1u;
+        float e = 0.f;
+        if (__any_sync(0xffffffffu, need)) e = __expf(df_diff(gt, S.g[col0 + j]));
+        xr[j] = bt * e * xr[j];
+        yr[j] = e * yr[j];
+      }
+      TC_MARK(4);
+
+      // ---- 4. once K S0 / Q S0 are done (regions 1 and 2 free): X, Y to region 1,
+      //         R = beta (V - gamma K S0) to region 3, output seeds gamma Q S0 to region 2
+      if (!mbar_wait(&S.bar_ks, ph, kWaitLimitNs)) S.err = 2;
+      tc_fence_after_sync();
+      if constexpr (kFused) {
+        if (tid == 0) bulk_wait_read_all();  // the S1 store has read the tile R goes into
+      }
+      if (__syncthreads_or(S.err)) goto fail;
+      TC_MARK(5);
       if (live) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if ((abits >> j) & 1u) sX[x_index(t, col0 + j)] = xr[j];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t w4[4] = {vreg[q].x, vreg[q].y, vreg[q].z, vreg[q].w};
-          float r[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            r[2 * e] = bt * (__uint_as_float(w4[e] << 16) - gam * ks[q * 8 + 2 * e]);
-            r[2 * e + 1] = bt * (__uint_as_float(w4[e] & 0xffff0000u) - gam * ks[q * 8 + 2 * e + 1]);
-          }
-          const int c4 = cq * 8 + q * 2;
-          *reinterpret_cast<float4*>(sU + u_index(t, c4)) = make_float4(r[0], r[1], r[2], r[3]);
-          *reinterpret_cast<float4*>(sU + u_index(t, c4 + 1)) =
-              make_float4(r[4], r[5], r[6], r[7]);
-        }
+          if ((abits >> j) & 1u) sXY[x_index(t, col0 + j)] = make_float2(xr[j], yr[j]);
+        if ((t >> 5) == cq) S.ydiag[t] = ydiag;
       }
-    }
-    {
-      float gq[32];
-      tmem_ld_32cols(trow + kColGqk + col0, gq);
+      {
+        float ks[32];
+        tmem_ld_32cols(trow + kColKS + col0, ks);
+        if (live) {
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        uint32_t hi[4], lo[4];
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t w4[4] = {vreg[q].x, vreg[q].y, vreg[q].z, vreg[q].w};
+            float r[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float y[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = g8 * 8 + 2 * i + e;
-            const int s = col0 + j;
-            const bool anc_s = live && ((abits >> j) & 1u);
-            float yv = (live && s == t) ? gq[j] : 0.f;
-            if (__any_sync(0xffffffffu, anc_s)) {
-              const float dec = __expf(df_diff(gt, S.g[s]));
-              if (anc_s) yv = dec * gq[j];
+            for (int e = 0; e < 4; ++e) {
+              r[2 * e] = bt * (__uint_as_float(w4[e] << 16) - gam * ks[q * 8 + 2 * e]);
+              r[2 * e + 1] =
+                  bt * (__uint_as_float(w4[e] & 0xffff0000u) - gam * ks[q * 8 + 2 * e + 1]);
             }
-            y[e] = yv;
+            const int c4 = cq * 8 + q * 2;
+            *reinterpret_cast<float4*>(sU + u_index(t, c4)) = make_float4(r[0], r[1], r[2], r[3]);
+            *reinterpret_cast<float4*>(sU + u_index(t, c4 + 1)) =
+                make_float4(r[4], r[5], r[6], r[7]);
           }
-          split2(y[0], y[1], hi[i], lo[i]);
         }
-        const uint32_t off = sw128_chunk(t, cq * 4 + g8);
-        *reinterpret_cast<uint4*>(smem + OFF_YH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + OFF_YL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+      {
+        float qs[32];
+        tmem_ld_32cols(trow + kColQS + col0, qs);
+        if (live) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(sP + u_index(t, cq * 8 + q)) =
+                make_float4(gam * qs[4 * q], gam * qs[4 * q + 1], gam * qs[4 * q + 2],
+                            gam * qs[4 * q + 3]);
+        }
+      }
+      if (cq == 0) S.ready[t] = 0;
+      tc_fence_before_sync();
+      __syncthreads();
     }
-    tc_fence_before_sync();
-    __syncthreads();
 
-    // ---- 6. forward substitution as a dataflow over the tree ------------------------
-    // u_t = r_t - sum over ancestors a of X[t,a] u_a.  Warp w takes the nodes at
-    // positions w, w + 16, ... of the depth order.  For node t it waits (acquire)
-    // on the ready flag of t's grandparent -- every ancestor but the parent is
-    // then final -- sums those terms four at a time (lane = 4 value columns),
-    // then waits on the parent and adds its term, publishes u_t and raises t's
-    // flag (release).  So a link of the dependency chain costs one term, not the
-    // whole ancestor sum.  No cycle of waits can form: the unfinished node of
-    // lowest depth order never waits (its ancestors come earlier in that order).
+    // ---- 5. forward substitution as a dataflow over the tree ------------------------
+    // u_t = r_t - sum over ancestors a of X[t,a] u_a and o_t = seed_t + sum over
+    // t's path of Y[t,s] u_s.  Warp w takes the nodes at positions w, w + 16, ... of
+    // the depth order.  For node t it waits (acquire) on the ready flag of t's
+    // grandparent -- every ancestor but the parent is then final -- sums those
+    // terms four at a time (lane = 4 value columns), then waits on the parent and
+    // adds its term, publishes u_t and raises t's flag (release); the parent's and
+    // t's own output terms follow.  So a link of the dependency chain costs one
+    // term, not the whole ancestor sum.  No cycle of waits can form: the
+    // unfinished node of lowest depth order never waits (its ancestors come
+    // earlier in that order).
     TC_MARK(6);
     {
       int* ready = S.ready;
-      float* Ubh = U + ((size_t)b * Hv + h) * N * kD;
+      float* Ubh = U + (size_t)unit * N * kD;
+      __nv_bfloat16* obh = o + ((size_t)b * N * Hv + h) * kD;
       bool timed_out = false;
       auto wait_ready = [&](int node) {
         uint32_t spins = 0;
@@ -710,134 +732,87 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int i = warp; i < N; i += kWarps) {
         const int tn = S.order[i];
         const int dep = S.depth[tn];
-        const uint8_t* pth = sPath + tn * kTile;
-        const float* xrow = sX + x_index(tn, 0);
+        const uint8_t* pth = sPath + tn * kTile;  // pth[dep - 1] = tn, pth[0] = its root
+        const float2* xyrow = sXY + x_index(tn, 0);
         float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
+        float4 py = *reinterpret_cast<const float4*>(sP + u_index(tn, lane));
+        float yp = 0.f;
+        float4 up = make_float4(0.f, 0.f, 0.f, 0.f);
         if (dep > 1) {
-          if (dep > 2) wait_ready(pth[dep - 2]);
-          int j = 1;
-          for (; j + 4 <= dep - 1; j += 4) {
+          if (dep > 2) wait_ready(pth[dep - 3]);
+          int j = 0;
+          for (; j + 4 <= dep - 2; j += 4) {
             int aa[4];
-            float xx[4];
+            float2 xy[4];
             float4 uu[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) aa[e] = pth[j + e];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              xx[e] = xrow[aa[e]];
+              xy[e] = xyrow[aa[e]];
               uu[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], lane));
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              acc.x = fmaf(-xx[e], uu[e].x, acc.x);
-              acc.y = fmaf(-xx[e], uu[e].y, acc.y);
-              acc.z = fmaf(-xx[e], uu[e].z, acc.z);
-              acc.w = fmaf(-xx[e], uu[e].w, acc.w);
+              acc = fma4(-xy[e].x, uu[e], acc);
+              py = fma4(xy[e].y, uu[e], py);
             }
           }
-          for (; j < dep - 1; ++j) {
+          for (; j < dep - 2; ++j) {
             const int a1 = pth[j];
-            const float x1 = xrow[a1];
+            const float2 xy1 = xyrow[a1];
             const float4 u1 = *reinterpret_cast<const float4*>(sU + u_index(a1, lane));
-            acc.x = fmaf(-x1, u1.x, acc.x);
-            acc.y = fmaf(-x1, u1.y, acc.y);
-            acc.z = fmaf(-x1, u1.z, acc.z);
-            acc.w = fmaf(-x1, u1.w, acc.w);
+            acc = fma4(-xy1.x, u1, acc);
+            py = fma4(xy1.y, u1, py);
           }
-          const int par = pth[dep - 1];
-          const float xp = xrow[par];
+          const int par = pth[dep - 2];
+          const float2 xyp = xyrow[par];
+          yp = xyp.y;
           wait_ready(par);
-          const float4 up = *reinterpret_cast<const float4*>(sU + u_index(par, lane));
-          acc.x = fmaf(-xp, up.x, acc.x);
-          acc.y = fmaf(-xp, up.y, acc.y);
-          acc.z = fmaf(-xp, up.z, acc.z);
-          acc.w = fmaf(-xp, up.w, acc.w);
+          up = *reinterpret_cast<const float4*>(sU + u_index(par, lane));
+          acc = fma4(-xyp.x, up, acc);
           *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
         }
         __syncwarp();
         if (lane == 0) st_release_shared(ready + tn, 1);
-        *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
+        py = fma4(yp, up, py);
+        py = fma4(S.ydiag[tn], acc, py);
+        if (write_out) {
+          *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
+          *reinterpret_cast<uint2*>(obh + (size_t)tn * Hv * kD + lane * 4) =
+              make_uint2(pack2f(py.x, py.y), pack2f(py.z, py.w));
+        }
       }
       if (timed_out) S.err = 4;
     }
-    if (__syncthreads_or(S.err)) goto fail;
-
-    // ---- 7. U^T (hi, lo) over X ----------------------------------------------------------
-    TC_MARK(7);
-#pragma unroll
-    for (int r = 0; r < (kD * 16) / kThreads; ++r) {
-      const int item = tid + r * kThreads;
-      const int n = item & (kD - 1), t8 = item >> 7;
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ta = t8 * 8 + 2 * i, tb = ta + 1;
-        const float x0 = ta < N ? sU[u_index(ta, n >> 2) + (n & 3)] : 0.f;
-        const float x1 = tb < N ? sU[u_index(tb, n >> 2) + (n & 3)] : 0.f;
-        split2(x0, x1, hi[i], lo[i]);
-      }
-      const uint32_t off = sw128_chunk(n, t8);
-      *reinterpret_cast<uint4*>(smem + OFF_UTH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + OFF_UTL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
+    // regions 1 and 3 are free: the next unit's operands start loading
     fence_proxy_async_smem();
     tc_fence_before_sync();
-    __syncthreads();
-
-    // ---- 8. Y U on the tensor cores (three bf16 passes) -------------------------------
-    TC_MARK(8);
-    if (tid == kIssuer) {
-      tc_fence_after_sync();
-      umma_128x128x128(tmem + kColYU, sbase + OFF_YH, sbase + OFF_UTH, false);
-      umma_128x128x128(tmem + kColYU, sbase + OFF_YH, sbase + OFF_UTL, true);
-      umma_128x128x128(tmem + kColYU, sbase + OFF_YL, sbase + OFF_UTH, true);
-      umma_commit(&S.bar_yu);
-      S.issued |= 4;
-    }
-    if (!mbar_wait(&S.bar_yu, 0, kWaitLimitNs)) S.err = 3;
-    tc_fence_after_sync();
     if (__syncthreads_or(S.err)) goto fail;
-
-    // ---- 9. O = gamma QS + Y U ----------------------------------------------------------
-    TC_MARK(9);
-    {
-      float yu[32], qs[32];
-      tmem_ld_32cols(trow + kColYU + col0, yu);
-      tmem_ld_32cols(trow + kColQS + col0, qs);
-      if (live) {
-        uint4* orow = reinterpret_cast<uint4*>(o + (((size_t)b * N + t) * Hv + h) * kD + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = q * 8 + 2 * e;
-            w4[e] = pack2f(fmaf(gam, qs[j], yu[j]), fmaf(gam, qs[j + 1], yu[j + 1]));
-          }
-          orow[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-      }
-    }
+    tc_fence_after_sync();
+    TC_MARK(7);
+    if (tid == kIssuer && unit + (int)gridDim.x < n_units)
+      issue_loads(S, smem, &tmK, &tmQ, &tmS, unit + gridDim.x, Hv, Hqk);
   }
-  TC_MARK(10);
   goto release;
 
 fail:
   // a bounded wait ran out: report it, let in-flight copies and MMAs drain
   // (again bounded), then free TMEM
-  if (tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
-drain:
-  if (tid == 0) {
-    mbar_wait(&S.bar_kq, 0, kWaitLimitNs);
-    mbar_wait(&S.bar_s0, 0, kWaitLimitNs);
-    if (S.issued & 1) mbar_wait(&S.bar_g, 0, kWaitLimitNs);
-    if (S.issued & 2) mbar_wait(&S.bar_ks, 0, kWaitLimitNs);
-    if (S.issued & 4) mbar_wait(&S.bar_yu, 0, kWaitLimitNs);
+  if (tid == 0 && dev_status && unit < n_units)
+    atomicMax(dev_status + unit / Hv, GDN_TREE_STATUS_TIMEOUT);
+  if (tid == kIssuer) {
+    if (S.n_loads > 0) {
+      mbar_wait(&S.bar_kq, (S.n_loads - 1) & 1, kWaitLimitNs);
+      mbar_wait(&S.bar_s0, (S.n_loads - 1) & 1, kWaitLimitNs);
+    }
+    if (S.n_g > 0) mbar_wait(&S.bar_g, (S.n_g - 1) & 1, kWaitLimitNs);
+    if (S.n_ks > 0) mbar_wait(&S.bar_ks, (S.n_ks - 1) & 1, kWaitLimitNs);
   }
 
 release:
   if constexpr (kFused) {
-    if (tid == 0) bulk_wait_all();  // the S1 store is complete before the CTA leaves
+    if (tid == 0) bulk_wait_all();  // every S1 store is complete before the CTA leaves
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -892,10 +867,23 @@ bool encode_state_map(CUtensorMap* map, const float* base, const gdn_tree_dims& 
 
 bool verify_tc_supported(const gdn_tree_dims& d) {
   return d.dtype == GDN_TREE_BF16 && d.dk == kD && d.dv == kD && d.N >= 1 && d.N <= kTile &&
-         tensor_map_encoder() != nullptr;
+         (long long)d.B * d.Hv < (1ll << 30) && tensor_map_encoder() != nullptr;
 }
 
 namespace {
+
+// streaming multiprocessors of the current device (cached per device)
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int n = (dev >= 0 && dev < 64) ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 
 template <bool kFused>
 cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
@@ -906,7 +894,13 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-  verify_tc_kernel<kFused><<<dim3(a.d.Hv, a.d.B), kThreads, kSmemBytes, stream>>>(
+  // persistent: one CTA per SM (the shared memory admits no second), each walking
+  // units blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int n_units = a.d.B * a.d.Hv;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return cudaErrorInvalidDevice;
+  const int grid = n_units < n_sm ? n_units : n_sm;
+  verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
       tmQ, tmK, tmS, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent,
       static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, fc);
   return cudaGetLastError();
@@ -934,8 +928,8 @@ cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stre
 }  // namespace gdn
 
 #ifdef GDN_TC_PROFILE
-extern "C" int gdn_tree_debug_tc_phases(unsigned long long* host, int n_ctas) {
-  return (int)cudaMemcpyFromSymbol(host, gdn::g_tc_phase,
-                                   sizeof(unsigned long long) * 16 * (n_ctas < 4096 ? n_ctas : 4096));
+extern "C" int gdn_tree_debug_tc_phases(unsigned long long* host, int n_units) {
+  return (int)cudaMemcpyFromSymbol(
+      host, gdn::g_tc_phase, sizeof(unsigned long long) * 16 * (n_units < 4096 ? n_units : 4096));
 }
 #endif
