@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstddef>
 #include <mutex>
 
 #include "common.cuh"
@@ -62,15 +63,16 @@ constexpr uint32_t kSpinLimit = 1u << 24;  // bounded wait on a solve ready flag
 #ifdef GDN_TC_PROFILE
 // per-unit phase timestamps for a profiling build (never in the product build)
 __device__ unsigned long long g_tc_phase[4096][16];
-#define TC_MARK(i)                                                               \
-  do {                                                                           \
-    if (threadIdx.x == 0 && unit < 4096) g_tc_phase[unit][i] = globaltimer_ns(); \
+#define TC_MARK_BY(thread, i)                                                           \
+  do {                                                                                  \
+    if (threadIdx.x == (thread) && unit < 4096) g_tc_phase[unit][i] = globaltimer_ns(); \
   } while (0)
 #else
-#define TC_MARK(i) \
-  do {             \
+#define TC_MARK_BY(thread, i) \
+  do {                        \
   } while (0)
 #endif
+#define TC_MARK(i) TC_MARK_BY(0, i)
 
 // shared memory map (byte offsets from a 1024-aligned base); three 64 KB regions
 // change roles within a unit
@@ -91,7 +93,7 @@ constexpr uint32_t OFF_P = 2 * kOpBytes;
 constexpr uint32_t OFF_U = 4 * kOpBytes;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
-constexpr uint32_t kSmallBytes = 11264;
+constexpr uint32_t kSmallBytes = 12800;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
@@ -111,6 +113,10 @@ struct Small {
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
   int ready[kTile];  // solve: node's u is final
+  // the next unit's tree and gates, prefetched (cp.async) while this unit runs
+  int pre_parent[kTile];
+  float pre_beta[kTile];
+  float pre_la[kTile];
   uint64_t bar_kq, bar_s0, bar_g, bar_ks;
   uint32_t tmem_base;
   int err;
@@ -125,6 +131,7 @@ struct Small {
   int cbad;
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
+static_assert(offsetof(Small, g) % 16 == 0, "path log-decays are read as float4");
 
 // byte offset of 16-byte chunk k8 (K elements 8*k8 .. 8*k8+7) of `row` in a
 // 128-row, 128-wide K-major bf16 tile stored with the 128-byte swizzle
@@ -184,6 +191,32 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (this thread's cp.async group)
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Tree group: starts the copies of a unit's parent links and gates (node = tid)
+// into the prefetch slots; tree_prep of that unit waits for them.
+__device__ __forceinline__ void prefetch_tree(Small& S, const int32_t* parent, const float* beta,
+                                              const float* log_alpha, int unit, int N, int Hv,
+                                              int tid) {
+  if (tid < N) {
+    const int b = unit / Hv, h = unit - b * Hv;
+    cp_async4(&S.pre_parent[tid], parent + (size_t)b * N + tid);
+    cp_async4(&S.pre_beta[tid], beta + ((size_t)b * N + tid) * Hv + h);
+    cp_async4(&S.pre_la[tid], log_alpha + ((size_t)b * N + tid) * Hv + h);
+  }
+  cp_async_commit();
+}
+
 // previous tree's accepted path for the fused delayed commitment
 struct FusedCommit {
   const int32_t* path;      // [B, Lmax]
@@ -230,21 +263,23 @@ __device__ __forceinline__ void issue_loads(Small& S, uint8_t* smem, const CUten
   ++S.n_loads;
 }
 
-// Tree group (threads 0..127): loads the unit's tree and gates, validates the
-// tree, then one upward walk per node gives its depth, its path log-decay g_t
-// (double-float), its strict-ancestor bitset and its path (sPath row, root
-// first); finally the nodes are ordered by depth.  An invalid tree is replaced
-// by all-roots (nothing of it is stored).
+// Tree group (threads 0..127): takes the unit's prefetched tree and gates,
+// validates the tree, then one upward walk per node gives its depth, its path
+// log-decay g_t (double-float) and its strict-ancestor bitset, and a second its
+// path (sPath row, root first); finally the nodes are ordered by depth.  An invalid tree is replaced by all-roots (nothing of it is stored).
+// Then the copies for the CTA's next unit (`next`, if < n_units) are started.
 __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_t* parent,
-                                          const float* beta, const float* log_alpha, int b,
-                                          int h, int N, int Hv, int tid, int lane, int warp) {
+                                          const float* beta,
+                                          const float* log_alpha, int next, int n_units, int N,
+                                          int Hv, int tid, int lane, int warp) {
   using TreeSync = NamedSync<1, 128>;
+  cp_async_wait_all();
   int p_in = -1;
   float be_in = 0.f, la_in = 0.f;
   if (tid < N) {
-    p_in = parent[(size_t)b * N + tid];
-    be_in = beta[((size_t)b * N + tid) * Hv + h];
-    la_in = log_alpha[((size_t)b * N + tid) * Hv + h];
+    p_in = S.pre_parent[tid];
+    be_in = S.pre_beta[tid];
+    la_in = S.pre_la[tid];
   }
   S.beta[tid] = be_in;
   S.la[tid] = la_in;
@@ -253,6 +288,8 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
   const int bad_any = bar_or<1, 128>(tid < N && (p_in < -1 || p_in >= tid));
   S.parent[tid] = bad_any ? -1 : p_in;
   if (tid == 0) S.bad = bad_any;
+  // every read of the prefetch slots has completed (their values are used above)
+  if (next < n_units) prefetch_tree(S, parent, beta, log_alpha, next, N, Hv, tid);
   TreeSync()();
   int dep = 0;
   if (tid < N) {
@@ -379,7 +416,7 @@ __device__ __forceinline__ void commit_weights(Small& S, int L, int lane) {
   if (lane == 0) S.cgamma = expf(df_value(GL));
 }
 
-// Operand group (threads 128..511, ot = tid - 128): checks the previous tree's
+// Warps 5-15 (ot = tid - 160; warp 4 issues the copies and MMAs meanwhile): checks the previous tree's
 // accepted path of sequence b (range, chain order, parent links), gathers its
 // log alpha, stages the first chunk of its k / U rows into region 2 and forms
 // the path weights.  Sets S.cbad, S.cL.
@@ -394,7 +431,7 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
     cbad |= (pj < 0 || pj >= fc.N);
     S.cpath[ot] = pj;
   }
-  cbad = bar_or<2, kThreads - 128>(cbad);
+  cbad = bar_or<2, kThreads - 160>(cbad);
   if (!cbad && ot < L) {
     const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
     cbad |= (ot > 0 && pj <= prev);
@@ -402,13 +439,13 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
     S.cla[ot] = fc.log_alpha[((size_t)b * fc.N + pj) * Hv + h];
   }
   if (!cbad)
-    commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 128);
-  cbad = bar_or<2, kThreads - 128>(cbad);
+    commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 160);
+  cbad = bar_or<2, kThreads - 160>(cbad);
   if (ot == 0) {
     S.cbad = cbad;
     S.cL = L;
   }
-  if (!cbad && warp == 4) commit_weights(S, L, lane);
+  if (!cbad && warp == 5) commit_weights(S, L, lane);
 }
 
 // K_P^T diag(w) U_P for this thread's 8x4 tile of the state (rows r8*8 .., columns
@@ -476,6 +513,52 @@ __device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small
   }
 }
 
+// S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the raw fp32 state tile in
+// region 3; the hi half is written first, so that Q S0_hi and K S0_hi run on the
+// tensor cores while the lo half is written; then K S0_lo, and bar_ks tracks all
+// of them.  Called by kCount threads (index gtid, the issuing thread among them)
+// that Sync synchronises.
+template <int kCount, typename Sync>
+__device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small& S, uint32_t tmem,
+                                            int gtid, bool issuer, bool issue) {
+  constexpr int kItems = kD * 16;  // 16-byte output chunks per half
+  constexpr int kRounds = (kItems + kCount - 1) / kCount;
+  const float* raw = reinterpret_cast<const float*>(smem + OFF_U);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int item = gtid + r * kCount;
+      if (kItems % kCount == 0 || item < kItems) {
+        const int n = item & (kD - 1), k8 = item >> 7;
+        const float* col = raw + (k8 * 8) * kD + n;
+        uint32_t part[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t hi, lo;
+          split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi, lo);
+          part[i] = half == 0 ? hi : lo;
+        }
+        *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + sw128_chunk(n, k8)) =
+            make_uint4(part[0], part[1], part[2], part[3]);
+      }
+    }
+    fence_proxy_async_smem();
+    Sync()();
+    if (issuer && issue) {
+      tc_fence_after_sync();
+      if (half == 0) {
+        umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+      } else {
+        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+        umma_commit(&S.bar_ks);
+        ++S.n_ks;
+      }
+    }
+  }
+}
+
 template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -522,6 +605,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     mbar_fence_init();
     if (unit < n_units) issue_loads(S, smem, &tmK, &tmQ, &tmS, unit, Hv, Hqk);
   }
+  if (warp < 4 && unit < n_units) prefetch_tree(S, parent, beta, log_alpha, unit, N, Hv, tid);
   if (warp == 5) tmem_alloc(&S.tmem_base, kTmemCols);
   tc_fence_before_sync();
   __syncthreads();
@@ -533,23 +617,36 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int b = unit / Hv, h = unit - b * Hv;
     const int hq = h / (Hv / Hqk);
 
-    // ---- 0. tree group (warps 0-3): the unit's tree; operand group (warps 4-15):
-    //         the fused commit's path, then the Gram MMAs once K and Q have landed
+    // ---- 0. tree group (warps 0-3): the unit's tree.  Operand group (warps 4-15):
+    //         the Gram MMAs once K and Q have landed; then, plain, S0^T and the
+    //         K S0 / Q S0 MMAs (1. below) while the tree group still works; fused,
+    //         the previous tree's accepted path (warps 5-15)
     TC_MARK(0);
     if (warp < 4) {
-      tree_prep(S, sPath, parent, beta, log_alpha, b, h, N, Hv, tid, lane, warp);
+      tree_prep(S, sPath, parent, beta, log_alpha, unit + gridDim.x, n_units, N, Hv, tid, lane, warp);
+      TC_MARK(8);
     } else {
-      if constexpr (kFused) commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 128, warp, lane);
+      if constexpr (kFused) {
+        if (warp > 4) commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 160, warp, lane);
+      }
       if (tid == kIssuer) {
         if (!mbar_wait(&S.bar_kq, ph, kWaitLimitNs)) {
           S.err = 1;
         } else {
+          TC_MARK_BY(kIssuer, 9);
           tc_fence_after_sync();
           umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
           umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
           umma_commit(&S.bar_g);
           ++S.n_g;
         }
+      }
+      if constexpr (!kFused) {
+        // ---- 1. (plain) S0^T from the landed state, by the operand group
+        const bool s0_ok = mbar_wait(&S.bar_s0, ph, kWaitLimitNs);
+        if (!s0_ok) S.err = 1;
+        split_state<kThreads - 128, NamedSync<2, kThreads - 128>>(
+            smem, sbase, S, tmem, tid - 128, tid == kIssuer, s0_ok && S.err == 0);
       }
     }
     tc_fence_before_sync();
@@ -558,53 +655,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (S.err) goto fail;
     TC_MARK(1);
 
-    // ---- 1. fused: S1 = gamma S0 + K_P^T diag(w) U_P on the landed state tile
-    //         (the product is formed while the state is still in flight)
-    {
+    if constexpr (kFused) {
+      // ---- 1. (fused) S1 = gamma S0 + K_P^T diag(w) U_P on the landed state tile (the
+      //         product is formed while the state is still in flight), then S0^T from S1
       float cacc[8][4];
-      if constexpr (kFused) {
-        if (!S.cbad) commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, cacc);
-      }
+      if (!S.cbad) commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, cacc);
       if (__syncthreads_or(!mbar_wait(&S.bar_s0, ph, kWaitLimitNs))) goto fail;
-      if constexpr (kFused) {
-        if (!S.cbad) commit_finish(fc, S, sU, unit, tid, cacc);
-      }
-    }
-    TC_MARK(2);
-
-    // ---- 2. S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the raw tile;
-    //         the hi half first, so that K S0_hi and Q S0_hi run on the tensor
-    //         cores while the lo half is written
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int r = 0; r < (kD * 16) / kThreads; ++r) {
-        const int item = tid + r * kThreads;
-        const int n = item & (kD - 1), k8 = item >> 7;
-        const float* col = sU + (k8 * 8) * kD + n;
-        uint32_t part[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t hi, lo;
-          split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi, lo);
-          part[i] = half == 0 ? hi : lo;
-        }
-        *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + sw128_chunk(n, k8)) =
-            make_uint4(part[0], part[1], part[2], part[3]);
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == kIssuer) {
-        tc_fence_after_sync();
-        if (half == 0) {
-          umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-          umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
-        } else {
-          umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
-          umma_commit(&S.bar_ks);
-          ++S.n_ks;
-        }
-      }
+      if (!S.cbad) commit_finish(fc, S, sU, unit, tid, cacc);
+      TC_MARK(2);
+      split_state<kThreads, BlockSync>(smem, sbase, S, tmem, tid, tid == kIssuer, true);
     }
     uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..)
 #pragma unroll
@@ -636,18 +695,32 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // ---- 3. X and Y entries of t's ancestors in registers while K S0 / Q S0 run
       if (!mbar_wait(&S.bar_g, ph, kWaitLimitNs)) S.err = 2;
       tc_fence_after_sync();
+      TC_MARK(10);
       float xr[32], yr[32];
       tmem_ld_32cols(trow + kColGkk + col0, xr);
       tmem_ld_32cols(trow + kColGqk + col0, yr);
+      TC_MARK(11);
       float ydiag = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (col0 + j == t) ydiag = yr[j];
-        const bool need = (abits >> j) & 1u;
-        float e = 0.f;
-        if (__any_sync(0xffffffffu, need)) e = __expf(df_diff(gt, S.g[col0 + j]));
-        xr[j] = bt * e * xr[j];
-        yr[j] = e * yr[j];
+      for (int j8 = 0; j8 < 4; ++j8) {
+        df gs[8];  // path log-decays of columns col0 + 8 j8 .., loaded together
+        const float4* g4 = reinterpret_cast<const float4*>(&S.g[col0 + j8 * 8]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 w = g4[e];
+          gs[2 * e] = df{w.x, w.y};
+          gs[2 * e + 1] = df{w.z, w.w};
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = j8 * 8 + e;
+          if (col0 + j == t) ydiag = yr[j];
+          const bool need = (abits >> j) & 1u;
+          float dec = 0.f;
+          if (__any_sync(0xffffffffu, need)) dec = __expf(df_diff(gt, gs[e]));
+          xr[j] = bt * dec * xr[j];
+          yr[j] = dec * yr[j];
+        }
       }
       TC_MARK(4);
 
