@@ -14,9 +14,11 @@
 //   a persistent grid, one CTA (512 threads, 512 TMEM columns) per SM, walks the
 //   (sequence b, v-head h) units; the next unit's operands are already being
 //   loaded while the current unit finishes.  Per unit:
-//   1. TMA (128-byte swizzle) brings K and Q of the q/k head and the fp32 state;
-//      threads turn S0 into S0^T = hi + lo, two bf16 K-major tiles, so K S0
-//      keeps fp32 accuracy (K is exact in bf16).
+//   1. TMA (128-byte swizzle) brings K and Q of the q/k head; each thread loads an
+//      8 x 4 tile of the fp32 state into registers and writes it as S0^T = hi + lo,
+//      two bf16 K-major tiles, so K S0 keeps fp32 accuracy (K is exact in bf16).
+//      (Fused with the delayed commitment, the tile is first committed in registers
+//      and stored as S1.)
 //   2. tcgen05.mma, accumulators in TMEM:  G_kk = K K^T, G_qk = Q K^T,
 //      KS = K S0_hi + K S0_lo, QS = Q S0_hi.
 //   3. TMEM -> registers (thread = tree node): the X and Y entries of the node's
@@ -56,9 +58,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kIssuer = 128;  // the one thread that issues every copy and MMA (warp 4, lane 0)
-constexpr int kS0BoxRows = 32;  // the state arrives as four 32-row boxes
 constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
-constexpr uint32_t kSpinLimit = 1u << 24;  // bounded wait on a solve ready flag
 
 #ifdef GDN_TC_PROFILE
 // per-unit phase timestamps for a profiling build (never in the product build)
@@ -89,11 +89,11 @@ constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;
 constexpr uint32_t OFF_S0H = 2 * kOpBytes;
 constexpr uint32_t OFF_S0L = 3 * kOpBytes;
 constexpr uint32_t OFF_P = 2 * kOpBytes;
-// region 3: the raw fp32 state (TMA) until S0^T is formed; then R / U
+// region 3: fused, the committed state tile on its way out (bulk store); then R / U
 constexpr uint32_t OFF_U = 4 * kOpBytes;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
-constexpr uint32_t kSmallBytes = 12800;
+constexpr uint32_t kSmallBytes = 13824;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
@@ -103,6 +103,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Small {
   int parent[kTile];
+  int jump[kTile];  // tree prep: pointer jumping
   df g[kTile];
   float beta[kTile];
   float la[kTile];
@@ -112,16 +113,16 @@ struct Small {
   int depth[kTile];
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
-  int ready[kTile];  // solve: node's u is final
+  uint64_t node_bar[kTile];  // solve: completes a phase per unit once the node's u is final
   // the next unit's tree and gates, prefetched (cp.async) while this unit runs
   int pre_parent[kTile];
   float pre_beta[kTile];
   float pre_la[kTile];
-  uint64_t bar_kq, bar_s0, bar_g, bar_ks;
+  uint64_t bar_kq, bar_g, bar_ks;
   uint32_t tmem_base;
   int err;
   int bad;  // the tree failed validation
-  int n_loads, n_g, n_ks;  // phases issued on bar_kq / bar_s0, bar_g, bar_ks
+  int n_kq, n_g, n_ks;  // phases issued on bar_kq, bar_g, bar_ks
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
   float cla[kMaxN];
@@ -162,12 +163,12 @@ __device__ __forceinline__ uint32_t pack2f(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// acc + a x, as two packed fp32x2 FMAs (same rounding as four fmaf)
 __device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
-  acc.x = fmaf(a, x.x, acc.x);
-  acc.y = fmaf(a, x.y, acc.y);
-  acc.z = fmaf(a, x.z, acc.z);
-  acc.w = fmaf(a, x.w, acc.w);
-  return acc;
+  const float2 aa = make_float2(a, a);
+  const float2 lo = __ffma2_rn(aa, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
+  const float2 hi = __ffma2_rn(aa, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // issue the 8 K-steps (K = 128) of D (+)= A B^T for two 128x128 K-major tiles
@@ -180,15 +181,6 @@ __device__ __forceinline__ void umma_128x128x128(uint32_t d_tmem, uint32_t a_bas
     umma_bf16(d_tmem, desc_sw128_kmajor(a_base + off), desc_sw128_kmajor(b_base + off), idesc,
               (accumulate || s > 0) ? 1u : 0u);
   }
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-      : "memory");
 }
 
 // 4-byte asynchronous copy global -> shared (this thread's cp.async group)
@@ -245,35 +237,33 @@ __device__ __forceinline__ int bar_or(int v) {
   return r;
 }
 
-// K and Q of the unit's q/k head into region 1 (bar_kq), its fp32 state into
-// region 3 (bar_s0); issuing thread only
-__device__ __forceinline__ void issue_loads(Small& S, uint8_t* smem, const CUtensorMap* tmK,
-                                            const CUtensorMap* tmQ, const CUtensorMap* tmS,
-                                            int unit, int Hv, int Hqk) {
+// K and Q of the unit's q/k head into region 1 (bar_kq); issuing thread only
+__device__ __forceinline__ void issue_kq(Small& S, uint8_t* smem, const CUtensorMap* tmK,
+                                         const CUtensorMap* tmQ, int unit, int Hv, int Hqk) {
   const int b = unit / Hv, h = unit - b * Hv, hq = h / (Hv / Hqk);
   mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
   tma_load_4d(smem + OFF_K, tmK, &S.bar_kq, 0, hq, 0, b);
   tma_load_4d(smem + OFF_K + kTileBytes, tmK, &S.bar_kq, 64, hq, 0, b);
   tma_load_4d(smem + OFF_Q, tmQ, &S.bar_kq, 0, hq, 0, b);
   tma_load_4d(smem + OFF_Q + kTileBytes, tmQ, &S.bar_kq, 64, hq, 0, b);
-  mbar_arrive_expect_tx(&S.bar_s0, kTile * kD * 4);
-#pragma unroll
-  for (int r = 0; r < kD; r += kS0BoxRows)  // four boxes land in parallel
-    tma_load_3d(smem + OFF_U + r * kD * 4, tmS, &S.bar_s0, 0, r, unit);
-  ++S.n_loads;
+  ++S.n_kq;
 }
 
 // Tree group (threads 0..127): takes the unit's prefetched tree and gates,
-// validates the tree, then one upward walk per node gives its depth, its path
-// log-decay g_t (double-float) and its strict-ancestor bitset, and a second its
-// path (sPath row, root first); finally the nodes are ordered by depth.  An invalid tree is replaced by all-roots (nothing of it is stored).
-// Then the copies for the CTA's next unit (`next`, if < n_units) are started.
+// validates the tree, then pointer jumping (ceil(log2 depth) rounds) gives every
+// node its strict-ancestor bitset and its path log-decay g_t (double-float); its
+// depth and its path (sPath row, root first: the ancestors in index order) follow
+// from the bitset; finally the nodes are ordered by depth.  An invalid tree is
+// replaced by all-roots (nothing of it is stored).  The copies
+// for the CTA's next unit (if `next` < `end`) start as soon as the prefetch
+// slots have been read.
 __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_t* parent,
-                                          const float* beta,
-                                          const float* log_alpha, int next, int n_units, int N,
-                                          int Hv, int tid, int lane, int warp) {
+                                          const float* beta, const float* log_alpha, int next,
+                                          int end, int N, int Hv, int tid, int lane, int warp,
+                                          int unit) {
   using TreeSync = NamedSync<1, 128>;
   cp_async_wait_all();
+  TC_MARK(12);
   int p_in = -1;
   float be_in = 0.f, la_in = 0.f;
   if (tid < N) {
@@ -289,34 +279,63 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
   S.parent[tid] = bad_any ? -1 : p_in;
   if (tid == 0) S.bad = bad_any;
   // every read of the prefetch slots has completed (their values are used above)
-  if (next < n_units) prefetch_tree(S, parent, beta, log_alpha, next, N, Hv, tid);
+  if (next < end) prefetch_tree(S, parent, beta, log_alpha, next, N, Hv, tid);
   TreeSync()();
+  TC_MARK(13);
+  // pointer jumping: after round r, jump[t] is t's 2^r-th ancestor (or -1) and
+  // anc[t], g[t] cover the part of t's path below it
+  int jmp = tid < N ? S.parent[tid] : -1;
+  df g = {la_in, 0.f};
+  uint4 a = make_uint4(0u, 0u, 0u, 0u);
+  if (jmp >= 0) {
+    const uint32_t bit = 1u << (jmp & 31);
+    a.x = (jmp >> 5) == 0 ? bit : 0u;
+    a.y = (jmp >> 5) == 1 ? bit : 0u;
+    a.z = (jmp >> 5) == 2 ? bit : 0u;
+    a.w = (jmp >> 5) == 3 ? bit : 0u;
+  }
+  S.jump[tid] = jmp;
+  S.g[tid] = g;
+  *reinterpret_cast<uint4*>(&S.anc[tid * kW]) = a;
+  while (bar_or<1, 128>(jmp >= 0)) {  // also the barrier after the last round's writes
+    int jj = -1;
+    df gj = {0.f, 0.f};
+    uint4 aj = make_uint4(0u, 0u, 0u, 0u);
+    if (jmp >= 0) {
+      jj = S.jump[jmp];
+      gj = S.g[jmp];
+      aj = *reinterpret_cast<const uint4*>(&S.anc[jmp * kW]);
+    }
+    TreeSync()();
+    if (jmp >= 0) {
+      g = df_add(g, gj);
+      a.x |= aj.x;
+      a.y |= aj.y;
+      a.z |= aj.z;
+      a.w |= aj.w;
+      jmp = jj;
+      S.jump[tid] = jmp;
+      S.g[tid] = g;
+      *reinterpret_cast<uint4*>(&S.anc[tid * kW]) = a;
+    }
+  }
   int dep = 0;
   if (tid < N) {
-    df g = {0.f, 0.f};
-    uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
-    for (int s = tid; s >= 0; s = S.parent[s]) {
-      g = df_add(g, df{S.la[s], 0.f});
-      const uint32_t bit = (s != tid) ? 1u << (s & 31) : 0u;
-      const int w = s >> 5;
-      a0 |= w == 0 ? bit : 0u;
-      a1 |= w == 1 ? bit : 0u;
-      a2 |= w == 2 ? bit : 0u;
-      a3 |= w == 3 ? bit : 0u;
-      ++dep;
-    }
-    S.g[tid] = g;
-    S.anc[tid * kW + 0] = a0;
-    S.anc[tid * kW + 1] = a1;
-    S.anc[tid * kW + 2] = a2;
-    S.anc[tid * kW + 3] = a3;
+    dep = __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w) + 1;
     S.depth[tid] = dep;
-    // path: sPath[t * 128 + depth(s) - 1] = s for every s on t's path
-    int ds = dep - 1;
-    for (int s = tid; s >= 0; s = S.parent[s]) sPath[tid * kTile + ds--] = (uint8_t)s;
+    // path: the strict ancestors in index order (root first), then t itself
+    uint8_t* row = sPath + tid * kTile;
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    int k = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      for (uint32_t m = aw[w]; m != 0u; m &= m - 1u) row[k++] = (uint8_t)(w * 32 + __ffs(m) - 1);
+    }
+    row[k] = (uint8_t)tid;
     atomicAdd(&S.level_start[dep], 1);
   }
   TreeSync()();
+  TC_MARK(14);
   if (warp == 0) {
     // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
     int cnt[5], run = 0;
@@ -344,6 +363,7 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
     }
   }
   TreeSync()();
+  TC_MARK(15);
   if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
 }
 
@@ -452,9 +472,9 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
 // c4*4 ..); needs no state, so it runs while the state is still in flight
 __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const Small& S,
                                                   uint8_t* smem, int b, int h, int hq, int Hqk,
-                                                  int Hv, int tid, float (&acc)[8][4]) {
+                                                  int Hv, int tid, int r8, int c4,
+                                                  float (&acc)[8][4]) {
   const int L = S.cL;
-  const int r8 = tid / 32, c4 = tid % 32;
   const float* sk = reinterpret_cast<const float*>(smem + OFF_CK);
   const float* su = reinterpret_cast<const float*>(smem + OFF_CU);
 #pragma unroll
@@ -475,76 +495,66 @@ __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const S
       const float4 uu = *reinterpret_cast<const float4*>(su + jj * kD + c4 * 4);
       const float kk[8] = {w * k0.x, w * k0.y, w * k0.z, w * k0.w,
                            w * k1.x, w * k1.y, w * k1.z, w * k1.w};
-      const float ul[4] = {uu.x, uu.y, uu.z, uu.w};
+      const float2 u01 = make_float2(uu.x, uu.y), u23 = make_float2(uu.z, uu.w);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(kk[i], ul[j], acc[i][j]);
+      for (int i = 0; i < 8; ++i) {  // packed fp32x2 FMAs (same rounding as fmaf)
+        const float2 ki = make_float2(kk[i], kk[i]);
+        const float2 lo = __ffma2_rn(ki, u01, make_float2(acc[i][0], acc[i][1]));
+        const float2 hi = __ffma2_rn(ki, u23, make_float2(acc[i][2], acc[i][3]));
+        acc[i][0] = lo.x;
+        acc[i][1] = lo.y;
+        acc[i][2] = hi.x;
+        acc[i][3] = hi.y;
+      }
     }
   }
 }
 
-// S1 = gamma S0 + acc on the raw fp32 state tile in shared memory (updated in
-// place: it is the state the next tree is verified from), then stored to fc.S1
-// as one bulk copy; all threads of the CTA
-__device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S, float* tile,
-                                              int unit, int tid, const float (&acc)[8][4]) {
-  const int r8 = tid / 32, c4 = tid % 32;
+// S1 = gamma S0 + acc on this thread's 8x4 tile of the state, in registers (it is
+// the state the next tree is verified from), also written to the fp32 tile at
+// `tile` (region 3, free at this point), which one bulk copy then stores to S1
+__device__ __forceinline__ void commit_finish(const Small& S, float* tile, int r8, int c4,
+                                              float4 (&st)[8], const float (&acc)[8][4]) {
   const float gamma = S.cgamma;
+  float* dst = tile + (r8 * 8) * kD + c4 * 4;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int row = r8 * 8 + i;
-    float4* cell = reinterpret_cast<float4*>(tile + row * kD + c4 * 4);
-    const float4 s0 = *cell;
-    float4 s1;
-    s1.x = fmaf(gamma, s0.x, acc[i][0]);
-    s1.y = fmaf(gamma, s0.y, acc[i][1]);
-    s1.z = fmaf(gamma, s0.z, acc[i][2]);
-    s1.w = fmaf(gamma, s0.w, acc[i][3]);
-    *cell = s1;
-  }
-  fence_proxy_async_smem();
-  __syncthreads();  // the committed state is in place before S0^T is formed from it
-  // the tile goes back to S1 as one bulk store; thread 0 waits for it to finish
-  // reading the tile before that region is reused
-  if (tid == 0) {
-    bulk_store(fc.S1 + (size_t)unit * kD * kD, tile, kD * kD * 4);
-    bulk_commit_group();
+    st[i].x = fmaf(gamma, st[i].x, acc[i][0]);
+    st[i].y = fmaf(gamma, st[i].y, acc[i][1]);
+    st[i].z = fmaf(gamma, st[i].z, acc[i][2]);
+    st[i].w = fmaf(gamma, st[i].w, acc[i][3]);
+    *reinterpret_cast<float4*>(dst + i * kD) = st[i];
   }
 }
 
-// S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from the raw fp32 state tile in
-// region 3; the hi half is written first, so that Q S0_hi and K S0_hi run on the
-// tensor cores while the lo half is written; then K S0_lo, and bar_ks tracks all
-// of them.  Called by kCount threads (index gtid, the issuing thread among them)
-// that Sync synchronises.
-template <int kCount, typename Sync>
+__device__ __forceinline__ float comp(const float4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from every thread's 8x4 tile of
+// the state (rows 8 r8 .., columns 4 c4 ..); the hi half is written first, so that
+// Q S0_hi and K S0_hi run on the tensor cores while the lo half is written; then
+// K S0_lo, and bar_ks tracks all of them.  All threads of the CTA.
 __device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small& S, uint32_t tmem,
-                                            int gtid, bool issuer, bool issue) {
-  constexpr int kItems = kD * 16;  // 16-byte output chunks per half
-  constexpr int kRounds = (kItems + kCount - 1) / kCount;
-  const float* raw = reinterpret_cast<const float*>(smem + OFF_U);
+                                            int r8, int c4, const float4 (&st)[8], bool issuer,
+                                            bool issue) {
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
-      const int item = gtid + r * kCount;
-      if (kItems % kCount == 0 || item < kItems) {
-        const int n = item & (kD - 1), k8 = item >> 7;
-        const float* col = raw + (k8 * 8) * kD + n;
-        uint32_t part[4];
+    for (int j = 0; j < 4; ++j) {  // column n = 4 c4 + j: rows 8 r8 .. 8 r8 + 7
+      uint32_t part[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t hi, lo;
-          split2(col[(2 * i) * kD], col[(2 * i + 1) * kD], hi, lo);
-          part[i] = half == 0 ? hi : lo;
-        }
-        *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + sw128_chunk(n, k8)) =
-            make_uint4(part[0], part[1], part[2], part[3]);
+      for (int i = 0; i < 4; ++i) {
+        uint32_t hi, lo;
+        split2(comp(st[2 * i], j), comp(st[2 * i + 1], j), hi, lo);
+        part[i] = half == 0 ? hi : lo;
       }
+      *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) +
+                                sw128_chunk(4 * c4 + j, r8)) =
+          make_uint4(part[0], part[1], part[2], part[3]);
     }
     fence_proxy_async_smem();
-    Sync()();
+    __syncthreads();
     if (issuer && issue) {
       tc_fence_after_sync();
       if (half == 0) {
@@ -562,11 +572,10 @@ __device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small
 template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmS,
-                 const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
-                 const float* __restrict__ beta, const int32_t* __restrict__ parent,
-                 __nv_bfloat16* __restrict__ o, float* __restrict__ U, gdn_tree_dims d,
-                 int32_t* dev_status, FusedCommit fc) {
+                 const float* S0, const __nv_bfloat16* __restrict__ v,
+                 const float* __restrict__ log_alpha, const float* __restrict__ beta,
+                 const int32_t* __restrict__ parent, __nv_bfloat16* __restrict__ o,
+                 float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, FusedCommit fc) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -587,25 +596,31 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int col0 = cq * 32;
   const bool live = t < N;
   const uint32_t trow_off = (uint32_t)(q4 * 32) << 16;
+  // state mapping: thread <-> 8x4 tile (rows 8 r8 .., columns 4 c4 ..); a warp holds
+  // 4 row blocks x 8 column groups, so its loads are 128-byte rows and its S0^T
+  // stores hit 8 distinct 16-byte bank groups
+  const int r8 = (warp >> 2) * 4 + (lane >> 3), c4 = (warp & 3) * 8 + (lane & 7);
   int unit = blockIdx.x;
 
   if (tid == kIssuer) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmS);
     mbar_init(&S.bar_kq, 1);
-    mbar_init(&S.bar_s0, 1);
     mbar_init(&S.bar_g, 1);
     mbar_init(&S.bar_ks, 1);
     S.err = 0;
-    S.n_loads = 0;
+    S.n_kq = 0;
     S.n_g = 0;
     S.n_ks = 0;
     S.cbad = 0;
     mbar_fence_init();
-    if (unit < n_units) issue_loads(S, smem, &tmK, &tmQ, &tmS, unit, Hv, Hqk);
+    if (unit < n_units) issue_kq(S, smem, &tmK, &tmQ, unit, Hv, Hqk);
   }
-  if (warp < 4 && unit < n_units) prefetch_tree(S, parent, beta, log_alpha, unit, N, Hv, tid);
+  if (warp < 4) {
+    if (unit < n_units) prefetch_tree(S, parent, beta, log_alpha, unit, N, Hv, tid);
+    mbar_init(&S.node_bar[tid], 1);  // one solve barrier per node (one arrival a phase)
+    mbar_fence_init();
+  }
   if (warp == 5) tmem_alloc(&S.tmem_base, kTmemCols);
   tc_fence_before_sync();
   __syncthreads();
@@ -616,20 +631,41 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t ph = it & 1u;
     const int b = unit / Hv, h = unit - b * Hv;
     const int hq = h / (Hv / Hqk);
+    const int next = unit + gridDim.x;
+
+    // this thread's 8x4 tile of the state, into registers (L2 hits: prefetched)
+    float4 st[8];
+    {
+      const float4* src =
+          reinterpret_cast<const float4*>(S0 + (size_t)unit * kD * kD + (r8 * 8) * kD + c4 * 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) st[i] = __ldg(src + i * (kD / 4));
+    }
 
     // ---- 0. tree group (warps 0-3): the unit's tree.  Operand group (warps 4-15):
-    //         the Gram MMAs once K and Q have landed; then, plain, S0^T and the
-    //         K S0 / Q S0 MMAs (1. below) while the tree group still works; fused,
-    //         the previous tree's accepted path (warps 5-15)
+    //         the Gram MMAs once K and Q have landed; fused, the previous tree's
+    //         accepted path (warps 5-15)
     TC_MARK(0);
     if (warp < 4) {
-      tree_prep(S, sPath, parent, beta, log_alpha, unit + gridDim.x, n_units, N, Hv, tid, lane, warp);
+      tree_prep(S, sPath, parent, beta, log_alpha, next, n_units, N, Hv, tid, lane, warp, unit);
       TC_MARK(8);
     } else {
       if constexpr (kFused) {
         if (warp > 4) commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 160, warp, lane);
       }
       if (tid == kIssuer) {
+        // the next unit's K, Q and state head for L2 now, so that their copies (issued
+        // when this unit's solve is over) hit L2
+        if (next < n_units) {
+          const int nb = next / Hv, nhq = (next - nb * Hv) / (Hv / Hqk);
+          tma_prefetch_l2_4d(&tmK, 0, nhq, 0, nb);
+          tma_prefetch_l2_4d(&tmK, 64, nhq, 0, nb);
+          tma_prefetch_l2_4d(&tmQ, 0, nhq, 0, nb);
+          tma_prefetch_l2_4d(&tmQ, 64, nhq, 0, nb);
+          const float* ns = S0 + (size_t)next * kD * kD;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) bulk_prefetch_l2(ns + r * (kD * kD / 4), kD * kD);
+        }
         if (!mbar_wait(&S.bar_kq, ph, kWaitLimitNs)) {
           S.err = 1;
         } else {
@@ -641,13 +677,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           ++S.n_g;
         }
       }
-      if constexpr (!kFused) {
-        // ---- 1. (plain) S0^T from the landed state, by the operand group
-        const bool s0_ok = mbar_wait(&S.bar_s0, ph, kWaitLimitNs);
-        if (!s0_ok) S.err = 1;
-        split_state<kThreads - 128, NamedSync<2, kThreads - 128>>(
-            smem, sbase, S, tmem, tid - 128, tid == kIssuer, s0_ok && S.err == 0);
-      }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -655,16 +684,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (S.err) goto fail;
     TC_MARK(1);
 
+    // ---- 1. fused: S1 = gamma S0 + K_P^T diag(w) U_P on the tile in registers, stored
+    //         to S1; then (both) S0^T from the tile
     if constexpr (kFused) {
-      // ---- 1. (fused) S1 = gamma S0 + K_P^T diag(w) U_P on the landed state tile (the
-      //         product is formed while the state is still in flight), then S0^T from S1
-      float cacc[8][4];
-      if (!S.cbad) commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, cacc);
-      if (__syncthreads_or(!mbar_wait(&S.bar_s0, ph, kWaitLimitNs))) goto fail;
-      if (!S.cbad) commit_finish(fc, S, sU, unit, tid, cacc);
+      if (!S.cbad) {
+        float cacc[8][4];
+        commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, r8, c4, cacc);
+        commit_finish(S, sU, r8, c4, st, cacc);
+      }
+      fence_proxy_async_smem();
+      __syncthreads();  // staged path rows read (S0^T goes over them); S1 tile complete
+      if (tid == 0 && !S.cbad) {  // thread 0 waits for its read before R goes into region 3
+        bulk_store(fc.S1 + (size_t)unit * kD * kD, sU, kD * kD * 4);
+        bulk_commit_group();
+      }
       TC_MARK(2);
-      split_state<kThreads, BlockSync>(smem, sbase, S, tmem, tid, tid == kIssuer, true);
     }
+    split_state(smem, sbase, S, tmem, r8, c4, st, tid == kIssuer, true);
     uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..)
 #pragma unroll
     for (int i = 0; i < 4; ++i) vreg[i] = make_uint4(0, 0, 0, 0);
@@ -753,9 +789,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               r[2 * e + 1] =
                   bt * (__uint_as_float(w4[e] & 0xffff0000u) - gam * ks[q * 8 + 2 * e + 1]);
             }
-            const int c4 = cq * 8 + q * 2;
-            *reinterpret_cast<float4*>(sU + u_index(t, c4)) = make_float4(r[0], r[1], r[2], r[3]);
-            *reinterpret_cast<float4*>(sU + u_index(t, c4 + 1)) =
+            const int cc = cq * 8 + q * 2;
+            *reinterpret_cast<float4*>(sU + u_index(t, cc)) = make_float4(r[0], r[1], r[2], r[3]);
+            *reinterpret_cast<float4*>(sU + u_index(t, cc + 1)) =
                 make_float4(r[4], r[5], r[6], r[7]);
           }
         }
@@ -771,7 +807,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                             gam * qs[4 * q + 3]);
         }
       }
-      if (cq == 0) S.ready[t] = 0;
       tc_fence_before_sync();
       __syncthreads();
     }
@@ -779,28 +814,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // ---- 5. forward substitution as a dataflow over the tree ------------------------
     // u_t = r_t - sum over ancestors a of X[t,a] u_a and o_t = seed_t + sum over
     // t's path of Y[t,s] u_s.  Warp w takes the nodes at positions w, w + 16, ... of
-    // the depth order.  For node t it waits (acquire) on the ready flag of t's
+    // the depth order.  For node t it waits (acquire) on the mbarrier of t's
     // grandparent -- every ancestor but the parent is then final -- sums those
     // terms four at a time (lane = 4 value columns), then waits on the parent and
-    // adds its term, publishes u_t and raises t's flag (release); the parent's and
-    // t's own output terms follow.  So a link of the dependency chain costs one
-    // term, not the whole ancestor sum.  No cycle of waits can form: the
-    // unfinished node of lowest depth order never waits (its ancestors come
-    // earlier in that order).
+    // adds its term, publishes u_t and arrives on t's mbarrier (release); the
+    // parent's and t's own output terms follow.  So a link of the dependency chain
+    // costs one term, not the whole ancestor sum.  No cycle of waits can form: the
+    // unfinished node of lowest depth order never waits (its ancestors come earlier
+    // in that order).
     TC_MARK(6);
     {
-      int* ready = S.ready;
       float* Ubh = U + (size_t)unit * N * kD;
       __nv_bfloat16* obh = o + ((size_t)b * N * Hv + h) * kD;
       bool timed_out = false;
+      // a waiting warp is suspended by the hardware instead of spinning
       auto wait_ready = [&](int node) {
-        uint32_t spins = 0;
-        while (ld_acquire_shared(ready + node) == 0) {
-          if (++spins > kSpinLimit) {
-            timed_out = true;
-            break;
-          }
-        }
+        if (!mbar_wait(&S.node_bar[node], ph, kWaitLimitNs)) timed_out = true;
       };
       for (int i = warp; i < N; i += kWarps) {
         const int tn = S.order[i];
@@ -847,7 +876,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
         }
         __syncwarp();
-        if (lane == 0) st_release_shared(ready + tn, 1);
+        if (lane == 0) mbar_arrive(&S.node_bar[tn]);
         py = fma4(yp, up, py);
         py = fma4(S.ydiag[tn], acc, py);
         if (write_out) {
@@ -858,14 +887,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       if (timed_out) S.err = 4;
     }
-    // regions 1 and 3 are free: the next unit's operands start loading
+    // region 1 is free: the next unit's K and Q start loading
     fence_proxy_async_smem();
     tc_fence_before_sync();
     if (__syncthreads_or(S.err)) goto fail;
     tc_fence_after_sync();
     TC_MARK(7);
-    if (tid == kIssuer && unit + (int)gridDim.x < n_units)
-      issue_loads(S, smem, &tmK, &tmQ, &tmS, unit + gridDim.x, Hv, Hqk);
+    if (tid == kIssuer && next < n_units) issue_kq(S, smem, &tmK, &tmQ, next, Hv, Hqk);
   }
   goto release;
 
@@ -875,10 +903,7 @@ fail:
   if (tid == 0 && dev_status && unit < n_units)
     atomicMax(dev_status + unit / Hv, GDN_TREE_STATUS_TIMEOUT);
   if (tid == kIssuer) {
-    if (S.n_loads > 0) {
-      mbar_wait(&S.bar_kq, (S.n_loads - 1) & 1, kWaitLimitNs);
-      mbar_wait(&S.bar_s0, (S.n_loads - 1) & 1, kWaitLimitNs);
-    }
+    if (S.n_kq > 0) mbar_wait(&S.bar_kq, (S.n_kq - 1) & 1, kWaitLimitNs);
     if (S.n_g > 0) mbar_wait(&S.bar_g, (S.n_g - 1) & 1, kWaitLimitNs);
     if (S.n_ks > 0) mbar_wait(&S.bar_ks, (S.n_ks - 1) & 1, kWaitLimitNs);
   }
@@ -923,19 +948,6 @@ bool encode_qk_map(CUtensorMap* map, const void* base, const gdn_tree_dims& d) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// S0 [B*Hv, dk, dv] fp32 -> 32-row boxes of one (b, h) state, unswizzled
-bool encode_state_map(CUtensorMap* map, const float* base, const gdn_tree_dims& d) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kD, (cuuint64_t)d.B * d.Hv};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)kD * kD * 4};
-  const cuuint32_t box[3] = {kD, kS0BoxRows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool verify_tc_supported(const gdn_tree_dims& d) {
@@ -960,9 +972,8 @@ int sm_count() {
 
 template <bool kFused>
 cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
-  CUtensorMap tmQ, tmK, tmS;
-  if (!encode_qk_map(&tmQ, a.q, a.d) || !encode_qk_map(&tmK, a.k, a.d) ||
-      !encode_state_map(&tmS, a.S0, a.d))
+  CUtensorMap tmQ, tmK;
+  if (!encode_qk_map(&tmQ, a.q, a.d) || !encode_qk_map(&tmK, a.k, a.d))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -974,7 +985,7 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   if (n_sm <= 0) return cudaErrorInvalidDevice;
   const int grid = n_units < n_sm ? n_units : n_sm;
   verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
-      tmQ, tmK, tmS, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent,
+      tmQ, tmK, a.S0, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent,
       static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, fc);
   return cudaGetLastError();
 }
