@@ -14,11 +14,13 @@
 //   a persistent grid, one CTA (512 threads, 512 TMEM columns) per SM, walks the
 //   (sequence b, v-head h) units; the next unit's operands are already being
 //   loaded while the current unit finishes.  Per unit:
-//   1. TMA (128-byte swizzle) brings K and Q of the q/k head; each thread loads an
+//   1. TMA (128-byte swizzle) brings K and Q of the q/k head and v of the unit
+//      (issued as soon as the previous unit's solve is over); each thread loads an
 //      8 x 4 tile of the fp32 state into registers and writes it as S0^T = hi + lo,
 //      two bf16 K-major tiles, so K S0 keeps fp32 accuracy (K is exact in bf16).
 //      (Fused with the delayed commitment, the tile is first committed in registers
-//      and stored as S1.)
+//      and stored as S1.)  No thread waits on its own global loads near shared-memory
+//      work: the state tile is its only per-thread load.
 //   2. tcgen05.mma, accumulators in TMEM:  G_kk = K K^T, G_qk = Q K^T,
 //      KS = K S0_hi + K S0_lo, QS = Q S0_hi.
 //   3. TMEM -> registers (thread = tree node): the X and Y entries of the node's
@@ -61,15 +63,36 @@ constexpr int kIssuer = 128;  // the one thread that issues every copy and MMA (
 constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
 
 #ifdef GDN_TC_PROFILE
-// per-unit phase timestamps for a profiling build (never in the product build)
-__device__ unsigned long long g_tc_phase[4096][16];
-#define TC_MARK_BY(thread, i)                                                           \
-  do {                                                                                  \
-    if (threadIdx.x == (thread) && unit < 4096) g_tc_phase[unit][i] = globaltimer_ns(); \
+// per-unit phase timestamps for a profiling build (never in the product build):
+// SM clock counts kept in shared memory during the unit, dumped with the unit's
+// global-timer span (slots 16, 17) once it is over
+constexpr int kMarks = 18;
+__device__ unsigned long long g_tc_phase[4096][kMarks];
+#define TC_MARK_BY(thread, i)                      \
+  do {                                             \
+    if (threadIdx.x == (thread)) S.marks[i] = clock64(); \
+  } while (0)
+#define TC_DUMP()                                                           \
+  do {                                                                      \
+    if (threadIdx.x == 0 && unit < 4096) {                                  \
+      for (int i_ = 0; i_ < 16; ++i_) g_tc_phase[unit][i_] = S.marks[i_];   \
+      g_tc_phase[unit][16] = S.gt0;                                         \
+      g_tc_phase[unit][17] = globaltimer_ns();                              \
+    }                                                                       \
+  } while (0)
+#define TC_START()                                  \
+  do {                                              \
+    if (threadIdx.x == 0) S.gt0 = globaltimer_ns(); \
   } while (0)
 #else
 #define TC_MARK_BY(thread, i) \
   do {                        \
+  } while (0)
+#define TC_DUMP() \
+  do {            \
+  } while (0)
+#define TC_START() \
+  do {             \
   } while (0)
 #endif
 #define TC_MARK(i) TC_MARK_BY(0, i)
@@ -89,8 +112,9 @@ constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;
 constexpr uint32_t OFF_S0H = 2 * kOpBytes;
 constexpr uint32_t OFF_S0L = 3 * kOpBytes;
 constexpr uint32_t OFF_P = 2 * kOpBytes;
-// region 3: fused, the committed state tile on its way out (bulk store); then R / U
+// region 3: v (TMA, 128-byte swizzle, first 32 KB) until it is read; then R / U
 constexpr uint32_t OFF_U = 4 * kOpBytes;
+constexpr uint32_t OFF_V = OFF_U;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
 constexpr uint32_t kSmallBytes = 13824;
@@ -118,11 +142,11 @@ struct Small {
   int pre_parent[kTile];
   float pre_beta[kTile];
   float pre_la[kTile];
-  uint64_t bar_kq, bar_g, bar_ks;
+  uint64_t bar_kq, bar_v, bar_g, bar_ks;
   uint32_t tmem_base;
   int err;
   int bad;  // the tree failed validation
-  int n_kq, n_g, n_ks;  // phases issued on bar_kq, bar_g, bar_ks
+  int n_kq, n_g, n_ks;  // phases issued on bar_kq (and bar_v), bar_g, bar_ks
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
   float cla[kMaxN];
@@ -130,6 +154,10 @@ struct Small {
   float cgamma;
   int cL;
   int cbad;
+#ifdef GDN_TC_PROFILE
+  unsigned long long marks[16];
+  unsigned long long gt0;
+#endif
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
 static_assert(offsetof(Small, g) % 16 == 0, "path log-decays are read as float4");
@@ -237,15 +265,20 @@ __device__ __forceinline__ int bar_or(int v) {
   return r;
 }
 
-// K and Q of the unit's q/k head into region 1 (bar_kq); issuing thread only
-__device__ __forceinline__ void issue_kq(Small& S, uint8_t* smem, const CUtensorMap* tmK,
-                                         const CUtensorMap* tmQ, int unit, int Hv, int Hqk) {
+// K and Q of the unit's q/k head into region 1 (bar_kq), its v rows into region 3
+// (bar_v); issuing thread only
+__device__ __forceinline__ void issue_kqv(Small& S, uint8_t* smem, const CUtensorMap* tmK,
+                                          const CUtensorMap* tmQ, const CUtensorMap* tmV,
+                                          int unit, int Hv, int Hqk) {
   const int b = unit / Hv, h = unit - b * Hv, hq = h / (Hv / Hqk);
   mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
   tma_load_4d(smem + OFF_K, tmK, &S.bar_kq, 0, hq, 0, b);
   tma_load_4d(smem + OFF_K + kTileBytes, tmK, &S.bar_kq, 64, hq, 0, b);
   tma_load_4d(smem + OFF_Q, tmQ, &S.bar_kq, 0, hq, 0, b);
   tma_load_4d(smem + OFF_Q + kTileBytes, tmQ, &S.bar_kq, 64, hq, 0, b);
+  mbar_arrive_expect_tx(&S.bar_v, 2 * kTileBytes);
+  tma_load_4d(smem + OFF_V, tmV, &S.bar_v, 0, h, 0, b);
+  tma_load_4d(smem + OFF_V + kTileBytes, tmV, &S.bar_v, 64, h, 0, b);
   ++S.n_kq;
 }
 
@@ -511,12 +544,12 @@ __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const S
 }
 
 // S1 = gamma S0 + acc on this thread's 8x4 tile of the state, in registers (it is
-// the state the next tree is verified from), also written to the fp32 tile at
-// `tile` (region 3, free at this point), which one bulk copy then stores to S1
-__device__ __forceinline__ void commit_finish(const Small& S, float* tile, int r8, int c4,
-                                              float4 (&st)[8], const float (&acc)[8][4]) {
+// the state the next tree is verified from), stored to fc.S1
+__device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S, int unit,
+                                              int r8, int c4, float4 (&st)[8],
+                                              const float (&acc)[8][4]) {
   const float gamma = S.cgamma;
-  float* dst = tile + (r8 * 8) * kD + c4 * 4;
+  float* dst = fc.S1 + (size_t)unit * kD * kD + (r8 * 8) * kD + c4 * 4;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     st[i].x = fmaf(gamma, st[i].x, acc[i][0]);
@@ -572,7 +605,7 @@ __device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small
 template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const float* S0, const __nv_bfloat16* __restrict__ v,
+                 const __grid_constant__ CUtensorMap tmV, const float* S0,
                  const float* __restrict__ log_alpha, const float* __restrict__ beta,
                  const int32_t* __restrict__ parent, __nv_bfloat16* __restrict__ o,
                  float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, FusedCommit fc) {
@@ -605,7 +638,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (tid == kIssuer) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmV);
     mbar_init(&S.bar_kq, 1);
+    mbar_init(&S.bar_v, 1);
     mbar_init(&S.bar_g, 1);
     mbar_init(&S.bar_ks, 1);
     S.err = 0;
@@ -614,7 +649,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     S.n_ks = 0;
     S.cbad = 0;
     mbar_fence_init();
-    if (unit < n_units) issue_kq(S, smem, &tmK, &tmQ, unit, Hv, Hqk);
+    if (unit < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, unit, Hv, Hqk);
   }
   if (warp < 4) {
     if (unit < n_units) prefetch_tree(S, parent, beta, log_alpha, unit, N, Hv, tid);
@@ -645,6 +680,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // ---- 0. tree group (warps 0-3): the unit's tree.  Operand group (warps 4-15):
     //         the Gram MMAs once K and Q have landed; fused, the previous tree's
     //         accepted path (warps 5-15)
+    TC_START();
     TC_MARK(0);
     if (warp < 4) {
       tree_prep(S, sPath, parent, beta, log_alpha, next, n_units, N, Hv, tid, lane, warp, unit);
@@ -662,6 +698,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           tma_prefetch_l2_4d(&tmK, 64, nhq, 0, nb);
           tma_prefetch_l2_4d(&tmQ, 0, nhq, 0, nb);
           tma_prefetch_l2_4d(&tmQ, 64, nhq, 0, nb);
+          tma_prefetch_l2_4d(&tmV, 0, next - nb * Hv, 0, nb);
+          tma_prefetch_l2_4d(&tmV, 64, next - nb * Hv, 0, nb);
           const float* ns = S0 + (size_t)next * kD * kD;
 #pragma unroll
           for (int r = 0; r < 4; ++r) bulk_prefetch_l2(ns + r * (kD * kD / 4), kD * kD);
@@ -690,26 +728,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!S.cbad) {
         float cacc[8][4];
         commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, r8, c4, cacc);
-        commit_finish(S, sU, r8, c4, st, cacc);
+        commit_finish(fc, S, unit, r8, c4, st, cacc);
       }
-      fence_proxy_async_smem();
-      __syncthreads();  // staged path rows read (S0^T goes over them); S1 tile complete
-      if (tid == 0 && !S.cbad) {  // thread 0 waits for its read before R goes into region 3
-        bulk_store(fc.S1 + (size_t)unit * kD * kD, sU, kD * kD * 4);
-        bulk_commit_group();
-      }
+      __syncthreads();  // the staged path rows are read before S0^T goes over them
       TC_MARK(2);
     }
     split_state(smem, sbase, S, tmem, r8, c4, st, tid == kIssuer, true);
-    uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vreg[i] = make_uint4(0, 0, 0, 0);
-    if (live) {
-      const uint4* vrow =
-          reinterpret_cast<const uint4*>(v + (((size_t)b * N + t) * Hv + h) * kD + col0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vreg[i] = __ldg(vrow + i);
-    }
     TC_MARK(3);
     const bool cbad = kFused && S.cbad;
     if (h == 0 && tid == 0) {
@@ -764,9 +788,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       //         R = beta (V - gamma K S0) to region 3, output seeds gamma Q S0 to region 2
       if (!mbar_wait(&S.bar_ks, ph, kWaitLimitNs)) S.err = 2;
       tc_fence_after_sync();
-      if constexpr (kFused) {
-        if (tid == 0) bulk_wait_read_all();  // the S1 store has read the tile R goes into
-      }
+      uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..), read before
+                      // R goes over them
+      if (!mbar_wait(&S.bar_v, ph, kWaitLimitNs)) S.err = 2;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        vreg[i] = *reinterpret_cast<const uint4*>(smem + OFF_V + sw128_chunk(t, cq * 4 + i));
       if (__syncthreads_or(S.err)) goto fail;
       TC_MARK(5);
       if (live) {
@@ -893,7 +920,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (__syncthreads_or(S.err)) goto fail;
     tc_fence_after_sync();
     TC_MARK(7);
-    if (tid == kIssuer && next < n_units) issue_kq(S, smem, &tmK, &tmQ, next, Hv, Hqk);
+    TC_DUMP();
+    if (tid == kIssuer && next < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, next, Hv, Hqk);
   }
   goto release;
 
@@ -903,15 +931,15 @@ fail:
   if (tid == 0 && dev_status && unit < n_units)
     atomicMax(dev_status + unit / Hv, GDN_TREE_STATUS_TIMEOUT);
   if (tid == kIssuer) {
-    if (S.n_kq > 0) mbar_wait(&S.bar_kq, (S.n_kq - 1) & 1, kWaitLimitNs);
+    if (S.n_kq > 0) {
+      mbar_wait(&S.bar_kq, (S.n_kq - 1) & 1, kWaitLimitNs);
+      mbar_wait(&S.bar_v, (S.n_kq - 1) & 1, kWaitLimitNs);
+    }
     if (S.n_g > 0) mbar_wait(&S.bar_g, (S.n_g - 1) & 1, kWaitLimitNs);
     if (S.n_ks > 0) mbar_wait(&S.bar_ks, (S.n_ks - 1) & 1, kWaitLimitNs);
   }
 
 release:
-  if constexpr (kFused) {
-    if (tid == 0) bulk_wait_all();  // every S1 store is complete before the CTA leaves
-  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
@@ -933,14 +961,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// q or k [B, N, Hqk, 128] bf16 -> boxes of 64 (K) x 128 (nodes); nodes past N
-// read as zeros
-bool encode_qk_map(CUtensorMap* map, const void* base, const gdn_tree_dims& d) {
+// q, k [B, N, Hqk, 128] or v [B, N, Hv, 128] bf16 (`heads` = Hqk or Hv) -> boxes
+// of 64 (columns) x 128 (nodes), 128-byte swizzled; nodes past N read as zeros
+bool encode_rows_map(CUtensorMap* map, const void* base, const gdn_tree_dims& d, int heads) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)d.Hqk, (cuuint64_t)d.N, (cuuint64_t)d.B};
-  const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)d.Hqk * kD * 2,
-                                 (cuuint64_t)d.N * d.Hqk * kD * 2};
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)d.N, (cuuint64_t)d.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2,
+                                 (cuuint64_t)d.N * heads * kD * 2};
   const cuuint32_t box[4] = {64, 1, kTile, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -972,8 +1000,9 @@ int sm_count() {
 
 template <bool kFused>
 cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
-  CUtensorMap tmQ, tmK;
-  if (!encode_qk_map(&tmQ, a.q, a.d) || !encode_qk_map(&tmK, a.k, a.d))
+  CUtensorMap tmQ, tmK, tmV;
+  if (!encode_rows_map(&tmQ, a.q, a.d, a.d.Hqk) || !encode_rows_map(&tmK, a.k, a.d, a.d.Hqk) ||
+      !encode_rows_map(&tmV, a.v, a.d, a.d.Hv))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -985,7 +1014,7 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   if (n_sm <= 0) return cudaErrorInvalidDevice;
   const int grid = n_units < n_sm ? n_units : n_sm;
   verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
-      tmQ, tmK, a.S0, static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent,
+      tmQ, tmK, tmV, a.S0, a.log_alpha, a.beta, a.parent,
       static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, fc);
   return cudaGetLastError();
 }
@@ -1014,6 +1043,7 @@ cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stre
 #ifdef GDN_TC_PROFILE
 extern "C" int gdn_tree_debug_tc_phases(unsigned long long* host, int n_units) {
   return (int)cudaMemcpyFromSymbol(
-      host, gdn::g_tc_phase, sizeof(unsigned long long) * 16 * (n_units < 4096 ? n_units : 4096));
+      host, gdn::g_tc_phase,
+      sizeof(unsigned long long) * gdn::kMarks * (n_units < 4096 ? n_units : 4096));
 }
 #endif
