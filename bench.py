@@ -145,16 +145,16 @@ def arithmetic_dtype(kernel: str) -> str:
 
 
 def profiled_traffic(kernel: str):
-    """dram read+write bytes per launch from the committed ncu summary, or None
-    when it was taken on a different kernel source."""
+    """dram read+write bytes per launch of `kernel` from the committed ncu record,
+    or None when the record was taken on a different kernel source or lacks it."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel") != kernel or rec.get("source_sha") != kernel_source_sha():
+    if rec.get("source_sha") != kernel_source_sha():
         return None
-    return rec.get("traffic_bytes_per_launch")
+    return rec.get("kernels", {}).get(kernel, {}).get("traffic_bytes_per_launch")
 
 
 class ClockSampler:
@@ -473,7 +473,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                                / (hbm * 1e9),
                                "roofline_frac": t_roof_sep / (sep_ms * 1e-3),
                                "verify_flops": vf, "commit_flops": cf,
-                               "verify_kernel": verify_kernel_name(w)},
+                               "verify_kernel": verify_kernel_name(w),
+                               "verify_traffic": profiled_traffic(verify_kernel_name(w))},
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
