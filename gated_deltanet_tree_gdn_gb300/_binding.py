@@ -19,8 +19,8 @@ BF16, F32 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECUDA = 0, -1, -2, -3
 STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TIMEOUT = 0, 1, 2, 3
 
-SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_commit_verify", "gdn_tree_strerror",
-           "gdn_tree_version")
+SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_commit_verify",
+           "gdn_tree_verify_recurrent", "gdn_tree_strerror", "gdn_tree_version")
 
 
 class Dims(ctypes.Structure):
@@ -54,6 +54,8 @@ def load(path: str | None = None):
     vp, fp, ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
     lib.gdn_tree_verify.argtypes = [vp, vp, vp, fp, fp, ip, fp, vp, fp, Dims, ip, vp]
     lib.gdn_tree_verify.restype = ctypes.c_int
+    lib.gdn_tree_verify_recurrent.argtypes = [vp, vp, vp, fp, fp, ip, fp, vp, fp, Dims, ip, vp]
+    lib.gdn_tree_verify_recurrent.restype = ctypes.c_int
     lib.gdn_tree_commit.argtypes = [ip, ip, ip, fp, vp, fp, fp, fp, Dims, ctypes.c_int32, ip, vp]
     lib.gdn_tree_commit.restype = ctypes.c_int
     lib.gdn_tree_commit_verify.argtypes = [ip, ip, ip, fp, vp, fp, ctypes.c_int32, ctypes.c_int32,
@@ -122,6 +124,20 @@ def verify(q, k, v, log_alpha, beta, parent, S0, *, o=None, U=None, dev_status=N
     (q's dtype) and U [B,Hv,N,dv] fp32 are allocated when not given.
     dev_status, if given, is an int32 [B] CUDA tensor filled per sequence.
     """
+    return _verify("gdn_tree_verify", q, k, v, log_alpha, beta, parent, S0, o, U, dev_status,
+                   stream)
+
+
+def verify_recurrent(q, k, v, log_alpha, beta, parent, S0, *, o=None, U=None, dev_status=None,
+                     stream=None):
+    """Single-branch recurrent verification (C ABI gdn_tree_verify_recurrent), the
+    baseline the tree verification is measured against: same arguments and
+    outputs as ``verify``.  Returns (o, U)."""
+    return _verify("gdn_tree_verify_recurrent", q, k, v, log_alpha, beta, parent, S0, o, U,
+                   dev_status, stream)
+
+
+def _verify(symbol, q, k, v, log_alpha, beta, parent, S0, o, U, dev_status, stream):
     B, N, Hqk, dk = q.shape
     Hv, dv = v.shape[2], v.shape[3]
     dt = q.dtype
@@ -140,11 +156,11 @@ def verify(q, k, v, log_alpha, beta, parent, S0, *, o=None, U=None, dev_status=N
     _check(U, "U", torch.float32, (B, Hv, N, dv))
     if dev_status is not None:
         _check(dev_status, "dev_status", torch.int32, (B,))
-    rc = load().gdn_tree_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                                _ptr(parent), _ptr(S0), _ptr(o), _ptr(U), dims_of(q, v),
-                                _ptr(dev_status), _stream(stream))
+    rc = getattr(load(), symbol)(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(parent), _ptr(S0), _ptr(o), _ptr(U), dims_of(q, v),
+                                 _ptr(dev_status), _stream(stream))
     if rc != OK:
-        raise GdnTreeError(rc, "gdn_tree_verify")
+        raise GdnTreeError(rc, symbol)
     return o, U
 
 

@@ -81,6 +81,23 @@ int gdn_tree_verify(const void* q, const void* k, const void* v, const float* lo
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
 
+int gdn_tree_verify_recurrent(const void* q, const void* k, const void* v,
+                              const float* log_alpha, const float* beta,
+                              const int32_t* parent, const float* S0, void* o, float* U,
+                              gdn_tree_dims dims, int32_t* dev_status, void* stream) {
+  const int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  if (dims.B == 0 || dims.N == 0) return GDN_TREE_OK;  // nothing to do
+  const void* ptrs[] = {q, k, v, log_alpha, beta, parent, S0, o, U};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return GDN_TREE_EINVAL;
+  if (dims.Hv > 65535) return GDN_TREE_EUNSUPPORTED;  // the grid's y dimension
+  gdn::VerifyArgs a{q, k, v, log_alpha, beta, parent, S0, o, U, dims, dev_status};
+  const cudaError_t err = gdn::launch_verify_recurrent(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
 int gdn_tree_commit(const int32_t* path, const int32_t* path_len, const int32_t* parent,
                     const float* U, const void* k, const float* log_alpha, const float* S0,
                     float* S1, gdn_tree_dims dims, int32_t Lmax, int32_t* dev_status,

@@ -60,6 +60,9 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
 
+// single-branch recurrent verification (the measurement baseline)
+cudaError_t launch_verify_recurrent(const VerifyArgs& a, cudaStream_t stream);
+
 bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N);
 cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream);

@@ -159,6 +159,26 @@ int gdn_tree_commit_verify(const int32_t *prev_path, const int32_t *prev_path_le
                            const int32_t *parent, void *o, float *U, gdn_tree_dims dims,
                            int32_t *commit_status, int32_t *verify_status, void *stream);
 
+/*
+ * gdn_tree_verify_recurrent -- the same outputs as gdn_tree_verify, computed by
+ * single-branch recurrent verification: the baseline the tree verification is
+ * measured against.
+ *
+ * The DFlash-TfM page, results section ("Efficienza di Verifica"), compares its
+ * fused tree kernel with verifying every branch by its own recurrent pass.  Here
+ * every root-to-leaf branch of the tree runs the GDN recurrence of section 3
+ * ("Sfida") from its own copy of S0[b, h], node by node, writing o and U of each
+ * node it passes; a node shared by several branches is recomputed by each of
+ * them, with identical bits.  All arithmetic is fp32.
+ *
+ * Arguments, layouts, ownership, limits and dev_status exactly as for
+ * gdn_tree_verify.  The state of a branch is held on chip; nothing is allocated.
+ */
+int gdn_tree_verify_recurrent(const void *q, const void *k, const void *v,
+                              const float *log_alpha, const float *beta,
+                              const int32_t *parent, const float *S0, void *o, float *U,
+                              gdn_tree_dims dims, int32_t *dev_status, void *stream);
+
 /* Human-readable text for a return code or a device status code. */
 const char *gdn_tree_strerror(int code);
 
