@@ -17,10 +17,11 @@ from . import build as _build
 
 BF16, F32 = 0, 1
 OK, EINVAL, EUNSUPPORTED, ECUDA = 0, -1, -2, -3
-STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TIMEOUT = 0, 1, 2, 3
+STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TIMEOUT, STATUS_BAD_LAYOUT = 0, 1, 2, 3, 4
 
 SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_commit_verify",
-           "gdn_tree_verify_recurrent", "gdn_tree_strerror", "gdn_tree_version")
+           "gdn_tree_verify_recurrent", "gdn_tree_verify_packed", "gdn_tree_commit_packed",
+           "gdn_tree_commit_verify_packed", "gdn_tree_strerror", "gdn_tree_version")
 
 
 class Dims(ctypes.Structure):
@@ -62,6 +63,17 @@ def load(path: str | None = None):
                                            fp, fp, vp, vp, vp, fp, fp, ip, vp, fp, Dims, ip, ip,
                                            vp]
     lib.gdn_tree_commit_verify.restype = ctypes.c_int
+    i32 = ctypes.c_int32
+    lib.gdn_tree_verify_packed.argtypes = [vp, vp, vp, fp, fp, ip, ip, i32, fp, ip, i32, vp, fp,
+                                           Dims, ip, vp]
+    lib.gdn_tree_verify_packed.restype = ctypes.c_int
+    lib.gdn_tree_commit_packed.argtypes = [ip, ip, ip, ip, i32, fp, vp, fp, fp, fp, ip, i32, Dims,
+                                           i32, ip, vp]
+    lib.gdn_tree_commit_packed.restype = ctypes.c_int
+    lib.gdn_tree_commit_verify_packed.argtypes = [ip, ip, ip, ip, i32, fp, vp, fp, i32, i32, fp,
+                                                  fp, ip, i32, vp, vp, vp, fp, fp, ip, ip, i32,
+                                                  vp, fp, Dims, ip, ip, vp]
+    lib.gdn_tree_commit_verify_packed.restype = ctypes.c_int
     lib.gdn_tree_strerror.argtypes = [ctypes.c_int]
     lib.gdn_tree_strerror.restype = ctypes.c_char_p
     lib.gdn_tree_version.argtypes = []
@@ -243,3 +255,154 @@ def commit_verify(prev_path, prev_path_len, prev_U, prev_k, prev_log_alpha, S_pr
     if rc != OK:
         raise GdnTreeError(rc, "gdn_tree_commit_verify")
     return S1, o, U
+
+
+# ---------------------------------------------------------------------------
+# packed (ragged) batches with a state pool
+# ---------------------------------------------------------------------------
+
+def _packed_rows(cu_nodes, B):
+    _check(cu_nodes, "cu_nodes", torch.int32, (B + 1,))
+
+
+def _slots(state_slot, B, pool):
+    if state_slot is not None:
+        _check(state_slot, "state_slot", torch.int32, (B,))
+    return pool.shape[0]
+
+
+def verify_packed(q, k, v, log_alpha, beta, parent, cu_nodes, state_pool, *, state_slot=None,
+                  N_max=None, o=None, U=None, dev_status=None, stream=None):
+    """Tree verification of a packed (ragged) batch (C ABI gdn_tree_verify_packed).
+    Returns (o, U).
+
+    q, k [T,Hqk,dk], v [T,Hv,dv] (bf16 or fp32); log_alpha, beta [T,Hv]; parent
+    [T] (indices within each sequence); cu_nodes [B+1] int32 row offsets;
+    state_pool [n_slots,Hv,dk,dv] fp32 with state_slot [B] (None: slot b).
+    N_max is the largest tree (computed from cu_nodes on the host if None).
+    o [T,Hv,dv] and U [Hv,T,dv] are allocated when not given."""
+    T, Hqk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    B = cu_nodes.shape[0] - 1
+    dt = q.dtype
+    _packed_rows(cu_nodes, B)
+    _check(q, "q", dt)
+    _check(k, "k", dt, (T, Hqk, dk))
+    _check(v, "v", dt, (T, Hv, dv))
+    _check(log_alpha, "log_alpha", torch.float32, (T, Hv))
+    _check(beta, "beta", torch.float32, (T, Hv))
+    _check(parent, "parent", torch.int32, (T,))
+    _check(state_pool, "state_pool", torch.float32, (state_pool.shape[0], Hv, dk, dv))
+    n_slots = _slots(state_slot, B, state_pool)
+    if N_max is None:
+        N_max = int((cu_nodes[1:] - cu_nodes[:-1]).max().item()) if B > 0 else 0
+    if o is None:
+        o = torch.empty((T, Hv, dv), dtype=dt, device=q.device)
+    if U is None:
+        U = torch.empty((Hv, T, dv), dtype=torch.float32, device=q.device)
+    _check(o, "o", dt, (T, Hv, dv))
+    _check(U, "U", torch.float32, (Hv, T, dv))
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (B,))
+    d = Dims(B, N_max, Hqk, Hv, dk, dv, _dtype_code(q))
+    rc = load().gdn_tree_verify_packed(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                       _ptr(parent), _ptr(cu_nodes), T, _ptr(state_pool),
+                                       _ptr(state_slot), n_slots, _ptr(o), _ptr(U), d,
+                                       _ptr(dev_status), _stream(stream))
+    if rc != OK:
+        raise GdnTreeError(rc, "gdn_tree_verify_packed")
+    return o, U
+
+
+def commit_packed(path, path_len, U, k, log_alpha, cu_nodes, pool_in, *, pool_out=None,
+                  state_slot=None, parent=None, N_max=None, dev_status=None, stream=None):
+    """Delayed commitment of a packed batch (C ABI gdn_tree_commit_packed):
+    pool_out[state_slot[b]] = the state after sequence b's accepted path.  Returns
+    pool_out (pool_out=pool_in commits in place; a new pool starts as a copy of
+    pool_in, so that untouched slots keep their states)."""
+    T, Hqk, dk = k.shape
+    Hv, dv = pool_in.shape[1], pool_in.shape[3]
+    B = cu_nodes.shape[0] - 1
+    _packed_rows(cu_nodes, B)
+    _check(path, "path", torch.int32)
+    Lmax = path.shape[1]
+    _check(path_len, "path_len", torch.int32, (B,))
+    _check(U, "U", torch.float32, (Hv, T, dv))
+    _check(k, "k")
+    _check(log_alpha, "log_alpha", torch.float32, (T, Hv))
+    _check(pool_in, "pool_in", torch.float32)
+    n_slots = _slots(state_slot, B, pool_in)
+    if pool_out is None:
+        pool_out = pool_in.clone()
+    _check(pool_out, "pool_out", torch.float32, tuple(pool_in.shape))
+    if parent is not None:
+        _check(parent, "parent", torch.int32, (T,))
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (B,))
+    if N_max is None:
+        N_max = int((cu_nodes[1:] - cu_nodes[:-1]).max().item()) if B > 0 else 0
+    d = Dims(B, N_max, Hqk, Hv, dk, dv, _dtype_code(k))
+    rc = load().gdn_tree_commit_packed(_ptr(path), _ptr(path_len), _ptr(parent), _ptr(cu_nodes),
+                                       T, _ptr(U), _ptr(k), _ptr(log_alpha), _ptr(pool_in),
+                                       _ptr(pool_out), _ptr(state_slot), n_slots, d, Lmax,
+                                       _ptr(dev_status), _stream(stream))
+    if rc != OK:
+        raise GdnTreeError(rc, "gdn_tree_commit_packed")
+    return pool_out
+
+
+def commit_verify_packed(prev_path, prev_path_len, prev_U, prev_k, prev_log_alpha, prev_cu_nodes,
+                         pool_in, q, k, v, log_alpha, beta, parent, cu_nodes, *, pool_out=None,
+                         state_slot=None, prev_parent=None, prev_N_max=None, N_max=None, o=None,
+                         U=None, commit_status=None, verify_status=None, stream=None):
+    """One decoding iteration of a packed batch (C ABI gdn_tree_commit_verify_packed).
+    Returns (pool_out, o, U); pool_out=pool_in commits in place."""
+    T, Hqk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    Tp = prev_k.shape[0]
+    B = cu_nodes.shape[0] - 1
+    dt = q.dtype
+    _packed_rows(cu_nodes, B)
+    _packed_rows(prev_cu_nodes, B)
+    _check(prev_path, "prev_path", torch.int32)
+    Lmax = prev_path.shape[1]
+    _check(prev_path_len, "prev_path_len", torch.int32, (B,))
+    _check(prev_U, "prev_U", torch.float32, (Hv, Tp, dv))
+    _check(prev_k, "prev_k", dt, (Tp, Hqk, dk))
+    _check(prev_log_alpha, "prev_log_alpha", torch.float32, (Tp, Hv))
+    _check(pool_in, "pool_in", torch.float32)
+    n_slots = _slots(state_slot, B, pool_in)
+    _check(q, "q", dt)
+    _check(k, "k", dt, (T, Hqk, dk))
+    _check(v, "v", dt, (T, Hv, dv))
+    _check(log_alpha, "log_alpha", torch.float32, (T, Hv))
+    _check(beta, "beta", torch.float32, (T, Hv))
+    _check(parent, "parent", torch.int32, (T,))
+    if pool_out is None:
+        pool_out = pool_in.clone()
+    if o is None:
+        o = torch.empty((T, Hv, dv), dtype=dt, device=q.device)
+    if U is None:
+        U = torch.empty((Hv, T, dv), dtype=torch.float32, device=q.device)
+    _check(pool_out, "pool_out", torch.float32, tuple(pool_in.shape))
+    _check(o, "o", dt, (T, Hv, dv))
+    _check(U, "U", torch.float32, (Hv, T, dv))
+    if prev_parent is not None:
+        _check(prev_parent, "prev_parent", torch.int32, (Tp,))
+    for name, st in (("commit_status", commit_status), ("verify_status", verify_status)):
+        if st is not None:
+            _check(st, name, torch.int32, (B,))
+    if N_max is None:
+        N_max = int((cu_nodes[1:] - cu_nodes[:-1]).max().item()) if B > 0 else 0
+    if prev_N_max is None:
+        prev_N_max = int((prev_cu_nodes[1:] - prev_cu_nodes[:-1]).max().item()) if B > 0 else 0
+    d = Dims(B, N_max, Hqk, Hv, dk, dv, _dtype_code(q))
+    rc = load().gdn_tree_commit_verify_packed(
+        _ptr(prev_path), _ptr(prev_path_len), _ptr(prev_parent), _ptr(prev_cu_nodes), Tp,
+        _ptr(prev_U), _ptr(prev_k), _ptr(prev_log_alpha), prev_N_max, Lmax, _ptr(pool_in),
+        _ptr(pool_out), _ptr(state_slot), n_slots, _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+        _ptr(beta), _ptr(parent), _ptr(cu_nodes), T, _ptr(o), _ptr(U), d, _ptr(commit_status),
+        _ptr(verify_status), _stream(stream))
+    if rc != OK:
+        raise GdnTreeError(rc, "gdn_tree_commit_verify_packed")
+    return pool_out, o, U

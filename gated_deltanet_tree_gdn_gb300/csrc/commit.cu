@@ -41,7 +41,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
               const int32_t* __restrict__ parent, const float* __restrict__ U,
               const T* __restrict__ k, const float* __restrict__ log_alpha,
               const float* S0, float* S1, gdn_tree_dims d, int32_t Lmax,
-              int32_t* dev_status) {
+              int32_t* dev_status, SeqLayout lay) {
   // S0 and S1 may alias (in-place commit): the whole state is copied into
   // shared memory before any element of S1 is written.
   extern __shared__ __align__(128) float smem_f[];
@@ -54,12 +54,21 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   __shared__ uint64_t sBar;
   __shared__ float sGamma;
 
-  const int N = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
+  const int Nmax = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
   const int h = blockIdx.x, b = blockIdx.y, row0 = blockIdx.z * kRowsPerCta;
   const int hq = h / (Hv / Hqk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = min(kRowsPerCta, dk - row0);
-  const size_t sbase = ((size_t)b * Hv + h) * dk * dv;
+  // this sequence's tree rows and state
+  const int N = lay.count(b, Nmax), st = lay.state(b);
+  if (N < 0 || st < 0) {
+    if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
+      dev_status[b] = GDN_TREE_STATUS_BAD_LAYOUT;
+    return;
+  }
+  const size_t row = (size_t)lay.row0(b, Nmax);
+  const size_t urow = lay.urow0(b, h, Hv, Nmax);
+  const size_t sbase = ((size_t)st * Hv + h) * dk * dv;
 
   // ---- this CTA's rows of the (b, h) state start streaming in at once ----------
   if (tid == 0) {
@@ -88,20 +97,20 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     // the tree given it must also follow the parent links
     const int prev = tid == 0 ? -1 : sPath[tid - 1];
     bad |= (tid > 0 && pj <= prev);
-    if (parent) bad |= (parent[(size_t)b * N + pj] != prev);
-    sLa[tid] = log_alpha[((size_t)b * N + pj) * Hv + h];
+    if (parent) bad |= (parent[row + pj] != prev);
+    sLa[tid] = log_alpha[(row + pj) * Hv + h];
   }
   auto stage = [&](int j0, int nj) {
     for (int e = tid; e < nj * (rows / 4); e += kThreads) {
       const int jj = e / (rows / 4), c = (e % (rows / 4)) * 4;
-      const T* kr = k + (((size_t)b * N + sPath[j0 + jj]) * Hqk + hq) * dk + row0 + c;
+      const T* kr = k + ((row + sPath[j0 + jj]) * Hqk + hq) * dk + row0 + c;
       *reinterpret_cast<float4*>(sK + jj * kRowsPerCta + c) =
           make_float4(to_f32(kr[0]), to_f32(kr[1]), to_f32(kr[2]), to_f32(kr[3]));
     }
     for (int e = tid; e < nj * (dv / 4); e += kThreads) {
       const int jj = e / (dv / 4), c = (e % (dv / 4)) * 4;
       *reinterpret_cast<float4*>(sU + jj * dv + c) = *reinterpret_cast<const float4*>(
-          U + (((size_t)b * Hv + h) * N + sPath[j0 + jj]) * dv + c);
+          U + (urow + sPath[j0 + jj]) * dv + c);
     }
   };
   if (!bad) stage(0, min(kChunk, L));
@@ -222,14 +231,14 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     commit_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const __nv_bfloat16*>(a.k),
-        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status);
+        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
   } else {
     err = cudaFuncSetAttribute(commit_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
     commit_kernel<float><<<grid, kThreads, kSmemBytes, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const float*>(a.k),
-        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status);
+        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
   }
   return cudaGetLastError();
 }

@@ -15,6 +15,36 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// [a0, a0 + bytes) and [a1, a1 + bytes) overlap without being the same range
+bool partial_overlap(const void* p0, const void* p1, size_t bytes) {
+  const char* a0 = reinterpret_cast<const char*>(p0);
+  const char* a1 = reinterpret_cast<const char*>(p1);
+  return a0 != a1 && a0 < a1 + bytes && a1 < a0 + bytes;
+}
+
+// [a0, a0 + b0) and [a1, a1 + b1) overlap at all
+bool any_overlap(const void* p0, size_t b0, const void* p1, size_t b1) {
+  const char* a0 = reinterpret_cast<const char*>(p0);
+  const char* a1 = reinterpret_cast<const char*>(p1);
+  return b0 && b1 && a0 < a1 + b1 && a1 < a0 + b0;
+}
+
+// packed-layout arguments: offsets and slots (device pointers), row count, slots
+int check_packed(const int32_t* cu, int32_t T, const int32_t* slot, int32_t n_slots, int B,
+                 gdn::SeqLayout* lay) {
+  if (T < 0 || n_slots < 0) return GDN_TREE_EINVAL;
+  if (cu == nullptr || !aligned4(cu)) return GDN_TREE_EINVAL;
+  if (slot != nullptr && !aligned4(slot)) return GDN_TREE_EINVAL;
+  if (slot == nullptr && n_slots < B) return GDN_TREE_EINVAL;
+  lay->cu = cu;
+  lay->slot = slot;
+  lay->T = T;
+  lay->n_slots = n_slots;
+  return GDN_TREE_OK;
+}
+
 bool supported_head_dim(int d) { return d >= 16 && d <= gdn::kMaxDHost && d % 16 == 0; }
 
 int check_dims(const gdn_tree_dims& d) {
@@ -42,19 +72,28 @@ static bool force_generic() {
   return e && strcmp(e, "generic") == 0;
 }
 
+// the tensor-core kernel takes the shape (packed rows: at least one row, for its
+// tensor maps)
+static bool tc_takes(const VerifyArgs& a) {
+  return !force_generic() && verify_tc_supported(a.d) && (!a.lay.packed() || a.lay.T > 0);
+}
+
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
-  if (!force_generic() && verify_tc_supported(a.d)) return launch_verify_tc(a, stream);
+  if (tc_takes(a)) return launch_verify_tc(a, stream);
   return launch_verify_generic(a, stream);
 }
 
 cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream) {
-  if (!force_generic() && commit_verify_tc_supported(a.verify.d, a.prev_N))
+  if (tc_takes(a.verify) && commit_verify_tc_supported(a.verify.d, a.prev_N))
     return launch_commit_verify_tc(a, stream);
   // two launches on the same stream: commit S_prev -> S1, then verify from S1
   gdn_tree_dims dp = a.verify.d;
   dp.N = a.prev_N;
+  SeqLayout cl = a.prev_lay;  // the previous tree's rows, the verification's state slots
+  cl.slot = a.verify.lay.slot;
+  cl.n_slots = a.verify.lay.n_slots;
   const CommitArgs c{a.prev_path, a.prev_path_len, a.prev_parent, a.prev_U, a.prev_k,
-                     a.prev_log_alpha, a.S_prev, a.S1, dp, a.Lmax, a.commit_status};
+                     a.prev_log_alpha, a.S_prev, a.S1, dp, a.Lmax, a.commit_status, cl};
   cudaError_t err = launch_commit(c, stream);
   if (err != cudaSuccess) return err;
   VerifyArgs v = a.verify;
@@ -162,6 +201,109 @@ int gdn_tree_commit_verify(const int32_t* prev_path, const int32_t* prev_path_le
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
 
+int gdn_tree_verify_packed(const void* q, const void* k, const void* v, const float* log_alpha,
+                           const float* beta, const int32_t* parent, const int32_t* cu_nodes,
+                           int32_t T, const float* state_pool, const int32_t* state_slot,
+                           int32_t n_slots, void* o, float* U, gdn_tree_dims dims,
+                           int32_t* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  gdn::SeqLayout lay;
+  rc = check_packed(cu_nodes, T, state_slot, n_slots, dims.B, &lay);
+  if (rc != GDN_TREE_OK) return rc;
+  if (dims.B == 0 || dims.N == 0) return GDN_TREE_OK;  // nothing to do
+  const void* ptrs[] = {q, k, v, log_alpha, beta, parent, state_pool, o, U};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (dev_status && !aligned4(dev_status)) return GDN_TREE_EINVAL;
+  gdn::VerifyArgs a{q, k, v, log_alpha, beta, parent, state_pool, o, U, dims, dev_status, lay};
+  const cudaError_t err = gdn::launch_verify(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
+int gdn_tree_commit_packed(const int32_t* path, const int32_t* path_len, const int32_t* parent,
+                           const int32_t* cu_nodes, int32_t T, const float* U, const void* k,
+                           const float* log_alpha, const float* pool_in, float* pool_out,
+                           const int32_t* state_slot, int32_t n_slots, gdn_tree_dims dims,
+                           int32_t Lmax, int32_t* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  gdn::SeqLayout lay;
+  rc = check_packed(cu_nodes, T, state_slot, n_slots, dims.B, &lay);
+  if (rc != GDN_TREE_OK) return rc;
+  if (Lmax < 0) return GDN_TREE_EINVAL;
+  if (dims.B == 0) return GDN_TREE_OK;
+  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  const void* ptrs[] = {path_len, pool_in, pool_out};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (T > 0) {
+    const void* rows[] = {U, k, log_alpha};
+    for (const void* p : rows)
+      if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  }
+  if (Lmax > 0 && (path == nullptr || !aligned4(path))) return GDN_TREE_EINVAL;
+  if (parent && !aligned4(parent)) return GDN_TREE_EINVAL;
+  if (dev_status && !aligned4(dev_status)) return GDN_TREE_EINVAL;
+  const int slots = state_slot ? n_slots : dims.B;
+  if (partial_overlap(pool_in, pool_out, (size_t)slots * dims.Hv * dims.dk * dims.dv * 4))
+    return GDN_TREE_EINVAL;
+  gdn::CommitArgs a{path, path_len, parent, U, k, log_alpha, pool_in, pool_out,
+                    dims, Lmax, dev_status, lay};
+  const cudaError_t err = gdn::launch_commit(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
+int gdn_tree_commit_verify_packed(const int32_t* prev_path, const int32_t* prev_path_len,
+                                  const int32_t* prev_parent, const int32_t* prev_cu_nodes,
+                                  int32_t prev_T, const float* prev_U, const void* prev_k,
+                                  const float* prev_log_alpha, int32_t prev_N, int32_t Lmax,
+                                  const float* pool_in, float* pool_out,
+                                  const int32_t* state_slot, int32_t n_slots, const void* q,
+                                  const void* k, const void* v, const float* log_alpha,
+                                  const float* beta, const int32_t* parent,
+                                  const int32_t* cu_nodes, int32_t T, void* o, float* U,
+                                  gdn_tree_dims dims, int32_t* commit_status,
+                                  int32_t* verify_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != GDN_TREE_OK) return rc;
+  gdn_tree_dims dp = dims;
+  dp.N = prev_N;
+  if (prev_N < 0 || Lmax < 0) return GDN_TREE_EINVAL;
+  rc = check_dims(dp);
+  if (rc != GDN_TREE_OK) return rc;
+  gdn::SeqLayout lay, prev_lay;
+  rc = check_packed(cu_nodes, T, state_slot, n_slots, dims.B, &lay);
+  if (rc != GDN_TREE_OK) return rc;
+  rc = check_packed(prev_cu_nodes, prev_T, state_slot, n_slots, dims.B, &prev_lay);
+  if (rc != GDN_TREE_OK) return rc;
+  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (dims.B == 0) return GDN_TREE_OK;
+  if (prev_N == 0 || dims.N == 0) return GDN_TREE_EUNSUPPORTED;
+  const void* ptrs[] = {prev_path_len, prev_U, prev_k, prev_log_alpha, pool_in, pool_out,
+                        q, k, v, log_alpha, beta, parent, o, U};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
+  if (Lmax > 0 && (prev_path == nullptr || !aligned4(prev_path))) return GDN_TREE_EINVAL;
+  const void* small[] = {prev_parent, commit_status, verify_status};
+  for (const void* p : small)
+    if (p && !aligned4(p)) return GDN_TREE_EINVAL;
+  const int slots = state_slot ? n_slots : dims.B;
+  if (partial_overlap(pool_in, pool_out, (size_t)slots * dims.Hv * dims.dk * dims.dv * 4))
+    return GDN_TREE_EINVAL;
+  // the next tree's U must not overlap the previous one's (their row ranges differ)
+  if (any_overlap(U, (size_t)dims.Hv * T * dims.dv * 4, prev_U,
+                  (size_t)dims.Hv * prev_T * dims.dv * 4))
+    return GDN_TREE_EINVAL;
+  gdn::CommitVerifyArgs a{prev_path, prev_path_len, prev_parent, prev_U, prev_k, prev_log_alpha,
+                          prev_N, Lmax, pool_in, pool_out, commit_status,
+                          gdn::VerifyArgs{q, k, v, log_alpha, beta, parent, pool_out, o, U, dims,
+                                          verify_status, lay},
+                          prev_lay};
+  const cudaError_t err = gdn::launch_commit_verify(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
 const char* gdn_tree_strerror(int code) {
   switch (code) {
     case GDN_TREE_OK: return "ok";
@@ -171,6 +313,8 @@ const char* gdn_tree_strerror(int code) {
     case GDN_TREE_STATUS_BAD_TREE: return "device status: parent[] is not topologically ordered";
     case GDN_TREE_STATUS_BAD_PATH: return "device status: accepted path is invalid";
     case GDN_TREE_STATUS_TIMEOUT: return "device status: an on-device wait timed out";
+    case GDN_TREE_STATUS_BAD_LAYOUT:
+      return "device status: the sequence's packed row range or state slot is out of range";
     default: return "unknown code";
   }
 }

@@ -13,6 +13,41 @@ namespace gdn {
 constexpr int kMaxNHost = 256;  // largest tree the kernels take
 constexpr int kMaxDHost = 128;  // largest dk / dv
 
+// Where the rows and the state of sequence b live.
+//  - fixed layout (cu == nullptr): every sequence has dims.N nodes; node rows of
+//    q, k, v, o, log_alpha, beta, parent are at b * N + t; U is [B, Hv, N, dv].
+//  - packed (ragged) layout: sequence b owns rows cu[b] .. cu[b+1] - 1 of the
+//    packed arrays ([T, ...]); dims.N is the largest tree; U is [Hv, T, dv].
+//  - the state of sequence b is S[slot[b]] of a state pool (slot == nullptr:
+//    S[b]); n_slots bounds the slots.
+struct SeqLayout {
+  const int32_t* cu = nullptr;
+  const int32_t* slot = nullptr;
+  int32_t T = 0;
+  int32_t n_slots = 0;
+
+  __host__ __device__ bool packed() const { return cu != nullptr; }
+#ifdef __CUDACC__
+  // first row and node count of sequence b (count < 0: invalid offsets)
+  __device__ __forceinline__ int row0(int b, int N) const { return cu ? cu[b] : b * N; }
+  __device__ __forceinline__ int count(int b, int N) const {
+    if (!cu) return N;
+    const int a = cu[b], e = cu[b + 1];
+    return (a < 0 || e < a || e > T || e - a > N) ? -1 : e - a;
+  }
+  // state index of sequence b (-1: out of range)
+  __device__ __forceinline__ int state(int b) const {
+    if (!slot) return b;
+    const int s = slot[b];
+    return (s < 0 || s >= n_slots) ? -1 : s;
+  }
+  // row (in units of dv floats) of node 0 of unit (b, h) in U
+  __device__ __forceinline__ size_t urow0(int b, int h, int Hv, int N) const {
+    return cu ? (size_t)h * T + cu[b] : ((size_t)b * Hv + h) * N;
+  }
+#endif
+};
+
 struct VerifyArgs {
   const void *q, *k, *v;
   const float *log_alpha, *beta;
@@ -22,6 +57,7 @@ struct VerifyArgs {
   float* U;
   gdn_tree_dims d;
   int32_t* dev_status;
+  SeqLayout lay = {};
 };
 
 struct CommitArgs {
@@ -33,6 +69,7 @@ struct CommitArgs {
   gdn_tree_dims d;
   int32_t Lmax;
   int32_t* dev_status;
+  SeqLayout lay = {};
 };
 
 // delayed commitment of the previous tree's accepted path fused with the
@@ -47,6 +84,7 @@ struct CommitVerifyArgs {
   float* S1;
   int32_t* commit_status;
   VerifyArgs verify;  // verify.S0 is ignored (the state is S1)
+  SeqLayout prev_lay = {};  // the previous tree's rows (state slots: verify.lay's)
 };
 
 // picks the kernel for the shape and dtype

@@ -54,13 +54,14 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
                       const T* __restrict__ v, const float* __restrict__ log_alpha,
                       const float* __restrict__ beta, const int32_t* __restrict__ parent,
                       const float* __restrict__ S0, T* __restrict__ o,
-                      float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status) {
+                      float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status,
+                      SeqLayout lay) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int N = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
+  const int Nmax = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
   const int h = blockIdx.x, b = blockIdx.y;
   const int hq = h / (Hv / Hqk);
-  const int W = (N + 31) / 32;
-  const GenericSmem L = generic_smem_layout(N, dk, dv);
+  const int W = (Nmax + 31) / 32;
+  const GenericSmem L = generic_smem_layout(Nmax, dk, dv);
   float* sS0 = reinterpret_cast<float*>(smem + L.S0);
   float* sU = reinterpret_cast<float*>(smem + L.U);
   int* sPar = reinterpret_cast<int*>(smem + L.parent);
@@ -75,14 +76,22 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
   float* sRows = reinterpret_cast<float*>(smem + L.rows);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // this sequence's rows and state
+  const int N = lay.count(b, Nmax), st = lay.state(b);
+  if (N < 0 || st < 0) {
+    if (h == 0 && tid == 0 && dev_status) dev_status[b] = GDN_TREE_STATUS_BAD_LAYOUT;
+    return;
+  }
+  const size_t row = (size_t)lay.row0(b, Nmax);
+
   // ---- tree: load + validate -------------------------------------------
   int bad = 0;
   for (int t = tid; t < N; t += kThreads) {
-    const int p = parent[(size_t)b * N + t];
+    const int p = parent[row + t];
     sPar[t] = p;
     bad |= (p < -1 || p >= t);
-    sBeta[t] = beta[((size_t)b * N + t) * Hv + h];
-    sLa[t] = log_alpha[((size_t)b * N + t) * Hv + h];
+    sBeta[t] = beta[(row + t) * Hv + h];
+    sLa[t] = log_alpha[(row + t) * Hv + h];
   }
   bad = __syncthreads_or(bad);
   if (h == 0 && tid == 0 && dev_status)
@@ -92,7 +101,7 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
   tree_prepare(sPar, N, W, sLa, sJump, sAnc, sG);
 
   // ---- S0 tile into shared memory ----------------------------------------
-  const float* S0bh = S0 + ((size_t)b * Hv + h) * dk * dv;
+  const float* S0bh = S0 + ((size_t)st * Hv + h) * dk * dv;
   for (int i = tid * 4; i < dk * dv; i += kThreads * 4)
     *reinterpret_cast<float4*>(sS0 + i) = *reinterpret_cast<const float4*>(S0bh + i);
   __syncthreads();
@@ -102,12 +111,12 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
 
   // ---- R = diag(beta) (V - diag(gamma) K S0), one warp per node ----------
   for (int t = warp; t < N; t += kWarps) {
-    const T* kt = k + (((size_t)b * N + t) * Hqk + hq) * dk;
+    const T* kt = k + ((row + t) * Hqk + hq) * dk;
     for (int i = lane; i < dk; i += 32) myRow[i] = to_f32(kt[i]);
     __syncwarp();
     const float gam = expf(df_value(sG[t]));
     const float bt = sBeta[t];
-    const T* vt = v + (((size_t)b * N + t) * Hv + h) * dv;
+    const T* vt = v + ((row + t) * Hv + h) * dv;
     for (int m = 0; m < ncol; ++m) {
       const int c = lane + 32 * m;
       if (c < dv) {
@@ -143,12 +152,12 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
     __syncthreads();
     {
-      const T* kt = k + (((size_t)b * N + t) * Hqk + hq) * dk;
+      const T* kt = k + ((row + t) * Hqk + hq) * dk;
       const float bt = sBeta[t];
       const df gt = sG[t];
       for (int idx = warp; idx < nA; idx += kWarps) {
         const int s = sList[idx];
-        const T* ks = k + (((size_t)b * N + s) * Hqk + hq) * dk;
+        const T* ks = k + ((row + s) * Hqk + hq) * dk;
         float part = 0.f;
         for (int i = lane; i < dk; i += 32) part = fmaf(to_f32(kt[i]), to_f32(ks[i]), part);
         part = warp_sum(part);
@@ -175,7 +184,7 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
 
   // ---- outputs: o_t = gamma_t S0^T q_t + sum_{s in P(t)} Y[t,s] u_s --------
   for (int t = warp; t < N; t += kWarps) {
-    const T* qt = q + (((size_t)b * N + t) * Hqk + hq) * dk;
+    const T* qt = q + ((row + t) * Hqk + hq) * dk;
     for (int i = lane; i < dk; i += 32) myRow[i] = to_f32(qt[i]);
     __syncwarp();
     const df gt = sG[t];
@@ -204,7 +213,7 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
           s = i * 32 + __ffs(bits) - 1;
           bits &= bits - 1;
         }
-        const T* ks = k + (((size_t)b * N + s) * Hqk + hq) * dk;
+        const T* ks = k + ((row + s) * Hqk + hq) * dk;
         float part = 0.f;
         for (int e = lane; e < dk; e += 32) part = fmaf(myRow[e], to_f32(ks[e]), part);
         part = warp_sum(part);
@@ -217,8 +226,8 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
         if (self) break;
       }
     }
-    T* ot = o + (((size_t)b * N + t) * Hv + h) * dv;
-    float* Ut = U + (((size_t)b * Hv + h) * N + t) * dv;
+    T* ot = o + ((row + t) * Hv + h) * dv;
+    float* Ut = U + (lay.urow0(b, h, Hv, Nmax) + t) * dv;
 #pragma unroll
     for (int m = 0; m < kMaxD / 32; ++m) {
       const int c = lane + 32 * m;
@@ -248,7 +257,7 @@ cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream) {
     kern<<<grid, kThreads, smem, stream>>>(
         static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
         static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
-        static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status);
+        static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay);
   } else {
     auto kern = verify_generic_kernel<float>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -256,7 +265,7 @@ cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream) {
     kern<<<grid, kThreads, smem, stream>>>(
         static_cast<const float*>(a.q), static_cast<const float*>(a.k),
         static_cast<const float*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
-        static_cast<float*>(a.o), a.U, a.d, a.dev_status);
+        static_cast<float*>(a.o), a.U, a.d, a.dev_status, a.lay);
   }
   return cudaGetLastError();
 }

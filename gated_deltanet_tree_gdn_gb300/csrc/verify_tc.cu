@@ -223,16 +223,36 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// Where unit (b, h)'s nodes live: its node count n (0 when the sequence's layout
+// is invalid, flagged by bad), its first row, its state index, and the node /
+// sequence coordinates of its rows in the q/k/v tensor maps.
+struct UnitGeom {
+  int n, row0, st, c_node, c_seq;
+  bool bad;
+};
+__device__ __forceinline__ UnitGeom unit_geom(const SeqLayout& lay, int b, int Nmax) {
+  UnitGeom g;
+  const int n = lay.count(b, Nmax), st = lay.state(b);
+  g.bad = n < 0 || st < 0;
+  g.n = g.bad ? 0 : n;
+  g.st = g.bad ? 0 : st;
+  g.row0 = g.bad ? 0 : lay.row0(b, Nmax);
+  g.c_node = lay.packed() ? g.row0 : 0;
+  g.c_seq = lay.packed() ? 0 : b;
+  return g;
+}
+
 // Tree group: starts the copies of a unit's parent links and gates (node = tid)
 // into the prefetch slots; tree_prep of that unit waits for them.
 __device__ __forceinline__ void prefetch_tree(Small& S, const int32_t* parent, const float* beta,
-                                              const float* log_alpha, int unit, int N, int Hv,
-                                              int tid) {
-  if (tid < N) {
-    const int b = unit / Hv, h = unit - b * Hv;
-    cp_async4(&S.pre_parent[tid], parent + (size_t)b * N + tid);
-    cp_async4(&S.pre_beta[tid], beta + ((size_t)b * N + tid) * Hv + h);
-    cp_async4(&S.pre_la[tid], log_alpha + ((size_t)b * N + tid) * Hv + h);
+                                              const float* log_alpha, const SeqLayout& lay,
+                                              int unit, int Nmax, int Hv, int tid) {
+  const int b = unit / Hv, h = unit - b * Hv;
+  const UnitGeom g = unit_geom(lay, b, Nmax);
+  if (tid < g.n) {
+    cp_async4(&S.pre_parent[tid], parent + (size_t)g.row0 + tid);
+    cp_async4(&S.pre_beta[tid], beta + ((size_t)g.row0 + tid) * Hv + h);
+    cp_async4(&S.pre_la[tid], log_alpha + ((size_t)g.row0 + tid) * Hv + h);
   }
   cp_async_commit();
 }
@@ -241,13 +261,14 @@ __device__ __forceinline__ void prefetch_tree(Small& S, const int32_t* parent, c
 struct FusedCommit {
   const int32_t* path;      // [B, Lmax]
   const int32_t* path_len;  // [B]
-  const int32_t* parent;    // [B, N] or NULL
-  const float* U;           // [B, Hv, N, dv]
-  const __nv_bfloat16* k;   // [B, N, Hqk, dk]
-  const float* log_alpha;   // [B, N, Hv]
-  int32_t N, Lmax;
-  float* S1;                // [B, Hv, dk, dv] committed state (may alias the input state)
+  const int32_t* parent;    // node rows (see lay), or NULL
+  const float* U;           // [B, Hv, N, dv] or [Hv, T, dv]
+  const __nv_bfloat16* k;   // node rows x [Hqk, dk]
+  const float* log_alpha;   // node rows x [Hv]
+  int32_t N, Lmax;          // N: the previous tree's (largest) node count
+  float* S1;                // committed states, indexed like the input states (may alias them)
   int32_t* status;          // [B] or NULL
+  SeqLayout lay;            // the previous tree's rows (its state index is unused)
 };
 
 // reduction barrier over the first kCount threads (named barrier kId): OR of v
@@ -269,16 +290,19 @@ __device__ __forceinline__ int bar_or(int v) {
 // (bar_v); issuing thread only
 __device__ __forceinline__ void issue_kqv(Small& S, uint8_t* smem, const CUtensorMap* tmK,
                                           const CUtensorMap* tmQ, const CUtensorMap* tmV,
-                                          int unit, int Hv, int Hqk) {
+                                          const SeqLayout& lay, int unit, int Hv, int Hqk,
+                                          int Nmax) {
   const int b = unit / Hv, h = unit - b * Hv, hq = h / (Hv / Hqk);
+  const UnitGeom g = unit_geom(lay, b, Nmax);
+  const int cn = g.c_node, cs = g.c_seq;
   mbar_arrive_expect_tx(&S.bar_kq, 4 * kTileBytes);
-  tma_load_4d(smem + OFF_K, tmK, &S.bar_kq, 0, hq, 0, b);
-  tma_load_4d(smem + OFF_K + kTileBytes, tmK, &S.bar_kq, 64, hq, 0, b);
-  tma_load_4d(smem + OFF_Q, tmQ, &S.bar_kq, 0, hq, 0, b);
-  tma_load_4d(smem + OFF_Q + kTileBytes, tmQ, &S.bar_kq, 64, hq, 0, b);
+  tma_load_4d(smem + OFF_K, tmK, &S.bar_kq, 0, hq, cn, cs);
+  tma_load_4d(smem + OFF_K + kTileBytes, tmK, &S.bar_kq, 64, hq, cn, cs);
+  tma_load_4d(smem + OFF_Q, tmQ, &S.bar_kq, 0, hq, cn, cs);
+  tma_load_4d(smem + OFF_Q + kTileBytes, tmQ, &S.bar_kq, 64, hq, cn, cs);
   mbar_arrive_expect_tx(&S.bar_v, 2 * kTileBytes);
-  tma_load_4d(smem + OFF_V, tmV, &S.bar_v, 0, h, 0, b);
-  tma_load_4d(smem + OFF_V + kTileBytes, tmV, &S.bar_v, 64, h, 0, b);
+  tma_load_4d(smem + OFF_V, tmV, &S.bar_v, 0, h, cn, cs);
+  tma_load_4d(smem + OFF_V + kTileBytes, tmV, &S.bar_v, 64, h, cn, cs);
   ++S.n_kq;
 }
 
@@ -291,9 +315,9 @@ __device__ __forceinline__ void issue_kqv(Small& S, uint8_t* smem, const CUtenso
 // for the CTA's next unit (if `next` < `end`) start as soon as the prefetch
 // slots have been read.
 __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_t* parent,
-                                          const float* beta, const float* log_alpha, int next,
-                                          int end, int N, int Hv, int tid, int lane, int warp,
-                                          int unit) {
+                                          const float* beta, const float* log_alpha,
+                                          const SeqLayout& lay, int Nmax, int next, int end,
+                                          int N, int Hv, int tid, int lane, int warp, int unit) {
   using TreeSync = NamedSync<1, 128>;
   cp_async_wait_all();
   TC_MARK(12);
@@ -312,7 +336,7 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
   S.parent[tid] = bad_any ? -1 : p_in;
   if (tid == 0) S.bad = bad_any;
   // every read of the prefetch slots has completed (their values are used above)
-  if (next < end) prefetch_tree(S, parent, beta, log_alpha, next, N, Hv, tid);
+  if (next < end) prefetch_tree(S, parent, beta, log_alpha, lay, next, Nmax, Hv, tid);
   TreeSync()();
   TC_MARK(13);
   // pointer jumping: after round r, jump[t] is t's 2^r-th ancestor (or -1) and
@@ -405,12 +429,14 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
 __device__ __forceinline__ void commit_stage_rows(const FusedCommit& fc, const Small& S,
                                                   uint8_t* smem, int b, int h, int hq, int Hqk,
                                                   int Hv, int j0, int nj, int i0, int stride) {
+  const size_t prow0 = (size_t)fc.lay.row0(b, fc.N);
+  const size_t purow0 = fc.lay.urow0(b, h, Hv, fc.N);
   float* sk = reinterpret_cast<float*>(smem + OFF_CK);  // [kCommitChunk][kD]
   float* su = reinterpret_cast<float*>(smem + OFF_CU);  // [kCommitChunk][kD]
   for (int e = i0; e < nj * (kD / 8); e += stride) {
     const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
     const uint4 raw = *reinterpret_cast<const uint4*>(
-        fc.k + (((size_t)b * fc.N + S.cpath[j0 + jj]) * Hqk + hq) * kD + c);
+        fc.k + ((prow0 + S.cpath[j0 + jj]) * Hqk + hq) * kD + c);
     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
     float* dst = sk + jj * kD + c;
 #pragma unroll
@@ -422,7 +448,7 @@ __device__ __forceinline__ void commit_stage_rows(const FusedCommit& fc, const S
   for (int e = i0; e < nj * (kD / 4); e += stride) {
     const int jj = e / (kD / 4), c = (e % (kD / 4)) * 4;
     *reinterpret_cast<float4*>(su + jj * kD + c) = *reinterpret_cast<const float4*>(
-        fc.U + (((size_t)b * Hv + h) * fc.N + S.cpath[j0 + jj]) * kD + c);
+        fc.U + (purow0 + S.cpath[j0 + jj]) * kD + c);
   }
 }
 
@@ -472,30 +498,33 @@ __device__ __forceinline__ void commit_weights(Small& S, int L, int lane) {
 // Warps 5-15 (ot = tid - 160; warp 4 issues the copies and MMAs meanwhile): checks the previous tree's
 // accepted path of sequence b (range, chain order, parent links), gathers its
 // log alpha, stages the first chunk of its k / U rows into region 2 and forms
-// the path weights.  Sets S.cbad, S.cL.
+// the path weights.  Sets S.cbad (0 or the sequence's commit status), S.cL.
 __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S, uint8_t* smem,
                                                 int b, int h, int hq, int Hqk, int Hv, int ot,
                                                 int warp, int lane) {
+  const int pn = fc.lay.count(b, fc.N);  // the previous tree's node count (< 0: bad rows)
   const int L = fc.path_len[b];
   int pj = -1;
   if (ot < fc.Lmax) pj = fc.path[(size_t)b * fc.Lmax + ot];
-  int cbad = (L < 0 || L > fc.N || L > fc.Lmax);
+  int cbad = (pn < 0 || L < 0 || L > pn || L > fc.Lmax);
   if (!cbad && ot < L) {
-    cbad |= (pj < 0 || pj >= fc.N);
+    cbad |= (pj < 0 || pj >= pn);
     S.cpath[ot] = pj;
   }
   cbad = bar_or<2, kThreads - 160>(cbad);
   if (!cbad && ot < L) {
     const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
     cbad |= (ot > 0 && pj <= prev);
-    if (fc.parent) cbad |= (fc.parent[(size_t)b * fc.N + pj] != prev);
-    S.cla[ot] = fc.log_alpha[((size_t)b * fc.N + pj) * Hv + h];
+    const size_t prow0 = (size_t)fc.lay.row0(b, fc.N);
+    if (fc.parent) cbad |= (fc.parent[prow0 + pj] != prev);
+    S.cla[ot] = fc.log_alpha[(prow0 + pj) * Hv + h];
   }
   if (!cbad)
     commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 160);
   cbad = bar_or<2, kThreads - 160>(cbad);
   if (ot == 0) {
-    S.cbad = cbad;
+    S.cbad = !cbad ? GDN_TREE_STATUS_OK
+                   : (pn < 0 ? GDN_TREE_STATUS_BAD_LAYOUT : GDN_TREE_STATUS_BAD_PATH);
     S.cL = L;
   }
   if (!cbad && warp == 5) commit_weights(S, L, lane);
@@ -545,11 +574,11 @@ __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const S
 
 // S1 = gamma S0 + acc on this thread's 8x4 tile of the state, in registers (it is
 // the state the next tree is verified from), stored to fc.S1
-__device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S, int unit,
-                                              int r8, int c4, float4 (&st)[8],
+__device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S,
+                                              size_t state_unit, int r8, int c4, float4 (&st)[8],
                                               const float (&acc)[8][4]) {
   const float gamma = S.cgamma;
-  float* dst = fc.S1 + (size_t)unit * kD * kD + (r8 * 8) * kD + c4 * 4;
+  float* dst = fc.S1 + state_unit * kD * kD + (r8 * 8) * kD + c4 * 4;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     st[i].x = fmaf(gamma, st[i].x, acc[i][0]);
@@ -608,7 +637,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  const __grid_constant__ CUtensorMap tmV, const float* S0,
                  const float* __restrict__ log_alpha, const float* __restrict__ beta,
                  const int32_t* __restrict__ parent, __nv_bfloat16* __restrict__ o,
-                 float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, FusedCommit fc) {
+                 float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
+                 FusedCommit fc) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -619,7 +649,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   float2* sXY = reinterpret_cast<float2*>(smem + OFF_XY);
   uint8_t* sPath = smem + OFF_PATH;
 
-  const int N = d.N, Hv = d.Hv, Hqk = d.Hqk;
+  const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
   const int n_units = d.B * Hv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // row mapping: thread <-> (tree row t, 32-column quarter cq); warp w may only
@@ -627,7 +657,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int q4 = warp & 3, cq = warp >> 2;
   const int t = q4 * 32 + lane;
   const int col0 = cq * 32;
-  const bool live = t < N;
   const uint32_t trow_off = (uint32_t)(q4 * 32) << 16;
   // state mapping: thread <-> 8x4 tile (rows 8 r8 .., columns 4 c4 ..); a warp holds
   // 4 row blocks x 8 column groups, so its loads are 128-byte rows and its S0^T
@@ -649,10 +678,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     S.n_ks = 0;
     S.cbad = 0;
     mbar_fence_init();
-    if (unit < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, unit, Hv, Hqk);
+    if (unit < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, lay, unit, Hv, Hqk, Nmax);
   }
   if (warp < 4) {
-    if (unit < n_units) prefetch_tree(S, parent, beta, log_alpha, unit, N, Hv, tid);
+    if (unit < n_units) prefetch_tree(S, parent, beta, log_alpha, lay, unit, Nmax, Hv, tid);
     mbar_init(&S.node_bar[tid], 1);  // one solve barrier per node (one arrival a phase)
     mbar_fence_init();
   }
@@ -667,12 +696,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int b = unit / Hv, h = unit - b * Hv;
     const int hq = h / (Hv / Hqk);
     const int next = unit + gridDim.x;
+    // this unit's nodes (an invalid sequence layout runs as an empty tree, unwritten)
+    const UnitGeom geo = unit_geom(lay, b, Nmax);
+    const int N = geo.n;
+    const bool live = t < N;
+    const size_t state_unit = (size_t)geo.st * Hv + h;
 
     // this thread's 8x4 tile of the state, into registers (L2 hits: prefetched)
     float4 st[8];
     {
       const float4* src =
-          reinterpret_cast<const float4*>(S0 + (size_t)unit * kD * kD + (r8 * 8) * kD + c4 * 4);
+          reinterpret_cast<const float4*>(S0 + state_unit * kD * kD + (r8 * 8) * kD + c4 * 4);
 #pragma unroll
       for (int i = 0; i < 8; ++i) st[i] = __ldg(src + i * (kD / 4));
     }
@@ -683,7 +717,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     TC_START();
     TC_MARK(0);
     if (warp < 4) {
-      tree_prep(S, sPath, parent, beta, log_alpha, next, n_units, N, Hv, tid, lane, warp, unit);
+      tree_prep(S, sPath, parent, beta, log_alpha, lay, Nmax, next, n_units, N, Hv, tid, lane,
+                warp, unit);
       TC_MARK(8);
     } else {
       if constexpr (kFused) {
@@ -693,14 +728,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         // the next unit's K, Q and state head for L2 now, so that their copies (issued
         // when this unit's solve is over) hit L2
         if (next < n_units) {
-          const int nb = next / Hv, nhq = (next - nb * Hv) / (Hv / Hqk);
-          tma_prefetch_l2_4d(&tmK, 0, nhq, 0, nb);
-          tma_prefetch_l2_4d(&tmK, 64, nhq, 0, nb);
-          tma_prefetch_l2_4d(&tmQ, 0, nhq, 0, nb);
-          tma_prefetch_l2_4d(&tmQ, 64, nhq, 0, nb);
-          tma_prefetch_l2_4d(&tmV, 0, next - nb * Hv, 0, nb);
-          tma_prefetch_l2_4d(&tmV, 64, next - nb * Hv, 0, nb);
-          const float* ns = S0 + (size_t)next * kD * kD;
+          const int nb = next / Hv, nh = next - nb * Hv, nhq = nh / (Hv / Hqk);
+          const UnitGeom ng = unit_geom(lay, nb, Nmax);
+          tma_prefetch_l2_4d(&tmK, 0, nhq, ng.c_node, ng.c_seq);
+          tma_prefetch_l2_4d(&tmK, 64, nhq, ng.c_node, ng.c_seq);
+          tma_prefetch_l2_4d(&tmQ, 0, nhq, ng.c_node, ng.c_seq);
+          tma_prefetch_l2_4d(&tmQ, 64, nhq, ng.c_node, ng.c_seq);
+          tma_prefetch_l2_4d(&tmV, 0, nh, ng.c_node, ng.c_seq);
+          tma_prefetch_l2_4d(&tmV, 64, nh, ng.c_node, ng.c_seq);
+          const float* ns = S0 + ((size_t)ng.st * Hv + nh) * kD * kD;
 #pragma unroll
           for (int r = 0; r < 4; ++r) bulk_prefetch_l2(ns + r * (kD * kD / 4), kD * kD);
         }
@@ -725,25 +761,29 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // ---- 1. fused: S1 = gamma S0 + K_P^T diag(w) U_P on the tile in registers, stored
     //         to S1; then (both) S0^T from the tile
     if constexpr (kFused) {
-      if (!S.cbad) {
+      if (!S.cbad && !geo.bad) {  // (an invalid layout has no state of its own to commit)
         float cacc[8][4];
         commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, r8, c4, cacc);
-        commit_finish(fc, S, unit, r8, c4, st, cacc);
+        commit_finish(fc, S, state_unit, r8, c4, st, cacc);
       }
       __syncthreads();  // the staged path rows are read before S0^T goes over them
       TC_MARK(2);
     }
     split_state(smem, sbase, S, tmem, r8, c4, st, tid == kIssuer, true);
     TC_MARK(3);
-    const bool cbad = kFused && S.cbad;
+    const int cstat = kFused ? S.cbad : GDN_TREE_STATUS_OK;
+    const bool cbad = cstat != GDN_TREE_STATUS_OK;
     if (h == 0 && tid == 0) {
       if (dev_status)
-        dev_status[b] = cbad ? GDN_TREE_STATUS_BAD_PATH
-                             : (S.bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK);
-      if (kFused && fc.status) fc.status[b] = cbad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
+        dev_status[b] = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT
+                        : cbad  ? cstat
+                        : S.bad ? GDN_TREE_STATUS_BAD_TREE
+                                : GDN_TREE_STATUS_OK;
+      if (kFused && fc.status) fc.status[b] = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT : cstat;
     }
-    // an invalid tree (verified as all-roots) or path leaves the unit's outputs unwritten
-    const bool write_out = !S.bad && !cbad;
+    // an invalid layout, tree (verified as all-roots) or path leaves the unit's
+    // outputs unwritten
+    const bool write_out = !geo.bad && !S.bad && !cbad;
 
     {
       const uint32_t trow = tmem + trow_off;
@@ -851,8 +891,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // in that order).
     TC_MARK(6);
     {
-      float* Ubh = U + (size_t)unit * N * kD;
-      __nv_bfloat16* obh = o + ((size_t)b * N * Hv + h) * kD;
+      float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
+      __nv_bfloat16* obh = o + ((size_t)geo.row0 * Hv + h) * kD;
       bool timed_out = false;
       // a waiting warp is suspended by the hardware instead of spinning
       auto wait_ready = [&](int node) {
@@ -921,7 +961,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tc_fence_after_sync();
     TC_MARK(7);
     TC_DUMP();
-    if (tid == kIssuer && next < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, next, Hv, Hqk);
+    if (tid == kIssuer && next < n_units)
+      issue_kqv(S, smem, &tmK, &tmQ, &tmV, lay, next, Hv, Hqk, Nmax);
   }
   goto release;
 
@@ -963,12 +1004,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // q, k [B, N, Hqk, 128] or v [B, N, Hv, 128] bf16 (`heads` = Hqk or Hv) -> boxes
 // of 64 (columns) x 128 (nodes), 128-byte swizzled; nodes past N read as zeros
-bool encode_rows_map(CUtensorMap* map, const void* base, const gdn_tree_dims& d, int heads) {
+// `rows` x `seqs`: N x B for the fixed layout, T x 1 for packed rows
+bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int seqs, int heads) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)d.N, (cuuint64_t)d.B};
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)seqs};
   const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2,
-                                 (cuuint64_t)d.N * heads * kD * 2};
+                                 (cuuint64_t)rows * heads * kD * 2};
   const cuuint32_t box[4] = {64, 1, kTile, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -1001,8 +1043,10 @@ int sm_count() {
 template <bool kFused>
 cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
   CUtensorMap tmQ, tmK, tmV;
-  if (!encode_rows_map(&tmQ, a.q, a.d, a.d.Hqk) || !encode_rows_map(&tmK, a.k, a.d, a.d.Hqk) ||
-      !encode_rows_map(&tmV, a.v, a.d, a.d.Hv))
+  const int rows = a.lay.packed() ? a.lay.T : a.d.N, seqs = a.lay.packed() ? 1 : a.d.B;
+  if (!encode_rows_map(&tmQ, a.q, rows, seqs, a.d.Hqk) ||
+      !encode_rows_map(&tmK, a.k, rows, seqs, a.d.Hqk) ||
+      !encode_rows_map(&tmV, a.v, rows, seqs, a.d.Hv))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1015,7 +1059,7 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   const int grid = n_units < n_sm ? n_units : n_sm;
   verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
       tmQ, tmK, tmV, a.S0, a.log_alpha, a.beta, a.parent,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, fc);
+      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, fc);
   return cudaGetLastError();
 }
 
@@ -1032,7 +1076,7 @@ bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N) {
 cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stream) {
   FusedCommit fc{a.prev_path, a.prev_path_len, a.prev_parent, a.prev_U,
                  static_cast<const __nv_bfloat16*>(a.prev_k), a.prev_log_alpha, a.prev_N,
-                 a.Lmax, a.S1, a.commit_status};
+                 a.Lmax, a.S1, a.commit_status, a.prev_lay};
   VerifyArgs v = a.verify;
   v.S0 = a.S_prev;  // the kernel loads the previous state and commits it on chip
   return launch_tc<true>(v, fc, stream);

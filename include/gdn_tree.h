@@ -78,6 +78,8 @@ extern "C" {
                                       (with parent given) not a root chain     */
 #define GDN_TREE_STATUS_TIMEOUT 3  /* a bounded on-device wait (TMA or tensor-core
                                       completion) ran out; outputs incomplete   */
+#define GDN_TREE_STATUS_BAD_LAYOUT 4 /* packed layout: the sequence's row range or
+                                        state slot is out of range             */
 
 /* element type of q, k, v and o */
 #define GDN_TREE_BF16 0
@@ -178,6 +180,62 @@ int gdn_tree_verify_recurrent(const void *q, const void *k, const void *v,
                               const float *log_alpha, const float *beta,
                               const int32_t *parent, const float *S0, void *o, float *U,
                               gdn_tree_dims dims, int32_t *dev_status, void *stream);
+
+/*
+ * Packed (ragged) batches with a state pool -- the serving layout of the same
+ * calls: every sequence has its own tree size, and its recurrent state lives in
+ * a slot of a state pool (the DFlash-TfM page runs the verification inside
+ * SGLang, section 3 "Implementazione").  The DFlash-TfM page itself prints no
+ * layout; the packed variants are this library's.
+ *
+ *   cu_nodes      [B + 1] int32, device: sequence b owns node rows
+ *                 cu_nodes[b] .. cu_nodes[b+1]-1 of the packed arrays, and its
+ *                 tree's node t is row cu_nodes[b] + t; 0 <= cu_nodes[b] <=
+ *                 cu_nodes[b+1] <= T and cu_nodes[b+1] - cu_nodes[b] <= dims.N
+ *   T             rows of the packed arrays (>= 0)
+ *   q, k          [T, Hqk, dk];  v, o [T, Hv, dv];  log_alpha, beta [T, Hv];
+ *   parent        [T]: parent[cu_nodes[b] + t] is t's parent within sequence b
+ *                 (-1 <= parent < t)
+ *   U             [Hv, T, dv] fp32: the rows of sequence b, head h are contiguous
+ *   state_slot    [B] int32, device, or NULL (slot b): sequence b's state is
+ *                 pool[state_slot[b]] of a pool [n_slots, Hv, dk, dv] fp32;
+ *                 0 <= state_slot[b] < n_slots.  Commits need distinct slots.
+ *   dims          B sequences, N = the largest tree (the capacity the kernels are
+ *                 chosen for), heads and dtype as for the fixed layout.
+ * A sequence whose row range or slot is out of range gets
+ * GDN_TREE_STATUS_BAD_LAYOUT in its status and its outputs are left unwritten.
+ * Everything else -- dtypes, alignment, ownership, asynchrony, tree and path
+ * validity -- is as for the fixed-layout calls.
+ */
+int gdn_tree_verify_packed(const void *q, const void *k, const void *v, const float *log_alpha,
+                           const float *beta, const int32_t *parent, const int32_t *cu_nodes,
+                           int32_t T, const float *state_pool, const int32_t *state_slot,
+                           int32_t n_slots, void *o, float *U, gdn_tree_dims dims,
+                           int32_t *dev_status, void *stream);
+
+/* Delayed commitment in the packed layout: path/path_len [B, Lmax] / [B] index
+ * each sequence's own nodes; pool_out[state_slot[b]] = the state after the path,
+ * from pool_in[state_slot[b]] (pool_out may be pool_in: in-place). */
+int gdn_tree_commit_packed(const int32_t *path, const int32_t *path_len, const int32_t *parent,
+                           const int32_t *cu_nodes, int32_t T, const float *U, const void *k,
+                           const float *log_alpha, const float *pool_in, float *pool_out,
+                           const int32_t *state_slot, int32_t n_slots, gdn_tree_dims dims,
+                           int32_t Lmax, int32_t *dev_status, void *stream);
+
+/* One decoding iteration in the packed layout: the previous tree (prev_cu_nodes,
+ * prev_T, prev_N its largest tree) is committed from pool_in into pool_out and
+ * the next tree is verified from pool_out, as gdn_tree_commit_verify. */
+int gdn_tree_commit_verify_packed(const int32_t *prev_path, const int32_t *prev_path_len,
+                                  const int32_t *prev_parent, const int32_t *prev_cu_nodes,
+                                  int32_t prev_T, const float *prev_U, const void *prev_k,
+                                  const float *prev_log_alpha, int32_t prev_N, int32_t Lmax,
+                                  const float *pool_in, float *pool_out,
+                                  const int32_t *state_slot, int32_t n_slots, const void *q,
+                                  const void *k, const void *v, const float *log_alpha,
+                                  const float *beta, const int32_t *parent,
+                                  const int32_t *cu_nodes, int32_t T, void *o, float *U,
+                                  gdn_tree_dims dims, int32_t *commit_status,
+                                  int32_t *verify_status, void *stream);
 
 /* Human-readable text for a return code or a device status code. */
 const char *gdn_tree_strerror(int code);
