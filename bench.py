@@ -416,6 +416,24 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     rec_ms = max_over_ranks(float(sum(evr[i][0].elapsed_time(evr[i][1]) for i in range(Kr))),
                             dist, dev) / Kr
 
+    # the step before the verification: top-w best-first construction of trees of
+    # the same size (c = w = 4 candidates and pops, depth <= 24), from seeded
+    # candidate log-probabilities
+    lp = torch.from_numpy(np.log(np.random.default_rng(7).uniform(
+        1e-6, 1.0, size=(w.B, w.N, 4))).astype(np.float32)).to(dev)
+    tb_par = torch.empty((w.B, w.N), dtype=torch.int32, device=dev)
+    tb_j = torch.empty_like(tb_par)
+    tb_s = torch.empty((w.B, w.N), dtype=torch.float32, device=dev)
+    tb_n = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    Kt = min(K, 100)
+    evt = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Kt)]
+    for i in range(Kt):
+        evt[i][0].record(stream)
+        gt.build_topw(lp, 4, 24, parent=tb_par, cand_index=tb_j, score=tb_s, n_built=tb_n)
+        evt[i][1].record(stream)
+    torch.cuda.synchronize()
+    tb_us = 1e3 * statistics.mean(evt[i][0].elapsed_time(evt[i][1]) for i in range(Kt))
+
     # end to end through the public API: every step copies the tree's inputs and
     # the accepted path from pinned host memory (the recurrent state stays
     # resident on the device, as in a decoding loop), runs one decoding
@@ -497,6 +515,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "tree_verify_speedup": rec_ms / statistics.mean(t_ver),
             "page": "fused tree kernel 7.1x faster than single-branch recurrent verification "
                     "at 126 tree tokens, NVIDIA B200 (DFlash-TfM, results)"}
+        line["tree_build"] = {"kernel": "tree_topw_kernel", "us": tb_us, "B": w.B, "N": w.N,
+                              "c": 4, "w": 4, "max_depth": 24,
+                              "rounds": -(-(w.N - 1) // 4)}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)

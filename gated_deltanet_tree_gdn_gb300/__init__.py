@@ -8,6 +8,7 @@ Python face of libgdntree (C ABI in include/gdn_tree.h):
     o, U = verify_recurrent(...)    # baseline: one recurrent pass per branch
     o, U = verify_packed(...)       # ragged batch, states in a pool (also commit_packed,
                                     # commit_verify_packed)
+    parent, j, score, n = build_topw(cand_logp, w, max_depth)   # the draft tree
 
 Build the library first with ``python -m gated_deltanet_tree_gdn_gb300.build``.
 """
@@ -16,7 +17,7 @@ from ._binding import (  # noqa: F401
     BF16, F32, OK, EINVAL, EUNSUPPORTED, ECUDA, STATUS_OK, STATUS_BAD_TREE,
     STATUS_BAD_PATH, STATUS_TIMEOUT, SYMBOLS, Dims, GdnTreeError, commit, commit_verify,
     library_path, load, strerror, verify, verify_recurrent, verify_packed, commit_packed,
-    commit_verify_packed, STATUS_BAD_LAYOUT,
+    commit_verify_packed, STATUS_BAD_LAYOUT, build_topw,
 )
 from .build import build_library  # noqa: F401
 

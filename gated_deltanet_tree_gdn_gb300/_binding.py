@@ -21,7 +21,8 @@ STATUS_OK, STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TIMEOUT, STATUS_BAD_LAYOUT =
 
 SYMBOLS = ("gdn_tree_verify", "gdn_tree_commit", "gdn_tree_commit_verify",
            "gdn_tree_verify_recurrent", "gdn_tree_verify_packed", "gdn_tree_commit_packed",
-           "gdn_tree_commit_verify_packed", "gdn_tree_strerror", "gdn_tree_version")
+           "gdn_tree_commit_verify_packed", "gdn_tree_build_topw", "gdn_tree_strerror",
+           "gdn_tree_version")
 
 
 class Dims(ctypes.Structure):
@@ -74,6 +75,8 @@ def load(path: str | None = None):
                                                   fp, ip, i32, vp, vp, vp, fp, fp, ip, ip, i32,
                                                   vp, fp, Dims, ip, ip, vp]
     lib.gdn_tree_commit_verify_packed.restype = ctypes.c_int
+    lib.gdn_tree_build_topw.argtypes = [fp, i32, i32, i32, i32, i32, ip, ip, fp, ip, vp]
+    lib.gdn_tree_build_topw.restype = ctypes.c_int
     lib.gdn_tree_strerror.argtypes = [ctypes.c_int]
     lib.gdn_tree_strerror.restype = ctypes.c_char_p
     lib.gdn_tree_version.argtypes = []
@@ -406,3 +409,37 @@ def commit_verify_packed(prev_path, prev_path_len, prev_U, prev_k, prev_log_alph
     if rc != OK:
         raise GdnTreeError(rc, "gdn_tree_commit_verify_packed")
     return pool_out, o, U
+
+
+# ---------------------------------------------------------------------------
+# draft-tree construction
+# ---------------------------------------------------------------------------
+
+def build_topw(cand_logp, w: int, max_depth: int, *, parent=None, cand_index=None, score=None,
+               n_built=None, stream=None):
+    """Top-w best-first draft-tree construction (C ABI gdn_tree_build_topw).
+
+    cand_logp [B, N, c] fp32: the log-probabilities of each node's c candidate
+    children.  Returns (parent [B, N] int32, cand_index [B, N] int32, score [B, N]
+    fp32, n_built [B] int32); outputs are allocated when not given."""
+    _check(cand_logp, "cand_logp", torch.float32)
+    B, N, c = cand_logp.shape
+    dev = cand_logp.device
+    if parent is None:
+        parent = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if cand_index is None:
+        cand_index = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if score is None:
+        score = torch.empty((B, N), dtype=torch.float32, device=dev)
+    if n_built is None:
+        n_built = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(parent, "parent", torch.int32, (B, N))
+    _check(cand_index, "cand_index", torch.int32, (B, N))
+    _check(score, "score", torch.float32, (B, N))
+    _check(n_built, "n_built", torch.int32, (B,))
+    rc = load().gdn_tree_build_topw(_ptr(cand_logp), B, N, c, w, max_depth, _ptr(parent),
+                                    _ptr(cand_index), _ptr(score), _ptr(n_built),
+                                    _stream(stream))
+    if rc != OK:
+        raise GdnTreeError(rc, "gdn_tree_build_topw")
+    return parent, cand_index, score, n_built

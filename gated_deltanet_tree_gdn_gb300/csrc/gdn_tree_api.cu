@@ -304,6 +304,23 @@ int gdn_tree_commit_verify_packed(const int32_t* prev_path, const int32_t* prev_
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
 
+int gdn_tree_build_topw(const float* cand_logp, int32_t B, int32_t N, int32_t c, int32_t w,
+                        int32_t max_depth, int32_t* parent, int32_t* cand_index, float* score,
+                        int32_t* n_built, void* stream) {
+  if (B < 0 || N < 1 || c < 1 || w < 1 || max_depth < 1) return GDN_TREE_EINVAL;
+  if (N > gdn::kMaxNHost || c > 32 || w > N) return GDN_TREE_EUNSUPPORTED;
+  if (B == 0) return GDN_TREE_OK;
+  if (cand_logp == nullptr || parent == nullptr || !aligned4(cand_logp) || !aligned4(parent))
+    return GDN_TREE_EINVAL;
+  const void* opt[] = {cand_index, score, n_built};
+  for (const void* p : opt)
+    if (p && !aligned4(p)) return GDN_TREE_EINVAL;
+  const cudaError_t err = gdn::launch_tree_topw(cand_logp, B, N, c, w, max_depth, parent,
+                                                cand_index, score, n_built,
+                                                static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
+}
+
 const char* gdn_tree_strerror(int code) {
   switch (code) {
     case GDN_TREE_OK: return "ok";

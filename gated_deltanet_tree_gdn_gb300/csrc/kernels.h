@@ -98,6 +98,12 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
 
+// top-w best-first draft-tree construction
+size_t tree_topw_smem_bytes(int N, int c);
+cudaError_t launch_tree_topw(const float* cand_logp, int B, int N, int c, int w, int max_depth,
+                             int32_t* parent, int32_t* cand_index, float* score, int32_t* n_built,
+                             cudaStream_t stream);
+
 // single-branch recurrent verification (the measurement baseline)
 cudaError_t launch_verify_recurrent(const VerifyArgs& a, cudaStream_t stream);
 

@@ -237,6 +237,36 @@ int gdn_tree_commit_verify_packed(const int32_t *prev_path, const int32_t *prev_
                                   gdn_tree_dims dims, int32_t *commit_status,
                                   int32_t *verify_status, void *stream);
 
+/*
+ * gdn_tree_build_topw -- the draft tree, by top-w best-first growth.
+ *
+ * The DFlash-TfM page, section 2 ("Costruzione dell'Albero"), builds the draft
+ * tree with DySpec's best-first growth, modified to pop the top-w candidates of
+ * the heap and expand all w at once: a tree of N nodes in ceil(N / w) rounds.
+ * Reading taken: node 0 is the root (score 0, depth 1); every node of depth <
+ * max_depth offers c candidate children, candidate j of node p scoring
+ * score(p) + cand_logp[b, p, j] (an fp32 addition); a round takes the
+ * min(w, N - built) best live candidates (higher score first, ties to the lower
+ * p * c + j, i.e. creation order) as new nodes in that order, after which they
+ * offer their own candidates.  A -inf candidate is never taken; if candidates run
+ * out first, fewer than N nodes are built.
+ *
+ *   cand_logp   [B, N, c] fp32, device: the log-probabilities of node p's c
+ *               candidates (rows of nodes that are never built are not read);
+ *               no NaN
+ *   parent      [B, N] int32, device, out: the tree (topologically ordered,
+ *               -1 for the root), ready for gdn_tree_verify; -2 past n_built
+ *   cand_index  [B, N] int32 or NULL, out: j of the parent's candidate each node
+ *               is (-1 root, -2 past n_built)
+ *   score       [B, N] fp32 or NULL, out: the node's score (NaN past n_built)
+ *   n_built     [B] int32 or NULL, out: nodes built per sequence
+ * Limits: 1 <= N <= 256, 1 <= c <= 32, 1 <= w <= N, max_depth >= 1, B >= 0.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+int gdn_tree_build_topw(const float *cand_logp, int32_t B, int32_t N, int32_t c, int32_t w,
+                        int32_t max_depth, int32_t *parent, int32_t *cand_index, float *score,
+                        int32_t *n_built, void *stream);
+
 /* Human-readable text for a return code or a device status code. */
 const char *gdn_tree_strerror(int code);
 
