@@ -117,7 +117,7 @@ constexpr uint32_t OFF_U = 4 * kOpBytes;
 constexpr uint32_t OFF_V = OFF_U;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
-constexpr uint32_t kSmallBytes = 13824;
+constexpr uint32_t kSmallBytes = 14848;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
@@ -149,6 +149,8 @@ struct Small {
   int n_kq, n_g, n_ks;  // phases issued on bar_kq (and bar_v), bar_g, bar_ks
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
+  int pre_path[kMaxN];  // the next unit's accepted path and its length, prefetched
+  int pre_plen;
   float cla[kMaxN];
   float cw[kMaxN];
   float cgamma;
@@ -495,23 +497,35 @@ __device__ __forceinline__ void commit_weights(Small& S, int L, int lane) {
   if (lane == 0) S.cgamma = expf(df_value(GL));
 }
 
+// Warps 5-15 (ot = tid - 160): start the copies of a unit's accepted path and
+// its length into the prefetch slots (the unit's prologue waits for them).
+__device__ __forceinline__ void prefetch_path(const FusedCommit& fc, Small& S, int b, int ot) {
+  if (ot < fc.Lmax) cp_async4(&S.pre_path[ot], fc.path + (size_t)b * fc.Lmax + ot);
+  if (ot == 0) cp_async4(&S.pre_plen, fc.path_len + b);
+  cp_async_commit();
+}
+
 // Warps 5-15 (ot = tid - 160; warp 4 issues the copies and MMAs meanwhile): checks the previous tree's
 // accepted path of sequence b (range, chain order, parent links), gathers its
 // log alpha, stages the first chunk of its k / U rows into region 2 and forms
 // the path weights.  Sets S.cbad (0 or the sequence's commit status), S.cL.
 __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S, uint8_t* smem,
                                                 int b, int h, int hq, int Hqk, int Hv, int ot,
-                                                int warp, int lane) {
+                                                int warp, int lane, int next_b) {
   const int pn = fc.lay.count(b, fc.N);  // the previous tree's node count (< 0: bad rows)
-  const int L = fc.path_len[b];
+  cp_async_wait_all();  // this unit's path, prefetched during the previous unit
+  NamedSync<2, kThreads - 160>()();
+  const int L = S.pre_plen;
   int pj = -1;
-  if (ot < fc.Lmax) pj = fc.path[(size_t)b * fc.Lmax + ot];
+  if (ot < fc.Lmax) pj = S.pre_path[ot];
   int cbad = (pn < 0 || L < 0 || L > pn || L > fc.Lmax);
   if (!cbad && ot < L) {
     cbad |= (pj < 0 || pj >= pn);
     S.cpath[ot] = pj;
   }
   cbad = bar_or<2, kThreads - 160>(cbad);
+  // every read of the prefetch slots is done: the next unit's path starts coming
+  if (next_b >= 0) prefetch_path(fc, S, next_b, ot);
   if (!cbad && ot < L) {
     const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
     cbad |= (ot > 0 && pj <= prev);
@@ -680,6 +694,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     mbar_fence_init();
     if (unit < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, lay, unit, Hv, Hqk, Nmax);
   }
+  if constexpr (kFused) {
+    if (warp > 4 && unit < n_units) prefetch_path(fc, S, unit / Hv, tid - 160);
+  }
   if (warp < 4) {
     if (unit < n_units) prefetch_tree(S, parent, beta, log_alpha, lay, unit, Nmax, Hv, tid);
     mbar_init(&S.node_bar[tid], 1);  // one solve barrier per node (one arrival a phase)
@@ -722,7 +739,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       TC_MARK(8);
     } else {
       if constexpr (kFused) {
-        if (warp > 4) commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 160, warp, lane);
+        if (warp > 4)
+          commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 160, warp, lane,
+                          next < n_units ? next / Hv : -1);
       }
       if (tid == kIssuer) {
         // the next unit's K, Q and state head for L2 now, so that their copies (issued
