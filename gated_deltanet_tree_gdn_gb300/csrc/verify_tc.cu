@@ -61,6 +61,10 @@ constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kIssuer = 128;  // the one thread that issues every copy and MMA (warp 4, lane 0)
 constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
+// while every |g_t| of a unit is at most this, e^{g_t - g_s} is formed as
+// e^{g_t} e^{-g_s} (both factors, and their product, stay normal fp32 numbers);
+// beyond it, from the double-float difference
+constexpr float kProductDecayLimit = 40.f;
 
 #ifdef GDN_TC_PROFILE
 // per-unit phase timestamps for a profiling build (never in the product build):
@@ -117,7 +121,7 @@ constexpr uint32_t OFF_U = 4 * kOpBytes;
 constexpr uint32_t OFF_V = OFF_U;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
-constexpr uint32_t kSmallBytes = 14848;
+constexpr uint32_t kSmallBytes = 15872;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
@@ -129,6 +133,7 @@ struct Small {
   int parent[kTile];
   int jump[kTile];  // tree prep: pointer jumping
   df g[kTile];
+  float eg[kTile], emg[kTile];  // e^{g_t}, e^{-g_t}
   float beta[kTile];
   float la[kTile];
   float ydiag[kTile];  // Y[t,t] = q_t . k_t
@@ -145,7 +150,8 @@ struct Small {
   uint64_t bar_kq, bar_v, bar_g, bar_ks;
   uint32_t tmem_base;
   int err;
-  int bad;  // the tree failed validation
+  int bad;     // the tree failed validation
+  int wide_g;  // some |g_t| > kProductDecayLimit
   int n_kq, n_g, n_ks;  // phases issued on bar_kq (and bar_v), bar_g, bar_ks
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
@@ -162,7 +168,10 @@ struct Small {
 #endif
 };
 static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
-static_assert(offsetof(Small, g) % 16 == 0, "path log-decays are read as float4");
+// members read or written as 16-byte vectors
+static_assert(offsetof(Small, g) % 16 == 0 && offsetof(Small, emg) % 16 == 0,
+              "path log-decays are read as float4");
+static_assert(offsetof(Small, anc) % 16 == 0, "ancestor rows are read and written as uint4");
 
 // byte offset of 16-byte chunk k8 (K elements 8*k8 .. 8*k8+7) of `row` in a
 // 128-row, 128-wide K-major bf16 tile stored with the 128-byte swizzle
@@ -393,7 +402,15 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
     row[k] = (uint8_t)tid;
     atomicAdd(&S.level_start[dep], 1);
   }
-  TreeSync()();
+  int wide = 0;
+  if (tid < N) {
+    const float gv = df_value(g);
+    S.eg[tid] = expf(gv);
+    S.emg[tid] = expf(-gv);
+    wide = fabsf(gv) > kProductDecayLimit;
+  }
+  wide = bar_or<1, 128>(wide);  // (also the barrier before the level scan)
+  if (tid == 0) S.wide_g = wide;
   TC_MARK(14);
   if (warp == 0) {
     // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
@@ -820,6 +837,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       tmem_ld_32cols(trow + kColGqk + col0, yr);
       TC_MARK(11);
       float ydiag = 0.f;
+      if (!S.wide_g) {  // CTA-uniform: e^{g_t - g_s} = e^{g_t} e^{-g_s}
+        const float egt = live ? S.eg[t] : 0.f;
+#pragma unroll
+        for (int j8 = 0; j8 < 4; ++j8) {
+          const float4 m0 = *reinterpret_cast<const float4*>(&S.emg[col0 + j8 * 8]);
+          const float4 m1 = *reinterpret_cast<const float4*>(&S.emg[col0 + j8 * 8 + 4]);
+          const float em[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = j8 * 8 + e;
+            if (col0 + j == t) ydiag = yr[j];
+            const float dec = ((abits >> j) & 1u) ? egt * em[e] : 0.f;
+            xr[j] = bt * dec * xr[j];
+            yr[j] = dec * yr[j];
+          }
+        }
+      } else {
 #pragma unroll
       for (int j8 = 0; j8 < 4; ++j8) {
         df gs[8];  // path log-decays of columns col0 + 8 j8 .., loaded together
@@ -840,6 +874,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           xr[j] = bt * dec * xr[j];
           yr[j] = dec * yr[j];
         }
+      }
       }
       TC_MARK(4);
 
