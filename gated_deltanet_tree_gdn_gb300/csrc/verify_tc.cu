@@ -113,6 +113,7 @@ constexpr uint32_t OFF_XY = 0;
 // MMAs end; then the output rows (seeded with gamma Q S0, finished by the solve)
 constexpr uint32_t OFF_CK = 2 * kOpBytes;
 constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;
+constexpr uint32_t OFF_CKRAW = 2 * kOpBytes + 2 * kCommitChunk * kD * 4;  // k rows as bf16
 constexpr uint32_t OFF_S0H = 2 * kOpBytes;
 constexpr uint32_t OFF_S0L = 3 * kOpBytes;
 constexpr uint32_t OFF_P = 2 * kOpBytes;
@@ -232,6 +233,15 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// waits for all but this thread's most recent cp.async group
+__device__ __forceinline__ void cp_async_wait_but_last() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+// 16-byte asynchronous copy global -> shared (L2 only)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
 }
 
 // Where unit (b, h)'s nodes live: its node count n (0 when the sequence's layout
@@ -471,6 +481,44 @@ __device__ __forceinline__ void commit_stage_rows(const FusedCommit& fc, const S
   }
 }
 
+// The first chunk of path rows, asynchronously: the k rows (bf16, as they are) and
+// the U rows are copied with cp.async (one group); stage_rows_finish, by the same
+// threads, waits for it and widens the k rows to fp32.
+__device__ __forceinline__ void stage_rows_issue(const FusedCommit& fc, const Small& S,
+                                                 uint8_t* smem, int b, int h, int hq, int Hqk,
+                                                 int Hv, int nj, int i0, int stride) {
+  const size_t prow0 = (size_t)fc.lay.row0(b, fc.N);
+  const size_t purow0 = fc.lay.urow0(b, h, Hv, fc.N);
+  uint8_t* kraw = smem + OFF_CKRAW;  // [kCommitChunk][kD] bf16
+  float* su = reinterpret_cast<float*>(smem + OFF_CU);
+  for (int e = i0; e < nj * (kD / 8); e += stride) {
+    const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
+    cp_async16(kraw + (jj * kD + c) * 2, fc.k + ((prow0 + S.cpath[jj]) * Hqk + hq) * kD + c);
+  }
+  for (int e = i0; e < nj * (kD / 4); e += stride) {
+    const int jj = e / (kD / 4), c = (e % (kD / 4)) * 4;
+    cp_async16(su + jj * kD + c, fc.U + (purow0 + S.cpath[jj]) * kD + c);
+  }
+  cp_async_commit();
+}
+
+__device__ __forceinline__ void stage_rows_finish(uint8_t* smem, int nj, int i0, int stride) {
+  const uint8_t* kraw = smem + OFF_CKRAW;
+  float* sk = reinterpret_cast<float*>(smem + OFF_CK);
+  for (int e = i0; e < nj * (kD / 8); e += stride) {
+    const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
+    const uint4 raw = *reinterpret_cast<const uint4*>(kraw + (jj * kD + c) * 2);
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    float* dst = sk + jj * kD + c;
+    *reinterpret_cast<float4*>(dst) =
+        make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xffff0000u),
+                    __uint_as_float(w4[1] << 16), __uint_as_float(w4[1] & 0xffff0000u));
+    *reinterpret_cast<float4*>(dst + 4) =
+        make_float4(__uint_as_float(w4[2] << 16), __uint_as_float(w4[2] & 0xffff0000u),
+                    __uint_as_float(w4[3] << 16), __uint_as_float(w4[3] & 0xffff0000u));
+  }
+}
+
 // w_j = exp(G_L - G_j) and gamma_L = exp(G_L) along the committed path, with
 // G_j the inclusive double-float prefix sums of log alpha; one warp
 __device__ __forceinline__ void commit_weights(Small& S, int L, int lane) {
@@ -541,8 +589,10 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
     S.cpath[ot] = pj;
   }
   cbad = bar_or<2, kThreads - 160>(cbad);
-  // every read of the prefetch slots is done: the next unit's path starts coming
-  if (next_b >= 0) prefetch_path(fc, S, next_b, ot);
+  // the entries are in range: the first chunk of k / U rows starts coming while
+  // the chain check and log alpha are fetched (rows of a failed check go unused)
+  const int nj0 = min(kCommitChunk, L);
+  if (!cbad) stage_rows_issue(fc, S, smem, b, h, hq, Hqk, Hv, nj0, ot, kThreads - 160);
   if (!cbad && ot < L) {
     const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
     cbad |= (ot > 0 && pj <= prev);
@@ -550,8 +600,14 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
     if (fc.parent) cbad |= (fc.parent[prow0 + pj] != prev);
     S.cla[ot] = fc.log_alpha[(prow0 + pj) * Hv + h];
   }
-  if (!cbad)
-    commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, 0, min(kCommitChunk, L), ot, kThreads - 160);
+  // every read of the prefetch slots is done: the next unit's path starts coming
+  // (its own cp.async group, left in flight by the wait below)
+  if (next_b >= 0) prefetch_path(fc, S, next_b, ot);
+  else cp_async_commit();  // an empty group keeps the wait's count right
+  if (!cbad) {
+    cp_async_wait_but_last();
+    stage_rows_finish(smem, nj0, ot, kThreads - 160);
+  }
   cbad = bar_or<2, kThreads - 160>(cbad);
   if (ot == 0) {
     S.cbad = !cbad ? GDN_TREE_STATUS_OK
