@@ -31,9 +31,42 @@ constexpr int kChunk = 32;   // path entries staged per round
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on the S0 copy wait
 
 // dynamic shared memory: S0 rows (kRowsPerCta x dv fp32) | k rows [kChunk][kRowsPerCta] |
-// u rows [kChunk][dv]
+// u rows [kChunk][dv] | path, log alpha, w_j [path capacity] each
 constexpr size_t kSmemBytes =
     (size_t)(kRowsPerCta * kMaxD + kChunk * kRowsPerCta + kChunk * kMaxD) * sizeof(float);
+
+// path capacity: Lmax rounded up to a whole scan block (at least kMaxN)
+__host__ __device__ inline int path_capacity(int Lmax) { return Lmax <= kMaxN ? kMaxN : (Lmax + 255) / 256 * 256; }
+
+// One warp: G[e] = base + (inclusive prefix sum of la[j0 ..] up to entry
+// j0 + lane*8 + e), double-float, entries at or past L counting as 0.  Each lane
+// reads only its own eight entries.
+__device__ __forceinline__ void warp_scan_256(const float* la, int j0, int L, df base, int lane,
+                                              df (&G)[8]) {
+  df loc[8];
+  df run = {0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int j = j0 + lane * 8 + e;
+    run = df_add(run, df{j < L ? la[j] : 0.f, 0.f});
+    loc[e] = run;
+  }
+  df pre = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    df up;
+    up.hi = __shfl_up_sync(0xffffffffu, pre.hi, o);
+    up.lo = __shfl_up_sync(0xffffffffu, pre.lo, o);
+    if (lane >= o) pre = df_add(pre, up);
+  }
+  df excl;
+  excl.hi = __shfl_up_sync(0xffffffffu, pre.hi, 1);
+  excl.lo = __shfl_up_sync(0xffffffffu, pre.lo, 1);
+  if (lane == 0) excl = df{0.f, 0.f};
+  excl = df_add(base, excl);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) G[e] = df_add(excl, loc[e]);
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 4)
@@ -48,9 +81,10 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   float* sS0 = smem_f;                            // [rows][dv]
   float* sK = sS0 + kRowsPerCta * kMaxD;          // [kChunk][rows]
   float* sU = sK + kChunk * kRowsPerCta;          // [kChunk][dv]
-  __shared__ int sPath[kMaxN];
-  __shared__ float sLa[kMaxN];                    // log alpha along the path
-  __shared__ float sW[kMaxN];                     // w_j
+  const int cap = path_capacity(Lmax);
+  int* sPath = reinterpret_cast<int*>(sU + kChunk * kMaxD);  // [cap]
+  float* sLa = reinterpret_cast<float*>(sPath + cap);         // log alpha (then G_j.lo)
+  float* sW = sLa + cap;                                      // w_j (G_j.hi during the scan)
   __shared__ uint64_t sBar;
   __shared__ float sGamma;
 
@@ -79,7 +113,8 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     sm100::bulk_load(sS0, S0 + sbase + (size_t)row0 * dv, bytes, &sBar);
   }
 
-  // ---- round 1: path length and entries (range-checked) ----------------------
+  // ---- round 1: path length and entries (range-checked); the first kThreads
+  //      entries are loaded together with the length ------------------------------
   const int L = path_len[b];
   int pj = -1;
   if (tid < Lmax) pj = path[(size_t)b * Lmax + tid];
@@ -88,17 +123,32 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     bad |= (pj < 0 || pj >= N);
     sPath[tid] = pj;
   }
+  if (!bad) {
+    for (int j = tid + kThreads; j < L; j += kThreads) {  // paths past kThreads entries
+      const int pv = path[(size_t)b * Lmax + j];
+      bad |= (pv < 0 || pv >= N);
+      sPath[j] = pv;
+    }
+  }
   bad = __syncthreads_or(bad);
 
   // ---- round 2: chain check, log alpha, and the first chunk of k / u rows,
   //      all issued together (indices are in range from here on) ----------------
+  // a root-to-node path is strictly increasing in a topological order; with the
+  // tree given it must also follow the parent links
   if (!bad && tid < L) {
-    // a root-to-node path is strictly increasing in a topological order; with
-    // the tree given it must also follow the parent links
     const int prev = tid == 0 ? -1 : sPath[tid - 1];
     bad |= (tid > 0 && pj <= prev);
     if (parent) bad |= (parent[row + pj] != prev);
     sLa[tid] = log_alpha[(row + pj) * Hv + h];
+  }
+  if (!bad) {
+    for (int j = tid + kThreads; j < L; j += kThreads) {
+      const int pv = sPath[j], prev = sPath[j - 1];
+      bad |= (pv <= prev);
+      if (parent) bad |= (parent[row + pv] != prev);
+      sLa[j] = log_alpha[(row + pv) * Hv + h];
+    }
   }
   auto stage = [&](int j0, int nj) {
     for (int e = tid; e < nj * (rows / 4); e += kThreads) {
@@ -124,46 +174,48 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 
   // ---- G_j: inclusive double-float prefix sums of log alpha along the path ------
   if (warp == 0) {
-    // lane l owns entries l*8 .. l*8+7 (L <= 256)
-    df loc[8];
-    df run = {0.f, 0.f};
+    if (L <= 256) {
+      // lane l owns entries l*8 .. l*8+7
+      df G[8];
+      warp_scan_256(sLa, 0, L, df{0.f, 0.f}, lane, G);
+      // G_L lives in the lane that owns entry L-1
+      const int owner = L > 0 ? (L - 1) >> 3 : 0, slot = L > 0 ? (L - 1) & 7 : 0;
+      df mine = G[0];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int j = lane * 8 + e;
-      run = df_add(run, df{j < L ? sLa[j] : 0.f, 0.f});
-      loc[e] = run;
+      for (int e = 1; e < 8; ++e)
+        if (e == slot) mine = G[e];
+      df GL;
+      GL.hi = __shfl_sync(0xffffffffu, mine.hi, owner);
+      GL.lo = __shfl_sync(0xffffffffu, mine.lo, owner);
+      if (L == 0) GL = df{0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = lane * 8 + e;
+        if (j < L) sW[j] = expf(df_diff(GL, G[e]));
+      }
+      if (lane == 0) sGamma = expf(df_value(GL));
+    } else {
+      // blocks of 256 entries with a running carry; G_j parks in (sW, sLa)
+      df carry = {0.f, 0.f};
+      for (int j0 = 0; j0 < L; j0 += 256) {
+        df G[8];
+        warp_scan_256(sLa, j0, L, carry, lane, G);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int j = j0 + lane * 8 + e;
+          if (j < L) {
+            sW[j] = G[e].hi;
+            sLa[j] = G[e].lo;
+          }
+        }
+        __syncwarp();
+        const int last = min(L, j0 + 256) - 1;
+        carry = df{sW[last], sLa[last]};
+      }
+      const df GL = carry;
+      for (int j = lane; j < L; j += 32) sW[j] = expf(df_diff(GL, df{sW[j], sLa[j]}));
+      if (lane == 0) sGamma = expf(df_value(GL));
     }
-    df pre = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      df up;
-      up.hi = __shfl_up_sync(0xffffffffu, pre.hi, o);
-      up.lo = __shfl_up_sync(0xffffffffu, pre.lo, o);
-      if (lane >= o) pre = df_add(pre, up);
-    }
-    df excl;
-    excl.hi = __shfl_up_sync(0xffffffffu, pre.hi, 1);
-    excl.lo = __shfl_up_sync(0xffffffffu, pre.lo, 1);
-    if (lane == 0) excl = df{0.f, 0.f};
-    df G[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) G[e] = df_add(excl, loc[e]);
-    // G_L lives in the lane that owns entry L-1
-    const int owner = L > 0 ? (L - 1) >> 3 : 0, slot = L > 0 ? (L - 1) & 7 : 0;
-    df mine = G[0];
-#pragma unroll
-    for (int e = 1; e < 8; ++e)
-      if (e == slot) mine = G[e];
-    df GL;
-    GL.hi = __shfl_sync(0xffffffffu, mine.hi, owner);
-    GL.lo = __shfl_sync(0xffffffffu, mine.lo, owner);
-    if (L == 0) GL = df{0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int j = lane * 8 + e;
-      if (j < L) sW[j] = expf(df_diff(GL, G[e]));
-    }
-    if (lane == 0) sGamma = expf(df_value(GL));
   }
   __syncthreads();
 
@@ -224,19 +276,20 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
   const dim3 grid(a.d.Hv, a.d.B, (a.d.dk + kRowsPerCta - 1) / kRowsPerCta);
+  const size_t smem = kSmemBytes + (size_t)path_capacity(a.Lmax) * 3 * sizeof(float);
   cudaError_t err;
   if (a.d.dtype == GDN_TREE_BF16) {
     err = cudaFuncSetAttribute(commit_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    commit_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, stream>>>(
+    commit_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const __nv_bfloat16*>(a.k),
         a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
   } else {
     err = cudaFuncSetAttribute(commit_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmemBytes);
+                               (int)smem);
     if (err != cudaSuccess) return err;
-    commit_kernel<float><<<grid, kThreads, kSmemBytes, stream>>>(
+    commit_kernel<float><<<grid, kThreads, smem, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const float*>(a.k),
         a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
   }

@@ -19,7 +19,8 @@
 
 namespace gdn {
 
-constexpr int kMaxN = 256;
+constexpr int kMaxN = 256;       // largest tree of the kernels that keep it all on chip
+constexpr int kMaxNLong = 1024;  // largest tree of the chunked kernel and of a commit path
 constexpr int kMaxD = 128;
 
 // ---- double-float arithmetic (Knuth TwoSum / Dekker FastTwoSum) -----------

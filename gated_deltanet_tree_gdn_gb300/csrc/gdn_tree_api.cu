@@ -52,7 +52,7 @@ int check_dims(const gdn_tree_dims& d) {
     return GDN_TREE_EINVAL;
   if (d.Hv % d.Hqk != 0) return GDN_TREE_EINVAL;
   if (d.dtype != GDN_TREE_BF16 && d.dtype != GDN_TREE_F32) return GDN_TREE_EUNSUPPORTED;
-  if (d.N > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (d.N > gdn::kMaxNLongHost) return GDN_TREE_EUNSUPPORTED;
   if (!supported_head_dim(d.dk) || !supported_head_dim(d.dv)) return GDN_TREE_EUNSUPPORTED;
   // every flat index must fit comfortably in the kernels' size_t arithmetic and
   // the grid's y dimension
@@ -64,13 +64,15 @@ int check_dims(const gdn_tree_dims& d) {
 
 namespace gdn {
 
-// GDN_TREE_KERNEL=generic forces the CUDA-core kernel (used by the tests to
-// cover both kernels on the same shapes); the default picks the tensor-core
-// kernel whenever it takes the shape.
-static bool force_generic() {
+// GDN_TREE_KERNEL=generic forces the CUDA-core kernels and GDN_TREE_KERNEL=long
+// the chunked one (used by the tests to cover every kernel on the same shapes);
+// the default picks the tensor-core kernel whenever it takes the shape, the
+// on-chip CUDA-core kernel up to kMaxNHost nodes and the chunked one beyond.
+static bool kernel_forced(const char* name) {
   const char* e = getenv("GDN_TREE_KERNEL");
-  return e && strcmp(e, "generic") == 0;
+  return e && strcmp(e, name) == 0;
 }
+static bool force_generic() { return kernel_forced("generic") || kernel_forced("long"); }
 
 // the tensor-core kernel takes the shape (packed rows: at least one row, for its
 // tensor maps)
@@ -80,11 +82,12 @@ static bool tc_takes(const VerifyArgs& a) {
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   if (tc_takes(a)) return launch_verify_tc(a, stream);
+  if (a.d.N > kMaxNHost || kernel_forced("long")) return launch_verify_long(a, stream);
   return launch_verify_generic(a, stream);
 }
 
 cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream) {
-  if (tc_takes(a.verify) && commit_verify_tc_supported(a.verify.d, a.prev_N))
+  if (tc_takes(a.verify) && commit_verify_tc_supported(a.verify.d, a.prev_N, a.Lmax))
     return launch_commit_verify_tc(a, stream);
   // two launches on the same stream: commit S_prev -> S1, then verify from S1
   gdn_tree_dims dp = a.verify.d;
@@ -126,6 +129,7 @@ int gdn_tree_verify_recurrent(const void* q, const void* k, const void* v,
                               gdn_tree_dims dims, int32_t* dev_status, void* stream) {
   const int rc = check_dims(dims);
   if (rc != GDN_TREE_OK) return rc;
+  if (dims.N > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;  // the path table is on chip
   if (dims.B == 0 || dims.N == 0) return GDN_TREE_OK;  // nothing to do
   const void* ptrs[] = {q, k, v, log_alpha, beta, parent, S0, o, U};
   for (const void* p : ptrs)
@@ -145,7 +149,7 @@ int gdn_tree_commit(const int32_t* path, const int32_t* path_len, const int32_t*
   if (rc != GDN_TREE_OK) return rc;
   if (Lmax < 0) return GDN_TREE_EINVAL;
   if (dims.B == 0) return GDN_TREE_OK;
-  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (Lmax > gdn::kMaxNLongHost) return GDN_TREE_EUNSUPPORTED;
   const void* ptrs[] = {path_len, U, k, log_alpha, S0, S1};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
@@ -177,7 +181,7 @@ int gdn_tree_commit_verify(const int32_t* prev_path, const int32_t* prev_path_le
   if (prev_N < 0 || Lmax < 0) return GDN_TREE_EINVAL;
   rc = check_dims(dp);
   if (rc != GDN_TREE_OK) return rc;
-  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (Lmax > gdn::kMaxNLongHost) return GDN_TREE_EUNSUPPORTED;
   if (dims.B == 0) return GDN_TREE_OK;
   if (prev_N == 0 || dims.N == 0) return GDN_TREE_EUNSUPPORTED;
   const void* ptrs[] = {prev_path_len, prev_U, prev_k, prev_log_alpha, S_prev, S1,
@@ -233,7 +237,7 @@ int gdn_tree_commit_packed(const int32_t* path, const int32_t* path_len, const i
   if (rc != GDN_TREE_OK) return rc;
   if (Lmax < 0) return GDN_TREE_EINVAL;
   if (dims.B == 0) return GDN_TREE_OK;
-  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (Lmax > gdn::kMaxNLongHost) return GDN_TREE_EUNSUPPORTED;
   const void* ptrs[] = {path_len, pool_in, pool_out};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
@@ -277,7 +281,7 @@ int gdn_tree_commit_verify_packed(const int32_t* prev_path, const int32_t* prev_
   if (rc != GDN_TREE_OK) return rc;
   rc = check_packed(prev_cu_nodes, prev_T, state_slot, n_slots, dims.B, &prev_lay);
   if (rc != GDN_TREE_OK) return rc;
-  if (Lmax > gdn::kMaxNHost) return GDN_TREE_EUNSUPPORTED;
+  if (Lmax > gdn::kMaxNLongHost) return GDN_TREE_EUNSUPPORTED;
   if (dims.B == 0) return GDN_TREE_OK;
   if (prev_N == 0 || dims.N == 0) return GDN_TREE_EUNSUPPORTED;
   const void* ptrs[] = {prev_path_len, prev_U, prev_k, prev_log_alpha, pool_in, pool_out,

@@ -10,7 +10,8 @@
 
 namespace gdn {
 
-constexpr int kMaxNHost = 256;  // largest tree the kernels take
+constexpr int kMaxNHost = 256;       // largest tree of the on-chip kernels
+constexpr int kMaxNLongHost = 1024;  // largest tree of the chunked kernel and commit path
 constexpr int kMaxDHost = 128;  // largest dk / dv
 
 // Where the rows and the state of sequence b live.
@@ -93,6 +94,10 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);
 size_t verify_generic_smem_bytes(int N, int dk, int dv);
 cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream);
 
+// trees longer than kMaxNHost: the two-level chunk pass
+size_t verify_long_smem_bytes(int N, int dk, int dv);
+cudaError_t launch_verify_long(const VerifyArgs& a, cudaStream_t stream);
+
 bool verify_tc_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 
@@ -107,7 +112,7 @@ cudaError_t launch_tree_topw(const float* cand_logp, int B, int N, int c, int w,
 // single-branch recurrent verification (the measurement baseline)
 cudaError_t launch_verify_recurrent(const VerifyArgs& a, cudaStream_t stream);
 
-bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N);
+bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N, int Lmax);
 cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stream);
 cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream);
 

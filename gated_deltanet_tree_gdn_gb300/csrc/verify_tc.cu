@@ -1179,8 +1179,9 @@ cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream) {
   return launch_tc<false>(a, FusedCommit{}, stream);
 }
 
-bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N) {
-  return verify_tc_supported(d) && prev_N >= 1 && prev_N <= kMaxN;
+bool commit_verify_tc_supported(const gdn_tree_dims& d, int prev_N, int Lmax) {
+  // the path prefetch copies min(Lmax, 352) entries into a kMaxN slot
+  return verify_tc_supported(d) && prev_N >= 1 && prev_N <= kMaxN && Lmax <= kMaxN;
 }
 
 cudaError_t launch_commit_verify_tc(const CommitVerifyArgs& a, cudaStream_t stream) {

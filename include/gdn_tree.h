@@ -53,7 +53,10 @@
  *    path        [B, Lmax]         int32 accepted root-to-node path, -1 padded
  *    path_len    [B]               int32, 0 <= path_len[b] <= min(N, Lmax)
  *
- * Limits: 1 <= N <= 256; dk, dv in {16, 32, 48, ..., 128}; B, Hv >= 1.
+ * Limits: 1 <= N <= 1024 and Lmax <= 1024; dk, dv in {16, 32, 48, ..., 128};
+ * B, Hv >= 1.  Trees of up to 256 nodes are verified on chip; longer trees go
+ * through a two-level chunk pass (chunks of 128 nodes on chip, earlier chunks'
+ * U rows read back from U), which is correct for every shape but slower.
  * B == 0 or N == 0 is a valid empty call that enqueues nothing.
  */
 #ifndef GDN_TREE_H
@@ -68,7 +71,7 @@ extern "C" {
 /* return codes */
 #define GDN_TREE_OK 0
 #define GDN_TREE_EINVAL (-1)      /* NULL or misaligned pointer, bad dims       */
-#define GDN_TREE_EUNSUPPORTED (-2) /* N > 256, dk/dv outside the list, dtype   */
+#define GDN_TREE_EUNSUPPORTED (-2) /* N > 1024, dk/dv outside the list, dtype  */
 #define GDN_TREE_ECUDA (-3)       /* a CUDA call (launch, attribute) failed     */
 
 /* per-sequence device status codes written to dev_status[b] */
@@ -150,7 +153,7 @@ int gdn_tree_commit(const int32_t *path, const int32_t *path_len,
  *                   path also sets GDN_TREE_STATUS_BAD_PATH when the commit of
  *                   that sequence failed).  Whenever commit_status reports an
  *                   error, that sequence's S1, o and U are unspecified.
- * Limits as for the two calls; 1 <= prev_N <= 256; prev_k has the dtype of q.
+ * Limits as for the two calls; 1 <= prev_N <= 1024; prev_k has the dtype of q.
  */
 int gdn_tree_commit_verify(const int32_t *prev_path, const int32_t *prev_path_len,
                            const int32_t *prev_parent, const float *prev_U,
@@ -174,7 +177,9 @@ int gdn_tree_commit_verify(const int32_t *prev_path, const int32_t *prev_path_le
  * them, with identical bits.  All arithmetic is fp32.
  *
  * Arguments, layouts, ownership, limits and dev_status exactly as for
- * gdn_tree_verify.  The state of a branch is held on chip; nothing is allocated.
+ * gdn_tree_verify, except that N <= 256 (the branch's path is held on chip;
+ * GDN_TREE_EUNSUPPORTED beyond).  The state of a branch is held on chip;
+ * nothing is allocated.
  */
 int gdn_tree_verify_recurrent(const void *q, const void *k, const void *v,
                               const float *log_alpha, const float *beta,

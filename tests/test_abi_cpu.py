@@ -65,7 +65,7 @@ def _commit(lib, dims, ptr=16, Lmax=4):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(N=257), gt.EUNSUPPORTED),
+    (dict(N=1025), gt.EUNSUPPORTED),
     (dict(dk=24), gt.EUNSUPPORTED),
     (dict(dv=256), gt.EUNSUPPORTED),
     (dict(dtype=7), gt.EUNSUPPORTED),
@@ -83,7 +83,17 @@ def test_null_or_misaligned_pointers_rejected(lib):
     assert _verify(lib, _dims(), ptr=24) == gt.EINVAL  # 8-byte aligned only
     assert _commit(lib, _dims(), ptr=0) == gt.EINVAL
     assert _commit(lib, _dims(), Lmax=-1) == gt.EINVAL
-    assert _commit(lib, _dims(), Lmax=300) == gt.EUNSUPPORTED
+    assert _commit(lib, _dims(), Lmax=1025) == gt.EUNSUPPORTED
+
+
+def test_recurrent_baseline_keeps_the_on_chip_limit(lib):
+    # trees past 256 nodes verify through the chunked kernel; the single-branch
+    # baseline keeps its path in shared memory and refuses them before launch
+    p = ctypes.c_void_p(16)
+    assert lib.gdn_tree_verify_recurrent(*(p,) * 9, _dims(N=257), None, None) == gt.EUNSUPPORTED
+    # at 256 nodes the shape passes and the NULL pointers are what is refused
+    assert lib.gdn_tree_verify_recurrent(*(None,) * 9, _dims(N=256), None, None) == gt.EINVAL
+    assert _verify(lib, _dims(N=1024), ptr=0) == gt.EINVAL
 
 
 def test_partial_overlap_of_S0_and_S1_rejected(lib):
