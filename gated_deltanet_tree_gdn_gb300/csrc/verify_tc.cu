@@ -984,6 +984,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                             gam * qs[4 * q + 3]);
         }
       }
+      // nodes past this tree complete their solve phase too, so that every node's
+      // barrier stays in step with the unit count
+      if (cq == 0 && !live) mbar_arrive(&S.node_bar[t]);
       tc_fence_before_sync();
       __syncthreads();
     }

@@ -206,3 +206,52 @@ def test_bad_layout_reported_and_left_unwritten(kernel):
     assert (on[P.cu[3]:P.cu[4]] == 123.0).all()   # the bad-slot sequence's rows unwritten
     ref_o, _ = P.oracle_verify()
     assert H.rel_err(on[:P.cu[1]], ref_o[:P.cu[1]]) <= H.TOL_O[W.BF16]
+
+
+def test_many_units_of_varying_size(kernel):
+    """More (sequence, head) units than SMs, so the persistent tensor-core kernel
+    walks several units of different tree sizes (and empty sequences) per CTA."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    rng = np.random.default_rng(51)
+    Ns = [int(n) for n in rng.integers(0, 129, size=40)]
+    Ns[3], Ns[17] = 0, 128
+    P = Packed(51, Ns, 4, 8, 128, 128, W.BF16, n_slots=44)
+    x = P.device()
+    st = torch.full((P.B,), -7, dtype=torch.int32, device="cuda")
+    o, U = gt.verify_packed(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"],
+                            x["cu"], x["pool"], state_slot=x["slot"], dev_status=st)
+    torch.cuda.synchronize()
+    check_verify(P, o.float().cpu().numpy(), U.cpu().numpy(), st.cpu().numpy())
+
+
+def test_commit_verify_many_units_of_varying_size(kernel):
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    rng = np.random.default_rng(52)
+    n_prev = [int(n) for n in rng.integers(1, 129, size=24)]
+    n_next = [int(n) for n in rng.integers(0, 129, size=24)]
+    prev = Packed(52, n_prev, 4, 8, 128, 128, W.BF16, n_slots=30)
+    nxt = Packed(53, n_next, 4, 8, 128, 128, W.BF16, n_slots=30)
+    nxt.slot, nxt.pool = prev.slot, prev.pool
+    xp, xn = prev.device(), nxt.device()
+    _, Up = gt.verify_packed(xp["q"], xp["k"], xp["v"], xp["log_alpha"], xp["beta"],
+                             xp["parent"], xp["cu"], xp["pool"], state_slot=xp["slot"])
+    cs = torch.full((24,), -7, dtype=torch.int32, device="cuda")
+    vs = torch.full((24,), -7, dtype=torch.int32, device="cuda")
+    pool_b, o_b, U_b = gt.commit_verify_packed(
+        xp["path"], xp["path_len"], Up, xp["k"], xp["log_alpha"], xp["cu"], xp["pool"],
+        xn["q"], xn["k"], xn["v"], xn["log_alpha"], xn["beta"], xn["parent"], xn["cu"],
+        state_slot=xp["slot"], prev_parent=xp["parent"], commit_status=cs, verify_status=vs)
+    torch.cuda.synchronize()
+    assert (cs.cpu().numpy() == 0).all() and (vs.cpu().numpy() == 0).all()
+    ref_pool = prev.oracle_commit()
+    used = np.zeros(len(ref_pool), bool)
+    used[prev.slot] = True
+    assert H.rel_err(pool_b.cpu().numpy()[used], ref_pool[used]) <= H.TOL_S1
+    for b, w in enumerate(nxt.ws):
+        if w is not None:
+            w.S0 = ref_pool[prev.slot[b]][None].astype(np.float32)
+    ref_o, ref_U = nxt.oracle_verify()
+    assert H.rel_err(o_b.float().cpu().numpy(), ref_o) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U_b.cpu().numpy(), ref_U) <= 1e-3  # the state itself carries 1e-4
