@@ -122,7 +122,7 @@ constexpr uint32_t OFF_U = 4 * kOpBytes;
 constexpr uint32_t OFF_V = OFF_U;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
-constexpr uint32_t kSmallBytes = 15872;
+constexpr uint32_t kSmallBytes = 16384;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
@@ -143,6 +143,10 @@ struct Small {
   int depth[kTile];
   int level_start[kTile + 2];
   int level_cursor[kTile + 2];
+  int level_task[kTile + 2];  // first solve task of each depth
+  uint8_t task_pos[kTile];    // solve task k: nodes order[task_pos[k]] .. (task_n[k] of them,
+  uint8_t task_n[kTile];      // one or two, of one depth)
+  int n_tasks;
   uint64_t node_bar[kTile];  // solve: completes a phase per unit once the node's u is final
   // the next unit's tree and gates, prefetched (cp.async) while this unit runs
   int pre_parent[kTile];
@@ -423,13 +427,15 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
   if (tid == 0) S.wide_g = wide;
   TC_MARK(14);
   if (warp == 0) {
-    // exclusive scan of the level counts 0..kTile+1 (lane owns 5 entries)
+    // exclusive scans of the level counts 0..kTile+1 and of the solve tasks per
+    // level (pairs of nodes, ceil(count / 2)), packed in one int (each <= 128);
+    // lane owns 5 entries
     int cnt[5], run = 0;
 #pragma unroll
     for (int e = 0; e < 5; ++e) {
       const int l = lane * 5 + e;
       cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
-      run += cnt[e];
+      run += cnt[e] | (((cnt[e] + 1) >> 1) << 16);
     }
     int incl = run;
 #pragma unroll
@@ -442,15 +448,28 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
     for (int e = 0; e < 5; ++e) {
       const int l = lane * 5 + e;
       if (l < kTile + 2) {
-        S.level_start[l] = excl;
-        S.level_cursor[l] = excl;
+        S.level_start[l] = excl & 0xffff;
+        S.level_cursor[l] = excl & 0xffff;
+        S.level_task[l] = excl >> 16;
       }
-      excl += cnt[e];
+      excl += cnt[e] | (((cnt[e] + 1) >> 1) << 16);
     }
+    if (lane == 31) S.n_tasks = incl >> 16;
   }
   TreeSync()();
   TC_MARK(15);
-  if (tid < N) S.order[atomicAdd(&S.level_cursor[dep], 1)] = tid;
+  if (tid < N) {
+    // position in the depth order; every even rank within the level opens a task
+    // of two nodes (one at an odd-sized level's end)
+    const int pos = atomicAdd(&S.level_cursor[dep], 1);
+    S.order[pos] = tid;
+    const int r = pos - S.level_start[dep];
+    if ((r & 1) == 0) {
+      const int k = S.level_task[dep] + (r >> 1);
+      S.task_pos[k] = (uint8_t)pos;
+      S.task_n[k] = (uint8_t)(pos + 1 < S.level_start[dep + 1] ? 2 : 1);
+    }
+  }
 }
 
 // k and U rows of path entries j0 .. j0+nj-1 of the previous tree into the
@@ -1011,58 +1030,84 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       auto wait_ready = [&](int node) {
         if (!mbar_wait(&S.node_bar[node], ph, kWaitLimitNs)) timed_out = true;
       };
-      for (int i = warp; i < N; i += kWarps) {
-        const int tn = S.order[i];
-        const int dep = S.depth[tn];
+      // lanes: half-warp hf takes node hf of the task (a single task's second half
+      // shadows the first without writing); lane hl of the half owns value columns
+      // 4 hl .. 4 hl + 3 and 64 + 4 hl .. 64 + 4 hl + 3 (16-byte chunks hl, hl + 16)
+      const int hf = lane >> 4, hl = lane & 15;
+      const int n_tasks = S.n_tasks;
+      for (int k = warp; k < n_tasks; k += kWarps) {
+        const int pos = S.task_pos[k];
+        const bool on = hf < S.task_n[k];
+        const int tn = S.order[pos + (on ? hf : 0)];
+        const int dep = S.depth[tn];  // the task's two nodes share it
         const uint8_t* pth = sPath + tn * kTile;  // pth[dep - 1] = tn, pth[0] = its root
         const float2* xyrow = sXY + x_index(tn, 0);
-        float4 acc = *reinterpret_cast<const float4*>(sU + u_index(tn, lane));
-        float4 py = *reinterpret_cast<const float4*>(sP + u_index(tn, lane));
+        float4 acc0 = *reinterpret_cast<const float4*>(sU + u_index(tn, hl));
+        float4 acc1 = *reinterpret_cast<const float4*>(sU + u_index(tn, hl + 16));
+        float4 py0 = *reinterpret_cast<const float4*>(sP + u_index(tn, hl));
+        float4 py1 = *reinterpret_cast<const float4*>(sP + u_index(tn, hl + 16));
         float yp = 0.f;
-        float4 up = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 up0 = make_float4(0.f, 0.f, 0.f, 0.f), up1 = up0;
         if (dep > 1) {
           if (dep > 2) wait_ready(pth[dep - 3]);
           int j = 0;
-          for (; j + 4 <= dep - 2; j += 4) {
-            int aa[4];
-            float2 xy[4];
-            float4 uu[4];
+          for (; j + 2 <= dep - 2; j += 2) {
+            int aa[2];
+            float2 xy[2];
+            float4 u0[2], u1[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) aa[e] = pth[j + e];
+            for (int e = 0; e < 2; ++e) aa[e] = pth[j + e];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 2; ++e) {
               xy[e] = xyrow[aa[e]];
-              uu[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], lane));
+              u0[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], hl));
+              u1[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], hl + 16));
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc = fma4(-xy[e].x, uu[e], acc);
-              py = fma4(xy[e].y, uu[e], py);
+            for (int e = 0; e < 2; ++e) {
+              acc0 = fma4(-xy[e].x, u0[e], acc0);
+              acc1 = fma4(-xy[e].x, u1[e], acc1);
+              py0 = fma4(xy[e].y, u0[e], py0);
+              py1 = fma4(xy[e].y, u1[e], py1);
             }
           }
-          for (; j < dep - 2; ++j) {
+          if (j < dep - 2) {
             const int a1 = pth[j];
             const float2 xy1 = xyrow[a1];
-            const float4 u1 = *reinterpret_cast<const float4*>(sU + u_index(a1, lane));
-            acc = fma4(-xy1.x, u1, acc);
-            py = fma4(xy1.y, u1, py);
+            const float4 v0 = *reinterpret_cast<const float4*>(sU + u_index(a1, hl));
+            const float4 v1 = *reinterpret_cast<const float4*>(sU + u_index(a1, hl + 16));
+            acc0 = fma4(-xy1.x, v0, acc0);
+            acc1 = fma4(-xy1.x, v1, acc1);
+            py0 = fma4(xy1.y, v0, py0);
+            py1 = fma4(xy1.y, v1, py1);
           }
           const int par = pth[dep - 2];
           const float2 xyp = xyrow[par];
           yp = xyp.y;
           wait_ready(par);
-          up = *reinterpret_cast<const float4*>(sU + u_index(par, lane));
-          acc = fma4(-xyp.x, up, acc);
-          *reinterpret_cast<float4*>(sU + u_index(tn, lane)) = acc;
+          up0 = *reinterpret_cast<const float4*>(sU + u_index(par, hl));
+          up1 = *reinterpret_cast<const float4*>(sU + u_index(par, hl + 16));
+          acc0 = fma4(-xyp.x, up0, acc0);
+          acc1 = fma4(-xyp.x, up1, acc1);
+          if (on) {
+            *reinterpret_cast<float4*>(sU + u_index(tn, hl)) = acc0;
+            *reinterpret_cast<float4*>(sU + u_index(tn, hl + 16)) = acc1;
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.node_bar[tn]);
-        py = fma4(yp, up, py);
-        py = fma4(S.ydiag[tn], acc, py);
-        if (write_out) {
-          *reinterpret_cast<float4*>(Ubh + (size_t)tn * kD + lane * 4) = acc;
-          *reinterpret_cast<uint2*>(obh + (size_t)tn * Hv * kD + lane * 4) =
-              make_uint2(pack2f(py.x, py.y), pack2f(py.z, py.w));
+        if (on && hl == 0) mbar_arrive(&S.node_bar[tn]);
+        const float yd = S.ydiag[tn];
+        py0 = fma4(yd, acc0, fma4(yp, up0, py0));
+        py1 = fma4(yd, acc1, fma4(yp, up1, py1));
+        if (write_out && on) {
+          float* urow = Ubh + (size_t)tn * kD;
+          *reinterpret_cast<float4*>(urow + hl * 4) = acc0;
+          *reinterpret_cast<float4*>(urow + 64 + hl * 4) = acc1;
+          __nv_bfloat16* orow = obh + (size_t)tn * Hv * kD;
+          *reinterpret_cast<uint2*>(orow + hl * 4) =
+              make_uint2(pack2f(py0.x, py0.y), pack2f(py0.z, py0.w));
+          *reinterpret_cast<uint2*>(orow + 64 + hl * 4) =
+              make_uint2(pack2f(py1.x, py1.y), pack2f(py1.z, py1.w));
         }
       }
       if (timed_out) S.err = 4;
