@@ -10,6 +10,7 @@ invalid trees/paths, empty paths and in-place commits."""
 import numpy as np
 import pytest
 
+import oracle
 import workloads as W
 from tests import harness as H
 
@@ -152,3 +153,30 @@ def test_sibling_permutation_on_gpu(kernel):
     assert H.rel_err(b["o"][0], a["o"][0, perm]) <= 1e-2
     assert H.rel_err(b["U"][0], a["U"][0][:, perm]) <= 1e-4
     assert H.rel_err(b["S1"], a["S1"]) <= 1e-4
+
+
+def test_invalid_tree_among_many_units(kernel):
+    """More units than SMs: every v-head of a sequence with an invalid tree is left
+    unwritten and reported, whichever CTA walks it and whatever it walked before."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    w = W.make_custom(seed=9, B=20, N=64, Hqk=8, Hv=16, dk=128, dv=128, dtype=W.BF16,
+                      tree="mixed", max_depth=24)
+    w.parent[5, 40] = 50   # not topologically ordered
+    w.parent[6, 3] = -5    # out of range
+    x = H.to_device(w)
+    st = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    o = torch.full((w.B, w.N, w.Hv, w.dv), 123.0, dtype=torch.bfloat16, device="cuda")
+    o, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"],
+                     x["S0"], o=o, dev_status=st)
+    torch.cuda.synchronize()
+    want = [gt.STATUS_OK] * w.B
+    want[5] = want[6] = gt.STATUS_BAD_TREE
+    assert st.cpu().tolist() == want
+    on = o.float().cpu().numpy()
+    assert (on[5] == 123.0).all() and (on[6] == 123.0).all()
+    ok = [b for b in range(w.B) if b not in (5, 6)]
+    ref_o, ref_U = oracle.verify(w.q[ok], w.k[ok], w.v[ok], w.log_alpha[ok], w.beta[ok],
+                                 w.parent[ok], w.S0[ok])
+    assert H.rel_err(on[ok], ref_o) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U.cpu().numpy()[ok], ref_U) <= H.TOL_U
