@@ -212,6 +212,21 @@ __device__ __forceinline__ uint64_t desc_sw128_kmajor(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand stored with the
+// 128-byte swizzle: atoms of 8 K-rows x 64 bf16 (128 bytes, the MN elements
+// contiguous) = 1024 bytes, swizzled like the K-major atom; `lbo` = byte offset
+// between atoms along MN (64-element blocks), `sbo` = between atoms along K
+// (8-row groups).  Atom bases 1024-byte aligned.
+__device__ __forceinline__ uint64_t desc_sw128_mnmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);     // start address, bits 0-13
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset, bits 16-29
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;  // stride byte offset, bits 32-45
+  d |= (uint64_t)1 << 46;                       // descriptor version for sm_100
+  d |= (uint64_t)2 << 61;                       // layout: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16: A, B bf16 K-major, D fp32, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                        // D format: f32
@@ -219,6 +234,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                     // B format: bf16
          | ((uint32_t)(N >> 3) << 17)     // N / 8
          | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+
+// The same with B MN-major (B given as K x N, N contiguous).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);  // transpose B
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

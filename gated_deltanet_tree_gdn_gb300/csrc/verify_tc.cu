@@ -16,8 +16,9 @@
 //   loaded while the current unit finishes.  Per unit:
 //   1. TMA (128-byte swizzle) brings K and Q of the q/k head and v of the unit
 //      (issued as soon as the previous unit's solve is over); each thread loads an
-//      8 x 4 tile of the fp32 state into registers and writes it as S0^T = hi + lo,
-//      two bf16 K-major tiles, so K S0 keeps fp32 accuracy (K is exact in bf16).
+//      8 x 4 tile of the fp32 state into registers and writes it as S0 = hi + lo,
+//      two bf16 tiles laid out MN-major for the MMA's B operand, so K S0 keeps fp32
+//      accuracy (K is exact in bf16).
 //      (Fused with the delayed commitment, the tile is first committed in registers
 //      and stored as S1.)  No thread waits on its own global loads near shared-memory
 //      work: the state tile is its only per-thread load.
@@ -223,6 +224,30 @@ __device__ __forceinline__ void umma_128x128x128(uint32_t d_tmem, uint32_t a_bas
   for (int s = 0; s < 8; ++s) {
     const uint32_t off = (uint32_t)((s >> 2) * kTileBytes + (s & 3) * 32);
     umma_bf16(d_tmem, desc_sw128_kmajor(a_base + off), desc_sw128_kmajor(b_base + off), idesc,
+              (accumulate || s > 0) ? 1u : 0u);
+  }
+}
+
+// The state operand S0 (K = dk rows x N = dv columns, bf16) is stored MN-major:
+// the 16-byte chunk n8 (columns 8 n8 .. 8 n8 + 7) of row k sits in the 1024-byte
+// atom of rows 8 (k / 8) .. and columns 64 (n8 / 8) .., atoms of one row group
+// 1 KB apart along N and row groups 2 KB apart, chunks swizzled by the row.
+constexpr uint32_t kS0Lbo = 1024, kS0Sbo = 2048;
+__device__ __forceinline__ uint32_t s0_chunk(int k, int n8) {
+  const int r = k & 7;
+  return (uint32_t)((k >> 3) * kS0Sbo + (n8 >> 3) * kS0Lbo + r * 128 + (((n8 & 7) ^ r) << 4));
+}
+
+// issue the 8 K-steps (K = 128) of D (+)= A S for a 128x128 K-major tile A and
+// the MN-major state tile S (a K-step of 16 rows spans two row groups)
+__device__ __forceinline__ void umma_128x128x128_s0(uint32_t d_tmem, uint32_t a_base,
+                                                    uint32_t s_base, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32_bmn(128, 128);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t a_off = (uint32_t)((s >> 2) * kTileBytes + (s & 3) * 32);
+    umma_bf16(d_tmem, desc_sw128_kmajor(a_base + a_off),
+              desc_sw128_mnmajor(s_base + (uint32_t)s * 2 * kS0Sbo, kS0Lbo, kS0Sbo), idesc,
               (accumulate || s > 0) ? 1u : 0u);
   }
 }
@@ -695,30 +720,41 @@ __device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small
   }
 }
 
-__device__ __forceinline__ float comp(const float4& v, int j) {
-  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-}
-
-// S0^T = hi + lo (bf16, K-major, 128-byte swizzle) from every thread's 8x4 tile of
-// the state (rows 8 r8 .., columns 4 c4 ..); the hi half is written first, so that
-// Q S0_hi and K S0_hi run on the tensor cores while the lo half is written; then
-// K S0_lo, and bar_ks tracks all of them.  All threads of the CTA.
+// S0 = hi + lo (bf16, MN-major, 128-byte swizzle: s0_chunk) from every thread's 8x4
+// tile of the state (rows 8 r8 .., columns 4 c4 ..).  The two lanes of a pair (c4
+// even, odd: one 16-byte chunk of columns) swap half their rows, so that each holds
+// whole chunks: rows 8 r8 .. + 3 in the even lane, 8 r8 + 4 .. + 7 in the odd one.
+// The hi half is written first, so that Q S0_hi and K S0_hi run on the tensor cores
+// while the lo half is written; then K S0_lo, and bar_ks tracks all of them.  All
+// threads of the CTA.
 __device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small& S, uint32_t tmem,
                                             int r8, int c4, const float4 (&st)[8], bool issuer,
                                             bool issue) {
+  const bool odd = c4 & 1;
+  float4 ch[4][2];  // chunk rows: 8 r8 + (odd ? 4 : 0) + i, columns 8 (c4 / 2) .. + 7
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 give = odd ? st[i] : st[4 + i];
+    float4 got;
+    got.x = __shfl_xor_sync(0xffffffffu, give.x, 1);
+    got.y = __shfl_xor_sync(0xffffffffu, give.y, 1);
+    got.z = __shfl_xor_sync(0xffffffffu, give.z, 1);
+    got.w = __shfl_xor_sync(0xffffffffu, give.w, 1);
+    ch[i][0] = odd ? got : st[i];
+    ch[i][1] = odd ? st[4 + i] : got;
+  }
+  const int row0 = 8 * r8 + (odd ? 4 : 0), n8 = c4 >> 1;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // column n = 4 c4 + j: rows 8 r8 .. 8 r8 + 7
-      uint32_t part[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t hi, lo;
-        split2(comp(st[2 * i], j), comp(st[2 * i + 1], j), hi, lo);
-        part[i] = half == 0 ? hi : lo;
-      }
-      *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) +
-                                sw128_chunk(4 * c4 + j, r8)) =
+    for (int i = 0; i < 4; ++i) {
+      uint32_t hi[4], lo[4];
+      split2(ch[i][0].x, ch[i][0].y, hi[0], lo[0]);
+      split2(ch[i][0].z, ch[i][0].w, hi[1], lo[1]);
+      split2(ch[i][1].x, ch[i][1].y, hi[2], lo[2]);
+      split2(ch[i][1].z, ch[i][1].w, hi[3], lo[3]);
+      const uint32_t* part = half == 0 ? hi : lo;
+      *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + s0_chunk(row0 + i, n8)) =
           make_uint4(part[0], part[1], part[2], part[3]);
     }
     fence_proxy_async_smem();
@@ -726,10 +762,10 @@ __device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small
     if (issuer && issue) {
       tc_fence_after_sync();
       if (half == 0) {
-        umma_128x128x128(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+        umma_128x128x128_s0(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+        umma_128x128x128_s0(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
       } else {
-        umma_128x128x128(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+        umma_128x128x128_s0(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
         umma_commit(&S.bar_ks);
         ++S.n_ks;
       }
@@ -765,8 +801,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int col0 = cq * 32;
   const uint32_t trow_off = (uint32_t)(q4 * 32) << 16;
   // state mapping: thread <-> 8x4 tile (rows 8 r8 .., columns 4 c4 ..); a warp holds
-  // 4 row blocks x 8 column groups, so its loads are 128-byte rows and its S0^T
-  // stores hit 8 distinct 16-byte bank groups
+  // 4 row blocks x 8 column groups, so its loads and stores are 128-byte rows
   const int r8 = (warp >> 2) * 4 + (lane >> 3), c4 = (warp & 3) * 8 + (lane & 7);
   int unit = blockIdx.x;
 
