@@ -351,12 +351,12 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], Sbuf[0],
               o=o, U=Ubuf[0])
 
-    def iteration(i, xx=None):
+    def iteration(i, xx=None, oo=None):
         xx = xx or x
         cur, nxt = i & 1, (i + 1) & 1
         gt.commit_verify(xx["path"], xx["path_len"], Ubuf[cur], xx["k"], xx["log_alpha"],
                          Sbuf[cur], xx["q"], xx["k"], xx["v"], xx["log_alpha"], xx["beta"],
-                         xx["parent"], S1=Sbuf[nxt], o=o, U=Ubuf[nxt],
+                         xx["parent"], S1=Sbuf[nxt], o=o if oo is None else oo, U=Ubuf[nxt],
                          prev_parent=xx["parent"])
 
     for i in range(args.warmup):
@@ -437,35 +437,86 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     torch.cuda.synchronize()
     tb_us = 1e3 * statistics.mean(evt[i][0].elapsed_time(evt[i][1]) for i in range(Kt))
 
+    # trees past the on-chip limit: the two-level chunk pass (verify, then the commit
+    # of paths into them) on 1024-node random trees of the same family (branching
+    # 1-4, depth <= 24), 8 sequences x the same heads
+    wl = W.make_custom(seed=1024 + rank, B=8, N=1024, Hqk=w.Hqk, Hv=w.Hv, dk=w.dk, dv=w.dv,
+                       dtype=w.dtype, tree="random", max_depth=24)
+    xl = {kk: torch.from_numpy(np.ascontiguousarray(getattr(wl, kk))).to(
+        device=dev, dtype=dt if kk in ("q", "k", "v") else None)
+        for kk in ("q", "k", "v", "log_alpha", "beta", "parent", "S0", "path", "path_len")}
+    ol = torch.empty((wl.B, wl.N, wl.Hv, wl.dv), dtype=dt, device=dev)
+    Ul = torch.empty((wl.B, wl.Hv, wl.N, wl.dv), dtype=torch.float32, device=dev)
+    S1l = torch.empty_like(xl["S0"])
+    Kl = max(3, min(K, 10))
+    evl = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Kl + 1)]
+    for i in range(Kl + 1):  # the first round is a warm-up
+        flush.zero_()
+        evl[i][0].record(stream)
+        gt.verify(xl["q"], xl["k"], xl["v"], xl["log_alpha"], xl["beta"], xl["parent"],
+                  xl["S0"], o=ol, U=Ul)
+        evl[i][1].record(stream)
+        gt.commit(xl["path"], xl["path_len"], Ul, xl["k"], xl["log_alpha"], xl["S0"], S1=S1l,
+                  parent=xl["parent"])
+        evl[i][2].record(stream)
+    torch.cuda.synchronize()
+    lv_us = 1e3 * statistics.mean(evl[i][0].elapsed_time(evl[i][1]) for i in range(1, Kl + 1))
+    lc_us = 1e3 * statistics.mean(evl[i][1].elapsed_time(evl[i][2]) for i in range(1, Kl + 1))
+
     # end to end through the public API: every step copies the tree's inputs and
     # the accepted path from pinned host memory (the recurrent state stays
     # resident on the device, as in a decoding loop), runs one decoding
-    # iteration, and reads o and the committed state back into pinned memory
+    # iteration, and reads its result, the tree's outputs o, back into pinned memory.
+    # As a serving loop runs it: step i's inputs copy in on one stream while step
+    # i - 1 computes, and step i - 1's outputs copy out on another (inputs and o
+    # double-buffered; every copy of every step is inside the timed region)
     h_o = torch.empty(o.shape, dtype=dt).pin_memory()
-    h_S1 = torch.empty(S1.shape, dtype=torch.float32).pin_memory()
     per_step_inputs = [kk for kk in hin if kk != "S0"]
     h2d = sum(hin[kk].numel() * hin[kk].element_size() for kk in per_step_inputs)
-    d2h = h_o.numel() * h_o.element_size() + h_S1.numel() * h_S1.element_size()
+    d2h = h_o.numel() * h_o.element_size()
     Ke = max(3, min(K, 50))
-    xe = {kk: torch.empty_like(t) for kk, t in x.items()}
+    xe = [{kk: torch.empty_like(t) for kk, t in x.items()} for _ in range(2)]
+    oe = [o, torch.empty_like(o)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step(i):
-        for kk in per_step_inputs:
-            xe[kk].copy_(hin[kk], non_blocking=True)
-        iteration(i, xe)
-        h_o.copy_(o, non_blocking=True)
-        h_S1.copy_(Sbuf[(i + 1) & 1], non_blocking=True)
+    def e2e_step(i, first):
+        j = i & 1
+        if not first[j]:
+            s_in.wait_event(ev_comp[j])    # step i - 2 has read these input buffers
+            stream.wait_event(ev_out[j])   # and its o has been copied out
+        with torch.cuda.stream(s_in):
+            for kk in per_step_inputs:
+                xe[j][kk].copy_(hin[kk], non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        iteration(i, xe[j], oe[j])
+        ev_comp[j].record(stream)
+        s_out.wait_event(ev_comp[j])
+        with torch.cuda.stream(s_out):
+            h_o.copy_(oe[j], non_blocking=True)
+            ev_out[j].record(s_out)
+        first[j] = False
 
-    for i in range(3):
-        e2e_step(i)
+    def e2e_run(n):
+        first = [True, True]
+        for i in range(n):
+            e2e_step(i, first)
+        stream.wait_event(ev_out[(n - 1) & 1])
+        if n > 1:
+            stream.wait_event(ev_out[n & 1])
+
+    e2e_run(3)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(Ke):
-        e2e_step(i)
+    s_in.wait_event(e0)
+    e2e_run(Ke)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, dist, dev)
@@ -521,6 +572,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         line["tree_build"] = {"kernel": "tree_topw_kernel", "us": tb_us, "B": w.B, "N": w.N,
                               "c": 4, "w": 4, "max_depth": 24,
                               "rounds": -(-(w.N - 1) // 4)}
+        line["long_trees"] = {
+            "kernel": "verify_long_kernel + commit_kernel",
+            "workload": f"B={wl.B} seqs x Hv={wl.Hv} v-heads (Hqk={wl.Hqk}), N={wl.N}-node random "
+                        "trees (branching 1-4, depth<=24), accepted paths <= depth",
+            "verify_us": lv_us, "commit_us": lc_us,
+            "nodes_per_s": wl.B * wl.N / ((lv_us + lc_us) * 1e-6),
+            "verify_roofline_frac": verify_bytes(wl) / (lv_us * 1e-6) / (hbm * 1e9),
+            "commit_roofline_frac": commit_bytes(wl) / (lc_us * 1e-6) / (hbm * 1e9)}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
