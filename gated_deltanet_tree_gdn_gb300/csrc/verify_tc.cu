@@ -614,6 +614,27 @@ __device__ __forceinline__ void prefetch_path(const FusedCommit& fc, Small& S, i
   cp_async_commit();
 }
 
+// Warps 5-15 (ot = tid - 160), as they finish their part of a unit's solve: the
+// next unit's accepted path (landed in the prefetch slots during this unit) sends
+// the rows its commit will read (U, k, log alpha, parent link of every entry in
+// range) to L2, so that the next unit's prologue finds them there.  The entries
+// are only read here; the prologue checks them.
+__device__ __forceinline__ void prefetch_path_rows_l2(const FusedCommit& fc, Small& S, int nb,
+                                                      int nh, int nhq, int Hqk, int Hv, int ot) {
+  cp_async_wait_all();  // this thread's slot entries
+  if (ot < fc.Lmax) {
+    const int pj = S.pre_path[ot];
+    const int pn = fc.lay.count(nb, fc.N);
+    if (pj >= 0 && pj < pn) {
+      const size_t prow0 = (size_t)fc.lay.row0(nb, fc.N);
+      bulk_prefetch_l2(fc.U + (fc.lay.urow0(nb, nh, Hv, fc.N) + pj) * kD, kD * 4);
+      bulk_prefetch_l2(fc.k + ((prow0 + pj) * Hqk + nhq) * kD, kD * 2);
+      prefetch_l2(fc.log_alpha + (prow0 + pj) * Hv + nh);
+      if (fc.parent) prefetch_l2(fc.parent + prow0 + pj);
+    }
+  }
+}
+
 // Warps 5-15 (ot = tid - 160; warp 4 issues the copies and MMAs meanwhile): checks the previous tree's
 // accepted path of sequence b (range, chain order, parent links), gathers its
 // log alpha, stages the first chunk of its k / U rows into region 2 and forms
@@ -1146,6 +1167,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
       if (timed_out) S.err = 4;
+      if constexpr (kFused) {
+        if (warp > 4 && next < n_units) {
+          const int nb = next / Hv, nh = next - nb * Hv;
+          prefetch_path_rows_l2(fc, S, nb, nh, nh / (Hv / Hqk), Hqk, Hv, tid - 160);
+        }
+      }
     }
     // region 1 is free: the next unit's K and Q start loading
     fence_proxy_async_smem();
