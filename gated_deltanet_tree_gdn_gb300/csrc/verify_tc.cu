@@ -512,10 +512,11 @@ __device__ __forceinline__ void commit_stage_rows(const FusedCommit& fc, const S
         fc.k + ((prow0 + S.cpath[j0 + jj]) * Hqk + hq) * kD + c);
     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
     float* dst = sk + jj * kD + c;
+    const float w = S.cw[j0 + jj];  // weighted as in stage_rows_finish
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      dst[2 * q] = __uint_as_float(w4[q] << 16);
-      dst[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+      dst[2 * q] = w * __uint_as_float(w4[q] << 16);
+      dst[2 * q + 1] = w * __uint_as_float(w4[q] & 0xffff0000u);
     }
   }
   for (int e = i0; e < nj * (kD / 4); e += stride) {
@@ -546,20 +547,24 @@ __device__ __forceinline__ void stage_rows_issue(const FusedCommit& fc, const Sm
   cp_async_commit();
 }
 
-__device__ __forceinline__ void stage_rows_finish(uint8_t* smem, int nj, int i0, int stride) {
+// widens the staged bf16 k rows to fp32, each scaled by its path weight w_j
+// (the products w_j k are the ones the accumulation would form)
+__device__ __forceinline__ void stage_rows_finish(const Small& S, uint8_t* smem, int nj, int i0,
+                                                  int stride) {
   const uint8_t* kraw = smem + OFF_CKRAW;
   float* sk = reinterpret_cast<float*>(smem + OFF_CK);
   for (int e = i0; e < nj * (kD / 8); e += stride) {
     const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
+    const float w = S.cw[jj];
     const uint4 raw = *reinterpret_cast<const uint4*>(kraw + (jj * kD + c) * 2);
     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
     float* dst = sk + jj * kD + c;
     *reinterpret_cast<float4*>(dst) =
-        make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xffff0000u),
-                    __uint_as_float(w4[1] << 16), __uint_as_float(w4[1] & 0xffff0000u));
+        make_float4(w * __uint_as_float(w4[0] << 16), w * __uint_as_float(w4[0] & 0xffff0000u),
+                    w * __uint_as_float(w4[1] << 16), w * __uint_as_float(w4[1] & 0xffff0000u));
     *reinterpret_cast<float4*>(dst + 4) =
-        make_float4(__uint_as_float(w4[2] << 16), __uint_as_float(w4[2] & 0xffff0000u),
-                    __uint_as_float(w4[3] << 16), __uint_as_float(w4[3] & 0xffff0000u));
+        make_float4(w * __uint_as_float(w4[2] << 16), w * __uint_as_float(w4[2] & 0xffff0000u),
+                    w * __uint_as_float(w4[3] << 16), w * __uint_as_float(w4[3] & 0xffff0000u));
   }
 }
 
@@ -669,17 +674,19 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
   // (its own cp.async group, left in flight by the wait below)
   if (next_b >= 0) prefetch_path(fc, S, next_b, ot);
   else cp_async_commit();  // an empty group keeps the wait's count right
-  if (!cbad) {
-    cp_async_wait_but_last();
-    stage_rows_finish(smem, nj0, ot, kThreads - 160);
-  }
-  cbad = bar_or<2, kThreads - 160>(cbad);
+  cbad = bar_or<2, kThreads - 160>(cbad);  // (also: every log alpha is in place)
   if (ot == 0) {
     S.cbad = !cbad ? GDN_TREE_STATUS_OK
                    : (pn < 0 ? GDN_TREE_STATUS_BAD_LAYOUT : GDN_TREE_STATUS_BAD_PATH);
     S.cL = L;
   }
-  if (!cbad && warp == 5) commit_weights(S, L, lane);
+  if (!cbad) {
+    // the weights while the rows land, then the k rows widened and weighted
+    if (warp == 5) commit_weights(S, L, lane);
+    cp_async_wait_but_last();
+    NamedSync<2, kThreads - 160>()();
+    stage_rows_finish(S, smem, nj0, ot, kThreads - 160);
+  }
 }
 
 // K_P^T diag(w) U_P for this thread's 8x4 tile of the state (rows r8*8 .., columns
@@ -703,12 +710,11 @@ __device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const S
       __syncthreads();
     }
     for (int jj = 0; jj < nj; ++jj) {
-      const float w = S.cw[j0 + jj];
+      // the staged k rows already carry their weights w_j
       const float4 k0 = *reinterpret_cast<const float4*>(sk + jj * kD + r8 * 8);
       const float4 k1 = *reinterpret_cast<const float4*>(sk + jj * kD + r8 * 8 + 4);
       const float4 uu = *reinterpret_cast<const float4*>(su + jj * kD + c4 * 4);
-      const float kk[8] = {w * k0.x, w * k0.y, w * k0.z, w * k0.w,
-                           w * k1.x, w * k1.y, w * k1.z, w * k1.w};
+      const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
       const float2 u01 = make_float2(uu.x, uu.y), u23 = make_float2(uu.z, uu.w);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {  // packed fp32x2 FMAs (same rounding as fmaf)
