@@ -26,6 +26,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -167,7 +168,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples: $GDN_BENCH_CLOCKS_DIR if set, else the temporary directory
+        out = os.environ.get("GDN_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out, f"gdn_bench_clocks_gpu{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -450,7 +453,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     S1l = torch.empty_like(xl["S0"])
     Kl = max(3, min(K, 10))
     evl = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Kl + 1)]
-    for i in range(Kl + 1):  # the first round is a warm-up
+    for i in range(Kl + 1):  # the first iteration is a warm-up
         flush.zero_()
         evl[i][0].record(stream)
         gt.verify(xl["q"], xl["k"], xl["v"], xl["log_alpha"], xl["beta"], xl["parent"],

@@ -12,7 +12,7 @@
 // Grid: (Hv, B, dk / 64), 256 threads, four CTAs per SM.  Each CTA owns 64 rows
 // of one (b, h) state, bulk-copied into shared memory the moment the CTA
 // starts, so that the state
-// stream overlaps the path-dependent gathers, which take two rounds: the path
+// stream overlaps the path-dependent gathers, which take two steps: the path
 // and its length together, then (with indices range-checked) the parent-link
 // check, log alpha and the k and U rows of the path all at once.  Thread
 // (r8, c4) keeps an 8x4 register tile (rows r8*8.., columns c4*4..); k and U
@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kRowsPerCta = 64;  // each CTA owns half of a (b, h) state's rows
-constexpr int kChunk = 32;   // path entries staged per round
+constexpr int kChunk = 32;   // path entries staged per pass
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on the S0 copy wait
 
 // dynamic shared memory: S0 rows (kRowsPerCta x dv fp32) | k rows [kChunk][kRowsPerCta] |
@@ -113,7 +113,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     sm100::bulk_load(sS0, S0 + sbase + (size_t)row0 * dv, bytes, &sBar);
   }
 
-  // ---- round 1: path length and entries (range-checked); the first kThreads
+  // ---- gather 1: path length and entries (range-checked); the first kThreads
   //      entries are loaded together with the length ------------------------------
   const int L = path_len[b];
   int pj = -1;
@@ -132,7 +132,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   }
   bad = __syncthreads_or(bad);
 
-  // ---- round 2: chain check, log alpha, and the first chunk of k / u rows,
+  // ---- gather 2: chain check, log alpha, and the first chunk of k / u rows,
   //      all issued together (indices are in range from here on) ----------------
   // a root-to-node path is strictly increasing in a topological order; with the
   // tree given it must also follow the parent links
