@@ -180,3 +180,61 @@ def test_invalid_tree_among_many_units(kernel):
                                  w.parent[ok], w.S0[ok])
     assert H.rel_err(on[ok], ref_o) <= H.TOL_O[W.BF16]
     assert H.rel_err(U.cpu().numpy()[ok], ref_U) <= H.TOL_U
+
+
+def test_linearity_on_gpu(kernel):
+    """Invariant I5 on the GPU path, without the oracle: o and U are linear in (V, S0)
+    jointly, so scaling both by 2 (exact in binary floating point) scales o and U by 2."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    w = W.make_custom(seed=12, B=3, N=100, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="mixed", max_depth=24)
+    x = H.to_device(w)
+    o1, U1 = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"])
+    o2, U2 = gt.verify(x["q"], x["k"], 2 * x["v"], x["log_alpha"], x["beta"], x["parent"],
+                       2 * x["S0"])
+    torch.cuda.synchronize()
+    assert H.rel_err(o2.float().cpu().numpy(), 2 * o1.float().cpu().numpy()) <= 1e-2
+    assert H.rel_err(U2.cpu().numpy(), 2 * U1.cpu().numpy()) <= 1e-6
+
+
+def test_graft_on_gpu(kernel):
+    """Invariant I4 on the GPU path, without the oracle: committing an accepted path
+    and verifying the next tree from S1 gives that tree's outputs of verifying, from
+    S0, the path as a chain with the next tree grafted below its last node."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    A = W.make_custom(seed=13, B=2, N=40, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="chain", max_depth=40)  # accepted paths of 24 and 23 nodes
+    T = W.make_custom(seed=14, B=2, N=50, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="mixed", max_depth=10)
+    L = int(A.path_len.min())
+    A.path_len[:] = L
+    xa, xt = H.to_device(A), H.to_device(T)
+    _, Ua = gt.verify(xa["q"], xa["k"], xa["v"], xa["log_alpha"], xa["beta"], xa["parent"],
+                      xa["S0"])
+    S1 = gt.commit(xa["path"], xa["path_len"], Ua, xa["k"], xa["log_alpha"], xa["S0"],
+                   parent=xa["parent"])
+    o_t, U_t = gt.verify(xt["q"], xt["k"], xt["v"], xt["log_alpha"], xt["beta"], xt["parent"],
+                         S1)
+    # the grafted tree: the path's L nodes as a chain, then T's nodes below it
+    B, Ng = A.B, L + T.N
+    par = np.empty((B, Ng), np.int32)
+    par[:, :L] = np.arange(-1, L - 1)
+    par[:, L:] = np.where(T.parent >= 0, T.parent + L, L - 1)
+    rows = [np.concatenate([A.path[b, :L], A.N + np.arange(T.N)]) for b in range(B)]
+
+    def cat(name):
+        a, t = getattr(A, name), getattr(T, name)
+        both = np.concatenate([a, t], axis=1)
+        return np.stack([both[b][rows[b]] for b in range(B)])
+
+    G = W.Workload(name="graft", B=B, N=Ng, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                   q=cat("q"), k=cat("k"), v=cat("v"), log_alpha=cat("log_alpha"),
+                   beta=cat("beta"), parent=par, S0=A.S0, path=A.path, path_len=A.path_len)
+    xg = H.to_device(G)
+    o_g, U_g = gt.verify(xg["q"], xg["k"], xg["v"], xg["log_alpha"], xg["beta"], xg["parent"],
+                         xg["S0"])
+    torch.cuda.synchronize()
+    assert H.rel_err(o_t.float().cpu().numpy(), o_g[:, L:].float().cpu().numpy()) <= 1e-2
+    assert H.rel_err(U_t.cpu().numpy(), U_g[:, :, L:].cpu().numpy()) <= 1e-4
