@@ -7,8 +7,12 @@
 //    full fp32 relative accuracy even when |g| grows to hundreds (strong
 //    decay over deep chains).  A plain fp32 prefix sum would lose ~1e-4 of
 //    relative accuracy there.
-//  * exp is always taken of (g_t - g_s) with s on t's path, an argument <= 0
-//    for log alpha <= 0, never as exp(g_t) * exp(-g_s) (which overflows).
+//  * A decay weight exp(g_t - g_s), s on t's path, has an argument <= 0 for
+//    log alpha <= 0.  It is taken from the double-float difference, except in
+//    the tensor-core kernel while every |g_t| of the tree is at most 40: there
+//    it is the product exp(g_t) * exp(-g_s) of two per-node factors, both (and
+//    the product) normal fp32 numbers within that bound.  Past the bound the
+//    product could overflow, so the difference form is used.
 #pragma once
 
 #include <cuda_bf16.h>

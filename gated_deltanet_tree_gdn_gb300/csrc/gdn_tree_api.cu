@@ -197,6 +197,14 @@ int gdn_tree_commit_verify(const int32_t* prev_path, const int32_t* prev_path_le
   const char* a0 = reinterpret_cast<const char*>(S_prev);
   const char* a1 = reinterpret_cast<const char*>(S1);
   if (a0 != a1 && a0 < a1 + sbytes && a1 < a0 + sbytes) return GDN_TREE_EINVAL;
+  // U may be prev_U itself only when both trees have the same node count: then
+  // each (b, h) slice sits at the same place in both and is read before it is
+  // written.  Any other overlap would let one unit's U rows land on another
+  // unit's previous rows before those are read.
+  const size_t ubytes = (size_t)dims.B * dims.Hv * dims.N * dims.dv * sizeof(float);
+  const size_t pubytes = (size_t)dims.B * dims.Hv * prev_N * dims.dv * sizeof(float);
+  if (!(U == prev_U && prev_N == dims.N) && any_overlap(U, ubytes, prev_U, pubytes))
+    return GDN_TREE_EINVAL;
   gdn::CommitVerifyArgs a{prev_path, prev_path_len, prev_parent, prev_U, prev_k, prev_log_alpha,
                           prev_N, Lmax, S_prev, S1, commit_status,
                           gdn::VerifyArgs{q, k, v, log_alpha, beta, parent, S1, o, U, dims,

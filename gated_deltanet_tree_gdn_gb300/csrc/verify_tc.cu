@@ -71,7 +71,7 @@ constexpr float kProductDecayLimit = 40.f;
 // per-unit phase timestamps for a profiling build (never in the product build):
 // SM clock counts kept in shared memory during the unit, dumped with the unit's
 // global-timer span (slots 16, 17) once it is over
-constexpr int kMarks = 18;
+constexpr int kMarks = 26;
 __device__ unsigned long long g_tc_phase[4096][kMarks];
 #define TC_MARK_BY(thread, i)                      \
   do {                                             \
@@ -80,9 +80,9 @@ __device__ unsigned long long g_tc_phase[4096][kMarks];
 #define TC_DUMP()                                                           \
   do {                                                                      \
     if (threadIdx.x == 0 && unit < 4096) {                                  \
-      for (int i_ = 0; i_ < 16; ++i_) g_tc_phase[unit][i_] = S.marks[i_];   \
-      g_tc_phase[unit][16] = S.gt0;                                         \
-      g_tc_phase[unit][17] = globaltimer_ns();                              \
+      for (int i_ = 0; i_ < 24; ++i_) g_tc_phase[unit][i_] = S.marks[i_];   \
+      g_tc_phase[unit][24] = S.gt0;                                         \
+      g_tc_phase[unit][25] = globaltimer_ns();                              \
     }                                                                       \
   } while (0)
 #define TC_START()                                  \
@@ -123,7 +123,11 @@ constexpr uint32_t OFF_U = 4 * kOpBytes;
 constexpr uint32_t OFF_V = OFF_U;
 constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
+#ifdef GDN_TC_PROFILE
+constexpr uint32_t kSmallBytes = 16384 + 512;  // room for the phase stamps
+#else
 constexpr uint32_t kSmallBytes = 16384;
+#endif
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
@@ -169,7 +173,7 @@ struct Small {
   int cL;
   int cbad;
 #ifdef GDN_TC_PROFILE
-  unsigned long long marks[16];
+  unsigned long long marks[24];
   unsigned long long gt0;
 #endif
 };
@@ -896,6 +900,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (warp > 4)
           commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 160, warp, lane,
                           next < n_units ? next / Hv : -1);
+        TC_MARK_BY(160, 16);
       }
       if (tid == kIssuer) {
         // the next unit's K, Q and state head for L2 now, so that their copies (issued
@@ -922,6 +927,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
           umma_commit(&S.bar_g);
           ++S.n_g;
+          TC_MARK_BY(kIssuer, 17);
         }
       }
     }
@@ -1172,6 +1178,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               make_uint2(pack2f(py1.x, py1.y), pack2f(py1.z, py1.w));
         }
       }
+      TC_MARK_BY(0, 18);
+      TC_MARK_BY(480, 19);
       if (timed_out) S.err = 4;
       if constexpr (kFused) {
         if (warp > 4 && next < n_units) {

@@ -146,8 +146,9 @@ int gdn_tree_commit(const int32_t *path, const int32_t *path_len,
  *                   and log_alpha [B, prev_N, Hv]
  *   S_prev -> S1    [B, Hv, dk, dv] fp32; S1 may alias S_prev exactly
  *   q .. parent     the next tree, shapes as for gdn_tree_verify (dims.N nodes)
- *   o, U            its outputs; U may alias prev_U exactly (each (b, h) slice
- *                   is read before it is written)
+ *   o, U            its outputs; U may be prev_U itself when prev_N == dims.N
+ *                   (each (b, h) slice is then read before it is written); any
+ *                   other overlap of U and prev_U returns GDN_TREE_EINVAL
  *   commit_status   [B] or NULL: as gdn_tree_commit's dev_status
  *   verify_status   [B] or NULL: as gdn_tree_verify's dev_status (the fused
  *                   path also sets GDN_TREE_STATUS_BAD_PATH when the commit of

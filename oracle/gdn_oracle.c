@@ -11,9 +11,10 @@
  *
  *   GDN recurrence (section 3, "Sfida"):
  *       S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
- *   with S in R^{dk x dv}.  In a topologically ordered draft tree (section 3,
- *   "L'albero e' ordinato topologicamente") S_{t-1} is the state of t's
- *   parent, or the committed state S0 when t hangs off it (parent = -1).
+ *   with S in R^{dk x dv}.  The draft tree is in topological order (section 3,
+ *   "Soluzione": every node comes after its ancestors, i.e. parent[i] < i);
+ *   S_{t-1} is the state of t's parent, or the committed state S0 when t hangs
+ *   off it (parent = -1).
  *   The verified output of node t is o_t = S_t^T q_t: the result of running
  *   the recurrence along t's own root-to-node path, which is exactly the
  *   "single-branch recurrent" verification the page compares against

@@ -107,3 +107,25 @@ def test_empty_calls_are_noops(lib):
     assert _verify(lib, _dims(B=0), ptr=0) == gt.OK
     assert _verify(lib, _dims(N=0), ptr=0) == gt.OK
     assert _commit(lib, _dims(B=0), ptr=0) == gt.OK
+
+
+def _commit_verify(lib, dims, prev_N, U, prev_U):
+    """gdn_tree_commit_verify with distinct, aligned placeholder pointers except
+    for U and prev_U (no call here gets past the host checks)."""
+    P = [ctypes.c_void_p((1 << 36) + (i << 28)) for i in range(16)]
+    return lib.gdn_tree_commit_verify(
+        P[0], P[1], None, ctypes.c_void_p(prev_U), P[2], P[3], prev_N, 4, P[4], P[5],
+        P[6], P[7], P[8], P[9], P[10], P[11], P[12], ctypes.c_void_p(U), dims, None, None,
+        None)
+
+
+def test_commit_verify_refuses_U_overlapping_prev_U(lib):
+    d = _dims(N=16)
+    base = 1 << 44
+    unit_bytes = d.Hv * 16 * d.dv * 4
+    # the same buffer but trees of different sizes: units would overwrite each
+    # other's previous rows before reading them
+    assert _commit_verify(lib, d, 12, base, base) == gt.EINVAL
+    # a partial overlap
+    assert _commit_verify(lib, d, 16, base + unit_bytes, base) == gt.EINVAL
+    assert _commit_verify(lib, d, 16, base, base + 256) == gt.EINVAL
