@@ -52,6 +52,53 @@ def test_two_rank_aggregation_over_gloo():
     assert out[0][1] == pytest.approx(2 * 32 * 128 / 3e-3)
 
 
+def _small(cfg, seed):
+    return W.make_custom(seed=seed, B=2, N=12, Hqk=1, Hv=2, dk=16, dv=16, dtype=W.F32,
+                         tree="mixed")
+
+
+def _shard_rank(rank, world, port, out):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import oracle
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = bench.rank_workload(3, rank, make=_small)
+    o, U = oracle.verify_workload(w, threads=1)
+    S1 = oracle.commit_workload(w, threads=1)
+    got = {k: bench.gather_sequences(torch.from_numpy(np.ascontiguousarray(a)), dist, world)
+           for k, a in (("o", o), ("U", U), ("S1", S1))}
+    out[rank] = {k: v.numpy() for k, v in got.items()}
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_batches_reassemble_to_the_job():
+    """Each rank verifies its own seeded batch; gathered in rank order, the
+    per-sequence results equal the job computed in one process over the
+    concatenated batches (rank r's sequences at index r * B)."""
+    import numpy as np
+    import oracle
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    port = 29700 + os.getpid() % 1000
+    ps = [ctx.Process(target=_shard_rank, args=(r, 2, port, out)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(120)
+        assert p.exitcode == 0
+    ws = [bench.rank_workload(3, r, make=_small) for r in range(2)]
+    assert not np.array_equal(ws[0].q, ws[1].q)  # independent batches
+    for r in range(2):
+        o, U = oracle.verify_workload(ws[r], threads=1)
+        S1 = oracle.commit_workload(ws[r], threads=1)
+        for k, a in (("o", o), ("U", U), ("S1", S1)):
+            for rank in range(2):
+                np.testing.assert_array_equal(out[rank][k][r * 2:(r + 1) * 2], a)
+
+
 def test_reference_arm_prints_one_json_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
@@ -62,3 +109,7 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "nodes/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the whole layer is timed every step, with the same workload keys as our arm
+    assert "whole layer" in d["cpu_baseline"]["sample"]
+    w = W.make_config(3)
+    assert d["config"] == bench.workload_config(w, 1)

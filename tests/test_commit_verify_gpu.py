@@ -111,3 +111,49 @@ def test_commit_verify_empty_and_invalid_paths():
                            prev.v[[0, 2]], prev.log_alpha[[0, 2]], prev.beta[[0, 2]],
                            prev.S0[[0, 2]])
     assert H.rel_err(g["S1"][[0, 2]], S1_ref) <= H.TOL_S1
+
+
+def test_bench_step_two_iterations_match_oracle():
+    """Exactly the benchmark's timed step: the serving workload (32 sequences x 32
+    v-heads, 128-node trees) on the fixed layout, gdn_tree_commit_verify over two
+    consecutive decoding iterations with ping-pong state and U buffers, each
+    iteration committing the accepted path of the tree verified before it and
+    verifying the next tree from the committed state.  Checked against the
+    oracle's commit (the recurrence along the path) then verification, chained
+    the same way.  U is held to its bound against the oracle run from the state
+    the GPU committed, and against the oracle's own chain with the state's
+    bound carried through (U is linear in the state)."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    w = W.make_config(3)
+    x = H.to_device(w)
+    o = torch.empty((w.B, w.N, w.Hv, w.dv), dtype=torch.bfloat16, device="cuda")
+    Sb = [x["S0"].clone(), torch.empty_like(x["S0"])]
+    Ub = [torch.empty((w.B, w.Hv, w.N, w.dv), dtype=torch.float32, device="cuda")
+          for _ in range(2)]
+    gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], Sb[0], o=o,
+              U=Ub[0])
+    S_ref = w.S0.astype(np.float64)
+    for i in range(2):
+        cur, nxt = i & 1, (i + 1) & 1
+        cs = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+        vs = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+        gt.commit_verify(x["path"], x["path_len"], Ub[cur], x["k"], x["log_alpha"], Sb[cur],
+                         x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"],
+                         S1=Sb[nxt], o=o, U=Ub[nxt], prev_parent=x["parent"],
+                         commit_status=cs, verify_status=vs)
+        torch.cuda.synchronize()
+        assert (cs.cpu().numpy() == 0).all() and (vs.cpu().numpy() == 0).all()
+        S_gpu, U_gpu = Sb[nxt].cpu().numpy(), Ub[nxt].cpu().numpy()
+        o_gpu = o.float().cpu().numpy()
+        S_ref = oracle.commit(w.path, w.path_len, w.k, w.v, w.log_alpha, w.beta, S_ref,
+                              parent=w.parent)
+        o_ref, U_ref = oracle.verify(w.q, w.k, w.v, w.log_alpha, w.beta, w.parent, S_ref)
+        _, U_own = oracle.verify(w.q, w.k, w.v, w.log_alpha, w.beta, w.parent, S_gpu)
+        errs = dict(o=H.rel_err(o_gpu, o_ref), U=H.rel_err(U_gpu, U_own),
+                    S1=H.rel_err(S_gpu, S_ref))
+        H.report(w, errs, tag=f"bench-step iteration {i}")
+        assert errs["S1"] <= H.TOL_S1, errs
+        assert errs["o"] <= H.TOL_O[W.BF16], errs
+        assert errs["U"] <= H.TOL_U, errs
+        assert H.rel_err(U_gpu, U_ref) <= H.TOL_U + (i + 1) * H.TOL_S1

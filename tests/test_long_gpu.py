@@ -163,20 +163,20 @@ def test_commit_verify_with_a_long_previous_tree(monkeypatch):
                                  S1_ref.astype(np.float32))
     assert H.rel_err(S1.cpu().numpy(), S1_ref) <= H.TOL_S1
     assert H.rel_err(o.float().cpu().numpy(), o_ref) <= H.TOL_O[W.BF16]
-    assert H.rel_err(U.cpu().numpy(), U_ref) <= 1e-3  # the state itself carries 1e-4
+    # U against the oracle run from the state the GPU committed (U is linear in it)
+    _, U_own = oracle.verify(nxt.q, nxt.k, nxt.v, nxt.log_alpha, nxt.beta, nxt.parent,
+                             S1.cpu().numpy())
+    assert H.rel_err(U.cpu().numpy(), U_own) <= H.TOL_U
 
 
 def test_stress_workload_on_the_chunked_kernel(monkeypatch):
     """The stress workload (64 x 32 units of 256-node chains, stars and random trees,
-    log alpha down to -4, a beta = 0.99 sequence) through the chunked kernel, on a
-    sample of units that covers every tree family."""
+    log alpha down to -4, a beta = 0.99 sequence) through the chunked kernel,
+    compared over the whole tensor."""
     monkeypatch.setenv("GDN_TREE_KERNEL", "long")
     w = W.make_config(4)
     gpu = H.run_gpu(w)
     assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
-    rng = np.random.default_rng(44)
-    seqs = sorted(set([0, 1, 2, 3, 4, 5, w.B - 1]) | set(rng.choice(w.B, 6, replace=False)))
-    units = sorted(set(b * w.Hv + int(h) for b in seqs for h in rng.choice(w.Hv, 4, replace=False)))
-    errs = H.compare(w, gpu, H.run_oracle(w, units=units), units=units)
+    errs = H.compare(w, gpu, H.run_oracle(w))
     H.assert_parity(w, errs)
     assert np.isfinite(gpu["o"]).all() and np.isfinite(gpu["U"]).all()

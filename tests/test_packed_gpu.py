@@ -181,9 +181,16 @@ def test_commit_verify_packed_matches_separate_calls(kernel):
     for b, w in enumerate(nxt.ws):
         if w is not None:
             w.S0 = ref_pool[prev.slot[b]][None].astype(np.float32)
-    ref_o, ref_U = nxt.oracle_verify()
+    ref_o, _ = nxt.oracle_verify()
     assert H.rel_err(o_b.float().cpu().numpy(), ref_o) <= H.TOL_O[W.BF16]
-    assert H.rel_err(U_b.cpu().numpy(), ref_U) <= 1e-3  # the state itself carries 1e-4
+    # U against the oracle run from the state the GPU committed (U is linear in
+    # the state, so this separates the verification's error from the commit's)
+    got_pool = pool_b.cpu().numpy()
+    for b, w in enumerate(nxt.ws):
+        if w is not None:
+            w.S0 = got_pool[prev.slot[b]][None]
+    _, own_U = nxt.oracle_verify()
+    assert H.rel_err(U_b.cpu().numpy(), own_U) <= H.TOL_U
 
 
 def test_bad_layout_reported_and_left_unwritten(kernel):
@@ -252,6 +259,13 @@ def test_commit_verify_many_units_of_varying_size(kernel):
     for b, w in enumerate(nxt.ws):
         if w is not None:
             w.S0 = ref_pool[prev.slot[b]][None].astype(np.float32)
-    ref_o, ref_U = nxt.oracle_verify()
+    ref_o, _ = nxt.oracle_verify()
     assert H.rel_err(o_b.float().cpu().numpy(), ref_o) <= H.TOL_O[W.BF16]
-    assert H.rel_err(U_b.cpu().numpy(), ref_U) <= 1e-3  # the state itself carries 1e-4
+    # U against the oracle run from the state the GPU committed (U is linear in
+    # the state, so this separates the verification's error from the commit's)
+    got_pool = pool_b.cpu().numpy()
+    for b, w in enumerate(nxt.ws):
+        if w is not None:
+            w.S0 = got_pool[prev.slot[b]][None]
+    _, own_U = nxt.oracle_verify()
+    assert H.rel_err(U_b.cpu().numpy(), own_U) <= H.TOL_U
