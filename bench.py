@@ -38,6 +38,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "GDN tree-verify nodes/sec per layer on 1 GB300; % of HBM/tensor roofline"
 UNIT = "nodes/s"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context beside the measured peak)
 WORKLOAD_CFG = 3
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "gated_deltanet_tree_gdn_gb300", "csrc", f)
@@ -172,7 +173,22 @@ class ClockSampler:
         out = os.environ.get("GDN_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(out, f"gdn_bench_clocks_gpu{gpu_index}.csv")
 
+    def sample_once(self) -> None:
+        """One synchronous sample appended to the record (taken right before and
+        right after the timed loop, so that a loop shorter than the sampling
+        period still has clock readings)."""
+        try:
+            r = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                "--format=csv,noheader,nounits", "-i", str(self.gpu)],
+                               capture_output=True, text=True, timeout=10)
+        except (OSError, subprocess.TimeoutExpired):
+            return
+        if r.returncode == 0 and r.stdout.strip():
+            self.extra.append(r.stdout.strip())
+
     def __enter__(self):
+        self.extra = []
+        self.sample_once()
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
@@ -191,14 +207,17 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+        self.sample_once()
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return None
+        lines = list(self.extra)
+        if self.proc is not None and os.path.exists(self.path):
+            with open(self.path) as f:
+                lines += f.read().splitlines()
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
+        if True:
+            for line in lines:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) < 9:
                     continue
@@ -232,6 +251,25 @@ def job_throughput(world: int, B: int, N: int, ms_per_step: float) -> float:
     return world * B * N / (ms_per_step * 1e-3)
 
 
+def rank_workload(cfg: int, rank: int, make=None) -> W.Workload:
+    """Rank r's batch: its own seeded draw of the workload (seed 1000 + cfg + r),
+    so that under N ranks the job is the concatenation of N independent batches,
+    sequences of rank r first at index r * B (weak scaling, no data exchange)."""
+    make = make or W.make_config
+    return make(cfg, seed=1000 + cfg + rank)
+
+
+def gather_sequences(x, dist, world: int):
+    """The ranks' per-sequence results (leading axis = sequences) concatenated in
+    rank order, on every rank (identity when not distributed)."""
+    if dist is None or world == 1:
+        return x
+    import torch
+    parts = [torch.empty_like(x) for _ in range(world)]
+    dist.all_gather(parts, x)
+    return torch.cat(parts, dim=0)
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -239,12 +277,16 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def workload_config(w: W.Workload) -> dict:
+def workload_config(w: W.Workload, world: int) -> dict:
+    """The workload a step runs (the same dictionary for both arms)."""
     return {"workload": f"{w.name}: B={w.B} seqs x Hv={w.Hv} v-heads (Hqk={w.Hqk}), "
                         f"dk=dv={w.dk}, {w.dtype} q/k/v, fp32 S0, N={w.N}-node random trees "
                         "(branching 1-4, depth<=24), accepted paths <=24",
             "B": w.B, "N": w.N, "Hqk": w.Hqk, "Hv": w.Hv, "dk": w.dk, "dv": w.dv,
-            "l2": "flushed before every timed step (256 MiB write, outside the events)"}
+            "l2": "flushed before every timed step (256 MiB write, outside the events)",
+            "parallelism": f"dp{world}",
+            "step": "one decoding iteration: commit of the previous accepted path and "
+                    "verification of the next tree"}
 
 
 # ---------------------------------------------------------------------------
@@ -252,49 +294,58 @@ def workload_config(w: W.Workload) -> dict:
 # ---------------------------------------------------------------------------
 
 def run_reference(args, rank: int) -> None:
+    """The oracle as it stands, timed on the host cores: every step verifies the
+    whole layer's trees (all sequences and heads, memoised fp64 recurrence) and
+    commits every accepted path, exactly the work of one step of our arm."""
     if rank != 0:
         return
     import oracle
     oracle.build()
     w = W.make_config(WORKLOAD_CFG)
     cores = cpu_cores()
-    units_all = w.B * w.Hv
-    per_step = w.Hv  # one random sequence (all its v-heads) per step
-    rng = np.random.default_rng(0)
 
     def step():
-        b = int(rng.integers(w.B))
-        sl = slice(b, b + 1)  # the oracle is handed that sequence's rows only
         t0 = time.perf_counter()
-        oracle.verify(w.q[sl], w.k[sl], w.v[sl], w.log_alpha[sl], w.beta[sl], w.parent[sl],
-                      w.S0[sl], mode="memo", threads=cores)
-        oracle.commit(w.path[sl], w.path_len[sl], w.k[sl], w.v[sl], w.log_alpha[sl],
-                      w.beta[sl], w.S0[sl], parent=w.parent[sl], threads=cores)
+        oracle.verify_workload(w, mode="memo", threads=cores)
+        oracle.commit_workload(w, threads=cores)
         return time.perf_counter() - t0
 
     for _ in range(args.warmup):
         step()
     ts = [step() for _ in range(args.steps)]
-    t_unit = sum(ts) / (len(ts) * per_step)        # seconds per (b, h) unit
-    t_layer = t_unit * units_all                    # a whole layer's step
-    value = w.B * w.N / t_layer
+    t_step = sum(ts) / len(ts)
+    value = w.B * w.N / t_step
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * t_layer, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": 1e3 * t_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"each step: one random sequence ({per_step} (sequence, "
-                                       f"head) units of the {units_all}), memoised fp64 "
-                                       "recurrence + commit, scaled to the whole layer"},
+                             "sample": f"each step: the whole layer ({w.B * w.Hv} (sequence, "
+                                       "head) units), memoised fp64 recurrence + commit, "
+                                       f"{cores} threads"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
 
+def first_sequences(w: W.Workload, nb: int) -> W.Workload:
+    """The first nb sequences of a workload (every head, tree and path of each)."""
+    import dataclasses
+    sl = slice(0, nb)
+    return dataclasses.replace(
+        w, name=f"{w.name}[:{nb}]", B=nb, q=w.q[sl], k=w.k[sl], v=w.v[sl],
+        log_alpha=w.log_alpha[sl], beta=w.beta[sl], parent=w.parent[sl], S0=w.S0[sl],
+        path=w.path[sl], path_len=w.path_len[sl])
+
+
 def cpu_baseline(w: W.Workload) -> dict:
-    """The oracle as it stands on all host cores, on the whole workload."""
+    """The oracle as it stands on the host cores.  Headline: the whole workload,
+    memoised fp64 recurrence + commit, all cores.  Beside it: the same on one
+    core (a sample of sequences, scaled per node), and the literal path walk
+    (every node re-runs its whole root-to-node path: the single-branch
+    recurrent verification) on the small workloads and on a sample of this one."""
     import oracle
     oracle.build()
     cores = cpu_cores()
@@ -302,9 +353,31 @@ def cpu_baseline(w: W.Workload) -> dict:
     oracle.verify_workload(w, mode="memo", threads=cores)
     oracle.commit_workload(w, threads=cores)
     dt = time.perf_counter() - t0
-    return {"value": w.B * w.N / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"the whole workload ({w.B * w.Hv} (sequence, head) units), memoised "
-                      f"fp64 recurrence + commit, {dt:.2f} s wall"}
+    out = {"value": w.B * w.N / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"the whole workload ({w.B * w.Hv} (sequence, head) units), memoised "
+                     f"fp64 recurrence + commit, {dt:.2f} s wall"}
+    extra = []
+
+    def timed(ww, mode, threads, label):
+        t = time.perf_counter()
+        oracle.verify_workload(ww, mode=mode, threads=threads)
+        oracle.commit_workload(ww, threads=threads)
+        sec = time.perf_counter() - t
+        extra.append({"workload": label, "mode": mode, "cores": threads, "seconds": sec,
+                      "nodes_per_s": ww.B * ww.N / sec})
+
+    nb = 4  # sequences of the sample (each with all its heads)
+    ws = first_sequences(w, nb)
+    timed(ws, "memo", 1, f"{w.name}, first {nb} sequences")
+    timed(ws, "path", cores, f"{w.name}, first {nb} sequences")
+    for cfg in (0, 1, 2):
+        wc = W.make_config(cfg)
+        if wc.S0 is None:
+            wc.S0 = oracle.warmup_state(wc.warmup["k"], wc.warmup["v"], wc.warmup["log_alpha"],
+                                        wc.warmup["beta"], wc.Hv, wc.dk, wc.dv)
+        timed(wc, "path", cores, wc.name)
+    out["modes"] = extra
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -325,7 +398,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     gt.load()
     dev = torch.device("cuda", local_rank)
 
-    w = W.make_config(WORKLOAD_CFG, seed=1000 + WORKLOAD_CFG + rank)
+    w = rank_workload(WORKLOAD_CFG, rank)
     dt = torch.bfloat16 if w.dtype == W.BF16 else torch.float32
 
     def host(x, dtype=None):
@@ -469,16 +542,38 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # end to end through the public API: every step copies the tree's inputs and
     # the accepted path from pinned host memory (the recurrent state stays
     # resident on the device, as in a decoding loop), runs one decoding
-    # iteration, and reads its result, the tree's outputs o, back into pinned memory.
-    # As a serving loop runs it: step i's inputs copy in on one stream while step
-    # i - 1 computes, and step i - 1's outputs copy out on another (inputs and o
-    # double-buffered; every copy of every step is inside the timed region)
-    h_o = torch.empty(o.shape, dtype=dt).pin_memory()
+    # iteration, and reads its result, the tree's outputs o, back into pinned
+    # memory.  The inputs of a step sit in one packed pinned staging buffer and
+    # cross in ONE host-to-device copy (16-byte aligned sub-buffers, viewed as
+    # the call's tensors on the device); o comes back in one copy.  As a serving
+    # loop runs it: step i's inputs copy in on one stream while step i - 1
+    # computes, and step i - 1's outputs copy out on another (staging and o
+    # double-buffered; every copy of every step is inside the timed region).
     per_step_inputs = [kk for kk in hin if kk != "S0"]
-    h2d = sum(hin[kk].numel() * hin[kk].element_size() for kk in per_step_inputs)
+    offs, pos = {}, 0
+    for kk in per_step_inputs:
+        nbytes = hin[kk].numel() * hin[kk].element_size()
+        offs[kk] = (pos, nbytes)
+        pos += (nbytes + 255) // 256 * 256
+    stage_bytes = pos
+    h_stage = torch.empty(stage_bytes, dtype=torch.uint8).pin_memory()
+    for kk in per_step_inputs:
+        a, nbytes = offs[kk]
+        h_stage[a:a + nbytes].copy_(hin[kk].reshape(-1).view(torch.uint8))
+    d_stage = [torch.empty(stage_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def staged_views(buf):
+        out = {}
+        for kk in per_step_inputs:
+            a, nbytes = offs[kk]
+            out[kk] = buf[a:a + nbytes].view(hin[kk].dtype).view(hin[kk].shape)
+        return out
+
+    xe = [staged_views(d_stage[j]) for j in range(2)]
+    h_o = torch.empty(o.shape, dtype=dt).pin_memory()
+    h2d = stage_bytes
     d2h = h_o.numel() * h_o.element_size()
     Ke = max(3, min(K, 50))
-    xe = [{kk: torch.empty_like(t) for kk, t in x.items()} for _ in range(2)]
     oe = [o, torch.empty_like(o)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
@@ -488,14 +583,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     def e2e_step(i, first):
         j = i & 1
         if not first[j]:
-            s_in.wait_event(ev_comp[j])    # step i - 2 has read these input buffers
+            s_in.wait_event(ev_comp[j])    # step i - 2 has read this staging buffer
             stream.wait_event(ev_out[j])   # and its o has been copied out
         with torch.cuda.stream(s_in):
-            for kk in per_step_inputs:
-                xe[j][kk].copy_(hin[kk], non_blocking=True)
+            d_stage[j].copy_(h_stage, non_blocking=True)
             ev_in[j].record(s_in)
         stream.wait_event(ev_in[j])
-        iteration(i, xe[j], oe[j])
+        xx = dict(xe[j], S0=x["S0"])
+        iteration(i, xx, oe[j])
         ev_comp[j].record(stream)
         s_out.wait_event(ev_comp[j])
         with torch.cuda.stream(s_out):
@@ -524,6 +619,23 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, dist, dev)
 
+    # the link itself: the same staging copy alone, host to device and back
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c2 = torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        d_stage[0].copy_(h_stage, non_blocking=True)
+    c0.record(stream)
+    for _ in range(5):
+        d_stage[0].copy_(h_stage, non_blocking=True)
+    c1.record(stream)
+    for _ in range(5):
+        h_o.copy_(o, non_blocking=True)
+    c2.record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = 5 * stage_bytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    d2h_gbs = 5 * d2h / (c1.elapsed_time(c2) * 1e-3) / 1e9
+
     if rank == 0:
         peaks, peak_kind = measured_peaks()
         vb, cb, ib = verify_bytes(w), commit_bytes(w), iteration_bytes(w)
@@ -541,16 +653,19 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": arithmetic_dtype(kernel),
             "data": "synthetic",
-            "config": dict(workload_config(w), parallelism=f"dp{world}",
-                           step="one decoding iteration: commit of the previous accepted "
-                                "path fused with verification of the next tree"),
+            "config": workload_config(w, world),
             "clocks": clk.summary(),
             "e2e": {"value": job_throughput(world, w.B, w.N, e2e_ms), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "copies_per_step": {"h2d": 1, "d2h": 1},
+                    "link": {"h2d_gbs_copy_alone": h2d_gbs, "d2h_gbs_copy_alone": d2h_gbs,
+                             "h2d_ms_copy_alone": stage_bytes / (h2d_gbs * 1e9) * 1e3}},
             "gpu_launches": K,
             "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm,
                          "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": ib, "peak_source": peak_kind},
+                         "algorithmic_bytes_per_launch": ib, "peak_source": peak_kind,
+                         "peak_nominal": NOMINAL_HBM_GBS,
+                         "frac_nominal": achieved / NOMINAL_HBM_GBS},
             "step": {"iteration_us": 1e3 * it_ms, "iteration_bytes": ib,
                      "roofline_us": 1e6 * t_roof, "roofline_frac": t_roof / (it_ms * 1e-3),
                      "wall_s_timed_loop": wall},

@@ -28,7 +28,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerCta = 64;  // each CTA owns half of a (b, h) state's rows
 constexpr int kChunk = 32;   // path entries staged per pass
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on the S0 copy wait
 
 // dynamic shared memory: S0 rows (kRowsPerCta x dv fp32) | k rows [kChunk][kRowsPerCta] |
 // u rows [kChunk][dv] | path, log alpha, w_j [path capacity] each
@@ -74,7 +73,8 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
               const int32_t* __restrict__ parent, const float* __restrict__ U,
               const T* __restrict__ k, const float* __restrict__ log_alpha,
               const float* S0, float* S1, gdn_tree_dims d, int32_t Lmax,
-              int32_t* dev_status, SeqLayout lay) {
+              int32_t* dev_status, SeqLayout lay, WaitHooks hk) {
+  const uint64_t kWaitLimitNs = hk.limit_ns;  // bound on the S0 copy wait
   // S0 and S1 may alias (in-place commit): the whole state is copied into
   // shared memory before any element of S1 is written.
   extern __shared__ __align__(128) float smem_f[];
@@ -97,7 +97,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   const int N = lay.count(b, Nmax), st = lay.state(b);
   if (N < 0 || st < 0) {
     if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
-      dev_status[b] = GDN_TREE_STATUS_BAD_LAYOUT;
+      atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
     return;
   }
   const size_t row = (size_t)lay.row0(b, Nmax);
@@ -110,7 +110,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
     sm100::mbar_init(&sBar, 1);
     sm100::mbar_fence_init();
     sm100::mbar_arrive_expect_tx(&sBar, bytes);
-    sm100::bulk_load(sS0, S0 + sbase + (size_t)row0 * dv, bytes, &sBar);
+    if (b != hk.withhold_copy_seq) sm100::bulk_load(sS0, S0 + sbase + (size_t)row0 * dv, bytes, &sBar);
   }
 
   // ---- gather 1: path length and entries (range-checked); the first kThreads
@@ -165,8 +165,8 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   };
   if (!bad) stage(0, min(kChunk, L));
   bad = __syncthreads_or(bad);
-  if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
-    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_PATH : GDN_TREE_STATUS_OK;
+  if (bad && h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
+    atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_PATH);
   if (bad) {
     if (tid == 0) sm100::mbar_wait(&sBar, 0, kWaitLimitNs);  // drain the copy
     return;
@@ -277,6 +277,7 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
   const dim3 grid(a.d.Hv, a.d.B, (a.d.dk + kRowsPerCta - 1) / kRowsPerCta);
   const size_t smem = kSmemBytes + (size_t)path_capacity(a.Lmax) * 3 * sizeof(float);
+  const WaitHooks hk = wait_hooks();
   cudaError_t err;
   if (a.d.dtype == GDN_TREE_BF16) {
     err = cudaFuncSetAttribute(commit_kernel<__nv_bfloat16>,
@@ -284,14 +285,14 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     commit_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const __nv_bfloat16*>(a.k),
-        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
+        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay, hk);
   } else {
     err = cudaFuncSetAttribute(commit_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err != cudaSuccess) return err;
     commit_kernel<float><<<grid, kThreads, smem, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const float*>(a.k),
-        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
+        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay, hk);
   }
   return cudaGetLastError();
 }

@@ -5,6 +5,7 @@
 // data (tree and path validity) and report it through dev_status.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -60,9 +61,32 @@ int check_dims(const gdn_tree_dims& d) {
   return GDN_TREE_OK;
 }
 
+// Per-sequence status words start at GDN_TREE_STATUS_OK; the kernels raise
+// them with atomicMax, so that no unit's report can be lost to another's.
+cudaError_t clear_status(int32_t* st, int B, cudaStream_t stream) {
+  return st ? cudaMemsetAsync(st, 0, (size_t)B * sizeof(int32_t), stream) : cudaSuccess;
+}
+
 }  // namespace
 
 namespace gdn {
+
+WaitHooks wait_hooks() {
+  WaitHooks h;
+  if (const char* e = getenv("GDN_TREE_TEST_WAIT_LIMIT_NS")) {
+    const unsigned long long v = strtoull(e, nullptr, 10);
+    if (v > 0 && v < h.limit_ns) h.limit_ns = v;
+  }
+  if (const char* e = getenv("GDN_TREE_TEST_WITHHOLD_NODE")) {
+    int u = -1, n = -1;
+    if (sscanf(e, "%d:%d", &u, &n) == 2) {
+      h.withhold_unit = u;
+      h.withhold_node = n;
+    }
+  }
+  if (const char* e = getenv("GDN_TREE_TEST_WITHHOLD_COPY")) h.withhold_copy_seq = atoi(e);
+  return h;
+}
 
 // GDN_TREE_KERNEL=generic forces the CUDA-core kernels and GDN_TREE_KERNEL=long
 // the chunked one (used by the tests to cover every kernel on the same shapes);
@@ -119,6 +143,8 @@ int gdn_tree_verify(const void* q, const void* k, const void* v, const float* lo
     if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
   if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return GDN_TREE_EINVAL;
   gdn::VerifyArgs a{q, k, v, log_alpha, beta, parent, S0, o, U, dims, dev_status};
+  if (clear_status(dev_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_verify(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
@@ -137,6 +163,8 @@ int gdn_tree_verify_recurrent(const void* q, const void* k, const void* v,
   if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return GDN_TREE_EINVAL;
   if (dims.Hv > 65535) return GDN_TREE_EUNSUPPORTED;  // the grid's y dimension
   gdn::VerifyArgs a{q, k, v, log_alpha, beta, parent, S0, o, U, dims, dev_status};
+  if (clear_status(dev_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_verify_recurrent(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
@@ -163,6 +191,8 @@ int gdn_tree_commit(const int32_t* path, const int32_t* path_len, const int32_t*
   const char* a1 = reinterpret_cast<const char*>(S1);
   if (a0 != a1 && a0 < a1 + bytes && a1 < a0 + bytes) return GDN_TREE_EINVAL;
   gdn::CommitArgs a{path, path_len, parent, U, k, log_alpha, S0, S1, dims, Lmax, dev_status};
+  if (clear_status(dev_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_commit(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
@@ -209,6 +239,9 @@ int gdn_tree_commit_verify(const int32_t* prev_path, const int32_t* prev_path_le
                           prev_N, Lmax, S_prev, S1, commit_status,
                           gdn::VerifyArgs{q, k, v, log_alpha, beta, parent, S1, o, U, dims,
                                           verify_status}};
+  if (clear_status(commit_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      clear_status(verify_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_commit_verify(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
@@ -229,6 +262,8 @@ int gdn_tree_verify_packed(const void* q, const void* k, const void* v, const fl
     if (p == nullptr || !aligned16(p)) return GDN_TREE_EINVAL;
   if (dev_status && !aligned4(dev_status)) return GDN_TREE_EINVAL;
   gdn::VerifyArgs a{q, k, v, log_alpha, beta, parent, state_pool, o, U, dims, dev_status, lay};
+  if (clear_status(dev_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_verify(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
@@ -262,6 +297,8 @@ int gdn_tree_commit_packed(const int32_t* path, const int32_t* path_len, const i
     return GDN_TREE_EINVAL;
   gdn::CommitArgs a{path, path_len, parent, U, k, log_alpha, pool_in, pool_out,
                     dims, Lmax, dev_status, lay};
+  if (clear_status(dev_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_commit(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }
@@ -312,6 +349,9 @@ int gdn_tree_commit_verify_packed(const int32_t* prev_path, const int32_t* prev_
                           gdn::VerifyArgs{q, k, v, log_alpha, beta, parent, pool_out, o, U, dims,
                                           verify_status, lay},
                           prev_lay};
+  if (clear_status(commit_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      clear_status(verify_status, dims.B, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GDN_TREE_ECUDA;
   const cudaError_t err = gdn::launch_commit_verify(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? GDN_TREE_OK : GDN_TREE_ECUDA;
 }

@@ -88,6 +88,23 @@ struct CommitVerifyArgs {
   SeqLayout prev_lay = {};  // the previous tree's rows (state slots: verify.lay's)
 };
 
+// Bound of the on-device waits, and test-only controls that make one run out.
+// Normal calls use the defaults (2 s, nothing withheld); a test sets them
+// through the environment (read at every launch by wait_hooks()):
+//   GDN_TREE_TEST_WAIT_LIMIT_NS=<ns>       the bound of every wait
+//   GDN_TREE_TEST_WITHHOLD_NODE=<unit>:<node>  the tensor-core verification of unit
+//       (b * Hv + h) never arrives on that node's solve barrier, so the waits of
+//       its children and grandchildren run out (thread arrivals only: no copy or
+//       MMA is left in flight)
+//   GDN_TREE_TEST_WITHHOLD_COPY=<b>        the commit CTAs of sequence b expect their
+//       state copy but never issue it, so the wait for it runs out
+struct WaitHooks {
+  uint64_t limit_ns = 2000000000ull;
+  int withhold_unit = -1, withhold_node = -1;
+  int withhold_copy_seq = -1;
+};
+WaitHooks wait_hooks();
+
 // picks the kernel for the shape and dtype
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream);
 

@@ -79,7 +79,7 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
   // this sequence's rows and state
   const int N = lay.count(b, Nmax), st = lay.state(b);
   if (N < 0 || st < 0) {
-    if (h == 0 && tid == 0 && dev_status) dev_status[b] = GDN_TREE_STATUS_BAD_LAYOUT;
+    if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
     return;
   }
   const size_t row = (size_t)lay.row0(b, Nmax);
@@ -94,8 +94,7 @@ verify_generic_kernel(const T* __restrict__ q, const T* __restrict__ k,
     sLa[t] = log_alpha[(row + t) * Hv + h];
   }
   bad = __syncthreads_or(bad);
-  if (h == 0 && tid == 0 && dev_status)
-    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
+  if (bad && h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
   if (bad) return;
 
   tree_prepare(sPar, N, W, sLa, sJump, sAnc, sG);

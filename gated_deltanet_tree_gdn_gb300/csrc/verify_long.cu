@@ -117,7 +117,7 @@ verify_long_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 
   const int N = lay.count(b, Nmax), st = lay.state(b);
   if (N < 0 || st < 0) {
-    if (h == 0 && tid == 0 && dev_status) dev_status[b] = GDN_TREE_STATUS_BAD_LAYOUT;
+    if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
     return;
   }
   const size_t row = (size_t)lay.row0(b, Nmax);
@@ -134,8 +134,7 @@ verify_long_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     bad |= (p < -1 || p >= t);
   }
   bad = __syncthreads_or(bad);
-  if (h == 0 && tid == 0 && dev_status)
-    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
+  if (bad && h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
   if (bad) return;
 
   // ---- pointer jumping: g_t = sum of log alpha over P(t), depth_t = |P(t)| --------

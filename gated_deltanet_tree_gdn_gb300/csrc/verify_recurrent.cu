@@ -56,8 +56,7 @@ verify_recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k,
     has_child |= (p == leaf);
   }
   bad = __syncthreads_or(bad);
-  if (leaf == 0 && h == 0 && tid == 0 && dev_status)
-    dev_status[b] = bad ? GDN_TREE_STATUS_BAD_TREE : GDN_TREE_STATUS_OK;
+  if (bad && leaf == 0 && h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
   if (bad || __syncthreads_or(has_child)) return;
 
   // the branch root -> leaf

@@ -59,7 +59,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kW = kTile / 32;     // ancestor bitset words per node
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kIssuer = 128;  // the one thread that issues every copy and MMA (warp 4, lane 0)
 constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
 // while every |g_t| of a unit is at most this, e^{g_t - g_s} is formed as
@@ -811,7 +810,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  const float* __restrict__ log_alpha, const float* __restrict__ beta,
                  const int32_t* __restrict__ parent, __nv_bfloat16* __restrict__ o,
                  float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
-                 FusedCommit fc) {
+                 FusedCommit fc, WaitHooks hk) {
+  const uint64_t kWaitLimitNs = hk.limit_ns;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -953,12 +953,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int cstat = kFused ? S.cbad : GDN_TREE_STATUS_OK;
     const bool cbad = cstat != GDN_TREE_STATUS_OK;
     if (h == 0 && tid == 0) {
-      if (dev_status)
-        dev_status[b] = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT
+      const int vcode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT
                         : cbad  ? cstat
                         : S.bad ? GDN_TREE_STATUS_BAD_TREE
                                 : GDN_TREE_STATUS_OK;
-      if (kFused && fc.status) fc.status[b] = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT : cstat;
+      if (dev_status && vcode) atomicMax(dev_status + b, vcode);
+      const int ccode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT : cstat;
+      if (kFused && fc.status && ccode) atomicMax(fc.status + b, ccode);
     }
     // an invalid layout, tree (verified as all-roots) or path leaves the unit's
     // outputs unwritten
@@ -1163,7 +1164,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         }
         __syncwarp();
-        if (on && hl == 0) mbar_arrive(&S.node_bar[tn]);
+        if (on && hl == 0 && !(unit == hk.withhold_unit && tn == hk.withhold_node))
+          mbar_arrive(&S.node_bar[tn]);
         const float yd = S.ydiag[tn];
         py0 = fma4(yd, acc0, fma4(yp, up0, py0));
         py1 = fma4(yd, acc1, fma4(yp, up1, py1));
@@ -1201,10 +1203,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   goto release;
 
 fail:
-  // a bounded wait ran out: report it, let in-flight copies and MMAs drain
-  // (again bounded), then free TMEM
-  if (tid == 0 && dev_status && unit < n_units)
-    atomicMax(dev_status + unit / Hv, GDN_TREE_STATUS_TIMEOUT);
+  // a bounded wait ran out: report it for this unit's sequence and for the
+  // sequences of every unit this CTA has not reached (their outputs stay
+  // unwritten), let in-flight copies and MMAs drain (again bounded), then free
+  // TMEM
+  if (tid == 0) {
+    for (int u = unit; u < n_units; u += gridDim.x) {
+      if (dev_status) atomicMax(dev_status + u / Hv, GDN_TREE_STATUS_TIMEOUT);
+      if (kFused && fc.status) atomicMax(fc.status + u / Hv, GDN_TREE_STATUS_TIMEOUT);
+    }
+  }
+  cp_async_wait_all();  // this thread's prefetches into shared memory
   if (tid == kIssuer) {
     if (S.n_kq > 0) {
       mbar_wait(&S.bar_kq, (S.n_kq - 1) & 1, kWaitLimitNs);
@@ -1293,7 +1302,7 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   const int grid = n_units < n_sm ? n_units : n_sm;
   verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
       tmQ, tmK, tmV, a.S0, a.log_alpha, a.beta, a.parent,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, fc);
+      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, fc, wait_hooks());
   return cudaGetLastError();
 }
 

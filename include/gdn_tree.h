@@ -37,7 +37,11 @@
  *  - Shape/pointer problems are reported by the return value BEFORE any
  *    launch.  Problems that depend on device data (an invalid tree or path)
  *    are reported per sequence in `dev_status` (int32[B], device memory,
- *    may be NULL); the outputs of such a sequence are left unwritten.
+ *    may be NULL); the outputs of such a sequence are left unwritten.  The
+ *    call first sets every dev_status[b] to GDN_TREE_STATUS_OK on `stream`
+ *    (a stream-ordered fill, no allocation); each of the sequence's (b, h)
+ *    units then raises it to the largest code it reports, so a report is
+ *    never lost to another unit's.
  *  - The library is thread-safe and holds no global mutable state.
  *
  * Shapes (B sequences, Hqk query/key heads, Hv value heads, Hv % Hqk == 0,
@@ -79,8 +83,12 @@ extern "C" {
 #define GDN_TREE_STATUS_BAD_TREE 1 /* some parent[b][i] outside [-1, i-1]       */
 #define GDN_TREE_STATUS_BAD_PATH 2 /* path_len or a path entry out of range, or
                                       (with parent given) not a root chain     */
-#define GDN_TREE_STATUS_TIMEOUT 3  /* a bounded on-device wait (TMA or tensor-core
-                                      completion) ran out; outputs incomplete   */
+#define GDN_TREE_STATUS_TIMEOUT 3  /* a bounded on-device wait (a copy, a tensor-core
+                                      completion or a solve barrier; 2 s) ran
+                                      out: the sequence's outputs, and those of
+                                      the sequences the same CTA had not yet
+                                      reached (which report it too), are
+                                      incomplete; the context stays usable     */
 #define GDN_TREE_STATUS_BAD_LAYOUT 4 /* packed layout: the sequence's row range or
                                         state slot is out of range             */
 
@@ -101,7 +109,8 @@ typedef struct {
  * from S0[b, h]; U[b, h, t, :] is the node's write vector u_t (see above).
  * Reads q, k, v, log_alpha, beta, parent, S0; writes o and U.  S0 is never
  * written (the "rollback-free" property).  dev_status[b] (if non-NULL) is set
- * to GDN_TREE_STATUS_OK or GDN_TREE_STATUS_BAD_TREE for every b.
+ * to GDN_TREE_STATUS_OK or GDN_TREE_STATUS_BAD_TREE for every b (or
+ * GDN_TREE_STATUS_BAD_LAYOUT / GDN_TREE_STATUS_TIMEOUT, see above).
  */
 int gdn_tree_verify(const void *q, const void *k, const void *v,
                     const float *log_alpha, const float *beta,
