@@ -12,29 +12,28 @@
 // same in one launch, laid out for Blackwell:
 //
 //   a persistent grid, one CTA (512 threads, 512 TMEM columns) per SM, walks the
-//   (sequence b, v-head h) units; the next unit's operands are already being
-//   loaded while the current unit finishes.  Per unit:
-//   1. TMA (128-byte swizzle) brings K and Q of the q/k head and v of the unit
-//      (issued as soon as the previous unit's solve is over); each thread loads an
-//      8 x 4 tile of the fp32 state into registers and writes it as S0 = hi + lo,
-//      two bf16 tiles laid out MN-major for the MMA's B operand, so K S0 keeps fp32
-//      accuracy (K is exact in bf16).
-//      (Fused with the delayed commitment, the tile is first committed in registers
-//      and stored as S1.)  No thread waits on its own global loads near shared-memory
-//      work: the state tile is its only per-thread load.
+//   (sequence b, v-head h) units; the next unit's K, Q and state are already
+//   being copied while the current unit finishes.  Per unit:
+//   1. TMA brings K and Q of the q/k head (128-byte swizzle) and the fp32 state
+//      tile (four 32-column boxes).  Fused with the delayed commitment of the
+//      previous tree's accepted path, K_P^T diag(w) U_P is one tcgen05 MMA
+//      (both operands MN-major: the path's k rows as they are, exact in bf16,
+//      and w U split hi + lo), so that S1 = gamma S0 + that is formed row by
+//      row (thread = state row) and leaves by TMA store.  The same thread
+//      writes the row as S0 = hi + lo, the bf16 operand of the next MMAs.
 //   2. tcgen05.mma, accumulators in TMEM:  G_kk = K K^T, G_qk = Q K^T,
 //      KS = K S0_hi + K S0_lo, QS = Q S0_hi.
 //   3. TMEM -> registers (thread = tree node): the X and Y entries of the node's
-//      ancestors (masked, decay-weighted, fp32), R = beta (V - gamma KS) and the
-//      output seed gamma QS go to shared memory.
-//   4. forward substitution as a dataflow over the tree, a warp per node and a
-//      lane per 4 value columns: u_t = r_t - sum_a X[t,a] u_a, and in the same
-//      walk over t's path o_t = gamma_t (Q S0)_t + sum_s Y[t,s] u_s, both fp32;
-//      u_t and o_t are stored straight from the solve.
+//      ancestors (masked, decay-weighted, fp32), R = beta (V - gamma KS) and
+//      the output seed gamma QS go to shared memory.
+//   4. forward substitution as a dataflow over the tree, a half-warp per node
+//      and 8 value columns a lane: u_t = r_t - sum_a X[t,a] u_a and, in the
+//      same walk over t's path, o_t = gamma_t (Q S0)_t + sum_s Y[t,s] u_s, both
+//      fp32; u_t and o_t are stored straight from the solve.
 //
-// Precision: K S0, the solve and Y U are fp32-accurate (U feeds the commit's
-// 1e-4 bound); Q S0 uses S0_hi only, ample for the bf16 output.  Waits are
-// bounded; a timeout reports a device status.
+// Precision: K S0, the commit, the solve and Y U are fp32-accurate (U feeds the
+// commit's 1e-4 bound); Q S0 uses S0_hi only, ample for the bf16 output.  Waits
+// are bounded; a timeout reports a device status.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -58,9 +57,13 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kW = kTile / 32;     // ancestor bitset words per node
 constexpr uint32_t kTmemCols = 512;
+// TMEM columns: the Gram matrices, then K S0 (its columns first hold the fused
+// commit's rank-L update), Q S0
 constexpr uint32_t kColGkk = 0, kColGqk = 128, kColKS = 256, kColQS = 384;
+constexpr uint32_t kColCommit = 256;
 constexpr int kIssuer = 128;  // the one thread that issues every copy and MMA (warp 4, lane 0)
-constexpr int kCommitChunk = 32;  // fused commit: path entries staged per round
+constexpr int kCommitChunk = 32;  // fused commit: path entries staged per MMA round
+constexpr int kStagers = kThreads - 160;  // warps 5-15
 // while every |g_t| of a unit is at most this, e^{g_t - g_s} is formed as
 // e^{g_t} e^{-g_s} (both factors, and their product, stay normal fp32 numbers);
 // beyond it, from the double-float difference
@@ -69,7 +72,7 @@ constexpr float kProductDecayLimit = 40.f;
 #ifdef GDN_TC_PROFILE
 // per-unit phase timestamps for a profiling build (never in the product build):
 // SM clock counts kept in shared memory during the unit, dumped with the unit's
-// global-timer span (slots 16, 17) once it is over
+// global-timer span (slots 24, 25) once it is over
 constexpr int kMarks = 26;
 __device__ unsigned long long g_tc_phase[4096][kMarks];
 #define TC_MARK_BY(thread, i)                      \
@@ -105,22 +108,27 @@ __device__ unsigned long long g_tc_phase[4096][kMarks];
 // change roles within a unit
 constexpr uint32_t kTileBytes = 128 * 128;            // one 64-wide K block: 128 rows x 128 B
 constexpr uint32_t kOpBytes = 2 * kTileBytes;         // a 128 x 128 bf16 operand (2 K blocks)
-// region 1: K, Q (TMA) until the MMAs that read them end; then X, Y
+// region 1: K, Q (TMA) until the MMAs that read them end; then X, Y of each
+// node's ancestors (packed strictly-lower triangle, float2)
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = 1 * kOpBytes;
 constexpr uint32_t OFF_XY = 0;
-// region 2: the fused commit's staged path rows; S0^T hi, lo until the K S0 / Q S0
-// MMAs end; then the output rows (seeded with gamma Q S0, finished by the solve)
-constexpr uint32_t OFF_CK = 2 * kOpBytes;
-constexpr uint32_t OFF_CU = 2 * kOpBytes + kCommitChunk * kD * 4;
-constexpr uint32_t OFF_CKRAW = 2 * kOpBytes + 2 * kCommitChunk * kD * 4;  // k rows as bf16
-constexpr uint32_t OFF_S0H = 2 * kOpBytes;
-constexpr uint32_t OFF_S0L = 3 * kOpBytes;
-constexpr uint32_t OFF_P = 2 * kOpBytes;
-// region 3: v (TMA, 128-byte swizzle, first 32 KB) until it is read; then R / U
-constexpr uint32_t OFF_U = 4 * kOpBytes;
-constexpr uint32_t OFF_V = OFF_U;
-constexpr uint32_t OFF_PATH = OFF_U + kTile * kD * 4;   // uint8 [node][depth - 1] -> path node
+// region 2: fused, the commit's operand tiles (k rows; w U hi, lo: MN-major);
+// then S0 hi, lo (MN-major) until the K S0 / Q S0 MMAs end; then the output
+// rows (fp32, seeded with gamma Q S0, finished by the solve)
+constexpr uint32_t OFF_R2 = 2 * kOpBytes;
+constexpr uint32_t kCommitTile = kCommitChunk * kD * 2;  // 32 path rows of bf16
+constexpr uint32_t OFF_CA = OFF_R2;
+constexpr uint32_t OFF_CBH = OFF_R2 + kCommitTile;
+constexpr uint32_t OFF_CBL = OFF_R2 + 2 * kCommitTile;
+constexpr uint32_t OFF_S0H = OFF_R2;
+constexpr uint32_t OFF_S0L = OFF_R2 + kOpBytes;
+constexpr uint32_t OFF_P = OFF_R2;
+// region 3: the fp32 state (TMA: four boxes of 32 columns x 128 rows), S1 in
+// place until its TMA store has read it; then R / U (fp32 rows, same layout)
+constexpr uint32_t OFF_R3 = 4 * kOpBytes;
+constexpr uint32_t kBoxBytes = 32 * 4 * 128;  // 16 KB
+constexpr uint32_t OFF_PATH = OFF_R3 + kTile * kD * 4;  // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
 #ifdef GDN_TC_PROFILE
 constexpr uint32_t kSmallBytes = 16384 + 512;  // room for the phase stamps
@@ -130,8 +138,8 @@ constexpr uint32_t kSmallBytes = 16384;
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
 static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
-static_assert(2 * kCommitChunk * kD * 4 <= 2 * kOpBytes, "commit staging must fit in region 2");
-static_assert(OFF_U % 1024 == 0 && OFF_SMALL % 16 == 0, "alignment");
+static_assert(3 * kCommitTile <= 2 * kOpBytes, "commit tiles must fit in region 2");
+static_assert(OFF_R3 % 1024 == 0 && OFF_SMALL % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Small {
@@ -156,12 +164,16 @@ struct Small {
   int pre_parent[kTile];
   float pre_beta[kTile];
   float pre_la[kTile];
-  uint64_t bar_kq, bar_v, bar_g, bar_ks;
+  // K, Q landed; Gram done; K S0 / Q S0 done; state landed; commit rows staged;
+  // commit MMA done
+  uint64_t bar_kq, bar_g, bar_ks, bar_s, bar_stage, bar_c;
   uint32_t tmem_base;
   int err;
   int bad;     // the tree failed validation
   int wide_g;  // some |g_t| > kProductDecayLimit
-  int n_kq, n_g, n_ks;  // phases issued on bar_kq (and bar_v), bar_g, bar_ks
+  // phases issued on bar_kq, bar_g, bar_ks, bar_s, bar_c (for the drain)
+  int n_kq, n_g, n_ks, n_s, n_c;
+  int s1_pending;  // a TMA store of S1 is in flight
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
   int pre_path[kMaxN];  // the next unit's accepted path and its length, prefetched
@@ -189,10 +201,14 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int k8) {
   return (uint32_t)(kb * kTileBytes + row * 128 + ((j ^ (row & 7)) << 4));
 }
 
-// fp32 128 x 128 row tiles (R / U, output rows): row t, 4-float chunk c4 (0..31),
-// chunk index xor-swizzled by the row so that row-per-thread float4 accesses
-// are bank-conflict free
-__device__ __forceinline__ int u_index(int t, int c4) { return t * kD + ((c4 ^ (t & 7)) << 2); }
+// fp32 128 x 128 row tiles (the state, R / U) in the layout of four TMA boxes of
+// 32 columns x 128 rows with the 128-byte swizzle: row t, 4-float chunk c4
+// (0..31) sits in box c4 / 8, its 16-byte slot xor-swizzled by the row, so that
+// a row-per-thread float4 access and a half-warp reading one row's 16 chunks are
+// both bank-conflict free
+__device__ __forceinline__ uint32_t u_off(int t, int c4) {
+  return (uint32_t)((c4 >> 3) * kBoxBytes + t * 128 + (((c4 & 7) ^ (t & 7)) << 4));
+}
 
 // packed strictly-lower triangle of X and Y
 __device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
@@ -231,26 +247,41 @@ __device__ __forceinline__ void umma_128x128x128(uint32_t d_tmem, uint32_t a_bas
   }
 }
 
-// The state operand S0 (K = dk rows x N = dv columns, bf16) is stored MN-major:
-// the 16-byte chunk n8 (columns 8 n8 .. 8 n8 + 7) of row k sits in the 1024-byte
-// atom of rows 8 (k / 8) .. and columns 64 (n8 / 8) .., atoms of one row group
-// 1 KB apart along N and row groups 2 KB apart, chunks swizzled by the row.
-constexpr uint32_t kS0Lbo = 1024, kS0Sbo = 2048;
-__device__ __forceinline__ uint32_t s0_chunk(int k, int n8) {
+// An MN-major bf16 operand (K rows x 128 MN columns): the 16-byte chunk n8
+// (columns 8 n8 .. 8 n8 + 7) of row k sits in the 1024-byte atom of rows
+// 8 (k / 8) .. and columns 64 (n8 / 8) .., atoms of one row group 1 KB apart
+// along MN and row groups 2 KB apart, chunks swizzled by the row.  The state
+// operand S0 (K = dk), the output MMA's U (K = tree nodes) and the fused commit's
+// k rows and w U rows (K = path entries) all use it.
+constexpr uint32_t kMnLbo = 1024, kMnSbo = 2048;
+__device__ __forceinline__ uint32_t mn_chunk(int k, int n8) {
   const int r = k & 7;
-  return (uint32_t)((k >> 3) * kS0Sbo + (n8 >> 3) * kS0Lbo + r * 128 + (((n8 & 7) ^ r) << 4));
+  return (uint32_t)((k >> 3) * kMnSbo + (n8 >> 3) * kMnLbo + r * 128 + (((n8 & 7) ^ r) << 4));
 }
 
-// issue the 8 K-steps (K = 128) of D (+)= A S for a 128x128 K-major tile A and
-// the MN-major state tile S (a K-step of 16 rows spans two row groups)
-__device__ __forceinline__ void umma_128x128x128_s0(uint32_t d_tmem, uint32_t a_base,
-                                                    uint32_t s_base, bool accumulate) {
+// issue the 8 K-steps (K = 128) of D (+)= A B for a 128x128 K-major tile A and
+// a 128-row MN-major tile B (a K-step of 16 rows spans two row groups)
+__device__ __forceinline__ void umma_128x128x128_bmn(uint32_t d_tmem, uint32_t a_base,
+                                                     uint32_t b_base, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32_bmn(128, 128);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     const uint32_t a_off = (uint32_t)((s >> 2) * kTileBytes + (s & 3) * 32);
     umma_bf16(d_tmem, desc_sw128_kmajor(a_base + a_off),
-              desc_sw128_mnmajor(s_base + (uint32_t)s * 2 * kS0Sbo, kS0Lbo, kS0Sbo), idesc,
+              desc_sw128_mnmajor(b_base + (uint32_t)s * 2 * kMnSbo, kMnLbo, kMnSbo), idesc,
+              (accumulate || s > 0) ? 1u : 0u);
+  }
+}
+
+// issue the K-steps (16 path entries each) of D (+)= A^T B for MN-major tiles of
+// `ksteps` * 16 rows: A = the path's k rows, B = its w U rows
+__device__ __forceinline__ void umma_commit_rows(uint32_t d_tmem, uint32_t a_base,
+                                                 uint32_t b_base, int ksteps, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32_amn_bmn(128, 128);
+  for (int s = 0; s < ksteps; ++s) {
+    const uint32_t off = (uint32_t)s * 2 * kMnSbo;
+    umma_bf16(d_tmem, desc_sw128_mnmajor(a_base + off, kMnLbo, kMnSbo),
+              desc_sw128_mnmajor(b_base + off, kMnLbo, kMnSbo), idesc,
               (accumulate || s > 0) ? 1u : 0u);
   }
 }
@@ -265,10 +296,6 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-// waits for all but this thread's most recent cp.async group
-__device__ __forceinline__ void cp_async_wait_but_last() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 // 16-byte asynchronous copy global -> shared (L2 only)
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -339,12 +366,10 @@ __device__ __forceinline__ int bar_or(int v) {
   return r;
 }
 
-// K and Q of the unit's q/k head into region 1 (bar_kq), its v rows into region 3
-// (bar_v); issuing thread only
-__device__ __forceinline__ void issue_kqv(Small& S, uint8_t* smem, const CUtensorMap* tmK,
-                                          const CUtensorMap* tmQ, const CUtensorMap* tmV,
-                                          const SeqLayout& lay, int unit, int Hv, int Hqk,
-                                          int Nmax) {
+// K and Q of the unit's q/k head into region 1 (bar_kq); issuing thread only
+__device__ __forceinline__ void issue_kq(Small& S, uint8_t* smem, const CUtensorMap* tmK,
+                                         const CUtensorMap* tmQ, const SeqLayout& lay, int unit,
+                                         int Hv, int Hqk, int Nmax) {
   const int b = unit / Hv, h = unit - b * Hv, hq = h / (Hv / Hqk);
   const UnitGeom g = unit_geom(lay, b, Nmax);
   const int cn = g.c_node, cs = g.c_seq;
@@ -353,10 +378,20 @@ __device__ __forceinline__ void issue_kqv(Small& S, uint8_t* smem, const CUtenso
   tma_load_4d(smem + OFF_K + kTileBytes, tmK, &S.bar_kq, 64, hq, cn, cs);
   tma_load_4d(smem + OFF_Q, tmQ, &S.bar_kq, 0, hq, cn, cs);
   tma_load_4d(smem + OFF_Q + kTileBytes, tmQ, &S.bar_kq, 64, hq, cn, cs);
-  mbar_arrive_expect_tx(&S.bar_v, 2 * kTileBytes);
-  tma_load_4d(smem + OFF_V, tmV, &S.bar_v, 0, h, cn, cs);
-  tma_load_4d(smem + OFF_V + kTileBytes, tmV, &S.bar_v, 64, h, cn, cs);
   ++S.n_kq;
+}
+
+// the unit's fp32 state (four boxes of 32 columns) into region 3 (bar_s);
+// issuing thread only
+__device__ __forceinline__ void issue_state(Small& S, uint8_t* smem, const CUtensorMap* tmS,
+                                            const SeqLayout& lay, int unit, int Hv, int Nmax) {
+  const int b = unit / Hv, h = unit - b * Hv;
+  const UnitGeom g = unit_geom(lay, b, Nmax);
+  const int su = g.st * Hv + h;
+  mbar_arrive_expect_tx(&S.bar_s, 4 * kBoxBytes);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tma_load_3d(smem + OFF_R3 + c * kBoxBytes, tmS, &S.bar_s, 32 * c, 0, su);
+  ++S.n_s;
 }
 
 // Tree group (threads 0..127): takes the unit's prefetched tree and gates,
@@ -391,7 +426,6 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
   // every read of the prefetch slots has completed (their values are used above)
   if (next < end) prefetch_tree(S, parent, beta, log_alpha, lay, next, Nmax, Hv, tid);
   TreeSync()();
-  TC_MARK(13);
   // pointer jumping: after round r, jump[t] is t's 2^r-th ancestor (or -1) and
   // anc[t], g[t] cover the part of t's path below it
   int jmp = tid < N ? S.parent[tid] : -1;
@@ -453,7 +487,6 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
   }
   wide = bar_or<1, 128>(wide);  // (also the barrier before the level scan)
   if (tid == 0) S.wide_g = wide;
-  TC_MARK(14);
   if (warp == 0) {
     // exclusive scans of the level counts 0..kTile+1 and of the solve tasks per
     // level (pairs of nodes, ceil(count / 2)), packed in one int (each <= 128);
@@ -485,7 +518,6 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
     if (lane == 31) S.n_tasks = incl >> 16;
   }
   TreeSync()();
-  TC_MARK(15);
   if (tid < N) {
     // position in the depth order; every even rank within the level opens a task
     // of two nodes (one at an odd-sized level's end)
@@ -497,77 +529,6 @@ __device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_
       S.task_pos[k] = (uint8_t)pos;
       S.task_n[k] = (uint8_t)(pos + 1 < S.level_start[dep + 1] ? 2 : 1);
     }
-  }
-}
-
-// k and U rows of path entries j0 .. j0+nj-1 of the previous tree into the
-// staging area as fp32; items i0, i0 + stride, ... of the calling group
-__device__ __forceinline__ void commit_stage_rows(const FusedCommit& fc, const Small& S,
-                                                  uint8_t* smem, int b, int h, int hq, int Hqk,
-                                                  int Hv, int j0, int nj, int i0, int stride) {
-  const size_t prow0 = (size_t)fc.lay.row0(b, fc.N);
-  const size_t purow0 = fc.lay.urow0(b, h, Hv, fc.N);
-  float* sk = reinterpret_cast<float*>(smem + OFF_CK);  // [kCommitChunk][kD]
-  float* su = reinterpret_cast<float*>(smem + OFF_CU);  // [kCommitChunk][kD]
-  for (int e = i0; e < nj * (kD / 8); e += stride) {
-    const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
-    const uint4 raw = *reinterpret_cast<const uint4*>(
-        fc.k + ((prow0 + S.cpath[j0 + jj]) * Hqk + hq) * kD + c);
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    float* dst = sk + jj * kD + c;
-    const float w = S.cw[j0 + jj];  // weighted as in stage_rows_finish
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      dst[2 * q] = w * __uint_as_float(w4[q] << 16);
-      dst[2 * q + 1] = w * __uint_as_float(w4[q] & 0xffff0000u);
-    }
-  }
-  for (int e = i0; e < nj * (kD / 4); e += stride) {
-    const int jj = e / (kD / 4), c = (e % (kD / 4)) * 4;
-    *reinterpret_cast<float4*>(su + jj * kD + c) = *reinterpret_cast<const float4*>(
-        fc.U + (purow0 + S.cpath[j0 + jj]) * kD + c);
-  }
-}
-
-// The first chunk of path rows, asynchronously: the k rows (bf16, as they are) and
-// the U rows are copied with cp.async (one group); stage_rows_finish, by the same
-// threads, waits for it and widens the k rows to fp32.
-__device__ __forceinline__ void stage_rows_issue(const FusedCommit& fc, const Small& S,
-                                                 uint8_t* smem, int b, int h, int hq, int Hqk,
-                                                 int Hv, int nj, int i0, int stride) {
-  const size_t prow0 = (size_t)fc.lay.row0(b, fc.N);
-  const size_t purow0 = fc.lay.urow0(b, h, Hv, fc.N);
-  uint8_t* kraw = smem + OFF_CKRAW;  // [kCommitChunk][kD] bf16
-  float* su = reinterpret_cast<float*>(smem + OFF_CU);
-  for (int e = i0; e < nj * (kD / 8); e += stride) {
-    const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
-    cp_async16(kraw + (jj * kD + c) * 2, fc.k + ((prow0 + S.cpath[jj]) * Hqk + hq) * kD + c);
-  }
-  for (int e = i0; e < nj * (kD / 4); e += stride) {
-    const int jj = e / (kD / 4), c = (e % (kD / 4)) * 4;
-    cp_async16(su + jj * kD + c, fc.U + (purow0 + S.cpath[jj]) * kD + c);
-  }
-  cp_async_commit();
-}
-
-// widens the staged bf16 k rows to fp32, each scaled by its path weight w_j
-// (the products w_j k are the ones the accumulation would form)
-__device__ __forceinline__ void stage_rows_finish(const Small& S, uint8_t* smem, int nj, int i0,
-                                                  int stride) {
-  const uint8_t* kraw = smem + OFF_CKRAW;
-  float* sk = reinterpret_cast<float*>(smem + OFF_CK);
-  for (int e = i0; e < nj * (kD / 8); e += stride) {
-    const int jj = e / (kD / 8), c = (e % (kD / 8)) * 8;
-    const float w = S.cw[jj];
-    const uint4 raw = *reinterpret_cast<const uint4*>(kraw + (jj * kD + c) * 2);
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    float* dst = sk + jj * kD + c;
-    *reinterpret_cast<float4*>(dst) =
-        make_float4(w * __uint_as_float(w4[0] << 16), w * __uint_as_float(w4[0] & 0xffff0000u),
-                    w * __uint_as_float(w4[1] << 16), w * __uint_as_float(w4[1] & 0xffff0000u));
-    *reinterpret_cast<float4*>(dst + 4) =
-        make_float4(w * __uint_as_float(w4[2] << 16), w * __uint_as_float(w4[2] & 0xffff0000u),
-                    w * __uint_as_float(w4[3] << 16), w * __uint_as_float(w4[3] & 0xffff0000u));
   }
 }
 
@@ -643,16 +604,16 @@ __device__ __forceinline__ void prefetch_path_rows_l2(const FusedCommit& fc, Sma
   }
 }
 
-// Warps 5-15 (ot = tid - 160; warp 4 issues the copies and MMAs meanwhile): checks the previous tree's
+// Fused commit, warps 5-15 (ot = tid - 160): checks the previous tree's
 // accepted path of sequence b (range, chain order, parent links), gathers its
-// log alpha, stages the first chunk of its k / U rows into region 2 and forms
-// the path weights.  Sets S.cbad (0 or the sequence's commit status), S.cL.
-__device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S, uint8_t* smem,
-                                                int b, int h, int hq, int Hqk, int Hv, int ot,
-                                                int warp, int lane, int next_b) {
+// log alpha and forms the path weights.  Sets S.cbad (0 or the sequence's
+// commit status) and S.cL; returns whether the commit has rows to stage.
+__device__ __forceinline__ bool commit_prologue(const FusedCommit& fc, Small& S, int b, int h,
+                                                int Hv, int ot, int warp, int lane, int next_b,
+                                                int& L_out) {
   const int pn = fc.lay.count(b, fc.N);  // the previous tree's node count (< 0: bad rows)
   cp_async_wait_all();  // this unit's path, prefetched during the previous unit
-  NamedSync<2, kThreads - 160>()();
+  NamedSync<2, kStagers>()();
   const int L = S.pre_plen;
   int pj = -1;
   if (ot < fc.Lmax) pj = S.pre_path[ot];
@@ -661,11 +622,7 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
     cbad |= (pj < 0 || pj >= pn);
     S.cpath[ot] = pj;
   }
-  cbad = bar_or<2, kThreads - 160>(cbad);
-  // the entries are in range: the first chunk of k / U rows starts coming while
-  // the chain check and log alpha are fetched (rows of a failed check go unused)
-  const int nj0 = min(kCommitChunk, L);
-  if (!cbad) stage_rows_issue(fc, S, smem, b, h, hq, Hqk, Hv, nj0, ot, kThreads - 160);
+  cbad = bar_or<2, kStagers>(cbad);
   if (!cbad && ot < L) {
     const int prev = ot == 0 ? -1 : S.cpath[ot - 1];
     cbad |= (ot > 0 && pj <= prev);
@@ -674,183 +631,116 @@ __device__ __forceinline__ void commit_prologue(const FusedCommit& fc, Small& S,
     S.cla[ot] = fc.log_alpha[(prow0 + pj) * Hv + h];
   }
   // every read of the prefetch slots is done: the next unit's path starts coming
-  // (its own cp.async group, left in flight by the wait below)
   if (next_b >= 0) prefetch_path(fc, S, next_b, ot);
-  else cp_async_commit();  // an empty group keeps the wait's count right
-  cbad = bar_or<2, kThreads - 160>(cbad);  // (also: every log alpha is in place)
+  cbad = bar_or<2, kStagers>(cbad);  // (also: every log alpha is in place)
   if (ot == 0) {
     S.cbad = !cbad ? GDN_TREE_STATUS_OK
                    : (pn < 0 ? GDN_TREE_STATUS_BAD_LAYOUT : GDN_TREE_STATUS_BAD_PATH);
-    S.cL = L;
+    S.cL = cbad ? 0 : L;
   }
-  if (!cbad) {
-    // the weights while the rows land, then the k rows widened and weighted
-    if (warp == 5) commit_weights(S, L, lane);
-    cp_async_wait_but_last();
-    NamedSync<2, kThreads - 160>()();
-    stage_rows_finish(S, smem, nj0, ot, kThreads - 160);
-  }
+  L_out = cbad ? 0 : L;
+  if (cbad || L == 0) return false;
+  if (warp == 5) commit_weights(S, L, lane);
+  NamedSync<2, kStagers>()();  // the weights are in place
+  return true;
 }
 
-// K_P^T diag(w) U_P for this thread's 8x4 tile of the state (rows r8*8 .., columns
-// c4*4 ..); needs no state, so it runs while the state is still in flight
-__device__ __forceinline__ void commit_accumulate(const FusedCommit& fc, const Small& S,
-                                                  uint8_t* smem, int b, int h, int hq, int Hqk,
-                                                  int Hv, int tid, int r8, int c4,
-                                                  float (&acc)[8][4]) {
-  const int L = S.cL;
-  const float* sk = reinterpret_cast<const float*>(smem + OFF_CK);
-  const float* su = reinterpret_cast<const float*>(smem + OFF_CU);
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int j0 = 0; j0 < L; j0 += kCommitChunk) {
-    const int nj = min(kCommitChunk, L - j0);
-    if (j0 > 0) {  // the first chunk was staged by the operand group
-      __syncthreads();
-      commit_stage_rows(fc, S, smem, b, h, hq, Hqk, Hv, j0, nj, tid, kThreads);
-      __syncthreads();
-    }
-    for (int jj = 0; jj < nj; ++jj) {
-      // the staged k rows already carry their weights w_j
-      const float4 k0 = *reinterpret_cast<const float4*>(sk + jj * kD + r8 * 8);
-      const float4 k1 = *reinterpret_cast<const float4*>(sk + jj * kD + r8 * 8 + 4);
-      const float4 uu = *reinterpret_cast<const float4*>(su + jj * kD + c4 * 4);
-      const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-      const float2 u01 = make_float2(uu.x, uu.y), u23 = make_float2(uu.z, uu.w);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {  // packed fp32x2 FMAs (same rounding as fmaf)
-        const float2 ki = make_float2(kk[i], kk[i]);
-        const float2 lo = __ffma2_rn(ki, u01, make_float2(acc[i][0], acc[i][1]));
-        const float2 hi = __ffma2_rn(ki, u23, make_float2(acc[i][2], acc[i][3]));
-        acc[i][0] = lo.x;
-        acc[i][1] = lo.y;
-        acc[i][2] = hi.x;
-        acc[i][3] = hi.y;
-      }
-    }
+// Fused commit, warps 5-15: path entries j0 .. j0 + nj - 1 as the rows of the
+// commit MMA's MN-major operands: the k rows by cp.async (bf16, as they are,
+// exact) and the U rows scaled by w_j, split hi + lo; rows nj .. up to the next
+// multiple of 16 are zeroed.  Waits for its own copies and makes its writes
+// visible to the tensor cores.
+__device__ __forceinline__ void commit_stage(const FusedCommit& fc, const Small& S, uint8_t* smem,
+                                             int b, int h, int hq, int Hqk, int Hv, int j0,
+                                             int nj, int ot) {
+  const size_t prow0 = (size_t)fc.lay.row0(b, fc.N);
+  const size_t purow0 = fc.lay.urow0(b, h, Hv, fc.N);
+  for (int e = ot; e < nj * 16; e += kStagers) {
+    const int jj = e >> 4, c = e & 15;
+    cp_async16(smem + OFF_CA + mn_chunk(jj, c),
+               fc.k + ((prow0 + S.cpath[j0 + jj]) * Hqk + hq) * kD + 8 * c);
   }
-}
-
-// S1 = gamma S0 + acc on this thread's 8x4 tile of the state, in registers (it is
-// the state the next tree is verified from), stored to fc.S1
-__device__ __forceinline__ void commit_finish(const FusedCommit& fc, const Small& S,
-                                              size_t state_unit, int r8, int c4, float4 (&st)[8],
-                                              const float (&acc)[8][4]) {
-  const float gamma = S.cgamma;
-  float* dst = fc.S1 + state_unit * kD * kD + (r8 * 8) * kD + c4 * 4;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    st[i].x = fmaf(gamma, st[i].x, acc[i][0]);
-    st[i].y = fmaf(gamma, st[i].y, acc[i][1]);
-    st[i].z = fmaf(gamma, st[i].z, acc[i][2]);
-    st[i].w = fmaf(gamma, st[i].w, acc[i][3]);
-    *reinterpret_cast<float4*>(dst + i * kD) = st[i];
+  cp_async_commit();
+  const int npad = ((nj + 15) & ~15) - nj;
+  for (int e = ot; e < npad * 16; e += kStagers) {
+    const int jj = nj + (e >> 4), c = e & 15;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(smem + OFF_CA + mn_chunk(jj, c)) = z;
+    *reinterpret_cast<uint4*>(smem + OFF_CBH + mn_chunk(jj, c)) = z;
+    *reinterpret_cast<uint4*>(smem + OFF_CBL + mn_chunk(jj, c)) = z;
   }
-}
-
-// S0 = hi + lo (bf16, MN-major, 128-byte swizzle: s0_chunk) from every thread's 8x4
-// tile of the state (rows 8 r8 .., columns 4 c4 ..).  The two lanes of a pair (c4
-// even, odd: one 16-byte chunk of columns) swap half their rows, so that each holds
-// whole chunks: rows 8 r8 .. + 3 in the even lane, 8 r8 + 4 .. + 7 in the odd one.
-// The hi half is written first, so that Q S0_hi and K S0_hi run on the tensor cores
-// while the lo half is written; then K S0_lo, and bar_ks tracks all of them.  All
-// threads of the CTA.
-__device__ __forceinline__ void split_state(uint8_t* smem, uint32_t sbase, Small& S, uint32_t tmem,
-                                            int r8, int c4, const float4 (&st)[8], bool issuer,
-                                            bool issue) {
-  const bool odd = c4 & 1;
-  float4 ch[4][2];  // chunk rows: 8 r8 + (odd ? 4 : 0) + i, columns 8 (c4 / 2) .. + 7
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 give = odd ? st[i] : st[4 + i];
-    float4 got;
-    got.x = __shfl_xor_sync(0xffffffffu, give.x, 1);
-    got.y = __shfl_xor_sync(0xffffffffu, give.y, 1);
-    got.z = __shfl_xor_sync(0xffffffffu, give.z, 1);
-    got.w = __shfl_xor_sync(0xffffffffu, give.w, 1);
-    ch[i][0] = odd ? got : st[i];
-    ch[i][1] = odd ? st[4 + i] : got;
+  for (int e = ot; e < nj * 16; e += kStagers) {
+    const int jj = e >> 4, c = e & 15;
+    const float w = S.cw[j0 + jj];
+    const float4* src =
+        reinterpret_cast<const float4*>(fc.U + (purow0 + S.cpath[j0 + jj]) * kD + 8 * c);
+    const float4 u0 = src[0], u1 = src[1];
+    uint32_t hi[4], lo[4];
+    split2(w * u0.x, w * u0.y, hi[0], lo[0]);
+    split2(w * u0.z, w * u0.w, hi[1], lo[1]);
+    split2(w * u1.x, w * u1.y, hi[2], lo[2]);
+    split2(w * u1.z, w * u1.w, hi[3], lo[3]);
+    *reinterpret_cast<uint4*>(smem + OFF_CBH + mn_chunk(jj, c)) =
+        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(smem + OFF_CBL + mn_chunk(jj, c)) =
+        make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
-  const int row0 = 8 * r8 + (odd ? 4 : 0), n8 = c4 >> 1;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t hi[4], lo[4];
-      split2(ch[i][0].x, ch[i][0].y, hi[0], lo[0]);
-      split2(ch[i][0].z, ch[i][0].w, hi[1], lo[1]);
-      split2(ch[i][1].x, ch[i][1].y, hi[2], lo[2]);
-      split2(ch[i][1].z, ch[i][1].w, hi[3], lo[3]);
-      const uint32_t* part = half == 0 ? hi : lo;
-      *reinterpret_cast<uint4*>(smem + (half == 0 ? OFF_S0H : OFF_S0L) + s0_chunk(row0 + i, n8)) =
-          make_uint4(part[0], part[1], part[2], part[3]);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (issuer && issue) {
-      tc_fence_after_sync();
-      if (half == 0) {
-        umma_128x128x128_s0(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
-        umma_128x128x128_s0(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
-      } else {
-        umma_128x128x128_s0(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
-        umma_commit(&S.bar_ks);
-        ++S.n_ks;
-      }
-    }
-  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();
 }
 
 template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const float* S0,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
+                 const __grid_constant__ CUtensorMap tmS1, const float* S0,
                  const float* __restrict__ log_alpha, const float* __restrict__ beta,
-                 const int32_t* __restrict__ parent, __nv_bfloat16* __restrict__ o,
-                 float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
-                 FusedCommit fc, WaitHooks hk) {
+                 const int32_t* __restrict__ parent, const __nv_bfloat16* __restrict__ v,
+                 __nv_bfloat16* __restrict__ o, float* __restrict__ U, gdn_tree_dims d,
+                 int32_t* dev_status, SeqLayout lay, FusedCommit fc, WaitHooks hk) {
   const uint64_t kWaitLimitNs = hk.limit_ns;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   const uint32_t sbase = smem_addr(smem);
   Small& S = *reinterpret_cast<Small*>(smem + OFF_SMALL);
-  float* sU = reinterpret_cast<float*>(smem + OFF_U);
-  float* sP = reinterpret_cast<float*>(smem + OFF_P);
   float2* sXY = reinterpret_cast<float2*>(smem + OFF_XY);
+  uint8_t* sR3 = smem + OFF_R3;
+  uint8_t* sP = smem + OFF_P;
   uint8_t* sPath = smem + OFF_PATH;
 
   const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
   const int n_units = d.B * Hv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // row mapping: thread <-> (tree row t, 32-column quarter cq); warp w may only
-  // touch TMEM lanes 32*(w%4) .. 32*(w%4)+31
+  // row mapping: thread <-> (tree row / state row t, 32-column quarter cq); warp
+  // w may only touch TMEM lanes 32*(w%4) .. 32*(w%4)+31
   const int q4 = warp & 3, cq = warp >> 2;
   const int t = q4 * 32 + lane;
   const int col0 = cq * 32;
   const uint32_t trow_off = (uint32_t)(q4 * 32) << 16;
-  // state mapping: thread <-> 8x4 tile (rows 8 r8 .., columns 4 c4 ..); a warp holds
-  // 4 row blocks x 8 column groups, so its loads and stores are 128-byte rows
-  const int r8 = (warp >> 2) * 4 + (lane >> 3), c4 = (warp & 3) * 8 + (lane & 7);
   int unit = blockIdx.x;
 
   if (tid == kIssuer) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmS);
+    if (kFused) tma_prefetch_desc(&tmS1);
     mbar_init(&S.bar_kq, 1);
-    mbar_init(&S.bar_v, 1);
     mbar_init(&S.bar_g, 1);
     mbar_init(&S.bar_ks, 1);
+    mbar_init(&S.bar_s, 1);
+    mbar_init(&S.bar_stage, 1);
+    mbar_init(&S.bar_c, 1);
     S.err = 0;
-    S.n_kq = 0;
-    S.n_g = 0;
-    S.n_ks = 0;
+    S.n_kq = S.n_g = S.n_ks = S.n_s = S.n_c = 0;
+    S.s1_pending = 0;
     S.cbad = 0;
+    S.cL = 0;
     mbar_fence_init();
-    if (unit < n_units) issue_kqv(S, smem, &tmK, &tmQ, &tmV, lay, unit, Hv, Hqk, Nmax);
+    if (unit < n_units) {
+      issue_kq(S, smem, &tmK, &tmQ, lay, unit, Hv, Hqk, Nmax);
+      issue_state(S, smem, &tmS, lay, unit, Hv, Nmax);
+    }
   }
   if constexpr (kFused) {
     if (warp > 4 && unit < n_units) prefetch_path(fc, S, unit / Hv, tid - 160);
@@ -865,6 +755,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = S.tmem_base;
+  const uint32_t trow = tmem + trow_off;
+  uint32_t stage_ph = 0;  // the issuer's count of bar_stage phases
 
   for (uint32_t it = 0; unit < n_units; unit += gridDim.x, ++it) {
     const uint32_t ph = it & 1u;
@@ -875,61 +767,88 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const UnitGeom geo = unit_geom(lay, b, Nmax);
     const int N = geo.n;
     const bool live = t < N;
-    const size_t state_unit = (size_t)geo.st * Hv + h;
-
-    // this thread's 8x4 tile of the state, into registers (L2 hits: prefetched)
-    float4 st[8];
-    {
-      const float4* src =
-          reinterpret_cast<const float4*>(S0 + state_unit * kD * kD + (r8 * 8) * kD + c4 * 4);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) st[i] = __ldg(src + i * (kD / 4));
-    }
+    const int nc0 = S.n_c;  // commit MMA phases before this unit
 
     // ---- 0. tree group (warps 0-3): the unit's tree.  Operand group (warps 4-15):
     //         the Gram MMAs once K and Q have landed; fused, the previous tree's
-    //         accepted path (warps 5-15)
+    //         accepted path is checked and staged (warps 5-15) and committed on the
+    //         tensor cores (warp 4)
     TC_START();
     TC_MARK(0);
     if (warp < 4) {
       tree_prep(S, sPath, parent, beta, log_alpha, lay, Nmax, next, n_units, N, Hv, tid, lane,
                 warp, unit);
       TC_MARK(8);
-    } else {
+    } else if (warp > 4) {
       if constexpr (kFused) {
-        if (warp > 4)
-          commit_prologue(fc, S, smem, b, h, hq, Hqk, Hv, tid - 160, warp, lane,
-                          next < n_units ? next / Hv : -1);
+        const int ot = tid - 160;
+        int L = 0;
+        const bool rows = commit_prologue(fc, S, b, h, Hv, ot, warp, lane,
+                                          next < n_units ? next / Hv : -1, L);
         TC_MARK_BY(160, 16);
+        const int nch = rows ? (L + kCommitChunk - 1) / kCommitChunk : 0;
+        for (int c = 0; c < nch; ++c) {
+          // the tiles are free once the previous chunk's MMA has read them
+          if (c > 0 && !mbar_wait(&S.bar_c, (uint32_t)(nc0 + c - 1) & 1u, kWaitLimitNs)) S.err = 1;
+          commit_stage(fc, S, smem, b, h, hq, Hqk, Hv, c * kCommitChunk,
+                       min(kCommitChunk, L - c * kCommitChunk), ot);
+          NamedSync<2, kStagers>()();
+          if (ot == 0) mbar_arrive(&S.bar_stage);
+        }
+        if (nch == 0 && ot == 0) mbar_arrive(&S.bar_stage);  // nothing to stage: one phase
       }
-      if (tid == kIssuer) {
-        // the next unit's K, Q and state head for L2 now, so that their copies (issued
-        // when this unit's solve is over) hit L2
-        if (next < n_units) {
-          const int nb = next / Hv, nh = next - nb * Hv, nhq = nh / (Hv / Hqk);
-          const UnitGeom ng = unit_geom(lay, nb, Nmax);
-          tma_prefetch_l2_4d(&tmK, 0, nhq, ng.c_node, ng.c_seq);
-          tma_prefetch_l2_4d(&tmK, 64, nhq, ng.c_node, ng.c_seq);
-          tma_prefetch_l2_4d(&tmQ, 0, nhq, ng.c_node, ng.c_seq);
-          tma_prefetch_l2_4d(&tmQ, 64, nhq, ng.c_node, ng.c_seq);
-          tma_prefetch_l2_4d(&tmV, 0, nh, ng.c_node, ng.c_seq);
-          tma_prefetch_l2_4d(&tmV, 64, nh, ng.c_node, ng.c_seq);
-          const float* ns = S0 + ((size_t)ng.st * Hv + nh) * kD * kD;
+    } else if (tid == kIssuer) {
+      // the next unit's K, Q, v and state head for L2 now, so that their copies
+      // (issued when this unit's solve is over) hit L2
+      if (next < n_units) {
+        const int nb = next / Hv, nh = next - nb * Hv, nhq = nh / (Hv / Hqk);
+        const UnitGeom ng = unit_geom(lay, nb, Nmax);
+        tma_prefetch_l2_4d(&tmK, 0, nhq, ng.c_node, ng.c_seq);
+        tma_prefetch_l2_4d(&tmK, 64, nhq, ng.c_node, ng.c_seq);
+        tma_prefetch_l2_4d(&tmQ, 0, nhq, ng.c_node, ng.c_seq);
+        tma_prefetch_l2_4d(&tmQ, 64, nhq, ng.c_node, ng.c_seq);
+        tma_prefetch_l2_4d(&tmV, 0, nh, ng.c_node, ng.c_seq);
+        tma_prefetch_l2_4d(&tmV, 64, nh, ng.c_node, ng.c_seq);
+        const float* ns = S0 + ((size_t)ng.st * Hv + nh) * kD * kD;
 #pragma unroll
-          for (int r = 0; r < 4; ++r) bulk_prefetch_l2(ns + r * (kD * kD / 4), kD * kD);
-        }
-        if (!mbar_wait(&S.bar_kq, ph, kWaitLimitNs)) {
-          S.err = 1;
-        } else {
-          TC_MARK_BY(kIssuer, 9);
+        for (int r = 0; r < 4; ++r) bulk_prefetch_l2(ns + r * (kD * kD / 4), kD * kD);
+      }
+      if (!mbar_wait(&S.bar_kq, ph, kWaitLimitNs)) {
+        S.err = 1;
+      } else {
+        TC_MARK_BY(kIssuer, 9);
+        tc_fence_after_sync();
+        umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
+        umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
+        umma_commit(&S.bar_g);
+        ++S.n_g;
+        TC_MARK_BY(kIssuer, 17);
+      }
+      if constexpr (kFused) {
+        // one bar_stage phase per staged chunk (one when there is nothing to stage)
+        for (int c = 0;; ++c) {
+          if (!mbar_wait(&S.bar_stage, stage_ph & 1u, kWaitLimitNs)) {
+            S.err = 1;
+            break;
+          }
+          ++stage_ph;
+          const int L = S.cL;
+          if (S.cbad || L == 0) break;
+          const int nj = min(kCommitChunk, L - c * kCommitChunk);
           tc_fence_after_sync();
-          umma_128x128x128(tmem + kColGkk, sbase + OFF_K, sbase + OFF_K, false);
-          umma_128x128x128(tmem + kColGqk, sbase + OFF_Q, sbase + OFF_K, false);
-          umma_commit(&S.bar_g);
-          ++S.n_g;
-          TC_MARK_BY(kIssuer, 17);
+          umma_commit_rows(tmem + kColCommit, sbase + OFF_CA, sbase + OFF_CBH, (nj + 15) >> 4,
+                           c > 0);
+          umma_commit_rows(tmem + kColCommit, sbase + OFF_CA, sbase + OFF_CBL, (nj + 15) >> 4,
+                           true);
+          umma_commit(&S.bar_c);
+          ++S.n_c;
+          if ((c + 1) * kCommitChunk >= L) break;
         }
       }
+#ifdef GDN_TC_PROFILE
+      mbar_wait(&S.bar_g, ph, kWaitLimitNs);
+      TC_MARK_BY(kIssuer, 21);
+#endif
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -937,112 +856,137 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (S.err) goto fail;
     TC_MARK(1);
 
-    // ---- 1. fused: S1 = gamma S0 + K_P^T diag(w) U_P on the tile in registers, stored
-    //         to S1; then (both) S0^T from the tile
-    if constexpr (kFused) {
-      if (!S.cbad && !geo.bad) {  // (an invalid layout has no state of its own to commit)
-        float cacc[8][4];
-        commit_accumulate(fc, S, smem, b, h, hq, Hqk, Hv, tid, r8, c4, cacc);
-        commit_finish(fc, S, state_unit, r8, c4, st, cacc);
+    {
+      // ---- 1. the state row t (columns col0 ..) from the TMA tile; fused: S1 =
+      //         gamma S0 + K_P^T diag(w) U_P from TMEM, written back for the TMA
+      //         store; then S0 = hi + lo (MN-major), eight columns at a time
+      const int cstat = kFused ? S.cbad : GDN_TREE_STATUS_OK;
+      const bool commit_ok = kFused && cstat == GDN_TREE_STATUS_OK && !geo.bad;
+      if (!mbar_wait(&S.bar_s, ph, kWaitLimitNs)) S.err = 2;
+      const bool add_commit = kFused && commit_ok && S.cL > 0;  // CTA-uniform
+      float gamma = 1.f;
+      if (add_commit) {
+        if (!mbar_wait(&S.bar_c, (uint32_t)(S.n_c - 1) & 1u, kWaitLimitNs)) S.err = 2;
+        tc_fence_after_sync();
+        gamma = S.cgamma;
       }
-      __syncthreads();  // the staged path rows are read before S0^T goes over them
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // columns col0 + 8 i .. + 7
+        uint8_t* p0 = sR3 + u_off(t, cq * 8 + 2 * i);
+        uint8_t* p1 = sR3 + u_off(t, cq * 8 + 2 * i + 1);
+        float4 a = *reinterpret_cast<const float4*>(p0);
+        float4 c = *reinterpret_cast<const float4*>(p1);
+        if (add_commit) {
+          float dd[8];
+          tmem_ld_8cols(trow + kColCommit + col0 + 8 * i, dd);  // warp-collective
+          a = make_float4(fmaf(gamma, a.x, dd[0]), fmaf(gamma, a.y, dd[1]),
+                          fmaf(gamma, a.z, dd[2]), fmaf(gamma, a.w, dd[3]));
+          c = make_float4(fmaf(gamma, c.x, dd[4]), fmaf(gamma, c.y, dd[5]),
+                          fmaf(gamma, c.z, dd[6]), fmaf(gamma, c.w, dd[7]));
+        }
+        if (commit_ok) {  // S1, in place for the TMA store
+          *reinterpret_cast<float4*>(p0) = a;
+          *reinterpret_cast<float4*>(p1) = c;
+        }
+        uint32_t hi[4], lo[4];
+        split2(a.x, a.y, hi[0], lo[0]);
+        split2(a.z, a.w, hi[1], lo[1]);
+        split2(c.x, c.y, hi[2], lo[2]);
+        split2(c.z, c.w, hi[3], lo[3]);
+        *reinterpret_cast<uint4*>(smem + OFF_S0H + mn_chunk(t, cq * 4 + i)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + OFF_S0L + mn_chunk(t, cq * 4 + i)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
       TC_MARK(2);
-    }
-    split_state(smem, sbase, S, tmem, r8, c4, st, tid == kIssuer, true);
-    TC_MARK(3);
-    const int cstat = kFused ? S.cbad : GDN_TREE_STATUS_OK;
-    const bool cbad = cstat != GDN_TREE_STATUS_OK;
-    if (h == 0 && tid == 0) {
-      const int vcode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT
-                        : cbad  ? cstat
-                        : S.bad ? GDN_TREE_STATUS_BAD_TREE
-                                : GDN_TREE_STATUS_OK;
-      if (dev_status && vcode) atomicMax(dev_status + b, vcode);
-      const int ccode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT : cstat;
-      if (kFused && fc.status && ccode) atomicMax(fc.status + b, ccode);
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncthreads();
+      if (tid == kIssuer) {
+        tc_fence_after_sync();
+        if (commit_ok) {
+          const int su = geo.st * Hv + h;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tma_store_3d(&tmS1, smem + OFF_R3 + c * kBoxBytes, 32 * c, 0, su);
+          bulk_commit_group();
+          S.s1_pending = 1;
+        }
+        umma_128x128x128_bmn(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
+        umma_128x128x128_bmn(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
+        umma_128x128x128_bmn(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0L, true);
+        umma_commit(&S.bar_ks);
+        ++S.n_ks;
+        TC_MARK_BY(kIssuer, 22);
+      }
+      TC_MARK(3);
+      if (h == 0 && tid == 0) {
+        const int vcode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT
+                          : cstat ? cstat
+                          : S.bad ? GDN_TREE_STATUS_BAD_TREE
+                                  : GDN_TREE_STATUS_OK;
+        if (dev_status && vcode) atomicMax(dev_status + b, vcode);
+        const int ccode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT : cstat;
+        if (kFused && fc.status && ccode) atomicMax(fc.status + b, ccode);
+      }
     }
     // an invalid layout, tree (verified as all-roots) or path leaves the unit's
     // outputs unwritten
-    const bool write_out = !geo.bad && !S.bad && !cbad;
+    const bool write_out =
+        !geo.bad && !S.bad && (!kFused || S.cbad == GDN_TREE_STATUS_OK);
 
     {
-      const uint32_t trow = tmem + trow_off;
       const float bt = live ? S.beta[t] : 0.f;
       const df gt = live ? S.g[t] : df{0.f, 0.f};
       const float gam = __expf(df_value(gt));
       const uint32_t abits = live ? S.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
+      const bool wide = S.wide_g;  // CTA-uniform
 
       // ---- 3. X and Y entries of t's ancestors in registers while K S0 / Q S0 run
+      //         (X[t,s] = beta_t e^{g_t - g_s} G_kk[t,s], Y[t,s] = e^{g_t - g_s} G_qk[t,s])
+      TC_MARK(13);
       if (!mbar_wait(&S.bar_g, ph, kWaitLimitNs)) S.err = 2;
+      TC_MARK(14);
       tc_fence_after_sync();
       TC_MARK(10);
-      float xr[32], yr[32];
-      tmem_ld_32cols(trow + kColGkk + col0, xr);
-      tmem_ld_32cols(trow + kColGqk + col0, yr);
-      TC_MARK(11);
-      float ydiag = 0.f;
-      if (!S.wide_g) {  // CTA-uniform: e^{g_t - g_s} = e^{g_t} e^{-g_s}
-        const float egt = live ? S.eg[t] : 0.f;
+      // X while K S0 / Q S0 run, written back over G_kk in TMEM (nothing is held in
+      // registers across the wait); Y is formed once they are done
+      const float egt = live ? S.eg[t] : 0.f;
+      if (!wide) {  // e^{g_t - g_s} = e^{g_t} e^{-g_s}
+        float xr[32];
+        tmem_ld_32cols(trow + kColGkk + col0, xr);
+        TC_MARK(11);
 #pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
-          const float4 m0 = *reinterpret_cast<const float4*>(&S.emg[col0 + j8 * 8]);
-          const float4 m1 = *reinterpret_cast<const float4*>(&S.emg[col0 + j8 * 8 + 4]);
-          const float em[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 m = *reinterpret_cast<const float4*>(&S.emg[col0 + j4 * 4]);
+          const float em[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = j8 * 8 + e;
-            if (col0 + j == t) ydiag = yr[j];
-            const float dec = ((abits >> j) & 1u) ? egt * em[e] : 0.f;
-            xr[j] = bt * dec * xr[j];
-            yr[j] = dec * yr[j];
-          }
+          for (int e = 0; e < 4; ++e) xr[j4 * 4 + e] *= bt * egt * em[e];
         }
-      } else {
-#pragma unroll
-      for (int j8 = 0; j8 < 4; ++j8) {
-        df gs[8];  // path log-decays of columns col0 + 8 j8 .., loaded together
-        const float4* g4 = reinterpret_cast<const float4*>(&S.g[col0 + j8 * 8]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 w = g4[e];
-          gs[2 * e] = df{w.x, w.y};
-          gs[2 * e + 1] = df{w.z, w.w};
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = j8 * 8 + e;
-          if (col0 + j == t) ydiag = yr[j];
-          const bool need = (abits >> j) & 1u;
-          float dec = 0.f;
-          if (__any_sync(0xffffffffu, need)) dec = __expf(df_diff(gt, gs[e]));
-          xr[j] = bt * dec * xr[j];
-          yr[j] = dec * yr[j];
-        }
-      }
+        tmem_st_32cols(trow + kColGkk + col0, xr);
       }
       TC_MARK(4);
 
-      // ---- 4. once K S0 / Q S0 are done (regions 1 and 2 free): X, Y to region 1,
-      //         R = beta (V - gamma K S0) to region 3, output seeds gamma Q S0 to region 2
+      // ---- 4. once K S0 / Q S0 are done (regions 1 and 2 free) and the S1 store
+      //         has read region 3: X, Y to region 1, R = beta (V - gamma K S0) to
+      //         region 3, output seeds gamma Q S0 to region 2
+      uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..)
+      if (live) {
+        const uint4* vsrc =
+            reinterpret_cast<const uint4*>(v + (((size_t)geo.row0 + t) * Hv + h) * kD + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vreg[i] = vsrc[i];
+      }
       if (!mbar_wait(&S.bar_ks, ph, kWaitLimitNs)) S.err = 2;
       tc_fence_after_sync();
-      uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..), read before
-                      // R goes over them
-      if (!mbar_wait(&S.bar_v, ph, kWaitLimitNs)) S.err = 2;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        vreg[i] = *reinterpret_cast<const uint4*>(smem + OFF_V + sw128_chunk(t, cq * 4 + i));
+      if (tid == kIssuer && S.s1_pending) {
+        bulk_wait_read_all();
+        S.s1_pending = 0;
+      }
       if (__syncthreads_or(S.err)) goto fail;
       TC_MARK(5);
-      if (live) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((abits >> j) & 1u) sXY[x_index(t, col0 + j)] = make_float2(xr[j], yr[j]);
-        if ((t >> 5) == cq) S.ydiag[t] = ydiag;
-      }
       {
         float ks[32];
-        tmem_ld_32cols(trow + kColKS + col0, ks);
+        tmem_ld_32cols(trow + kColKS + col0, ks);  // warp-collective: every lane
         if (live) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -1054,20 +998,59 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               r[2 * e + 1] =
                   bt * (__uint_as_float(w4[e] & 0xffff0000u) - gam * ks[q * 8 + 2 * e + 1]);
             }
-            const int cc = cq * 8 + q * 2;
-            *reinterpret_cast<float4*>(sU + u_index(t, cc)) = make_float4(r[0], r[1], r[2], r[3]);
-            *reinterpret_cast<float4*>(sU + u_index(t, cc + 1)) =
+            *reinterpret_cast<float4*>(sR3 + u_off(t, cq * 8 + q * 2)) =
+                make_float4(r[0], r[1], r[2], r[3]);
+            *reinterpret_cast<float4*>(sR3 + u_off(t, cq * 8 + q * 2 + 1)) =
                 make_float4(r[4], r[5], r[6], r[7]);
+          }
+        }
+      }
+      if (!wide) {
+        float xr[32], yr[32];
+        tmem_ld_32cols(trow + kColGkk + col0, xr);  // warp-collective: every lane
+        tmem_ld_32cols(trow + kColGqk + col0, yr);
+        if (live) {
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 m = *reinterpret_cast<const float4*>(&S.emg[col0 + j4 * 4]);
+            const float em[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = j4 * 4 + e;
+              if ((abits >> j) & 1u)
+                sXY[x_index(t, col0 + j)] = make_float2(xr[j], egt * em[e] * yr[j]);
+              if (col0 + j == t) S.ydiag[t] = yr[j];
+            }
+          }
+        }
+      } else {
+        // some |g| of the tree is past the product form's bound: each decay from
+        // the double-float difference, eight columns at a time, straight to
+        // shared memory (rare trees; kept off the register budget of the
+        // common path)
+#pragma unroll 1
+        for (int j8 = 0; j8 < 4; ++j8) {
+          float gk[8], gq[8];
+          tmem_ld_8cols(trow + kColGkk + col0 + 8 * j8, gk);  // warp-collective
+          tmem_ld_8cols(trow + kColGqk + col0 + 8 * j8, gq);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = 8 * j8 + e;
+            const bool need = (abits >> j) & 1u;
+            if (live && col0 + j == t) S.ydiag[t] = gq[e];
+            float dec = 0.f;
+            if (__any_sync(0xffffffffu, need)) dec = need ? __expf(df_diff(gt, S.g[col0 + j])) : 0.f;
+            if (need) sXY[x_index(t, col0 + j)] = make_float2(bt * dec * gk[e], dec * gq[e]);
           }
         }
       }
       {
         float qs[32];
-        tmem_ld_32cols(trow + kColQS + col0, qs);
+        tmem_ld_32cols(trow + kColQS + col0, qs);  // warp-collective: every lane
         if (live) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(sP + u_index(t, cq * 8 + q)) =
+            *reinterpret_cast<float4*>(sP + u_off(t, cq * 8 + q)) =
                 make_float4(gam * qs[4 * q], gam * qs[4 * q + 1], gam * qs[4 * q + 2],
                             gam * qs[4 * q + 3]);
         }
@@ -1081,15 +1064,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
     // ---- 5. forward substitution as a dataflow over the tree ------------------------
     // u_t = r_t - sum over ancestors a of X[t,a] u_a and o_t = seed_t + sum over
-    // t's path of Y[t,s] u_s.  Warp w takes the nodes at positions w, w + 16, ... of
-    // the depth order.  For node t it waits (acquire) on the mbarrier of t's
-    // grandparent -- every ancestor but the parent is then final -- sums those
-    // terms four at a time (lane = 4 value columns), then waits on the parent and
-    // adds its term, publishes u_t and arrives on t's mbarrier (release); the
-    // parent's and t's own output terms follow.  So a link of the dependency chain
-    // costs one term, not the whole ancestor sum.  No cycle of waits can form: the
-    // unfinished node of lowest depth order never waits (its ancestors come earlier
-    // in that order).
+    // t's path of Y[t,s] u_s.  Tasks (two nodes of one depth, one per half-warp)
+    // go to the warps in depth order.  For node t a half-warp waits (acquire) on
+    // the mbarrier of t's grandparent -- every ancestor but the parent is then
+    // final -- sums those terms two at a time, then waits on the parent, adds its
+    // term, publishes u_t and arrives on t's mbarrier (release); the parent's and
+    // t's own output terms follow.  So a link of the dependency chain costs one
+    // term, not the whole ancestor sum.  No cycle of waits can form: the
+    // unfinished node of lowest depth order never waits (its ancestors come
+    // earlier in that order).
     TC_MARK(6);
     {
       float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
@@ -1111,10 +1094,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const int dep = S.depth[tn];  // the task's two nodes share it
         const uint8_t* pth = sPath + tn * kTile;  // pth[dep - 1] = tn, pth[0] = its root
         const float2* xyrow = sXY + x_index(tn, 0);
-        float4 acc0 = *reinterpret_cast<const float4*>(sU + u_index(tn, hl));
-        float4 acc1 = *reinterpret_cast<const float4*>(sU + u_index(tn, hl + 16));
-        float4 py0 = *reinterpret_cast<const float4*>(sP + u_index(tn, hl));
-        float4 py1 = *reinterpret_cast<const float4*>(sP + u_index(tn, hl + 16));
+        float4 acc0 = *reinterpret_cast<const float4*>(sR3 + u_off(tn, hl));
+        float4 acc1 = *reinterpret_cast<const float4*>(sR3 + u_off(tn, hl + 16));
+        float4 py0 = *reinterpret_cast<const float4*>(sP + u_off(tn, hl));
+        float4 py1 = *reinterpret_cast<const float4*>(sP + u_off(tn, hl + 16));
         float yp = 0.f;
         float4 up0 = make_float4(0.f, 0.f, 0.f, 0.f), up1 = up0;
         if (dep > 1) {
@@ -1129,8 +1112,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               xy[e] = xyrow[aa[e]];
-              u0[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], hl));
-              u1[e] = *reinterpret_cast<const float4*>(sU + u_index(aa[e], hl + 16));
+              u0[e] = *reinterpret_cast<const float4*>(sR3 + u_off(aa[e], hl));
+              u1[e] = *reinterpret_cast<const float4*>(sR3 + u_off(aa[e], hl + 16));
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -1143,8 +1126,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if (j < dep - 2) {
             const int a1 = pth[j];
             const float2 xy1 = xyrow[a1];
-            const float4 v0 = *reinterpret_cast<const float4*>(sU + u_index(a1, hl));
-            const float4 v1 = *reinterpret_cast<const float4*>(sU + u_index(a1, hl + 16));
+            const float4 v0 = *reinterpret_cast<const float4*>(sR3 + u_off(a1, hl));
+            const float4 v1 = *reinterpret_cast<const float4*>(sR3 + u_off(a1, hl + 16));
             acc0 = fma4(-xy1.x, v0, acc0);
             acc1 = fma4(-xy1.x, v1, acc1);
             py0 = fma4(xy1.y, v0, py0);
@@ -1154,13 +1137,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           const float2 xyp = xyrow[par];
           yp = xyp.y;
           wait_ready(par);
-          up0 = *reinterpret_cast<const float4*>(sU + u_index(par, hl));
-          up1 = *reinterpret_cast<const float4*>(sU + u_index(par, hl + 16));
+          up0 = *reinterpret_cast<const float4*>(sR3 + u_off(par, hl));
+          up1 = *reinterpret_cast<const float4*>(sR3 + u_off(par, hl + 16));
           acc0 = fma4(-xyp.x, up0, acc0);
           acc1 = fma4(-xyp.x, up1, acc1);
           if (on) {
-            *reinterpret_cast<float4*>(sU + u_index(tn, hl)) = acc0;
-            *reinterpret_cast<float4*>(sU + u_index(tn, hl + 16)) = acc1;
+            *reinterpret_cast<float4*>(sR3 + u_off(tn, hl)) = acc0;
+            *reinterpret_cast<float4*>(sR3 + u_off(tn, hl + 16)) = acc1;
           }
         }
         __syncwarp();
@@ -1190,23 +1173,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    // region 1 is free: the next unit's K and Q start loading
-    fence_proxy_async_smem();
+    // regions 1 and 3 are free: the next unit's K, Q and state start loading
     tc_fence_before_sync();
     if (__syncthreads_or(S.err)) goto fail;
     tc_fence_after_sync();
     TC_MARK(7);
     TC_DUMP();
-    if (tid == kIssuer && next < n_units)
-      issue_kqv(S, smem, &tmK, &tmQ, &tmV, lay, next, Hv, Hqk, Nmax);
+    if (tid == kIssuer && next < n_units) {
+      issue_kq(S, smem, &tmK, &tmQ, lay, next, Hv, Hqk, Nmax);
+      issue_state(S, smem, &tmS, lay, next, Hv, Nmax);
+    }
   }
   goto release;
 
 fail:
   // a bounded wait ran out: report it for this unit's sequence and for the
   // sequences of every unit this CTA has not reached (their outputs stay
-  // unwritten), let in-flight copies and MMAs drain (again bounded), then free
-  // TMEM
+  // unwritten), let in-flight copies, stores and MMAs drain (again bounded),
+  // then free TMEM
   if (tid == 0) {
     for (int u = unit; u < n_units; u += gridDim.x) {
       if (dev_status) atomicMax(dev_status + u / Hv, GDN_TREE_STATUS_TIMEOUT);
@@ -1215,15 +1199,15 @@ fail:
   }
   cp_async_wait_all();  // this thread's prefetches into shared memory
   if (tid == kIssuer) {
-    if (S.n_kq > 0) {
-      mbar_wait(&S.bar_kq, (S.n_kq - 1) & 1, kWaitLimitNs);
-      mbar_wait(&S.bar_v, (S.n_kq - 1) & 1, kWaitLimitNs);
-    }
+    if (S.n_kq > 0) mbar_wait(&S.bar_kq, (S.n_kq - 1) & 1, kWaitLimitNs);
     if (S.n_g > 0) mbar_wait(&S.bar_g, (S.n_g - 1) & 1, kWaitLimitNs);
     if (S.n_ks > 0) mbar_wait(&S.bar_ks, (S.n_ks - 1) & 1, kWaitLimitNs);
+    if (S.n_s > 0) mbar_wait(&S.bar_s, (S.n_s - 1) & 1, kWaitLimitNs);
+    if (S.n_c > 0) mbar_wait(&S.bar_c, (S.n_c - 1) & 1, kWaitLimitNs);
   }
 
 release:
+  if (tid == kIssuer) bulk_wait_all();  // the last S1 store has landed
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
@@ -1261,6 +1245,20 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int seqs, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 states [n_states, 128, 128] (n_states = (B or n_slots) x Hv) -> boxes of 32
+// columns x 128 rows, 128-byte swizzled (four per state)
+bool encode_state_map(CUtensorMap* map, const float* base, long long n_states) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kD, (cuuint64_t)n_states};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)kD * kD * 4};
+  const cuuint32_t box[3] = {32, kD, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool verify_tc_supported(const gdn_tree_dims& d) {
@@ -1285,11 +1283,14 @@ int sm_count() {
 
 template <bool kFused>
 cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
-  CUtensorMap tmQ, tmK, tmV;
+  CUtensorMap tmQ, tmK, tmV, tmS, tmS1;
   const int rows = a.lay.packed() ? a.lay.T : a.d.N, seqs = a.lay.packed() ? 1 : a.d.B;
+  const long long n_states = (long long)(a.lay.slot ? a.lay.n_slots : a.d.B) * a.d.Hv;
   if (!encode_rows_map(&tmQ, a.q, rows, seqs, a.d.Hqk) ||
       !encode_rows_map(&tmK, a.k, rows, seqs, a.d.Hqk) ||
-      !encode_rows_map(&tmV, a.v, rows, seqs, a.d.Hv))
+      !encode_rows_map(&tmV, a.v, rows, seqs, a.d.Hv) ||
+      !encode_state_map(&tmS, a.S0, n_states) ||
+      !encode_state_map(&tmS1, kFused ? fc.S1 : a.S0, n_states))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1301,8 +1302,9 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   if (n_sm <= 0) return cudaErrorInvalidDevice;
   const int grid = n_units < n_sm ? n_units : n_sm;
   verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
-      tmQ, tmK, tmV, a.S0, a.log_alpha, a.beta, a.parent,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, fc, wait_hooks());
+      tmQ, tmK, tmV, tmS, tmS1, a.S0, a.log_alpha, a.beta, a.parent,
+      static_cast<const __nv_bfloat16*>(a.v), static_cast<__nv_bfloat16*>(a.o), a.U, a.d,
+      a.dev_status, a.lay, fc, wait_hooks());
   return cudaGetLastError();
 }
 

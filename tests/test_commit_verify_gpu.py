@@ -83,9 +83,12 @@ def test_commit_verify_matches_oracle_and_separate_calls(idx):
     assert H.rel_err(g["S1"], S1_ref) <= H.TOL_S1
     assert H.rel_err(g["U"], U_ref) <= H.TOL_U
     assert H.rel_err(g["o"], o_ref) <= H.TOL_O[dt]
-    # and it is the same computation as the two calls
-    assert H.rel_err(g["S1"], g["S1_sep"]) <= 1e-6
-    assert H.rel_err(g["U"], g["U_sep"]) <= 1e-5
+    # and it is the same computation as the two calls: the fused commit runs on
+    # the tensor cores with w U split into bf16 hi + lo (each product to about
+    # 2^-17 relative), the separate one in fp32 FMAs, so the two states agree to
+    # a few 2^-17 of the state's scale (and U, from them, likewise)
+    assert H.rel_err(g["S1"], g["S1_sep"]) <= 2e-5
+    assert H.rel_err(g["U"], g["U_sep"]) <= 2e-5
     assert H.rel_err(g["o"], g["o_sep"]) <= 1e-2
 
 
