@@ -108,11 +108,11 @@ __device__ unsigned long long g_tc_phase[4096][kMarks];
 // change roles within a unit
 constexpr uint32_t kTileBytes = 128 * 128;            // one 64-wide K block: 128 rows x 128 B
 constexpr uint32_t kOpBytes = 2 * kTileBytes;         // a 128 x 128 bf16 operand (2 K blocks)
-// region 1: K, Q (TMA) until the MMAs that read them end; then R / U (fp32 rows,
-// the layout of u_off)
+// region 1: K, Q (TMA) until the MMAs that read them end; then X, Y of each
+// node's ancestors (packed strictly-lower triangle, float2)
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = 1 * kOpBytes;
-constexpr uint32_t OFF_U = 0;
+constexpr uint32_t OFF_XY = 0;
 // region 2: fused, the commit's operand tiles (k rows; w U hi, lo: MN-major);
 // then S0 hi, lo (MN-major) until the K S0 / Q S0 MMAs end; then the output
 // rows (fp32, seeded with gamma Q S0, finished by the solve)
@@ -125,10 +125,8 @@ constexpr uint32_t OFF_S0H = OFF_R2;
 constexpr uint32_t OFF_S0L = OFF_R2 + kOpBytes;
 constexpr uint32_t OFF_P = OFF_R2;
 // region 3: the fp32 state (TMA: four boxes of 32 columns x 128 rows), S1 in
-// place until its TMA store has read it; then X, Y of each node's ancestors
-// (packed strictly-lower triangle, float2)
+// place until its TMA store has read it; then R / U (fp32 rows, same layout)
 constexpr uint32_t OFF_R3 = 4 * kOpBytes;
-constexpr uint32_t OFF_XY = OFF_R3;
 constexpr uint32_t kBoxBytes = 32 * 4 * 128;  // 16 KB
 constexpr uint32_t OFF_PATH = OFF_R3 + kTile * kD * 4;  // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
@@ -139,49 +137,43 @@ constexpr uint32_t kSmallBytes = 16384;
 #endif
 constexpr uint32_t kSmemBytes = OFF_SMALL + kSmallBytes + 1024;  // + alignment slack
 
-static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 3");
+static_assert(kTile * (kTile - 1) / 2 * 8 <= 2 * kOpBytes, "X, Y must fit in region 1");
 static_assert(3 * kCommitTile <= 2 * kOpBytes, "commit tiles must fit in region 2");
 static_assert(OFF_R3 % 1024 == 0 && OFF_SMALL % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// The structure of one sequence's tree, shared by all its v-heads: built once
-// per sequence by tree_table_kernel, copied (bulk) into every unit's CTA.
-struct TreeMeta {
-  uint32_t anc[kTile * kW];   // strict-ancestor bitsets
-  uint8_t par[kTile];         // parent (0xFF: hangs off the state; invalid trees: all roots)
-  uint8_t depth[kTile];       // path length (0 past the tree)
-  uint8_t order[kTile];       // nodes in depth order
-  uint8_t task_pos[kTile];    // solve task k: nodes order[task_pos[k]] .. (task_n[k] of them,
-  uint8_t task_n[kTile];      // one or two, of one depth)
-  int32_t n_tasks, bad, pad0, pad1;
-};
-static_assert(sizeof(TreeMeta) % 16 == 0, "bulk-copied");
-struct TreeTable {
-  uint8_t path[kTile * kTile];  // row t: t's strict ancestors root first, then t
-  TreeMeta meta;
-};
-static_assert(sizeof(TreeTable) % 16 == 0, "tables are 16-byte aligned");
-
 struct Small {
-  TreeMeta tm;      // this unit's tree (bulk copy from the sequence's table)
-  int jump[kTile];  // pointer jumping of the path log-decays
+  int parent[kTile];
+  int jump[kTile];  // tree prep: pointer jumping
   df g[kTile];
   float eg[kTile], emg[kTile];  // e^{g_t}, e^{-g_t}
   float beta[kTile];
+  float la[kTile];
   float ydiag[kTile];  // Y[t,t] = q_t . k_t
+  uint32_t anc[kTile * kW];
+  int order[kTile];
+  int depth[kTile];
+  int level_start[kTile + 2];
+  int level_cursor[kTile + 2];
+  int level_task[kTile + 2];  // first solve task of each depth
+  uint8_t task_pos[kTile];    // solve task k: nodes order[task_pos[k]] .. (task_n[k] of them,
+  uint8_t task_n[kTile];      // one or two, of one depth)
+  int n_tasks;
   uint64_t node_bar[kTile];  // solve: completes a phase per unit once the node's u is final
-  // the next unit's gates, prefetched (cp.async) while this unit runs
+  // the next unit's tree and gates, prefetched (cp.async) while this unit runs
+  int pre_parent[kTile];
   float pre_beta[kTile];
   float pre_la[kTile];
-  // K, Q landed; Gram done; K S0 / Q S0 done; state landed; tree table landed;
-  // commit rows staged; commit MMA done
-  uint64_t bar_kq, bar_g, bar_ks, bar_s, bar_t, bar_stage, bar_c;
-  uint64_t bar_r3;  // region 3 is free for X, Y (the S1 store has read it)
+  // K, Q landed; Gram done; K S0 / Q S0 done; state landed; commit rows staged;
+  // commit MMA done
+  uint64_t bar_kq, bar_g, bar_ks, bar_s, bar_stage, bar_c;
   uint32_t tmem_base;
   int err;
+  int bad;     // the tree failed validation
   int wide_g;  // some |g_t| > kProductDecayLimit
-  // phases issued on bar_kq, bar_g, bar_ks, bar_s, bar_t, bar_c (for the drain)
-  int n_kq, n_g, n_ks, n_s, n_t, n_c;
+  // phases issued on bar_kq, bar_g, bar_ks, bar_s, bar_c (for the drain)
+  int n_kq, n_g, n_ks, n_s, n_c;
+  int s1_pending;  // a TMA store of S1 is in flight
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
   int pre_path[kMaxN];  // the next unit's accepted path and its length, prefetched
@@ -200,7 +192,7 @@ static_assert(sizeof(Small) <= kSmallBytes, "small state too large");
 // members read or written as 16-byte vectors
 static_assert(offsetof(Small, g) % 16 == 0 && offsetof(Small, emg) % 16 == 0,
               "path log-decays are read as float4");
-static_assert(offsetof(Small, tm) % 16 == 0, "the tree is bulk-copied");
+static_assert(offsetof(Small, anc) % 16 == 0, "ancestor rows are read and written as uint4");
 
 // byte offset of 16-byte chunk k8 (K elements 8*k8 .. 8*k8+7) of `row` in a
 // 128-row, 128-wide K-major bf16 tile stored with the 128-byte swizzle
@@ -330,14 +322,15 @@ __device__ __forceinline__ UnitGeom unit_geom(const SeqLayout& lay, int b, int N
   return g;
 }
 
-// Tree group: starts the copies of a unit's gates (node = tid) into the prefetch
-// slots; tree_gates of that unit waits for them.
-__device__ __forceinline__ void prefetch_gates(Small& S, const float* beta,
-                                               const float* log_alpha, const SeqLayout& lay,
-                                               int unit, int Nmax, int Hv, int tid) {
+// Tree group: starts the copies of a unit's parent links and gates (node = tid)
+// into the prefetch slots; tree_prep of that unit waits for them.
+__device__ __forceinline__ void prefetch_tree(Small& S, const int32_t* parent, const float* beta,
+                                              const float* log_alpha, const SeqLayout& lay,
+                                              int unit, int Nmax, int Hv, int tid) {
   const int b = unit / Hv, h = unit - b * Hv;
   const UnitGeom g = unit_geom(lay, b, Nmax);
   if (tid < g.n) {
+    cp_async4(&S.pre_parent[tid], parent + (size_t)g.row0 + tid);
     cp_async4(&S.pre_beta[tid], beta + ((size_t)g.row0 + tid) * Hv + h);
     cp_async4(&S.pre_la[tid], log_alpha + ((size_t)g.row0 + tid) * Hv + h);
   }
@@ -388,17 +381,6 @@ __device__ __forceinline__ void issue_kq(Small& S, uint8_t* smem, const CUtensor
   ++S.n_kq;
 }
 
-// the unit's tree table (its sequence's, built by tree_table_kernel): the path
-// table into its region and the rest into S.tm (bar_t); issuing thread only
-__device__ __forceinline__ void issue_table(Small& S, uint8_t* sPath, const TreeTable* tables,
-                                            int unit, int Hv) {
-  const TreeTable* tt = tables + unit / Hv;
-  mbar_arrive_expect_tx(&S.bar_t, (uint32_t)(sizeof(tt->path) + sizeof(TreeMeta)));
-  bulk_load(sPath, tt->path, (uint32_t)sizeof(tt->path), &S.bar_t);
-  bulk_load(&S.tm, &tt->meta, (uint32_t)sizeof(TreeMeta), &S.bar_t);
-  ++S.n_t;
-}
-
 // the unit's fp32 state (four boxes of 32 columns) into region 3 (bar_s);
 // issuing thread only
 __device__ __forceinline__ void issue_state(Small& S, uint8_t* smem, const CUtensorMap* tmS,
@@ -412,50 +394,89 @@ __device__ __forceinline__ void issue_state(Small& S, uint8_t* smem, const CUten
   ++S.n_s;
 }
 
-// Tree group (threads 0..127): takes the unit's prefetched gates and, once the
-// sequence's tree table has landed, gives every node its path log-decay g_t
-// (double-float) by pointer jumping over the parent links (ceil(log2 depth)
-// rounds), and e^{g_t}, e^{-g_t}.  The copies of the CTA's next unit's gates (if
-// `next` < `end`) start as soon as the prefetch slots have been read.
-__device__ __forceinline__ void tree_gates(Small& S, const float* beta, const float* log_alpha,
-                                           const SeqLayout& lay, int Nmax, int next, int end,
-                                           int N, int Hv, int tid, uint32_t ph,
-                                           uint64_t limit_ns) {
+// Tree group (threads 0..127): takes the unit's prefetched tree and gates,
+// validates the tree, then pointer jumping (ceil(log2 depth) rounds) gives every
+// node its strict-ancestor bitset and its path log-decay g_t (double-float); its
+// depth and its path (sPath row, root first: the ancestors in index order) follow
+// from the bitset; finally the nodes are ordered by depth.  An invalid tree is
+// replaced by all-roots (nothing of it is stored).  The copies
+// for the CTA's next unit (if `next` < `end`) start as soon as the prefetch
+// slots have been read.
+__device__ __forceinline__ void tree_prep(Small& S, uint8_t* sPath, const int32_t* parent,
+                                          const float* beta, const float* log_alpha,
+                                          const SeqLayout& lay, int Nmax, int next, int end,
+                                          int N, int Hv, int tid, int lane, int warp, int unit) {
   using TreeSync = NamedSync<1, 128>;
   cp_async_wait_all();
   TC_MARK(12);
+  int p_in = -1;
   float be_in = 0.f, la_in = 0.f;
   if (tid < N) {
+    p_in = S.pre_parent[tid];
     be_in = S.pre_beta[tid];
     la_in = S.pre_la[tid];
   }
   S.beta[tid] = be_in;
-  if (!mbar_wait(&S.bar_t, ph, limit_ns)) S.err = 3;
-  TC_MARK(13);
-  const int p = S.tm.par[tid];
-  int jmp = tid < N && p != 0xFF ? p : -1;
+  S.la[tid] = la_in;
+  S.level_start[tid] = 0;
+  if (tid < 2) S.level_start[kTile + tid] = 0;
+  const int bad_any = bar_or<1, 128>(tid < N && (p_in < -1 || p_in >= tid));
+  S.parent[tid] = bad_any ? -1 : p_in;
+  if (tid == 0) S.bad = bad_any;
+  // every read of the prefetch slots has completed (their values are used above)
+  if (next < end) prefetch_tree(S, parent, beta, log_alpha, lay, next, Nmax, Hv, tid);
+  TreeSync()();
+  // pointer jumping: after round r, jump[t] is t's 2^r-th ancestor (or -1) and
+  // anc[t], g[t] cover the part of t's path below it
+  int jmp = tid < N ? S.parent[tid] : -1;
   df g = {la_in, 0.f};
+  uint4 a = make_uint4(0u, 0u, 0u, 0u);
+  if (jmp >= 0) {
+    const uint32_t bit = 1u << (jmp & 31);
+    a.x = (jmp >> 5) == 0 ? bit : 0u;
+    a.y = (jmp >> 5) == 1 ? bit : 0u;
+    a.z = (jmp >> 5) == 2 ? bit : 0u;
+    a.w = (jmp >> 5) == 3 ? bit : 0u;
+  }
   S.jump[tid] = jmp;
   S.g[tid] = g;
-  // every read of the prefetch slots has completed (their values are used above)
-  TreeSync()();
-  if (next < end) prefetch_gates(S, beta, log_alpha, lay, next, Nmax, Hv, tid);
-  // after round r, jump[t] is t's 2^r-th ancestor (or -1) and g[t] covers the
-  // part of t's path below it
+  *reinterpret_cast<uint4*>(&S.anc[tid * kW]) = a;
   while (bar_or<1, 128>(jmp >= 0)) {  // also the barrier after the last round's writes
     int jj = -1;
     df gj = {0.f, 0.f};
+    uint4 aj = make_uint4(0u, 0u, 0u, 0u);
     if (jmp >= 0) {
       jj = S.jump[jmp];
       gj = S.g[jmp];
+      aj = *reinterpret_cast<const uint4*>(&S.anc[jmp * kW]);
     }
     TreeSync()();
     if (jmp >= 0) {
       g = df_add(g, gj);
+      a.x |= aj.x;
+      a.y |= aj.y;
+      a.z |= aj.z;
+      a.w |= aj.w;
       jmp = jj;
       S.jump[tid] = jmp;
       S.g[tid] = g;
+      *reinterpret_cast<uint4*>(&S.anc[tid * kW]) = a;
     }
+  }
+  int dep = 0;
+  if (tid < N) {
+    dep = __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w) + 1;
+    S.depth[tid] = dep;
+    // path: the strict ancestors in index order (root first), then t itself
+    uint8_t* row = sPath + tid * kTile;
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    int k = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      for (uint32_t m = aw[w]; m != 0u; m &= m - 1u) row[k++] = (uint8_t)(w * 32 + __ffs(m) - 1);
+    }
+    row[k] = (uint8_t)tid;
+    atomicAdd(&S.level_start[dep], 1);
   }
   int wide = 0;
   if (tid < N) {
@@ -464,8 +485,51 @@ __device__ __forceinline__ void tree_gates(Small& S, const float* beta, const fl
     S.emg[tid] = expf(-gv);
     wide = fabsf(gv) > kProductDecayLimit;
   }
-  wide = bar_or<1, 128>(wide);
+  wide = bar_or<1, 128>(wide);  // (also the barrier before the level scan)
   if (tid == 0) S.wide_g = wide;
+  if (warp == 0) {
+    // exclusive scans of the level counts 0..kTile+1 and of the solve tasks per
+    // level (pairs of nodes, ceil(count / 2)), packed in one int (each <= 128);
+    // lane owns 5 entries
+    int cnt[5], run = 0;
+#pragma unroll
+    for (int e = 0; e < 5; ++e) {
+      const int l = lane * 5 + e;
+      cnt[e] = l < kTile + 2 ? S.level_start[l] : 0;
+      run += cnt[e] | (((cnt[e] + 1) >> 1) << 16);
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += up;
+    }
+    int excl = incl - run;
+#pragma unroll
+    for (int e = 0; e < 5; ++e) {
+      const int l = lane * 5 + e;
+      if (l < kTile + 2) {
+        S.level_start[l] = excl & 0xffff;
+        S.level_cursor[l] = excl & 0xffff;
+        S.level_task[l] = excl >> 16;
+      }
+      excl += cnt[e] | (((cnt[e] + 1) >> 1) << 16);
+    }
+    if (lane == 31) S.n_tasks = incl >> 16;
+  }
+  TreeSync()();
+  if (tid < N) {
+    // position in the depth order; every even rank within the level opens a task
+    // of two nodes (one at an odd-sized level's end)
+    const int pos = atomicAdd(&S.level_cursor[dep], 1);
+    S.order[pos] = tid;
+    const int r = pos - S.level_start[dep];
+    if ((r & 1) == 0) {
+      const int k = S.level_task[dep] + (r >> 1);
+      S.task_pos[k] = (uint8_t)pos;
+      S.task_n[k] = (uint8_t)(pos + 1 < S.level_start[dep + 1] ? 2 : 1);
+    }
+  }
 }
 
 // w_j = exp(G_L - G_j) and gamma_L = exp(G_L) along the committed path, with
@@ -625,141 +689,15 @@ __device__ __forceinline__ void commit_stage(const FusedCommit& fc, const Small&
   fence_proxy_async_smem();
 }
 
-// One CTA (one thread per node) per sequence: validates the tree of sequence b
-// and builds its table -- strict-ancestor bitsets by pointer jumping
-// (ceil(log2 depth) rounds), depths, root-first paths (the ancestors in index
-// order, then the node), the depth order, and the solve's tasks (two nodes of
-// one depth; one at an odd-sized level's end).  An invalid tree is built as all
-// roots (the verification reports it and writes nothing of it).  Every v-head
-// of the sequence reads this one table.
-__global__ void __launch_bounds__(kTile)
-tree_table_kernel(const int32_t* __restrict__ parent, SeqLayout lay, int Nmax,
-                  TreeTable* __restrict__ tables) {
-  struct Build {
-    TreeTable tt;  // first, so that it is copied out as it stands
-    int jump[kTile];
-    int level_start[kTile + 2], level_cursor[kTile + 2], level_task[kTile + 2];
-  };
-  __shared__ __align__(16) Build B;
-  TreeMeta& m = B.tt.meta;
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cnt = lay.count(b, Nmax);
-  const int N = cnt < 0 ? 0 : cnt;  // (an invalid layout is reported by the verification)
-  int p_in = -1;
-  if (tid < N) p_in = parent[(size_t)lay.row0(b, Nmax) + tid];
-  B.level_start[tid] = 0;
-  if (tid < 2) B.level_start[kTile + tid] = 0;
-  const int bad = __syncthreads_or(tid < N && (p_in < -1 || p_in >= tid));
-  int jmp = (tid < N && !bad) ? p_in : -1;
-  m.par[tid] = jmp < 0 ? (uint8_t)0xFF : (uint8_t)jmp;
-  uint4 a = make_uint4(0u, 0u, 0u, 0u);
-  if (jmp >= 0) {
-    const uint32_t bit = 1u << (jmp & 31);
-    a.x = (jmp >> 5) == 0 ? bit : 0u;
-    a.y = (jmp >> 5) == 1 ? bit : 0u;
-    a.z = (jmp >> 5) == 2 ? bit : 0u;
-    a.w = (jmp >> 5) == 3 ? bit : 0u;
-  }
-  B.jump[tid] = jmp;
-  *reinterpret_cast<uint4*>(&m.anc[tid * kW]) = a;
-  // after round r, jump[t] is t's 2^r-th ancestor (or -1) and anc[t] covers the
-  // part of t's path below it
-  while (__syncthreads_or(jmp >= 0)) {
-    int jj = -1;
-    uint4 aj = make_uint4(0u, 0u, 0u, 0u);
-    if (jmp >= 0) {
-      jj = B.jump[jmp];
-      aj = *reinterpret_cast<const uint4*>(&m.anc[jmp * kW]);
-    }
-    __syncthreads();
-    if (jmp >= 0) {
-      a.x |= aj.x;
-      a.y |= aj.y;
-      a.z |= aj.z;
-      a.w |= aj.w;
-      jmp = jj;
-      B.jump[tid] = jmp;
-      *reinterpret_cast<uint4*>(&m.anc[tid * kW]) = a;
-    }
-  }
-  int dep = 0;
-  if (tid < N) {
-    dep = __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w) + 1;
-    uint8_t* row = B.tt.path + tid * kTile;
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    int k = 0;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      for (uint32_t mm = aw[w]; mm != 0u; mm &= mm - 1u) row[k++] = (uint8_t)(w * 32 + __ffs(mm) - 1);
-    }
-    row[k] = (uint8_t)tid;
-    atomicAdd(&B.level_start[dep], 1);
-  }
-  m.depth[tid] = (uint8_t)dep;
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scans of the level counts 0..kTile+1 and of the solve tasks per
-    // level (pairs of nodes, ceil(count / 2)), packed in one int (each <= 128);
-    // lane owns 5 entries
-    int c5[5], run = 0;
-#pragma unroll
-    for (int e = 0; e < 5; ++e) {
-      const int l = lane * 5 + e;
-      c5[e] = l < kTile + 2 ? B.level_start[l] : 0;
-      run += c5[e] | (((c5[e] + 1) >> 1) << 16);
-    }
-    int incl = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int up = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += up;
-    }
-    int excl = incl - run;
-#pragma unroll
-    for (int e = 0; e < 5; ++e) {
-      const int l = lane * 5 + e;
-      if (l < kTile + 2) {
-        B.level_start[l] = excl & 0xffff;
-        B.level_cursor[l] = excl & 0xffff;
-        B.level_task[l] = excl >> 16;
-      }
-      excl += c5[e] | (((c5[e] + 1) >> 1) << 16);
-    }
-    if (lane == 31) m.n_tasks = incl >> 16;
-  }
-  __syncthreads();
-  if (tid < N) {
-    // position in the depth order; every even rank within the level opens a task
-    // of two nodes (one at an odd-sized level's end)
-    const int pos = atomicAdd(&B.level_cursor[dep], 1);
-    m.order[pos] = (uint8_t)tid;
-    const int r = pos - B.level_start[dep];
-    if ((r & 1) == 0) {
-      const int k = B.level_task[dep] + (r >> 1);
-      m.task_pos[k] = (uint8_t)pos;
-      m.task_n[k] = (uint8_t)(pos + 1 < B.level_start[dep + 1] ? 2 : 1);
-    }
-  }
-  if (tid == 0) {
-    m.bad = bad;
-    m.pad0 = m.pad1 = 0;
-  }
-  __syncthreads();
-  const uint4* src = reinterpret_cast<const uint4*>(&B.tt);
-  uint4* dst = reinterpret_cast<uint4*>(tables + b);
-  for (int i = tid; i < (int)(sizeof(TreeTable) / 16); i += kTile) dst[i] = src[i];
-}
-
 template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmS1, const float* S0,
                  const float* __restrict__ log_alpha, const float* __restrict__ beta,
-                 const __nv_bfloat16* __restrict__ v,
+                 const int32_t* __restrict__ parent, const __nv_bfloat16* __restrict__ v,
                  __nv_bfloat16* __restrict__ o, float* __restrict__ U, gdn_tree_dims d,
-                 int32_t* dev_status, SeqLayout lay, FusedCommit fc, WaitHooks hk,
-                 const TreeTable* __restrict__ tables) {
+                 int32_t* dev_status, SeqLayout lay, FusedCommit fc, WaitHooks hk) {
   const uint64_t kWaitLimitNs = hk.limit_ns;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -768,7 +706,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   Small& S = *reinterpret_cast<Small*>(smem + OFF_SMALL);
   float2* sXY = reinterpret_cast<float2*>(smem + OFF_XY);
   uint8_t* sR3 = smem + OFF_R3;
-  uint8_t* sU = smem + OFF_U;
   uint8_t* sP = smem + OFF_P;
   uint8_t* sPath = smem + OFF_PATH;
 
@@ -792,25 +729,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     mbar_init(&S.bar_g, 1);
     mbar_init(&S.bar_ks, 1);
     mbar_init(&S.bar_s, 1);
-    mbar_init(&S.bar_t, 1);
-    mbar_init(&S.bar_r3, 1);
     mbar_init(&S.bar_stage, 1);
     mbar_init(&S.bar_c, 1);
     S.err = 0;
-    S.n_kq = S.n_g = S.n_ks = S.n_s = S.n_t = S.n_c = 0;
+    S.n_kq = S.n_g = S.n_ks = S.n_s = S.n_c = 0;
+    S.s1_pending = 0;
     S.cbad = 0;
     S.cL = 0;
     mbar_fence_init();
     if (unit < n_units) {
-      issue_table(S, sPath, tables, unit, Hv);
       issue_kq(S, smem, &tmK, &tmQ, lay, unit, Hv, Hqk, Nmax);
+      issue_state(S, smem, &tmS, lay, unit, Hv, Nmax);
     }
   }
   if constexpr (kFused) {
     if (warp > 4 && unit < n_units) prefetch_path(fc, S, unit / Hv, tid - 160);
   }
   if (warp < 4) {
-    if (unit < n_units) prefetch_gates(S, beta, log_alpha, lay, unit, Nmax, Hv, tid);
+    if (unit < n_units) prefetch_tree(S, parent, beta, log_alpha, lay, unit, Nmax, Hv, tid);
     mbar_init(&S.node_bar[tid], 1);  // one solve barrier per node (one arrival a phase)
     mbar_fence_init();
   }
@@ -840,7 +776,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     TC_START();
     TC_MARK(0);
     if (warp < 4) {
-      tree_gates(S, beta, log_alpha, lay, Nmax, next, n_units, N, Hv, tid, ph, kWaitLimitNs);
+      tree_prep(S, sPath, parent, beta, log_alpha, lay, Nmax, next, n_units, N, Hv, tid, lane,
+                warp, unit);
       TC_MARK(8);
     } else if (warp > 4) {
       if constexpr (kFused) {
@@ -876,11 +813,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int r = 0; r < 4; ++r) bulk_prefetch_l2(ns + r * (kD * kD / 4), kD * kD);
       }
-      const bool kq = mbar_wait(&S.bar_kq, ph, kWaitLimitNs);
-      // region 3 is free (the previous unit's solve is over) and K, Q have had the
-      // copy engine to themselves: the state starts coming
-      issue_state(S, smem, &tmS, lay, unit, Hv, Nmax);
-      if (!kq) {
+      if (!mbar_wait(&S.bar_kq, ph, kWaitLimitNs)) {
         S.err = 1;
       } else {
         TC_MARK_BY(kIssuer, 9);
@@ -976,6 +909,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
           for (int c = 0; c < 4; ++c) tma_store_3d(&tmS1, smem + OFF_R3 + c * kBoxBytes, 32 * c, 0, su);
           bulk_commit_group();
+          S.s1_pending = 1;
         }
         umma_128x128x128_bmn(tmem + kColQS, sbase + OFF_Q, sbase + OFF_S0H, false);
         umma_128x128x128_bmn(tmem + kColKS, sbase + OFF_K, sbase + OFF_S0H, false);
@@ -983,14 +917,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         umma_commit(&S.bar_ks);
         ++S.n_ks;
         TC_MARK_BY(kIssuer, 22);
-        if (commit_ok) bulk_wait_read_all();  // the S1 store has read region 3
-        mbar_arrive(&S.bar_r3);
       }
       TC_MARK(3);
       if (h == 0 && tid == 0) {
         const int vcode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT
                           : cstat ? cstat
-                          : S.tm.bad ? GDN_TREE_STATUS_BAD_TREE
+                          : S.bad ? GDN_TREE_STATUS_BAD_TREE
                                   : GDN_TREE_STATUS_OK;
         if (dev_status && vcode) atomicMax(dev_status + b, vcode);
         const int ccode = geo.bad ? GDN_TREE_STATUS_BAD_LAYOUT : cstat;
@@ -1000,71 +932,43 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     // an invalid layout, tree (verified as all-roots) or path leaves the unit's
     // outputs unwritten
     const bool write_out =
-        !geo.bad && !S.tm.bad && (!kFused || S.cbad == GDN_TREE_STATUS_OK);
+        !geo.bad && !S.bad && (!kFused || S.cbad == GDN_TREE_STATUS_OK);
 
     {
       const float bt = live ? S.beta[t] : 0.f;
       const df gt = live ? S.g[t] : df{0.f, 0.f};
       const float gam = __expf(df_value(gt));
-      const uint32_t abits = live ? S.tm.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
+      const uint32_t abits = live ? S.anc[t * kW + cq] : 0u;  // ancestors among my 32 columns
       const bool wide = S.wide_g;  // CTA-uniform
 
-      // ---- 3. while K S0 / Q S0 run: X[t,s] = beta_t e^{g_t - g_s} G_kk[t,s] and
-      //         Y[t,s] = e^{g_t - g_s} G_qk[t,s] of t's ancestors s to region 3, as
-      //         soon as the S1 store has read it
+      // ---- 3. X and Y entries of t's ancestors in registers while K S0 / Q S0 run
+      //         (X[t,s] = beta_t e^{g_t - g_s} G_kk[t,s], Y[t,s] = e^{g_t - g_s} G_qk[t,s])
       TC_MARK(13);
       if (!mbar_wait(&S.bar_g, ph, kWaitLimitNs)) S.err = 2;
       TC_MARK(14);
       tc_fence_after_sync();
       TC_MARK(10);
+      // X while K S0 / Q S0 run, written back over G_kk in TMEM (nothing is held in
+      // registers across the wait); Y is formed once they are done
+      const float egt = live ? S.eg[t] : 0.f;
       if (!wide) {  // e^{g_t - g_s} = e^{g_t} e^{-g_s}
-        float xr[32], yr[32];
+        float xr[32];
         tmem_ld_32cols(trow + kColGkk + col0, xr);
-        tmem_ld_32cols(trow + kColGqk + col0, yr);
         TC_MARK(11);
-        const float egt = live ? S.eg[t] : 0.f;
-        if (!mbar_wait(&S.bar_r3, ph, kWaitLimitNs)) S.err = 2;
-        if (live) {
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 m = *reinterpret_cast<const float4*>(&S.emg[col0 + j4 * 4]);
-            const float em[4] = {m.x, m.y, m.z, m.w};
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 m = *reinterpret_cast<const float4*>(&S.emg[col0 + j4 * 4]);
+          const float em[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = j4 * 4 + e;
-              const float dec = egt * em[e];
-              if ((abits >> j) & 1u)
-                sXY[x_index(t, col0 + j)] = make_float2(bt * dec * xr[j], dec * yr[j]);
-              if (col0 + j == t) S.ydiag[t] = yr[j];
-            }
-          }
+          for (int e = 0; e < 4; ++e) xr[j4 * 4 + e] *= bt * egt * em[e];
         }
-      } else {
-        // some |g| of the tree is past the product form's bound: each decay from
-        // the double-float difference, eight columns at a time, straight to
-        // shared memory (rare trees; kept off the register budget of the
-        // common path)
-        if (!mbar_wait(&S.bar_r3, ph, kWaitLimitNs)) S.err = 2;
-#pragma unroll 1
-        for (int j8 = 0; j8 < 4; ++j8) {
-          float gk[8], gq[8];
-          tmem_ld_8cols(trow + kColGkk + col0 + 8 * j8, gk);  // warp-collective
-          tmem_ld_8cols(trow + kColGqk + col0 + 8 * j8, gq);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = 8 * j8 + e;
-            const bool need = (abits >> j) & 1u;
-            if (live && col0 + j == t) S.ydiag[t] = gq[e];
-            float dec = 0.f;
-            if (__any_sync(0xffffffffu, need)) dec = need ? __expf(df_diff(gt, S.g[col0 + j])) : 0.f;
-            if (need) sXY[x_index(t, col0 + j)] = make_float2(bt * dec * gk[e], dec * gq[e]);
-          }
-        }
+        tmem_st_32cols(trow + kColGkk + col0, xr);
       }
       TC_MARK(4);
 
-      // ---- 4. once K S0 / Q S0 are done (regions 1 and 2 free): R = beta (V - gamma
-      //         K S0) to region 1, output seeds gamma Q S0 to region 2
+      // ---- 4. once K S0 / Q S0 are done (regions 1 and 2 free) and the S1 store
+      //         has read region 3: X, Y to region 1, R = beta (V - gamma K S0) to
+      //         region 3, output seeds gamma Q S0 to region 2
       uint4 vreg[4];  // this thread's 32 values of v (row t, columns col0 ..)
       if (live) {
         const uint4* vsrc =
@@ -1074,6 +978,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       if (!mbar_wait(&S.bar_ks, ph, kWaitLimitNs)) S.err = 2;
       tc_fence_after_sync();
+      if (tid == kIssuer && S.s1_pending) {
+        bulk_wait_read_all();
+        S.s1_pending = 0;
+      }
       if (__syncthreads_or(S.err)) goto fail;
       TC_MARK(5);
       {
@@ -1090,10 +998,49 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
               r[2 * e + 1] =
                   bt * (__uint_as_float(w4[e] & 0xffff0000u) - gam * ks[q * 8 + 2 * e + 1]);
             }
-            *reinterpret_cast<float4*>(sU + u_off(t, cq * 8 + q * 2)) =
+            *reinterpret_cast<float4*>(sR3 + u_off(t, cq * 8 + q * 2)) =
                 make_float4(r[0], r[1], r[2], r[3]);
-            *reinterpret_cast<float4*>(sU + u_off(t, cq * 8 + q * 2 + 1)) =
+            *reinterpret_cast<float4*>(sR3 + u_off(t, cq * 8 + q * 2 + 1)) =
                 make_float4(r[4], r[5], r[6], r[7]);
+          }
+        }
+      }
+      if (!wide) {
+        float xr[32], yr[32];
+        tmem_ld_32cols(trow + kColGkk + col0, xr);  // warp-collective: every lane
+        tmem_ld_32cols(trow + kColGqk + col0, yr);
+        if (live) {
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 m = *reinterpret_cast<const float4*>(&S.emg[col0 + j4 * 4]);
+            const float em[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = j4 * 4 + e;
+              if ((abits >> j) & 1u)
+                sXY[x_index(t, col0 + j)] = make_float2(xr[j], egt * em[e] * yr[j]);
+              if (col0 + j == t) S.ydiag[t] = yr[j];
+            }
+          }
+        }
+      } else {
+        // some |g| of the tree is past the product form's bound: each decay from
+        // the double-float difference, eight columns at a time, straight to
+        // shared memory (rare trees; kept off the register budget of the
+        // common path)
+#pragma unroll 1
+        for (int j8 = 0; j8 < 4; ++j8) {
+          float gk[8], gq[8];
+          tmem_ld_8cols(trow + kColGkk + col0 + 8 * j8, gk);  // warp-collective
+          tmem_ld_8cols(trow + kColGqk + col0 + 8 * j8, gq);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = 8 * j8 + e;
+            const bool need = (abits >> j) & 1u;
+            if (live && col0 + j == t) S.ydiag[t] = gq[e];
+            float dec = 0.f;
+            if (__any_sync(0xffffffffu, need)) dec = need ? __expf(df_diff(gt, S.g[col0 + j])) : 0.f;
+            if (need) sXY[x_index(t, col0 + j)] = make_float2(bt * dec * gk[e], dec * gq[e]);
           }
         }
       }
@@ -1139,16 +1086,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       // shadows the first without writing); lane hl of the half owns value columns
       // 4 hl .. 4 hl + 3 and 64 + 4 hl .. 64 + 4 hl + 3 (16-byte chunks hl, hl + 16)
       const int hf = lane >> 4, hl = lane & 15;
-      const int n_tasks = S.tm.n_tasks;
+      const int n_tasks = S.n_tasks;
       for (int k = warp; k < n_tasks; k += kWarps) {
-        const int pos = S.tm.task_pos[k];
-        const bool on = hf < S.tm.task_n[k];
-        const int tn = S.tm.order[pos + (on ? hf : 0)];
-        const int dep = S.tm.depth[tn];  // the task's two nodes share it
+        const int pos = S.task_pos[k];
+        const bool on = hf < S.task_n[k];
+        const int tn = S.order[pos + (on ? hf : 0)];
+        const int dep = S.depth[tn];  // the task's two nodes share it
         const uint8_t* pth = sPath + tn * kTile;  // pth[dep - 1] = tn, pth[0] = its root
         const float2* xyrow = sXY + x_index(tn, 0);
-        float4 acc0 = *reinterpret_cast<const float4*>(sU + u_off(tn, hl));
-        float4 acc1 = *reinterpret_cast<const float4*>(sU + u_off(tn, hl + 16));
+        float4 acc0 = *reinterpret_cast<const float4*>(sR3 + u_off(tn, hl));
+        float4 acc1 = *reinterpret_cast<const float4*>(sR3 + u_off(tn, hl + 16));
         float4 py0 = *reinterpret_cast<const float4*>(sP + u_off(tn, hl));
         float4 py1 = *reinterpret_cast<const float4*>(sP + u_off(tn, hl + 16));
         float yp = 0.f;
@@ -1165,8 +1112,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               xy[e] = xyrow[aa[e]];
-              u0[e] = *reinterpret_cast<const float4*>(sU + u_off(aa[e], hl));
-              u1[e] = *reinterpret_cast<const float4*>(sU + u_off(aa[e], hl + 16));
+              u0[e] = *reinterpret_cast<const float4*>(sR3 + u_off(aa[e], hl));
+              u1[e] = *reinterpret_cast<const float4*>(sR3 + u_off(aa[e], hl + 16));
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -1179,8 +1126,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if (j < dep - 2) {
             const int a1 = pth[j];
             const float2 xy1 = xyrow[a1];
-            const float4 v0 = *reinterpret_cast<const float4*>(sU + u_off(a1, hl));
-            const float4 v1 = *reinterpret_cast<const float4*>(sU + u_off(a1, hl + 16));
+            const float4 v0 = *reinterpret_cast<const float4*>(sR3 + u_off(a1, hl));
+            const float4 v1 = *reinterpret_cast<const float4*>(sR3 + u_off(a1, hl + 16));
             acc0 = fma4(-xy1.x, v0, acc0);
             acc1 = fma4(-xy1.x, v1, acc1);
             py0 = fma4(xy1.y, v0, py0);
@@ -1190,13 +1137,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           const float2 xyp = xyrow[par];
           yp = xyp.y;
           wait_ready(par);
-          up0 = *reinterpret_cast<const float4*>(sU + u_off(par, hl));
-          up1 = *reinterpret_cast<const float4*>(sU + u_off(par, hl + 16));
+          up0 = *reinterpret_cast<const float4*>(sR3 + u_off(par, hl));
+          up1 = *reinterpret_cast<const float4*>(sR3 + u_off(par, hl + 16));
           acc0 = fma4(-xyp.x, up0, acc0);
           acc1 = fma4(-xyp.x, up1, acc1);
           if (on) {
-            *reinterpret_cast<float4*>(sU + u_off(tn, hl)) = acc0;
-            *reinterpret_cast<float4*>(sU + u_off(tn, hl + 16)) = acc1;
+            *reinterpret_cast<float4*>(sR3 + u_off(tn, hl)) = acc0;
+            *reinterpret_cast<float4*>(sR3 + u_off(tn, hl + 16)) = acc1;
           }
         }
         __syncwarp();
@@ -1226,7 +1173,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
-    // regions 1 and 3 are free: the next unit's K, Q and tree start loading
+    // regions 1 and 3 are free: the next unit's K, Q and state start loading
     tc_fence_before_sync();
     if (__syncthreads_or(S.err)) goto fail;
     tc_fence_after_sync();
@@ -1234,7 +1181,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     TC_DUMP();
     if (tid == kIssuer && next < n_units) {
       issue_kq(S, smem, &tmK, &tmQ, lay, next, Hv, Hqk, Nmax);
-      issue_table(S, sPath, tables, next, Hv);
+      issue_state(S, smem, &tmS, lay, next, Hv, Nmax);
     }
   }
   goto release;
@@ -1256,7 +1203,6 @@ fail:
     if (S.n_g > 0) mbar_wait(&S.bar_g, (S.n_g - 1) & 1, kWaitLimitNs);
     if (S.n_ks > 0) mbar_wait(&S.bar_ks, (S.n_ks - 1) & 1, kWaitLimitNs);
     if (S.n_s > 0) mbar_wait(&S.bar_s, (S.n_s - 1) & 1, kWaitLimitNs);
-    if (S.n_t > 0) mbar_wait(&S.bar_t, (S.n_t - 1) & 1, kWaitLimitNs);
     if (S.n_c > 0) mbar_wait(&S.bar_c, (S.n_c - 1) & 1, kWaitLimitNs);
   }
 
@@ -1349,27 +1295,17 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-  // the trees' tables (one per sequence), in stream-ordered scratch that is
-  // released on the same stream once the verification has read it
-  TreeTable* tables = nullptr;
-  err = cudaMallocAsync(reinterpret_cast<void**>(&tables), (size_t)a.d.B * sizeof(TreeTable),
-                        stream);
-  if (err != cudaSuccess) return err;
-  tree_table_kernel<<<a.d.B, kTile, 0, stream>>>(a.parent, a.lay, a.d.N, tables);
   // persistent: one CTA per SM (the shared memory admits no second), each walking
   // units blockIdx.x, blockIdx.x + gridDim.x, ...
   const int n_units = a.d.B * a.d.Hv;
   const int n_sm = sm_count();
-  const int grid = n_units < n_sm ? n_units : n_sm;
-  if (n_sm > 0)
-    verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
-        tmQ, tmK, tmV, tmS, tmS1, a.S0, a.log_alpha, a.beta,
-        static_cast<const __nv_bfloat16*>(a.v), static_cast<__nv_bfloat16*>(a.o), a.U, a.d,
-        a.dev_status, a.lay, fc, wait_hooks(), tables);
-  err = cudaGetLastError();
-  const cudaError_t ferr = cudaFreeAsync(tables, stream);
   if (n_sm <= 0) return cudaErrorInvalidDevice;
-  return err != cudaSuccess ? err : ferr;
+  const int grid = n_units < n_sm ? n_units : n_sm;
+  verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
+      tmQ, tmK, tmV, tmS, tmS1, a.S0, a.log_alpha, a.beta, a.parent,
+      static_cast<const __nv_bfloat16*>(a.v), static_cast<__nv_bfloat16*>(a.o), a.U, a.d,
+      a.dev_status, a.lay, fc, wait_hooks());
+  return cudaGetLastError();
 }
 
 }  // namespace
