@@ -12,9 +12,11 @@
 //   as new nodes in that order, and only then do they offer their candidates.
 //   A -inf candidate is never taken; construction stops when none is left.
 //
-// One warp per sequence.  The candidates live in shared memory indexed by their
-// key (slots of nodes not yet built, and taken candidates, hold -inf); a pop is
-// one strided scan per lane and a warp argmax over (score, key).
+// One warp per sequence.  Trees of up to 512 candidate slots with w <= 4 keep
+// them sorted in registers (tree_topw_warp_kernel); other shapes in shared
+// memory indexed by their key (slots of nodes not yet built, and taken
+// candidates, hold -inf), a pop being one strided scan per lane and a warp
+// argmax over (score, key).
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -112,6 +114,175 @@ tree_topw_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w
   if (lane == 0 && n_built) n_built[b] = n;
 }
 
+// Trees of up to 512 candidate slots, w <= 4: one warp per tree.  Lane l owns
+// the slots l, l + 32, ..., l + 480 (key = p * c + j): their log-probabilities,
+// and its live slots sorted best first, in registers, as 64-bit words (the
+// score's order-preserving bits, then the inverted key, so that one unsigned
+// comparison orders by score and then by lower key; 0 = empty).  A round takes
+// the warp's four best words at once -- a butterfly over the lanes merges their
+// sorted top four -- the owners drop what was taken from the front of their
+// arrays, and the new nodes' candidates are inserted by the lanes that own their
+// slots.  Same fp32 sums and tie rule as the general kernel, so the same tree.
+constexpr int kSlots = 16;
+constexpr int kTop = 4;
+
+// fp32 -> uint32 with the same order (no NaN)
+__device__ __forceinline__ uint32_t order_bits(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return u ^ ((u >> 31) ? 0xffffffffu : 0x80000000u);
+}
+__device__ __forceinline__ float from_order_bits(uint32_t o) {
+  return __uint_as_float(o ^ ((o >> 31) ? 0x80000000u : 0xffffffffu));
+}
+__device__ __forceinline__ uint64_t cand_word(float s, uint32_t key) {
+  return ((uint64_t)order_bits(s) << 32) | (uint64_t)(~key);
+}
+__device__ __forceinline__ uint32_t word_key(uint64_t x) { return ~(uint32_t)x; }
+__device__ __forceinline__ float word_score(uint64_t x) {
+  return from_order_bits((uint32_t)(x >> 32));
+}
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t x, int off) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)x, off);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(x >> 32), off);
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ void cswap_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 1)
+tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w,
+                      int max_depth, int32_t* __restrict__ parent,
+                      int32_t* __restrict__ cand_index, float* __restrict__ score,
+                      int32_t* __restrict__ n_built) {
+  __shared__ int s_ndepth[kWarpsPerCta][kSlots * 32];
+  __shared__ float s_lp[kWarpsPerCta][kSlots * 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kWarpsPerCta + warp;
+  if (b >= B) return;  // whole warps only: nothing below synchronises across warps
+  int* ndepth = s_ndepth[warp];
+  float* lp = s_lp[warp];  // the tree's candidate log-probabilities, by key
+  const float* lpb = cand_logp + (size_t)b * N * c;
+  int32_t* par = parent + (size_t)b * N;
+  int32_t* cix = cand_index ? cand_index + (size_t)b * N : nullptr;
+  float* sco = score ? score + (size_t)b * N : nullptr;
+  const float kNegInf = -CUDART_INF_F;
+  const int nslots = N * c;
+  // key / c as a multiply and shift (exact for key * c < 2^16: key < 512, c <= 32)
+  const uint32_t cinv = 65536u / (uint32_t)c + 1u;
+  auto node_of = [&](uint32_t key) { return (int)((key * cinv) >> 16); };
+
+  uint64_t srt[kSlots];  // this lane's live slots, best first (0 = empty)
+#pragma unroll
+  for (int m = 0; m < kSlots; ++m) {
+    const int k = lane + 32 * m;
+    lp[k] = k < nslots ? lpb[k] : kNegInf;
+    srt[m] = 0;
+  }
+  // a live candidate into the sorted array: its place is the number of larger
+  // words; the words from there on move down one (independent selects)
+  auto insert = [&](uint64_t x) {
+    int at = 0;
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) at += srt[i] > x;
+#pragma unroll
+    for (int i = kSlots - 1; i > 0; --i) srt[i] = i > at ? srt[i - 1] : (i == at ? x : srt[i]);
+    if (at == 0) srt[0] = x;
+  };
+  // the root (node 0, score 0, depth 1) offers its candidates (keys 0 .. c-1)
+  if (max_depth > 1) {
+    for (int k = lane; k < c; k += 32) {
+      const float s = 0.f + lp[k];
+      if (s != kNegInf) insert(cand_word(s, (uint32_t)k));
+    }
+  }
+  if (lane == 0) {
+    ndepth[0] = 1;
+    par[0] = -1;
+    if (cix) cix[0] = -1;
+    if (sco) sco[0] = 0.f;
+  }
+  __syncwarp();
+
+  int n = 1;
+  while (n < N) {
+    const int take = min(w, N - n);
+    // the warp's four best words: every lane ends with the same sorted list
+    uint64_t t[kTop] = {srt[0], srt[1], srt[2], srt[3]};
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      uint64_t o[kTop];
+#pragma unroll
+      for (int i = 0; i < kTop; ++i) o[i] = shfl_xor64(t[i], off);
+      // top four of two sorted lists: the larger of a[i] and b[3 - i] (a bitonic
+      // sequence), then sorted
+#pragma unroll
+      for (int i = 0; i < kTop; ++i) t[i] = t[i] > o[kTop - 1 - i] ? t[i] : o[kTop - 1 - i];
+      cswap_desc(t[0], t[2]);
+      cswap_desc(t[1], t[3]);
+      cswap_desc(t[0], t[1]);
+      cswap_desc(t[2], t[3]);
+    }
+    int popped = 0, mine = 0;
+#pragma unroll
+    for (int i = 0; i < kTop; ++i) {
+      if (i < take && t[i] != 0) {
+        ++popped;
+        mine += (int)(word_key(t[i]) & 31u) == lane;
+      }
+    }
+    if (popped == 0) break;  // no live candidate (uniform across the warp)
+    // this lane's taken words are the front of its array
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      uint64_t x = srt[i];
+#pragma unroll
+      for (int q = 1; q <= kTop; ++q)
+        if (mine == q) x = i + q < kSlots ? srt[(i + q) & (kSlots - 1)] : 0;
+      srt[i] = x;
+    }
+    // the new nodes n + i (i < popped): every lane has their words; their depth is
+    // their parent's + 1
+    int nd[kTop];
+#pragma unroll
+    for (int i = 0; i < kTop; ++i) nd[i] = i < popped ? ndepth[node_of(word_key(t[i]))] + 1 : 0;
+    // lane i < popped records node n + i
+    if (lane < popped) {
+      const uint64_t x = lane == 0 ? t[0] : lane == 1 ? t[1] : lane == 2 ? t[2] : t[3];
+      const uint32_t key = word_key(x);
+      const int node = n + lane, p = node_of(key), j = (int)key - p * c;
+      const float s = word_score(x);
+      ndepth[node] = lane == 0 ? nd[0] : lane == 1 ? nd[1] : lane == 2 ? nd[2] : nd[3];
+      par[node] = p;
+      if (cix) cix[node] = j;
+      if (sco) sco[node] = s;
+    }
+    // the new nodes offer their candidates: keys n c .. (n + popped) c - 1, the
+    // ones of this lane's slots (one insertion each)
+    const int k0 = n * c, k1 = (n + popped) * c;
+    for (int k = k0 + ((lane - k0) & 31); k < k1; k += 32) {
+      const int i = node_of((uint32_t)k) - n;
+      const uint64_t x = i == 0 ? t[0] : i == 1 ? t[1] : i == 2 ? t[2] : t[3];
+      const int d = i == 0 ? nd[0] : i == 1 ? nd[1] : i == 2 ? nd[2] : nd[3];
+      if (d < max_depth) {
+        const float s = word_score(x) + lp[k];
+        if (s != kNegInf) insert(cand_word(s, (uint32_t)k));
+      }
+    }
+    __syncwarp();  // the new nodes' depths are in place for the next round
+    n += popped;
+  }
+  // nodes that could not be built
+  for (int i = n + lane; i < N; i += 32) {
+    par[i] = -2;
+    if (cix) cix[i] = -2;
+    if (sco) sco[i] = CUDART_NAN_F;
+  }
+  if (lane == 0 && n_built) n_built[b] = n;
+}
+
 }  // namespace
 
 size_t tree_topw_smem_bytes(int N, int c) {
@@ -121,11 +292,16 @@ size_t tree_topw_smem_bytes(int N, int c) {
 cudaError_t launch_tree_topw(const float* cand_logp, int B, int N, int c, int w, int max_depth,
                              int32_t* parent, int32_t* cand_index, float* score, int32_t* n_built,
                              cudaStream_t stream) {
+  const int grid = (B + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (N * c <= kSlots * 32 && w <= kTop) {
+    tree_topw_warp_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(
+        cand_logp, B, N, c, w, max_depth, parent, cand_index, score, n_built);
+    return cudaGetLastError();
+  }
   const size_t smem = tree_topw_smem_bytes(N, c);
   cudaError_t err = cudaFuncSetAttribute(tree_topw_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const int grid = (B + kWarpsPerCta - 1) / kWarpsPerCta;
   tree_topw_kernel<<<grid, kWarpsPerCta * 32, smem, stream>>>(cand_logp, B, N, c, w, max_depth,
                                                                parent, cand_index, score, n_built);
   return cudaGetLastError();
