@@ -9,14 +9,20 @@
 //     w_j = exp(G_L - G_j),  gamma_L = exp(G_L),  G_j = sum_{i<=j} log alpha_{p_i},
 // a rank-L update of S0 that streams S0 in and S1 out once (HBM-bound).
 //
-// Grid: (Hv, B, dk / 64), 256 threads, four CTAs per SM.  Each CTA owns 64 rows
-// of one (b, h) state, bulk-copied into shared memory the moment the CTA
-// starts, so that the state
-// stream overlaps the path-dependent gathers, which take two steps: the path
-// and its length together, then (with indices range-checked) the parent-link
-// check, log alpha and the k and U rows of the path all at once.  Thread
-// (r8, c4) keeps an 8x4 register tile (rows r8*8.., columns c4*4..); k and U
-// rows are staged through shared memory in chunks of kChunk path entries.
+// One warp per block of 32 state rows (16 where dk is not a multiple of 32) of
+// one (b, h) state; no block-wide barrier anywhere, so that the latency of one
+// warp's two dependent gathers hides behind the other warps of the SM.  A warp
+// starts its S0 rows streaming into its shared-memory slot at once (cp.async,
+// no registers held), together with the path and its length; then, with the
+// entries known to be in range, the log alpha and parent links of the path
+// (into registers, one entry per lane) and the path's k and U rows (into the
+// warp's slots, eight entries at a time) all come in one round trip.  The
+// weights follow from a double-float prefix sum across the lanes; the block is
+// formed eight rows at a time and S1 leaves straight from the registers that
+// form it.  Only S0 in, S1 out and the path's rows cross HBM, each once.
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -25,274 +31,267 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kRowsPerCta = 64;  // each CTA owns half of a (b, h) state's rows
-constexpr int kChunk = 32;   // path entries staged per pass
+constexpr int kWarps = 2;  // warps per CTA
+constexpr int kThreads = 32 * kWarps;
+constexpr int kRB = 8;     // state rows formed at a time (a pass)
+constexpr int kMaxRows = 32;  // state rows of a warp's block
+constexpr int kBatch = 8;  // path entries whose k / U rows are on chip at a time
 
-// dynamic shared memory: S0 rows (kRowsPerCta x dv fp32) | k rows [kChunk][kRowsPerCta] |
-// u rows [kChunk][dv] | path, log alpha, w_j [path capacity] each
-constexpr size_t kSmemBytes =
-    (size_t)(kRowsPerCta * kMaxD + kChunk * kRowsPerCta + kChunk * kMaxD) * sizeof(float);
+// state rows of a warp's block: 32, or 16 where dk is not a multiple of 32
+__host__ __device__ inline int block_rows(int dk) { return dk % kMaxRows == 0 ? kMaxRows : 16; }
 
-// path capacity: Lmax rounded up to a whole scan block (at least kMaxN)
-__host__ __device__ inline int path_capacity(int Lmax) { return Lmax <= kMaxN ? kMaxN : (Lmax + 255) / 256 * 256; }
+// path entries a warp keeps (pj, G_j.hi then w_j, G_j.lo): Lmax rounded up to 32
+__host__ __device__ inline int path_capacity(int Lmax) { return Lmax <= 32 ? 32 : (Lmax + 31) / 32 * 32; }
 
-// One warp: G[e] = base + (inclusive prefix sum of la[j0 ..] up to entry
-// j0 + lane*8 + e), double-float, entries at or past L counting as 0.  Each lane
-// reads only its own eight entries.
-__device__ __forceinline__ void warp_scan_256(const float* la, int j0, int L, df base, int lane,
-                                              df (&G)[8]) {
-  df loc[8];
-  df run = {0.f, 0.f};
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int j = j0 + lane * 8 + e;
-    run = df_add(run, df{j < L ? la[j] : 0.f, 0.f});
-    loc[e] = run;
-  }
-  df pre = run;
+// per warp, in bytes: S0 rows [kMaxRows][dv] fp32 | U rows [kBatch][dv] fp32 |
+// k rows [kBatch][kMaxRows] (as given) | pj, G.hi / w, G.lo [cap] each
+__host__ __device__ inline uint32_t warp_smem_bytes(int dv, int tsize, int cap) {
+  return (uint32_t)kMaxRows * dv * 4 + (uint32_t)kBatch * dv * 4 +
+         (uint32_t)kBatch * kMaxRows * tsize + 3u * cap * 4;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_addr(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// inclusive double-float prefix sum of v across the warp's lanes
+__device__ __forceinline__ df warp_inclusive_scan(df v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     df up;
-    up.hi = __shfl_up_sync(0xffffffffu, pre.hi, o);
-    up.lo = __shfl_up_sync(0xffffffffu, pre.lo, o);
-    if (lane >= o) pre = df_add(pre, up);
+    up.hi = __shfl_up_sync(0xffffffffu, v.hi, o);
+    up.lo = __shfl_up_sync(0xffffffffu, v.lo, o);
+    if (lane >= o) v = df_add(v, up);
   }
-  df excl;
-  excl.hi = __shfl_up_sync(0xffffffffu, pre.hi, 1);
-  excl.lo = __shfl_up_sync(0xffffffffu, pre.lo, 1);
-  if (lane == 0) excl = df{0.f, 0.f};
-  excl = df_add(base, excl);
+  return v;
+}
+
+// the kRB entries of a staged k row, as fp32
+__device__ __forceinline__ void load_k(const __nv_bfloat16* p, float (&v)[kRB]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-  for (int e = 0; e < 8; ++e) G[e] = df_add(excl, loc[e]);
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load_k(const float* p, float (&v)[kRB]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 c = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 8)
 commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path_len,
               const int32_t* __restrict__ parent, const float* __restrict__ U,
               const T* __restrict__ k, const float* __restrict__ log_alpha,
               const float* S0, float* S1, gdn_tree_dims d, int32_t Lmax,
-              int32_t* dev_status, SeqLayout lay, WaitHooks hk) {
-  const uint64_t kWaitLimitNs = hk.limit_ns;  // bound on the S0 copy wait
-  // S0 and S1 may alias (in-place commit): the whole state is copied into
-  // shared memory before any element of S1 is written.
-  extern __shared__ __align__(128) float smem_f[];
-  float* sS0 = smem_f;                            // [rows][dv]
-  float* sK = sS0 + kRowsPerCta * kMaxD;          // [kChunk][rows]
-  float* sU = sK + kChunk * kRowsPerCta;          // [kChunk][dv]
-  const int cap = path_capacity(Lmax);
-  int* sPath = reinterpret_cast<int*>(sU + kChunk * kMaxD);  // [cap]
-  float* sLa = reinterpret_cast<float*>(sPath + cap);         // log alpha (then G_j.lo)
-  float* sW = sLa + cap;                                      // w_j (G_j.hi during the scan)
-  __shared__ uint64_t sBar;
-  __shared__ float sGamma;
-
+              int32_t* dev_status, SeqLayout lay) {
+  extern __shared__ __align__(16) uint8_t smem[];
   const int Nmax = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
-  const int h = blockIdx.x, b = blockIdx.y, row0 = blockIdx.z * kRowsPerCta;
-  const int hq = h / (Hv / Hqk);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rows = min(kRowsPerCta, dk - row0);
-  // this sequence's tree rows and state
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cap = path_capacity(Lmax);
+  uint8_t* ws = smem + (size_t)warp * warp_smem_bytes(dv, (int)sizeof(T), cap);
+  float* s_s = reinterpret_cast<float*>(ws);                    // [R][dv]
+  float* s_u = s_s + kMaxRows * dv;                             // [kBatch][dv]
+  T* s_k = reinterpret_cast<T*>(s_u + kBatch * dv);             // [kBatch][R]
+  int* s_pj = reinterpret_cast<int*>(s_k + kBatch * kMaxRows);  // [cap]
+  float* s_hi = reinterpret_cast<float*>(s_pj + cap);      // [cap]: G_j.hi, then w_j
+  float* s_lo = s_hi + cap;                                // [cap]: G_j.lo
+
+  // this warp's block: rows R rb .. R rb + R - 1 of state (b, h)
+  const int R = block_rows(dk), rbs = dk / R;
+  const long long item = (long long)blockIdx.x * kWarps + warp;
+  if (item >= (long long)d.B * Hv * rbs) return;
+  const int rb = (int)(item % rbs);
+  const int unit = (int)(item / rbs), b = unit / Hv, h = unit - b * Hv, hq = h / (Hv / Hqk);
   const int N = lay.count(b, Nmax), st = lay.state(b);
   if (N < 0 || st < 0) {
-    if (h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
-      atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
+    if (lane == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
     return;
   }
-  const size_t row = (size_t)lay.row0(b, Nmax);
-  const size_t urow = lay.urow0(b, h, Hv, Nmax);
-  const size_t sbase = ((size_t)st * Hv + h) * dk * dv;
+  const size_t row = (size_t)lay.row0(b, Nmax), urow = lay.urow0(b, h, Hv, Nmax);
+  // lane c < dv/4 owns columns 4c .. 4c+3 of the block's rows
+  const bool owner = lane < dv / 4;
+  const size_t sbase = ((size_t)st * Hv + h) * dk * dv + (size_t)rb * R * dv;
 
-  // ---- this CTA's rows of the (b, h) state start streaming in at once ----------
-  if (tid == 0) {
-    const uint32_t bytes = (uint32_t)(rows * dv * sizeof(float));
-    sm100::mbar_init(&sBar, 1);
-    sm100::mbar_fence_init();
-    sm100::mbar_arrive_expect_tx(&sBar, bytes);
-    if (b != hk.withhold_copy_seq) sm100::bulk_load(sS0, S0 + sbase + (size_t)row0 * dv, bytes, &sBar);
-  }
-
-  // ---- gather 1: path length and entries (range-checked); the first kThreads
-  //      entries are loaded together with the length ------------------------------
+  // ---- round trip 1: the block's S0 rows (into the slot), the path length and
+  // its first 32 entries.  S0 and S1 may alias (in-place commit): the block's
+  // rows are all on chip before any of its S1 rows is stored, and no two warps
+  // share a row.
+  for (int q = lane; q < R * dv / 4; q += 32) cp_async16(s_s + 4 * q, S0 + sbase + 4 * q);
   const int L = path_len[b];
-  int pj = -1;
-  if (tid < Lmax) pj = path[(size_t)b * Lmax + tid];
-  int bad = (L < 0 || L > N || L > Lmax);
-  if (!bad && tid < L) {
-    bad |= (pj < 0 || pj >= N);
-    sPath[tid] = pj;
-  }
-  if (!bad) {
-    for (int j = tid + kThreads; j < L; j += kThreads) {  // paths past kThreads entries
-      const int pv = path[(size_t)b * Lmax + j];
-      bad |= (pv < 0 || pv >= N);
-      sPath[j] = pv;
-    }
-  }
-  bad = __syncthreads_or(bad);
+  const int pj0 = lane < Lmax ? path[(size_t)b * Lmax + lane] : 0;
 
-  // ---- gather 2: chain check, log alpha, and the first chunk of k / u rows,
-  //      all issued together (indices are in range from here on) ----------------
-  // a root-to-node path is strictly increasing in a topological order; with the
-  // tree given it must also follow the parent links
-  if (!bad && tid < L) {
-    const int prev = tid == 0 ? -1 : sPath[tid - 1];
-    bad |= (tid > 0 && pj <= prev);
-    if (parent) bad |= (parent[row + pj] != prev);
-    sLa[tid] = log_alpha[(row + pj) * Hv + h];
-  }
-  if (!bad) {
-    for (int j = tid + kThreads; j < L; j += kThreads) {
-      const int pv = sPath[j], prev = sPath[j - 1];
-      bad |= (pv <= prev);
-      if (parent) bad |= (parent[row + pv] != prev);
-      sLa[j] = log_alpha[(row + pv) * Hv + h];
-    }
-  }
+  // k (the block's R entries) and U rows of path entries j0 .. j0 + nj - 1
+  // into the warp's slots, by 16-byte copies
   auto stage = [&](int j0, int nj) {
-    for (int e = tid; e < nj * (rows / 4); e += kThreads) {
-      const int jj = e / (rows / 4), c = (e % (rows / 4)) * 4;
-      const T* kr = k + ((row + sPath[j0 + jj]) * Hqk + hq) * dk + row0 + c;
-      *reinterpret_cast<float4*>(sK + jj * kRowsPerCta + c) =
-          make_float4(to_f32(kr[0]), to_f32(kr[1]), to_f32(kr[2]), to_f32(kr[3]));
+    const int uq = dv / 4, kq = R * (int)sizeof(T) / 16;
+    for (int q = lane; q < nj * uq; q += 32) {
+      const int jj = q / uq, c = q - jj * uq;
+      cp_async16(s_u + jj * dv + 4 * c, U + (urow + s_pj[j0 + jj]) * dv + 4 * c);
     }
-    for (int e = tid; e < nj * (dv / 4); e += kThreads) {
-      const int jj = e / (dv / 4), c = (e % (dv / 4)) * 4;
-      *reinterpret_cast<float4*>(sU + jj * dv + c) = *reinterpret_cast<const float4*>(
-          U + (urow + sPath[j0 + jj]) * dv + c);
+    for (int q = lane; q < nj * kq; q += 32) {
+      const int jj = q / kq, c = q - jj * kq;
+      const T* src = k + ((row + s_pj[j0 + jj]) * Hqk + hq) * dk + rb * R;
+      cp_async16(reinterpret_cast<uint8_t*>(s_k + jj * R) + 16 * c,
+                 reinterpret_cast<const uint8_t*>(src) + 16 * c);
     }
   };
-  if (!bad) stage(0, min(kChunk, L));
-  bad = __syncthreads_or(bad);
-  if (bad && h == 0 && blockIdx.z == 0 && tid == 0 && dev_status)
-    atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_PATH);
+
+  // ---- round trip 2, 32 entries (one a lane) at a time: range check; the
+  // first batch of k / U rows; log alpha and parent links; chain check (a
+  // root-to-node path is strictly increasing in a topological order and, with
+  // the tree given, follows the parent links); G_j, the inclusive double-float
+  // prefix sums of log alpha along the path
+  int bad = (L < 0 || L > N || L > Lmax);
+  const int nL = bad ? 0 : L;
+  df carry = {0.f, 0.f};
+  int last = -1;  // the previous chunk's last entry
+  for (int c0 = 0; c0 < nL; c0 += 32) {
+    const int e = c0 + lane;
+    const bool live = e < nL;
+    const int pj = c0 == 0 ? pj0 : (live ? path[(size_t)b * Lmax + e] : 0);
+    if (__any_sync(0xffffffffu, live && (pj < 0 || pj >= N))) {
+      bad = 1;
+      break;
+    }
+    if (live) s_pj[e] = pj;
+    if (c0 == 0) {
+      __syncwarp();
+      stage(0, min(kBatch, nL));
+    }
+    float la = 0.f;
+    int par = -1;
+    if (live) {
+      la = log_alpha[(row + pj) * Hv + h];
+      if (parent) par = parent[row + pj];
+    }
+    int prev = __shfl_up_sync(0xffffffffu, pj, 1);
+    if (lane == 0) prev = last;
+    if (__any_sync(0xffffffffu,
+                   live && ((e > 0 && pj <= prev) || (parent != nullptr && par != prev)))) {
+      bad = 1;
+      break;
+    }
+    const df G = df_add(carry, warp_inclusive_scan(df{la, 0.f}, lane));
+    if (live) {
+      s_hi[e] = G.hi;
+      s_lo[e] = G.lo;
+    }
+    // (lanes past the path add zeros: lane 31 holds G of the chunk's last entry)
+    carry.hi = __shfl_sync(0xffffffffu, G.hi, 31);
+    carry.lo = __shfl_sync(0xffffffffu, G.lo, 31);
+    last = __shfl_sync(0xffffffffu, pj, 31);
+  }
   if (bad) {
-    if (tid == 0) sm100::mbar_wait(&sBar, 0, kWaitLimitNs);  // drain the copy
-    return;
-  }
-
-  // ---- G_j: inclusive double-float prefix sums of log alpha along the path ------
-  if (warp == 0) {
-    if (L <= 256) {
-      // lane l owns entries l*8 .. l*8+7
-      df G[8];
-      warp_scan_256(sLa, 0, L, df{0.f, 0.f}, lane, G);
-      // G_L lives in the lane that owns entry L-1
-      const int owner = L > 0 ? (L - 1) >> 3 : 0, slot = L > 0 ? (L - 1) & 7 : 0;
-      df mine = G[0];
-#pragma unroll
-      for (int e = 1; e < 8; ++e)
-        if (e == slot) mine = G[e];
-      df GL;
-      GL.hi = __shfl_sync(0xffffffffu, mine.hi, owner);
-      GL.lo = __shfl_sync(0xffffffffu, mine.lo, owner);
-      if (L == 0) GL = df{0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = lane * 8 + e;
-        if (j < L) sW[j] = expf(df_diff(GL, G[e]));
-      }
-      if (lane == 0) sGamma = expf(df_value(GL));
-    } else {
-      // blocks of 256 entries with a running carry; G_j parks in (sW, sLa)
-      df carry = {0.f, 0.f};
-      for (int j0 = 0; j0 < L; j0 += 256) {
-        df G[8];
-        warp_scan_256(sLa, j0, L, carry, lane, G);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = j0 + lane * 8 + e;
-          if (j < L) {
-            sW[j] = G[e].hi;
-            sLa[j] = G[e].lo;
-          }
-        }
-        __syncwarp();
-        const int last = min(L, j0 + 256) - 1;
-        carry = df{sW[last], sLa[last]};
-      }
-      const df GL = carry;
-      for (int j = lane; j < L; j += 32) sW[j] = expf(df_diff(GL, df{sW[j], sLa[j]}));
-      if (lane == 0) sGamma = expf(df_value(GL));
-    }
-  }
-  __syncthreads();
-
-  // ---- S1 = gamma S0 + K_P^T diag(w) U_P ------------------------------------------
-  // thread (r8, c4): rows r8*8 .. r8*8+7, columns c4*4 .. c4*4+3
-  const int r8 = tid / 32, c4 = tid % 32;
-  const bool active = (r8 * 8 < rows) && (c4 * 4 < dv);
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int j0 = 0; j0 < L; j0 += kChunk) {
-    const int nj = min(kChunk, L - j0);
-    if (j0 > 0) {
-      __syncthreads();
-      stage(j0, nj);
-      __syncthreads();
-    }
-    if (active) {
-      for (int jj = 0; jj < nj; ++jj) {
-        const float w = sW[j0 + jj];
-        const float4 k0 = *reinterpret_cast<const float4*>(sK + jj * kRowsPerCta + r8 * 8);
-        const float4 k1 = *reinterpret_cast<const float4*>(sK + jj * kRowsPerCta + r8 * 8 + 4);
-        const float4 uu = *reinterpret_cast<const float4*>(sU + jj * dv + c4 * 4);
-        const float kk[8] = {w * k0.x, w * k0.y, w * k0.z, w * k0.w,
-                             w * k1.x, w * k1.y, w * k1.z, w * k1.w};
-        const float ul[4] = {uu.x, uu.y, uu.z, uu.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(kk[i], ul[j], acc[i][j]);
-      }
-    }
-  }
-  const float gamma = sGamma;
-  const bool landed = sm100::mbar_wait(&sBar, 0, kWaitLimitNs);
-  if (!landed) {
-    if (tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
+    cp_async_wait_all();  // the S0 rows and the copies of a batch already staged
+    if (lane == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_PATH);
     return;  // S1 left unwritten
   }
-  if (active) {
+
+  // ---- w_j = exp(G_L - G_j), gamma_L = exp(G_L) (G_L = carry; each lane
+  // rewrites the entries it wrote)
+  for (int e = lane; e < nL; e += 32) s_hi[e] = expf(df_diff(carry, df{s_hi[e], s_lo[e]}));
+  const float gamma = expf(df_value(carry));
+
+  // ---- S1 = gamma S0 + K_P^T diag(w) U_P on the block's rows, kRB rows (a
+  // pass) at a time; paths past one batch of entries keep the partial sums of
+  // the earlier batches in the S0 slot
+  const int nb = nL == 0 ? 1 : (nL + kBatch - 1) / kBatch;
+  for (int bi = 0; bi < nb; ++bi) {
+    const int j0 = bi * kBatch, nj = min(kBatch, nL - j0);
+    if (bi > 0) {  // the next batch's rows
+      __syncwarp();
+      stage(j0, nj);
+    }
+    cp_async_wait_all();
+    __syncwarp();  // every lane's copies (and weights) in place
+    if (owner) {
+      const bool first = bi == 0, final_ = bi == nb - 1;
+      for (int r0 = 0; r0 < R; r0 += kRB) {
+        float acc[kRB][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = r8 * 8 + i;
-      const float4 s0 = *reinterpret_cast<const float4*>(sS0 + row * dv + c4 * 4);
-      float4 s1;
-      s1.x = fmaf(gamma, s0.x, acc[i][0]);
-      s1.y = fmaf(gamma, s0.y, acc[i][1]);
-      s1.z = fmaf(gamma, s0.z, acc[i][2]);
-      s1.w = fmaf(gamma, s0.w, acc[i][3]);
-      *reinterpret_cast<float4*>(S1 + sbase + (size_t)(row0 + row) * dv + c4 * 4) = s1;
+        for (int i = 0; i < kRB; ++i)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
+        for (int jj = 0; jj < nj; ++jj) {
+          const float w = s_hi[j0 + jj];
+          const float4 uv = *reinterpret_cast<const float4*>(s_u + jj * dv + 4 * lane);
+          float kv[kRB];
+          load_k(s_k + jj * R + r0, kv);
+#pragma unroll
+          for (int i = 0; i < kRB; ++i) {
+            const float kk = w * kv[i];
+            acc[i][0] = fmaf(kk, uv.x, acc[i][0]);
+            acc[i][1] = fmaf(kk, uv.y, acc[i][1]);
+            acc[i][2] = fmaf(kk, uv.z, acc[i][2]);
+            acc[i][3] = fmaf(kk, uv.w, acc[i][3]);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kRB; ++i) {
+          float4* sp = reinterpret_cast<float4*>(s_s + (r0 + i) * dv + 4 * lane);
+          const float4 s = *sp;
+          const float4 v =
+              first ? make_float4(fmaf(gamma, s.x, acc[i][0]), fmaf(gamma, s.y, acc[i][1]),
+                                  fmaf(gamma, s.z, acc[i][2]), fmaf(gamma, s.w, acc[i][3]))
+                    : make_float4(s.x + acc[i][0], s.y + acc[i][1], s.z + acc[i][2],
+                                  s.w + acc[i][3]);
+          if (final_)
+            __stcs(reinterpret_cast<float4*>(S1 + sbase + (size_t)(r0 + i) * dv + 4 * lane), v);
+          else
+            *sp = v;
+        }
+      }
     }
   }
 }
 
 }  // namespace
 
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int n = (dev >= 0 && dev < 64) ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
-  const dim3 grid(a.d.Hv, a.d.B, (a.d.dk + kRowsPerCta - 1) / kRowsPerCta);
-  const size_t smem = kSmemBytes + (size_t)path_capacity(a.Lmax) * 3 * sizeof(float);
-  const WaitHooks hk = wait_hooks();
+  const long long n_blocks = (long long)a.d.B * a.d.Hv * (a.d.dk / block_rows(a.d.dk));
+  if (n_blocks == 0) return cudaSuccess;
+  const long long grid = (n_blocks + kWarps - 1) / kWarps;
+  if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  const int tsize = a.d.dtype == GDN_TREE_BF16 ? 2 : 4;
+  const size_t smem = (size_t)kWarps * warp_smem_bytes(a.d.dv, tsize, path_capacity(a.Lmax));
   cudaError_t err;
   if (a.d.dtype == GDN_TREE_BF16) {
     err = cudaFuncSetAttribute(commit_kernel<__nv_bfloat16>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    commit_kernel<__nv_bfloat16><<<grid, kThreads, smem, stream>>>(
+    commit_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, smem, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const __nv_bfloat16*>(a.k),
-        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay, hk);
+        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
   } else {
     err = cudaFuncSetAttribute(commit_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err != cudaSuccess) return err;
-    commit_kernel<float><<<grid, kThreads, smem, stream>>>(
+    commit_kernel<float><<<(unsigned)grid, kThreads, smem, stream>>>(
         a.path, a.path_len, a.parent, a.U, static_cast<const float*>(a.k),
-        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay, hk);
+        a.log_alpha, a.S0, a.S1, a.d, a.Lmax, a.dev_status, a.lay);
   }
   return cudaGetLastError();
 }

@@ -84,7 +84,6 @@ WaitHooks wait_hooks() {
       h.withhold_node = n;
     }
   }
-  if (const char* e = getenv("GDN_TREE_TEST_WITHHOLD_COPY")) h.withhold_copy_seq = atoi(e);
   return h;
 }
 

@@ -96,12 +96,9 @@ struct CommitVerifyArgs {
 //       (b * Hv + h) never arrives on that node's solve barrier, so the waits of
 //       its children and grandchildren run out (thread arrivals only: no copy or
 //       MMA is left in flight)
-//   GDN_TREE_TEST_WITHHOLD_COPY=<b>        the commit CTAs of sequence b expect their
-//       state copy but never issue it, so the wait for it runs out
 struct WaitHooks {
   uint64_t limit_ns = 2000000000ull;
   int withhold_unit = -1, withhold_node = -1;
-  int withhold_copy_seq = -1;
 };
 WaitHooks wait_hooks();
 
@@ -119,6 +116,9 @@ bool verify_tc_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+
+// streaming multiprocessors of the current device (cached per device; 0: no device)
+int sm_count();
 
 // top-w best-first draft-tree construction
 size_t tree_topw_smem_bytes(int N, int c);

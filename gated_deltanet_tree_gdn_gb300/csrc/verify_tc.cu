@@ -1268,19 +1268,6 @@ bool verify_tc_supported(const gdn_tree_dims& d) {
 
 namespace {
 
-// streaming multiprocessors of the current device (cached per device)
-int sm_count() {
-  static std::atomic<int> cached[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  int n = (dev >= 0 && dev < 64) ? cached[dev].load(std::memory_order_relaxed) : 0;
-  if (n == 0) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
-  }
-  return n;
-}
-
 template <bool kFused>
 cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t stream) {
   CUtensorMap tmQ, tmK, tmV, tmS, tmS1;

@@ -129,7 +129,9 @@ int gdn_tree_verify(const void *q, const void *k, const void *v,
  * given, the path must start at a node with parent -1 and follow parent
  * links, else the sequence gets GDN_TREE_STATUS_BAD_PATH.  path_len[b] == 0
  * gives S1 = S0.  S1 may alias S0 exactly (in-place commit); any other
- * overlap is undefined.  dev_status[b] (if non-NULL) is set for every b.
+ * overlap is undefined.  dev_status[b] (if non-NULL) is set for every b, to
+ * GDN_TREE_STATUS_OK, BAD_PATH or BAD_LAYOUT (this kernel has no on-device
+ * wait, so it never reports TIMEOUT).
  */
 int gdn_tree_commit(const int32_t *path, const int32_t *path_len,
                     const int32_t *parent, const float *U, const void *k,
