@@ -125,10 +125,16 @@ def kernel_source_sha() -> str:
 
 def verify_kernel_name(w: W.Workload) -> str:
     """The verify kernel the library dispatches for this shape (mirrors the
-    C-ABI's rule: tensor-core kernel for bf16, dk = dv = 128, N <= 128)."""
-    if (w.dtype == W.BF16 and w.dk == 128 and w.dv == 128 and w.N <= 128
-            and os.environ.get("GDN_TREE_KERNEL", "auto") != "generic"):
-        return "verify_tc_kernel"
+    C-ABI's rule: for bf16 with dk = dv = 128, the tensor-core kernel up to 128
+    nodes and the 256-node kernel up to 256)."""
+    forced = os.environ.get("GDN_TREE_KERNEL", "auto")
+    if w.dtype == W.BF16 and w.dk == 128 and w.dv == 128 and forced not in ("generic", "long"):
+        if w.N <= 128 and forced != "mid":
+            return "verify_tc_kernel"
+        if w.N <= 256:
+            return "verify_mid_kernel"
+    if w.N > 256 or forced == "long":
+        return "verify_long_kernel"
     return "verify_generic_kernel"
 
 
@@ -137,7 +143,7 @@ def iteration_kernel_name(w: W.Workload) -> str:
     with the delayed commitment fused in, where it takes the shape)."""
     if verify_kernel_name(w) == "verify_tc_kernel":
         return "verify_tc_kernel<fused commit>"
-    return "commit_kernel + verify_generic_kernel"
+    return "commit_kernel + " + verify_kernel_name(w)
 
 
 def arithmetic_dtype(kernel: str) -> str:
@@ -539,6 +545,32 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     lv_us = 1e3 * statistics.mean(evl[i][0].elapsed_time(evl[i][1]) for i in range(1, Kl + 1))
     lc_us = 1e3 * statistics.mean(evl[i][1].elapsed_time(evl[i][2]) for i in range(1, Kl + 1))
 
+    # the stress shapes: 64 sequences of 256-node trees mixing 256-deep chains,
+    # stars and random trees, strong decay and beta up to 0.99 (the CUDA-core
+    # on-chip kernel: the tensor-core kernel takes trees of up to 128 nodes)
+    w4 = W.make_config(4)
+    x4 = {kk: torch.from_numpy(np.ascontiguousarray(getattr(w4, kk))).to(
+        device=dev, dtype=dt if kk in ("q", "k", "v") else None)
+        for kk in ("q", "k", "v", "log_alpha", "beta", "parent", "S0", "path", "path_len")}
+    o4 = torch.empty((w4.B, w4.N, w4.Hv, w4.dv), dtype=dt, device=dev)
+    U4 = torch.empty((w4.B, w4.Hv, w4.N, w4.dv), dtype=torch.float32, device=dev)
+    S14 = torch.empty_like(x4["S0"])
+    K4 = max(3, min(K, 10))
+    ev4 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K4 + 1)]
+    for i in range(K4 + 1):  # the first iteration is a warm-up
+        flush.zero_()
+        ev4[i][0].record(stream)
+        gt.verify(x4["q"], x4["k"], x4["v"], x4["log_alpha"], x4["beta"], x4["parent"],
+                  x4["S0"], o=o4, U=U4)
+        ev4[i][1].record(stream)
+        gt.commit(x4["path"], x4["path_len"], U4, x4["k"], x4["log_alpha"], x4["S0"], S1=S14,
+                  parent=x4["parent"])
+        ev4[i][2].record(stream)
+    torch.cuda.synchronize()
+    c4v_us = 1e3 * statistics.mean(ev4[i][0].elapsed_time(ev4[i][1]) for i in range(1, K4 + 1))
+    c4c_us = 1e3 * statistics.mean(ev4[i][1].elapsed_time(ev4[i][2]) for i in range(1, K4 + 1))
+    del x4, o4, U4, S14
+
     # end to end through the public API: every step copies the tree's inputs and
     # the accepted path from pinned host memory (the recurrent state stays
     # resident on the device, as in a decoding loop), runs one decoding
@@ -698,6 +730,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "nodes_per_s": wl.B * wl.N / ((lv_us + lc_us) * 1e-6),
             "verify_roofline_frac": verify_bytes(wl) / (lv_us * 1e-6) / (hbm * 1e9),
             "commit_roofline_frac": commit_bytes(wl) / (lc_us * 1e-6) / (hbm * 1e9)}
+        line["config4"] = {
+            "kernel": verify_kernel_name(w4) + " + commit_kernel",
+            "workload": W.CONFIG_NAMES[4] + ": B=64 seqs x Hv=32 v-heads (Hqk=16), dk=dv=128, "
+                        "bf16, N=256-node trees (256-deep chains, stars, random trees), "
+                        "log alpha down to -4, beta up to 0.99",
+            "verify_us": c4v_us, "commit_us": c4c_us,
+            "nodes_per_s": w4.B * w4.N / ((c4v_us + c4c_us) * 1e-6),
+            "verify_roofline_frac": verify_bytes(w4) / (c4v_us * 1e-6) / (hbm * 1e9),
+            "commit_roofline_frac": commit_bytes(w4) / (c4c_us * 1e-6) / (hbm * 1e9)}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)

@@ -87,15 +87,18 @@ WaitHooks wait_hooks() {
   return h;
 }
 
-// GDN_TREE_KERNEL=generic forces the CUDA-core kernels and GDN_TREE_KERNEL=long
-// the chunked one (used by the tests to cover every kernel on the same shapes);
-// the default picks the tensor-core kernel whenever it takes the shape, the
-// on-chip CUDA-core kernel up to kMaxNHost nodes and the chunked one beyond.
+// GDN_TREE_KERNEL=generic forces the general CUDA-core kernel, =mid the
+// 256-node bf16 one and =long the chunked one (used by the tests to cover every
+// kernel on the same shapes); the default picks the tensor-core kernel whenever
+// it takes the shape, then the 256-node bf16 kernel, the general on-chip kernel
+// up to kMaxNHost nodes and the chunked one beyond.
 static bool kernel_forced(const char* name) {
   const char* e = getenv("GDN_TREE_KERNEL");
   return e && strcmp(e, name) == 0;
 }
-static bool force_generic() { return kernel_forced("generic") || kernel_forced("long"); }
+static bool force_generic() {
+  return kernel_forced("generic") || kernel_forced("long") || kernel_forced("mid");
+}
 
 // the tensor-core kernel takes the shape (packed rows: at least one row, for its
 // tensor maps)
@@ -105,6 +108,8 @@ static bool tc_takes(const VerifyArgs& a) {
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   if (tc_takes(a)) return launch_verify_tc(a, stream);
+  if (!kernel_forced("generic") && !kernel_forced("long") && verify_mid_supported(a.d))
+    return launch_verify_mid(a, stream);
   if (a.d.N > kMaxNHost || kernel_forced("long")) return launch_verify_long(a, stream);
   return launch_verify_generic(a, stream);
 }

@@ -112,6 +112,10 @@ cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream);
 size_t verify_long_smem_bytes(int N, int dk, int dv);
 cudaError_t launch_verify_long(const VerifyArgs& a, cudaStream_t stream);
 
+// bf16 trees of up to 256 nodes with dk = dv = 128 (CUDA cores, on chip)
+bool verify_mid_supported(const gdn_tree_dims& d);
+cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream);
+
 bool verify_tc_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 

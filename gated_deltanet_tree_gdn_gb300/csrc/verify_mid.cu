@@ -1,0 +1,470 @@
+// verify_mid.cu -- tree verification for bf16 trees of up to 256 nodes with
+// dk = dv = 128: the trees the tensor-core kernel (up to 128 nodes) does not take.
+//
+// Method: "DFlash-TfM: Trees from Marginals", section 3 ("Soluzione"): with
+// g_t the log-decay summed along the root-to-t path and gamma_t = e^{g_t},
+//   R = diag(beta)(V - diag(gamma) K S0),   (I + X) U = R,
+//   O = diag(gamma) Q S0 + Y U,
+//   X[t,s] = beta_t e^{g_t - g_s} k_t.k_s   (s a strict ancestor of t),
+//   Y[t,s] = e^{g_t - g_s} q_t.k_s         (s on the root-to-t path, t included).
+//
+// One CTA (512 threads) per (sequence b, v-head h), in four stages:
+//  1. the tree: parent links checked; strict-ancestor bitsets and g by pointer
+//     jumping; depths, and the nodes ordered by depth (the solve's task order);
+//  2. R and the output seeds gamma_t q_t^T S0 for every node at once, S0 in
+//     shared memory, four nodes per warp pass (each S0 row read once for four
+//     nodes); R stays in shared memory, the seeds park in the node's U row in
+//     global memory (overwritten by u_t at the end);
+//  3. K into shared memory (bf16, 16-byte chunks XOR-swizzled by row, so that
+//     32 lanes reading 32 rows at once hit distinct banks);
+//  4. the solve as a streaming dataflow over the tree, one warp per node in
+//     depth order: lane j forms X[t,s] and Y[t,s] for the path entries
+//     s = j, j+32, ... from the k rows on chip (no wait: K is static); then the
+//     warp walks t's path from the root, four ancestors at a time, waiting
+//     (bounded, on an mbarrier) only for the last of the four -- a path's nodes
+//     complete in path order -- and sums their terms into u_t and o_t (lane owns
+//     4 of the 128 columns); u_t is published and t's mbarrier arrived on, and
+//     o_t = seed + sum Y u closes the node.  A node keeps pace with its
+//     ancestors as they complete, so a link of a deep chain costs one group of
+//     terms, not the whole ancestor sum.
+// The unfinished node of lowest depth order never waits on an unfinished node,
+// so the waits cannot cycle.
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kD = 128;          // dk = dv
+constexpr int kMidN = 256;       // largest tree
+constexpr int kGroups = kMidN / 32;  // ancestor groups of 32 (one ancestor a lane)
+static_assert(kMidN <= kMaxN, "tree_prepare's bitsets hold kMaxN nodes");
+
+struct MidSmem {
+  // byte offsets into dynamic shared memory
+  size_t U, SK, stage, parent, jump, g, beta, la, anc, depth, order, bar, flag, total;
+};
+
+__host__ __device__ inline size_t align16m(size_t x) { return (x + 15) & ~size_t(15); }
+
+__host__ __device__ inline MidSmem mid_smem_layout(int N) {
+  MidSmem L;
+  const int W = (N + 31) / 32;
+  size_t o = 0;
+  L.U = o;      o = align16m(o + sizeof(float) * N * kD);           // R, then U
+  L.SK = o;     o = align16m(o + sizeof(float) * kD * kD);          // S0, then K (bf16)
+  L.stage = o;  o = align16m(o + sizeof(float) * kWarps * kD);      // q_t of each warp
+  L.parent = o; o = align16m(o + sizeof(int) * N);
+  L.jump = o;   o = align16m(o + sizeof(int) * N);
+  L.g = o;      o = align16m(o + sizeof(df) * N);
+  L.beta = o;   o = align16m(o + sizeof(float) * N);
+  L.la = o;     o = align16m(o + sizeof(float) * N);
+  L.anc = o;    o = align16m(o + sizeof(uint32_t) * N * W);
+  L.depth = o;  o = align16m(o + sizeof(int) * N);
+  L.order = o;  o = align16m(o + sizeof(int) * (N + kMidN + 1));   // order, then level starts
+  L.bar = o;    o = align16m(o + sizeof(uint64_t) * N);
+  L.flag = o;   o = align16m(o + sizeof(int) * 4);
+  L.total = o;
+  return L;
+}
+
+// byte offset of 16-byte chunk c (of 16) of k row r in the swizzled K tile
+__device__ __forceinline__ uint32_t k_chunk(int r, int c) {
+  return (uint32_t)r * (kD * 2) + (uint32_t)((c ^ (r & 15)) << 4);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 q, float (&v)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ float4 fma4m(float a, float4 x, float4 acc) {
+  acc.x = fmaf(a, x.x, acc.x);
+  acc.y = fmaf(a, x.y, acc.y);
+  acc.z = fmaf(a, x.z, acc.z);
+  acc.w = fmaf(a, x.w, acc.w);
+  return acc;
+}
+
+__device__ __forceinline__ void cp_async16m(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_addr(dst)),
+               "l"(src)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                  const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
+                  const float* __restrict__ beta, const int32_t* __restrict__ parent,
+                  const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
+                  float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
+                  WaitHooks hk) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int hq = h / (Hv / Hqk);
+  const int unit = b * Hv + h;
+  const MidSmem L = mid_smem_layout(Nmax);
+  float* sU = reinterpret_cast<float*>(smem + L.U);
+  unsigned char* sSK = smem + L.SK;
+  float* sStage = reinterpret_cast<float*>(smem + L.stage);
+  int* sPar = reinterpret_cast<int*>(smem + L.parent);
+  int* sJump = reinterpret_cast<int*>(smem + L.jump);
+  df* sG = reinterpret_cast<df*>(smem + L.g);
+  float* sBeta = reinterpret_cast<float*>(smem + L.beta);
+  float* sLa = reinterpret_cast<float*>(smem + L.la);
+  uint32_t* sAnc = reinterpret_cast<uint32_t*>(smem + L.anc);
+  int* sDepth = reinterpret_cast<int*>(smem + L.depth);
+  int* sOrder = reinterpret_cast<int*>(smem + L.order);
+  int* sLevel = sOrder + Nmax;  // [kMidN + 1]
+  uint64_t* sBar = reinterpret_cast<uint64_t*>(smem + L.bar);
+  int* sFlag = reinterpret_cast<int*>(smem + L.flag);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // this sequence's rows and state
+  const int N = lay.count(b, Nmax), st = lay.state(b);
+  if (N < 0 || st < 0) {
+    if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
+    return;
+  }
+  const int W = (N + 31) / 32;
+  const size_t row = (size_t)lay.row0(b, Nmax);
+  float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
+
+  // S0 starts streaming into shared memory at once
+  const float* S0bh = S0 + ((size_t)st * Hv + h) * kD * kD;
+  for (int i = tid; i < kD * kD / 4; i += kThreads)
+    cp_async16m(sSK + 16 * i, S0bh + 4 * i);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
+  // ---- 1. the tree ------------------------------------------------------------
+  int bad = 0;
+  if (tid < N) {
+    const int p = parent[row + tid];
+    sPar[tid] = p;
+    bad = (p < -1 || p >= tid);
+    sBeta[tid] = beta[(row + tid) * Hv + h];
+    sLa[tid] = log_alpha[(row + tid) * Hv + h];
+  }
+  if (tid <= kMidN) sLevel[tid] = 0;
+  if (tid == 0) sFlag[0] = 0;
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+  tree_prepare(sPar, N, W, sLa, sJump, sAnc, sG);
+  // depth, level sizes, then the depth order (index order within a level)
+  if (tid < N) {
+    int dep = 1;
+    for (int i = 0; i < W; ++i) dep += __popc(sAnc[tid * W + i]);
+    sDepth[tid] = dep;
+    atomicAdd(&sLevel[dep], 1);
+    sm100::mbar_init(&sBar[tid], 1);
+  }
+  sm100::mbar_fence_init();
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the level sizes, in place (depths 1 .. N)
+    int carry = 0;
+    for (int base = 0; base <= kMidN; base += 32) {
+      const int i = base + lane;
+      const int c = i <= kMidN ? sLevel[i] : 0;
+      int x = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (i <= kMidN) sLevel[i] = carry + x - c;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+  }
+  __syncthreads();
+  if (tid < N) {
+    const int dep = sDepth[tid];
+    int rank = 0;
+    for (int s = 0; s < tid; ++s) rank += (sDepth[s] == dep);
+    sOrder[sLevel[dep] + rank] = tid;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // ---- 2. R = diag(beta)(V - diag(gamma) K S0) and seeds gamma Q S0 -----------
+  // four nodes a warp pass; lane owns columns 4 lane .. 4 lane + 3
+  {
+    const float* sS0 = reinterpret_cast<const float*>(sSK);
+    for (int n0 = 4 * warp; n0 < N; n0 += 4 * kWarps) {
+      float4 ak[4], aq[4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) ak[n] = aq[n] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // the four k and q rows, eight entries (16 bytes) at a time, the next eight
+      // in flight while these are used
+      const __nv_bfloat16* kr[4];
+      const __nv_bfloat16* qr[4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int t = min(n0 + n, N - 1);  // (a node past the tree repeats the last)
+        kr[n] = k + ((row + t) * Hqk + hq) * kD;
+        qr[n] = q + ((row + t) * Hqk + hq) * kD;
+      }
+      uint4 kc[4], qc[4];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        kc[n] = *reinterpret_cast<const uint4*>(kr[n]);
+        qc[n] = *reinterpret_cast<const uint4*>(qr[n]);
+      }
+      for (int i0 = 0; i0 < kD; i0 += 8) {
+        uint4 kx[4], qx[4];
+        const int in = i0 + 8 < kD ? i0 + 8 : i0;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          kx[n] = *reinterpret_cast<const uint4*>(kr[n] + in);
+          qx[n] = *reinterpret_cast<const uint4*>(qr[n] + in);
+        }
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          const float4 s = *reinterpret_cast<const float4*>(sS0 + (i0 + ii) * kD + 4 * lane);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            const uint32_t kw = (&kc[n].x)[ii >> 1], qw = (&qc[n].x)[ii >> 1];
+            const float kf = __uint_as_float((ii & 1) ? (kw & 0xffff0000u) : (kw << 16));
+            const float qf = __uint_as_float((ii & 1) ? (qw & 0xffff0000u) : (qw << 16));
+            ak[n] = fma4m(kf, s, ak[n]);
+            aq[n] = fma4m(qf, s, aq[n]);
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          kc[n] = kx[n];
+          qc[n] = qx[n];
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int t = n0 + n;
+        if (t < N) {
+          const float gam = expf(df_value(sG[t]));
+          const float bt = sBeta[t];
+          const uint2 vv = *reinterpret_cast<const uint2*>(v + ((row + t) * Hv + h) * kD + 4 * lane);
+          const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
+          const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
+          *reinterpret_cast<float4*>(sU + t * kD + 4 * lane) =
+              make_float4(bt * (v0 - gam * ak[n].x), bt * (v1 - gam * ak[n].y),
+                          bt * (v2 - gam * ak[n].z), bt * (v3 - gam * ak[n].w));
+          *reinterpret_cast<float4*>(Ubh + (size_t)t * kD + 4 * lane) =
+              make_float4(gam * aq[n].x, gam * aq[n].y, gam * aq[n].z, gam * aq[n].w);
+        }
+      }
+    }
+  }
+  __syncthreads();  // S0 is no longer needed
+
+  // ---- 3. K into shared memory (bf16, swizzled) ---------------------------------
+  for (int e = tid; e < N * 16; e += kThreads) {
+    const int r = e >> 4, c = e & 15;
+    cp_async16m(sSK + k_chunk(r, c), k + ((row + r) * Hqk + hq) * kD + 8 * c);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // ---- 4. the solve -----------------------------------------------------------
+  bool timed_out = false;
+  auto wait_final = [&](int node) {
+    if (!sm100::mbar_wait(&sBar[node], 0, hk.limit_ns)) timed_out = true;
+  };
+  float* qs = sStage + warp * kD;
+  // q of the warp's next node, loaded one node ahead
+  auto q_of = [&](int task) {
+    return task < N ? *reinterpret_cast<const uint2*>(q + ((row + sOrder[task]) * Hqk + hq) * kD +
+                                                      4 * lane)
+                    : make_uint2(0u, 0u);
+  };
+  uint2 qnext = q_of(warp);
+  for (int task = warp; task < N; task += kWarps) {
+    const int t = sOrder[task];
+    const int nA = sDepth[t] - 1;  // strict ancestors
+    const df gt = sG[t];
+    const float bt = sBeta[t];
+    // the seed (parked in t's U row) comes while the node is worked on
+    float* urow = Ubh + (size_t)t * kD + 4 * lane;
+    const float4 seed = *reinterpret_cast<const float4*>(urow);
+    // q_t into the warp's stage (fp32); the next node's q starts coming
+    {
+      const uint2 qq = qnext;
+      *reinterpret_cast<float4*>(qs + 4 * lane) =
+          make_float4(__uint_as_float(qq.x << 16), __uint_as_float(qq.x & 0xffff0000u),
+                      __uint_as_float(qq.y << 16), __uint_as_float(qq.y & 0xffff0000u));
+      qnext = q_of(task + kWarps);
+    }
+    __syncwarp();
+    // X[t,s] and Y[t,s] for path entry n (strict ancestors in index order, then
+    // t itself), left in lane n % 32 as the n / 32-th of sn / xn / yn
+    int sn[kGroups];
+    float xn[kGroups], yn[kGroups];
+    const uint32_t* anc = sAnc + t * W;
+    // the n-th strict ancestor of t (n < nA): the n-th set bit of its bitset
+    auto nth_ancestor = [&](int n) {
+      int left = n;
+      for (int wi = 0; wi < W; ++wi) {
+        uint32_t bits = anc[wi];
+        const int c = __popc(bits);
+        if (left < c) {
+          for (int r = 0; r < left; ++r) bits &= bits - 1;
+          return wi * 32 + __ffs(bits) - 1;
+        }
+        left -= c;
+      }
+      return t;
+    };
+    // the two dots of entry s over 16-byte chunks c0 .. c1 - 1
+    auto dots = [&](int s, int c0, int c1, float& dkk, float& dqk) {
+      for (int c = c0; c < c1; ++c) {
+        float ks[8], kt[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sSK + k_chunk(s, c)), ks);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sSK + k_chunk(t, c)), kt);
+        const float4 q0 = *reinterpret_cast<const float4*>(qs + 8 * c);
+        const float4 q1 = *reinterpret_cast<const float4*>(qs + 8 * c + 4);
+        const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          dkk = fmaf(kt[e], ks[e], dkk);
+          dqk = fmaf(qv[e], ks[e], dqk);
+        }
+      }
+    };
+    const int nP = nA + 1;  // path entries
+    if (nP <= 16) {
+      // a short path: 32 / P lanes share an entry (P >= nP a power of two), each
+      // taking 16 / (32 / P) of the 16 chunks, and sum across those lanes
+      int P = 2;
+      while (P < nP) P <<= 1;
+      const int Lp = 32 / P, e = lane / Lp, part = lane % Lp, cpl = 16 / Lp;
+      const int s = e < nA ? nth_ancestor(e) : t;
+      float dkk = 0.f, dqk = 0.f;
+      if (e < nP) dots(s, part * cpl, part * cpl + cpl, dkk, dqk);
+      for (int off = 1; off < Lp; off <<= 1) {
+        dkk += __shfl_xor_sync(0xffffffffu, dkk, off);
+        dqk += __shfl_xor_sync(0xffffffffu, dqk, off);
+      }
+      const float dec = s == t ? 1.f : expf(df_diff(gt, sG[s]));
+      const float x = s == t ? 0.f : bt * dec * dkk, y = dec * dqk;
+      const int src = (lane < nP ? lane : 0) * Lp;
+      sn[0] = __shfl_sync(0xffffffffu, s, src);
+      xn[0] = __shfl_sync(0xffffffffu, x, src);
+      yn[0] = __shfl_sync(0xffffffffu, y, src);
+#pragma unroll
+      for (int gi = 1; gi < kGroups; ++gi) {
+        sn[gi] = -1;
+        xn[gi] = yn[gi] = 0.f;
+      }
+    } else {
+      // one entry a lane
+#pragma unroll
+      for (int gi = 0; gi < kGroups; ++gi) {
+        const int n = gi * 32 + lane;
+        sn[gi] = -1;
+        xn[gi] = yn[gi] = 0.f;
+        if (gi * 32 > nA) continue;  // (uniform)
+        const int s = n < nA ? nth_ancestor(n) : t;
+        if (n <= nA) {
+          float dkk = 0.f, dqk = 0.f;
+          dots(s, 0, 16, dkk, dqk);
+          const float dec = s == t ? 1.f : expf(df_diff(gt, sG[s]));
+          sn[gi] = s;
+          xn[gi] = s == t ? 0.f : bt * dec * dkk;
+          yn[gi] = dec * dqk;
+        }
+      }
+    }
+    // the terms of the strict ancestors (entries 0 .. nA-1, root first), four at a
+    // time as they become final: a path's nodes complete in path order, so the
+    // last of the four being final makes all four final
+    float4 au = make_float4(0.f, 0.f, 0.f, 0.f), ao = au;
+    float ymine = 0.f;  // Y[t,t], in the lane that formed entry nA
+#pragma unroll
+    for (int gi = 0; gi < kGroups; ++gi)
+      if (gi * 32 + lane == nA) ymine = yn[gi];
+    const float yself = __shfl_sync(0xffffffffu, ymine, nA & 31);
+#pragma unroll
+    for (int gi = 0; gi < kGroups; ++gi) {
+      const int cnt = min(32, nA - gi * 32);  // (<= 0 past the path: no work)
+      for (int j0 = 0; j0 < cnt; j0 += 4) {
+        const int m = min(4, cnt - j0);
+        wait_final(__shfl_sync(0xffffffffu, sn[gi], j0 + m - 1));
+        int sj[4];
+        float xj[4], yj[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int ss = __shfl_sync(0xffffffffu, sn[gi], (j0 + jj) & 31);
+          const float xx = __shfl_sync(0xffffffffu, xn[gi], (j0 + jj) & 31);
+          const float yy = __shfl_sync(0xffffffffu, yn[gi], (j0 + jj) & 31);
+          const bool use = jj < m;
+          sj[jj] = use ? ss : 0;
+          xj[jj] = use ? xx : 0.f;
+          yj[jj] = use ? yy : 0.f;
+        }
+        float4 us[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          us[jj] = *reinterpret_cast<const float4*>(sU + sj[jj] * kD + 4 * lane);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          au = fma4m(-xj[jj], us[jj], au);
+          ao = fma4m(yj[jj], us[jj], ao);
+        }
+      }
+    }
+    float4 ut = *reinterpret_cast<const float4*>(sU + t * kD + 4 * lane);  // r_t
+    ut.x += au.x;
+    ut.y += au.y;
+    ut.z += au.z;
+    ut.w += au.w;
+    *reinterpret_cast<float4*>(sU + t * kD + 4 * lane) = ut;
+    __syncwarp();
+    if (lane == 0 && !(unit == hk.withhold_unit && t == hk.withhold_node)) sm100::mbar_arrive(&sBar[t]);
+    // o_t = seed_t + sum over the path of Y[t,s] u_s; u_t replaces the seed in U
+    ao = fma4m(yself, ut, ao);
+    const float o0 = seed.x + ao.x, o1 = seed.y + ao.y, o2 = seed.z + ao.z, o3 = seed.w + ao.w;
+    __nv_bfloat16* orow = o + ((row + t) * Hv + h) * kD + 4 * lane;
+    const __nv_bfloat162 p01 = __floats2bfloat162_rn(o0, o1), p23 = __floats2bfloat162_rn(o2, o3);
+    *reinterpret_cast<uint2*>(orow) = make_uint2(*reinterpret_cast<const uint32_t*>(&p01),
+                                                 *reinterpret_cast<const uint32_t*>(&p23));
+    *reinterpret_cast<float4*>(urow) = ut;
+    __syncwarp();  // the stage is read before the next node's q_t lands in it
+  }
+  if (timed_out) atomicOr(sFlag, 1);
+  __syncthreads();
+  if (tid == 0 && sFlag[0] && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
+}
+
+}  // namespace
+
+bool verify_mid_supported(const gdn_tree_dims& d) {
+  return d.dtype == GDN_TREE_BF16 && d.dk == kD && d.dv == kD && d.N >= 1 && d.N <= kMidN &&
+         mid_smem_layout(d.N).total <= 227 * 1024;
+}
+
+cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream) {
+  const size_t smem = mid_smem_layout(a.d.N).total;
+  const dim3 grid(a.d.Hv, a.d.B);
+  cudaError_t err = cudaFuncSetAttribute(verify_mid_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  verify_mid_kernel<<<grid, kThreads, smem, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+      static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
+      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks());
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -19,10 +19,10 @@ def built_library():
     gt.load()
 
 
-@pytest.fixture(params=["auto", "generic"])
+@pytest.fixture(params=["auto", "generic", "mid"])
 def kernel(request, monkeypatch):
-    if request.param == "generic":
-        monkeypatch.setenv("GDN_TREE_KERNEL", "generic")
+    if request.param in ("generic", "mid"):
+        monkeypatch.setenv("GDN_TREE_KERNEL", request.param)
     else:
         monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
     return request.param

@@ -23,12 +23,14 @@ def built_library():
     gt.load()
 
 
-@pytest.fixture(params=["auto", "generic"])
+@pytest.fixture(params=["auto", "generic", "mid"])
 def kernel(request, monkeypatch):
     """Runs a test with the default kernel choice (the tensor-core kernel where
-    it takes the shape) and again with the CUDA-core kernel forced."""
-    if request.param == "generic":
-        monkeypatch.setenv("GDN_TREE_KERNEL", "generic")
+    it takes the shape), again with the general CUDA-core kernel forced, and
+    again with the 256-node bf16 kernel forced (shapes it does not take fall
+    back to the general kernel)."""
+    if request.param in ("generic", "mid"):
+        monkeypatch.setenv("GDN_TREE_KERNEL", request.param)
     else:
         monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
     return request.param
