@@ -486,6 +486,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     t_com = [evs[i][1].elapsed_time(evs[i][2]) for i in range(Ks)]
     sep_ms = max_over_ranks(float(sum(t_ver) + sum(t_com)), dist, dev) / Ks
 
+    # for scale: a plain device copy of the state bytes the commit streams (S0 in,
+    # S1 out), under the same flush and events
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ks)]
+    for i in range(Ks):
+        flush.zero_()
+        evc[i][0].record(stream)
+        S1.copy_(x["S0"])
+        evc[i][1].record(stream)
+    torch.cuda.synchronize()
+    state_copy_us = 1e3 * statistics.mean(evc[i][0].elapsed_time(evc[i][1]) for i in range(Ks))
+
     # the page's measurement baseline: single-branch recurrent verification of the
     # same trees (one recurrent pass per root-to-leaf branch), against which the
     # tree verification is compared
@@ -710,6 +721,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                                / (hbm * 1e9),
                                "roofline_frac": t_roof_sep / (sep_ms * 1e-3),
                                "verify_flops": vf, "commit_flops": cf,
+                               "state_copy_us": state_copy_us,
+                               "state_copy_bytes": 2 * x["S0"].numel() * 4,
                                "verify_kernel": verify_kernel_name(w),
                                "verify_traffic": profiled_traffic(verify_kernel_name(w))},
         }
