@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace gdn {
@@ -331,6 +332,65 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// ---- operand layouts and MMA sequences shared by the tensor-core kernels -------
+
+// one 64-wide K block of a 128-row K-major bf16 tile: 128 rows x 128 bytes
+constexpr uint32_t kSw128TileBytes = 128 * 128;
+
+// byte offset of 16-byte chunk k8 (K elements 8*k8 .. 8*k8+7) of `row` in a
+// 128-row, 128-wide K-major bf16 tile stored with the 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int k8) {
+  const int kb = k8 >> 3, j = k8 & 7;
+  return (uint32_t)(kb * kSw128TileBytes + row * 128 + ((j ^ (row & 7)) << 4));
+}
+
+// (a, b) -> bf16x2 hi parts and bf16x2 lo parts (x = hi + lo to ~2^-17)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// issue the 8 K-steps (K = 128) of D (+)= A B^T for two 128x128 K-major tiles
+__device__ __forceinline__ void umma_128x128x128(uint32_t d_tmem, uint32_t a_base,
+                                                 uint32_t b_base, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t off = (uint32_t)((s >> 2) * kSw128TileBytes + (s & 3) * 32);
+    umma_bf16(d_tmem, desc_sw128_kmajor(a_base + off), desc_sw128_kmajor(b_base + off), idesc,
+              (accumulate || s > 0) ? 1u : 0u);
+  }
+}
+
+// An MN-major bf16 operand (K rows x 128 MN columns): the 16-byte chunk n8
+// (columns 8 n8 .. 8 n8 + 7) of row k sits in the 1024-byte atom of rows
+// 8 (k / 8) .. and columns 64 (n8 / 8) .., atoms of one row group 1 KB apart
+// along MN and row groups 2 KB apart, chunks swizzled by the row.  The state
+// operand S0 (K = dk) and the fused commit's k rows and w U rows (K = path
+// entries) use it.
+constexpr uint32_t kMnLbo = 1024, kMnSbo = 2048;
+__device__ __forceinline__ uint32_t mn_chunk(int k, int n8) {
+  const int r = k & 7;
+  return (uint32_t)((k >> 3) * kMnSbo + (n8 >> 3) * kMnLbo + r * 128 + (((n8 & 7) ^ r) << 4));
+}
+
+// issue the 8 K-steps (K = 128) of D (+)= A B for a 128x128 K-major tile A and
+// a 128-row MN-major tile B (a K-step of 16 rows spans two row groups)
+__device__ __forceinline__ void umma_128x128x128_bmn(uint32_t d_tmem, uint32_t a_base,
+                                                     uint32_t b_base, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32_bmn(128, 128);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t a_off = (uint32_t)((s >> 2) * kSw128TileBytes + (s & 3) * 32);
+    umma_bf16(d_tmem, desc_sw128_kmajor(a_base + a_off),
+              desc_sw128_mnmajor(b_base + (uint32_t)s * 2 * kMnSbo, kMnLbo, kMnSbo), idesc,
+              (accumulate || s > 0) ? 1u : 0u);
+  }
 }
 
 // Arrive once on `bar` when all previously issued MMAs of this thread are done.

@@ -11,10 +11,13 @@
 // One CTA (512 threads) per (sequence b, v-head h), in four stages:
 //  1. the tree: parent links checked; strict-ancestor bitsets and g by pointer
 //     jumping; depths, and the nodes ordered by depth (the solve's task order);
-//  2. R and the output seeds gamma_t q_t^T S0 for every node at once, S0 in
-//     shared memory, four nodes per warp pass (each S0 row read once for four
-//     nodes); R stays in shared memory, the seeds park in the node's U row in
-//     global memory (overwritten by u_t at the end);
+//  2. R and the output seeds gamma_t q_t^T S0 for every node at once, on the
+//     tensor cores: K and Q (two 128-row tiles each, 128-byte swizzled K-major)
+//     and S0 = hi + lo (bf16, MN-major) in shared memory, K S0_hi + K S0_lo and
+//     Q S0_hi into the 512 TMEM columns by tcgen05.mma, read back by row (a
+//     thread per node, warps by TMEM lane group); R stays in shared memory, the
+//     seeds park in the node's U row in global memory (overwritten by u_t at
+//     the end);
 //  3. K into shared memory (bf16, 16-byte chunks XOR-swizzled by row, so that
 //     32 lanes reading 32 rows at once hit distinct banks);
 //  4. the solve as a streaming dataflow over the tree, one warp per node in
@@ -51,12 +54,15 @@ struct MidSmem {
 
 __host__ __device__ inline size_t align16m(size_t x) { return (x + 15) & ~size_t(15); }
 
+// from a 1024-byte aligned base: the U region (the K, Q operand tiles of stage 2,
+// then R / U) holds kMidN rows whatever the tree's size, since the four tiles
+// fill it
 __host__ __device__ inline MidSmem mid_smem_layout(int N) {
   MidSmem L;
   const int W = (N + 31) / 32;
   size_t o = 0;
-  L.U = o;      o = align16m(o + sizeof(float) * N * kD);           // R, then U
-  L.SK = o;     o = align16m(o + sizeof(float) * kD * kD);          // S0, then K (bf16)
+  L.U = o;      o = align16m(o + sizeof(float) * kMidN * kD);       // K, Q tiles; R, then U
+  L.SK = o;     o = align16m(o + sizeof(float) * kD * kD);          // S0, hi / lo; then K
   L.stage = o;  o = align16m(o + sizeof(float) * kWarps * kD);      // q_t of each warp
   L.parent = o; o = align16m(o + sizeof(int) * N);
   L.jump = o;   o = align16m(o + sizeof(int) * N);
@@ -67,10 +73,15 @@ __host__ __device__ inline MidSmem mid_smem_layout(int N) {
   L.depth = o;  o = align16m(o + sizeof(int) * N);
   L.order = o;  o = align16m(o + sizeof(int) * (N + kMidN + 1));   // order, then level starts
   L.bar = o;    o = align16m(o + sizeof(uint64_t) * N);
-  L.flag = o;   o = align16m(o + sizeof(int) * 4);
-  L.total = o;
+  L.flag = o;   o = align16m(o + sizeof(uint64_t) * 2);  // status flag, TMEM base; MMA barrier
+  L.total = o + 1024;  // + alignment slack
   return L;
 }
+
+// float offset of 4-float chunk c4 (of 32) of row t in the R / U rows (plain
+// rows: the solve's per-term address is its hottest arithmetic; the row-per-thread
+// stores of stage 2 pay the bank conflicts instead)
+__device__ __forceinline__ int u_at(int t, int c4) { return t * kD + 4 * c4; }
 
 // byte offset of 16-byte chunk c (of 16) of k row r in the swizzled K tile
 __device__ __forceinline__ uint32_t k_chunk(int r, int c) {
@@ -86,12 +97,12 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 q, float (&v)[8]) {
   }
 }
 
+// acc + a x, as two packed fp32x2 FMAs (same rounding as four fmaf)
 __device__ __forceinline__ float4 fma4m(float a, float4 x, float4 acc) {
-  acc.x = fmaf(a, x.x, acc.x);
-  acc.y = fmaf(a, x.y, acc.y);
-  acc.z = fmaf(a, x.z, acc.z);
-  acc.w = fmaf(a, x.w, acc.w);
-  return acc;
+  const float2 aa = make_float2(a, a);
+  const float2 lo = __ffma2_rn(aa, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
+  const float2 hi = __ffma2_rn(aa, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ void cp_async16m(void* dst, const void* src) {
@@ -107,7 +118,8 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
                   WaitHooks hk) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
   const int h = blockIdx.x, b = blockIdx.y;
   const int hq = h / (Hv / Hqk);
@@ -126,7 +138,8 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   int* sOrder = reinterpret_cast<int*>(smem + L.order);
   int* sLevel = sOrder + Nmax;  // [kMidN + 1]
   uint64_t* sBar = reinterpret_cast<uint64_t*>(smem + L.bar);
-  int* sFlag = reinterpret_cast<int*>(smem + L.flag);
+  int* sFlag = reinterpret_cast<int*>(smem + L.flag);  // [0] status flag, [1] TMEM base
+  uint64_t* sBarMma = reinterpret_cast<uint64_t*>(smem + L.flag) + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // this sequence's rows and state
@@ -139,10 +152,23 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const size_t row = (size_t)lay.row0(b, Nmax);
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
 
-  // S0 starts streaming into shared memory at once
+  // S0, K and Q start streaming into shared memory at once: S0 as it is (fp32),
+  // K and Q as 128-row tiles in the tensor cores' K-major 128-byte-swizzled
+  // layout (K_A, Q_A, K_B, Q_B; rows past the tree zero)
+  const int ntiles = N > 128 ? 2 : 1;
   const float* S0bh = S0 + ((size_t)st * Hv + h) * kD * kD;
   for (int i = tid; i < kD * kD / 4; i += kThreads)
     cp_async16m(sSK + 16 * i, S0bh + 4 * i);
+  const int nrows = 128 * ntiles;
+  for (int e = tid; e < 2 * nrows * 16; e += kThreads) {
+    const int c = e & 15, rq = e >> 4, isq = rq / nrows, r = rq - isq * nrows;  // r: node
+    unsigned char* dst =
+        smem + L.U + (size_t)(r >> 7) * 65536 + isq * 32768 + sm100::sw128_chunk(r & 127, c);
+    if (r < N)
+      cp_async16m(dst, (isq ? q : k) + ((row + r) * Hqk + hq) * kD + 8 * c);
+    else
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   // ---- 1. the tree ------------------------------------------------------------
@@ -162,6 +188,8 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
+  // the tree is valid: the CTA takes the SM's 512 TMEM columns (one CTA an SM)
+  if (warp == 0) sm100::tmem_alloc(reinterpret_cast<uint32_t*>(sFlag + 1), 512);
   tree_prepare(sPar, N, W, sLa, sJump, sAnc, sG);
   // depth, level sizes, then the depth order (index order within a level)
   if (tid < N) {
@@ -171,6 +199,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     atomicAdd(&sLevel[dep], 1);
     sm100::mbar_init(&sBar[tid], 1);
   }
+  if (tid == 0) sm100::mbar_init(sBarMma, 1);
   sm100::mbar_fence_init();
   __syncthreads();
   if (warp == 0) {  // exclusive scan of the level sizes, in place (depths 1 .. N)
@@ -199,74 +228,94 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   __syncthreads();
 
   // ---- 2. R = diag(beta)(V - diag(gamma) K S0) and seeds gamma Q S0 -----------
-  // four nodes a warp pass; lane owns columns 4 lane .. 4 lane + 3
+  // S0 = hi + lo (bf16), MN-major (K = dk rows, N = dv columns), in place of the
+  // fp32 tile: every thread takes its 32 values into registers first
   {
-    const float* sS0 = reinterpret_cast<const float*>(sSK);
-    for (int n0 = 4 * warp; n0 < N; n0 += 4 * kWarps) {
-      float4 ak[4], aq[4];
+    float sv[4][8];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) ak[n] = aq[n] = make_float4(0.f, 0.f, 0.f, 0.f);
-      // the four k and q rows, eight entries (16 bytes) at a time, the next eight
-      // in flight while these are used
-      const __nv_bfloat16* kr[4];
-      const __nv_bfloat16* qr[4];
+    for (int j = 0; j < 4; ++j) {
+      const int qd = tid * 4 + j, i = qd >> 4, n8 = qd & 15;
+      const float4 a = *reinterpret_cast<const float4*>(sSK + (i * kD + 8 * n8) * 4);
+      const float4 c = *reinterpret_cast<const float4*>(sSK + (i * kD + 8 * n8 + 4) * 4);
+      sv[j][0] = a.x; sv[j][1] = a.y; sv[j][2] = a.z; sv[j][3] = a.w;
+      sv[j][4] = c.x; sv[j][5] = c.y; sv[j][6] = c.z; sv[j][7] = c.w;
+    }
+    __syncthreads();
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const int t = min(n0 + n, N - 1);  // (a node past the tree repeats the last)
-        kr[n] = k + ((row + t) * Hqk + hq) * kD;
-        qr[n] = q + ((row + t) * Hqk + hq) * kD;
-      }
-      uint4 kc[4], qc[4];
+    for (int j = 0; j < 4; ++j) {
+      const int qd = tid * 4 + j, i = qd >> 4, n8 = qd & 15;
+      uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        kc[n] = *reinterpret_cast<const uint4*>(kr[n]);
-        qc[n] = *reinterpret_cast<const uint4*>(qr[n]);
-      }
-      for (int i0 = 0; i0 < kD; i0 += 8) {
-        uint4 kx[4], qx[4];
-        const int in = i0 + 8 < kD ? i0 + 8 : i0;
+      for (int e = 0; e < 4; ++e) sm100::split2(sv[j][2 * e], sv[j][2 * e + 1], hi[e], lo[e]);
+      *reinterpret_cast<uint4*>(sSK + sm100::mn_chunk(i, n8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sSK + 32768 + sm100::mn_chunk(i, n8)) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+  sm100::fence_proxy_async_smem();
+  sm100::tc_fence_before_sync();
+  __syncthreads();
+  sm100::tc_fence_after_sync();
+  const uint32_t tmem = static_cast<uint32_t>(sFlag[1]);
+  // TMEM columns: K S0 of tile A 0..127 and of tile B 128..255, Q S0 256..383 and
+  // 384..511 (node r of a tile in lane r)
+  if (tid == 0) {
+    const uint32_t ub = sm100::smem_addr(smem + L.U), sb = sm100::smem_addr(sSK);
+    for (int tl = 0; tl < ntiles; ++tl) {
+      const uint32_t kt = ub + tl * 65536, qt = kt + 32768;
+      sm100::umma_128x128x128_bmn(tmem + 128 * tl, kt, sb, false);
+      sm100::umma_128x128x128_bmn(tmem + 128 * tl, kt, sb + 32768, true);
+      sm100::umma_128x128x128_bmn(tmem + 256 + 128 * tl, qt, sb, false);
+    }
+    sm100::umma_commit(sBarMma);
+  }
+  if (!sm100::mbar_wait(sBarMma, 0, hk.limit_ns)) {
+    // (bounded again: the MMAs must be done before TMEM is read or freed)
+    sm100::mbar_wait(sBarMma, 0, hk.limit_ns);
+    if (tid == 0) sFlag[0] = 1;
+  }
+  sm100::tc_fence_after_sync();
+  {
+    // warp w reads accumulator w / 4 (K S0 tile A, B; Q S0 tile A, B) for its
+    // TMEM lane group w % 4: thread = node
+    const int acc = warp >> 2, lg = warp & 3;
+    if ((acc & 1) < ntiles) {  // (warp-uniform)
+      const int t = (acc & 1) * 128 + lg * 32 + lane;
+      const bool live = t < N;
+      const float gam = live ? expf(df_value(sG[t])) : 0.f;
+      const float bt = live ? sBeta[t] : 0.f;
+      const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16) + 128 * acc;
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        float r[32];
+        sm100::tmem_ld_32cols(taddr + 32 * c32, r);  // warp-collective: every lane
+        if (!live) continue;
+        if (acc < 2) {
+          const uint4* vr = reinterpret_cast<const uint4*>(v + ((row + t) * Hv + h) * kD + 32 * c32);
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          kx[n] = *reinterpret_cast<const uint4*>(kr[n] + in);
-          qx[n] = *reinterpret_cast<const uint4*>(qr[n] + in);
-        }
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii) {
-          const float4 s = *reinterpret_cast<const float4*>(sS0 + (i0 + ii) * kD + 4 * lane);
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            const uint32_t kw = (&kc[n].x)[ii >> 1], qw = (&qc[n].x)[ii >> 1];
-            const float kf = __uint_as_float((ii & 1) ? (kw & 0xffff0000u) : (kw << 16));
-            const float qf = __uint_as_float((ii & 1) ? (qw & 0xffff0000u) : (qw << 16));
-            ak[n] = fma4m(kf, s, ak[n]);
-            aq[n] = fma4m(qf, s, aq[n]);
+          for (int m = 0; m < 4; ++m) {
+            float vv[8];
+            bf16x8_to_f32(vr[m], vv);
+            *reinterpret_cast<float4*>(sU + u_at(t, 8 * c32 + 2 * m)) =
+                make_float4(bt * (vv[0] - gam * r[8 * m]), bt * (vv[1] - gam * r[8 * m + 1]),
+                            bt * (vv[2] - gam * r[8 * m + 2]), bt * (vv[3] - gam * r[8 * m + 3]));
+            *reinterpret_cast<float4*>(sU + u_at(t, 8 * c32 + 2 * m + 1)) =
+                make_float4(bt * (vv[4] - gam * r[8 * m + 4]), bt * (vv[5] - gam * r[8 * m + 5]),
+                            bt * (vv[6] - gam * r[8 * m + 6]), bt * (vv[7] - gam * r[8 * m + 7]));
           }
-        }
+        } else {
+          float4* sr = reinterpret_cast<float4*>(Ubh + (size_t)t * kD + 32 * c32);
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          kc[n] = kx[n];
-          qc[n] = qx[n];
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const int t = n0 + n;
-        if (t < N) {
-          const float gam = expf(df_value(sG[t]));
-          const float bt = sBeta[t];
-          const uint2 vv = *reinterpret_cast<const uint2*>(v + ((row + t) * Hv + h) * kD + 4 * lane);
-          const float v0 = __uint_as_float(vv.x << 16), v1 = __uint_as_float(vv.x & 0xffff0000u);
-          const float v2 = __uint_as_float(vv.y << 16), v3 = __uint_as_float(vv.y & 0xffff0000u);
-          *reinterpret_cast<float4*>(sU + t * kD + 4 * lane) =
-              make_float4(bt * (v0 - gam * ak[n].x), bt * (v1 - gam * ak[n].y),
-                          bt * (v2 - gam * ak[n].z), bt * (v3 - gam * ak[n].w));
-          *reinterpret_cast<float4*>(Ubh + (size_t)t * kD + 4 * lane) =
-              make_float4(gam * aq[n].x, gam * aq[n].y, gam * aq[n].z, gam * aq[n].w);
+          for (int m = 0; m < 8; ++m)
+            sr[m] = make_float4(gam * r[4 * m], gam * r[4 * m + 1], gam * r[4 * m + 2],
+                                gam * r[4 * m + 3]);
         }
       }
     }
   }
-  __syncthreads();  // S0 is no longer needed
+  sm100::tc_fence_before_sync();
+  __syncthreads();  // TMEM read, S0 no longer needed
+  if (warp == 0) sm100::tmem_dealloc(tmem, 512);
 
   // ---- 3. K into shared memory (bf16, swizzled) ---------------------------------
   for (int e = tid; e < N * 16; e += kThreads) {
@@ -390,6 +439,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // time as they become final: a path's nodes complete in path order, so the
     // last of the four being final makes all four final
     float4 au = make_float4(0.f, 0.f, 0.f, 0.f), ao = au;
+    const float* urow_lane = sU + 4 * lane;  // (u rows: row s at urow_lane + s kD)
     float ymine = 0.f;  // Y[t,t], in the lane that formed entry nA
 #pragma unroll
     for (int gi = 0; gi < kGroups; ++gi)
@@ -401,7 +451,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       for (int j0 = 0; j0 < cnt; j0 += 4) {
         const int m = min(4, cnt - j0);
         wait_final(__shfl_sync(0xffffffffu, sn[gi], j0 + m - 1));
-        int sj[4];
+        const float* uj[4];
         float xj[4], yj[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -409,14 +459,13 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           const float xx = __shfl_sync(0xffffffffu, xn[gi], (j0 + jj) & 31);
           const float yy = __shfl_sync(0xffffffffu, yn[gi], (j0 + jj) & 31);
           const bool use = jj < m;
-          sj[jj] = use ? ss : 0;
+          uj[jj] = urow_lane + (use ? ss : 0) * kD;
           xj[jj] = use ? xx : 0.f;
           yj[jj] = use ? yy : 0.f;
         }
         float4 us[4];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          us[jj] = *reinterpret_cast<const float4*>(sU + sj[jj] * kD + 4 * lane);
+        for (int jj = 0; jj < 4; ++jj) us[jj] = *reinterpret_cast<const float4*>(uj[jj]);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           au = fma4m(-xj[jj], us[jj], au);
@@ -424,12 +473,12 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         }
       }
     }
-    float4 ut = *reinterpret_cast<const float4*>(sU + t * kD + 4 * lane);  // r_t
+    float4 ut = *reinterpret_cast<const float4*>(sU + u_at(t, lane));  // r_t
     ut.x += au.x;
     ut.y += au.y;
     ut.z += au.z;
     ut.w += au.w;
-    *reinterpret_cast<float4*>(sU + t * kD + 4 * lane) = ut;
+    *reinterpret_cast<float4*>(sU + u_at(t, lane)) = ut;
     __syncwarp();
     if (lane == 0 && !(unit == hk.withhold_unit && t == hk.withhold_node)) sm100::mbar_arrive(&sBar[t]);
     // o_t = seed_t + sum over the path of Y[t,s] u_s; u_t replaces the seed in U

@@ -194,13 +194,6 @@ static_assert(offsetof(Small, g) % 16 == 0 && offsetof(Small, emg) % 16 == 0,
               "path log-decays are read as float4");
 static_assert(offsetof(Small, anc) % 16 == 0, "ancestor rows are read and written as uint4");
 
-// byte offset of 16-byte chunk k8 (K elements 8*k8 .. 8*k8+7) of `row` in a
-// 128-row, 128-wide K-major bf16 tile stored with the 128-byte swizzle
-__device__ __forceinline__ uint32_t sw128_chunk(int row, int k8) {
-  const int kb = k8 >> 3, j = k8 & 7;
-  return (uint32_t)(kb * kTileBytes + row * 128 + ((j ^ (row & 7)) << 4));
-}
-
 // fp32 128 x 128 row tiles (the state, R / U) in the layout of four TMA boxes of
 // 32 columns x 128 rows with the 128-byte swizzle: row t, 4-float chunk c4
 // (0..31) sits in box c4 / 8, its 16-byte slot xor-swizzled by the row, so that
@@ -213,15 +206,6 @@ __device__ __forceinline__ uint32_t u_off(int t, int c4) {
 // packed strictly-lower triangle of X and Y
 __device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
 
-// (a, b) -> bf16x2 hi parts and bf16x2 lo parts (x = hi + lo to ~2^-17)
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 __device__ __forceinline__ uint32_t pack2f(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -233,44 +217,6 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
   const float2 lo = __ffma2_rn(aa, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
   const float2 hi = __ffma2_rn(aa, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
   return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
-
-// issue the 8 K-steps (K = 128) of D (+)= A B^T for two 128x128 K-major tiles
-__device__ __forceinline__ void umma_128x128x128(uint32_t d_tmem, uint32_t a_base,
-                                                 uint32_t b_base, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t off = (uint32_t)((s >> 2) * kTileBytes + (s & 3) * 32);
-    umma_bf16(d_tmem, desc_sw128_kmajor(a_base + off), desc_sw128_kmajor(b_base + off), idesc,
-              (accumulate || s > 0) ? 1u : 0u);
-  }
-}
-
-// An MN-major bf16 operand (K rows x 128 MN columns): the 16-byte chunk n8
-// (columns 8 n8 .. 8 n8 + 7) of row k sits in the 1024-byte atom of rows
-// 8 (k / 8) .. and columns 64 (n8 / 8) .., atoms of one row group 1 KB apart
-// along MN and row groups 2 KB apart, chunks swizzled by the row.  The state
-// operand S0 (K = dk), the output MMA's U (K = tree nodes) and the fused commit's
-// k rows and w U rows (K = path entries) all use it.
-constexpr uint32_t kMnLbo = 1024, kMnSbo = 2048;
-__device__ __forceinline__ uint32_t mn_chunk(int k, int n8) {
-  const int r = k & 7;
-  return (uint32_t)((k >> 3) * kMnSbo + (n8 >> 3) * kMnLbo + r * 128 + (((n8 & 7) ^ r) << 4));
-}
-
-// issue the 8 K-steps (K = 128) of D (+)= A B for a 128x128 K-major tile A and
-// a 128-row MN-major tile B (a K-step of 16 rows spans two row groups)
-__device__ __forceinline__ void umma_128x128x128_bmn(uint32_t d_tmem, uint32_t a_base,
-                                                     uint32_t b_base, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32_bmn(128, 128);
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t a_off = (uint32_t)((s >> 2) * kTileBytes + (s & 3) * 32);
-    umma_bf16(d_tmem, desc_sw128_kmajor(a_base + a_off),
-              desc_sw128_mnmajor(b_base + (uint32_t)s * 2 * kMnSbo, kMnLbo, kMnSbo), idesc,
-              (accumulate || s > 0) ? 1u : 0u);
-  }
 }
 
 // issue the K-steps (16 path entries each) of D (+)= A^T B for MN-major tiles of
