@@ -35,7 +35,13 @@ constexpr int kWarps = 2;  // warps per CTA
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRB = 8;     // state rows formed at a time (a pass)
 constexpr int kMaxRows = 32;  // state rows of a warp's block
-constexpr int kBatch = 8;  // path entries whose k / U rows are on chip at a time
+constexpr int kPre = 8;       // 32-entry chunks of a path whose entries are fetched together
+
+// path entries whose k / U rows are on chip at a time (eight), and the slots
+// holding them: one for paths of up to 32 entries (the common case: the most warps
+// an SM), two (the next batch copied while one is used) for longer ones
+__host__ __device__ inline int batch_size(int Lmax) { return 8; }
+__host__ __device__ inline int batch_slots(int Lmax) { return Lmax > 32 ? 2 : 1; }
 
 // state rows of a warp's block: 32, or 16 where dk is not a multiple of 32
 __host__ __device__ inline int block_rows(int dk) { return dk % kMaxRows == 0 ? kMaxRows : 16; }
@@ -43,11 +49,14 @@ __host__ __device__ inline int block_rows(int dk) { return dk % kMaxRows == 0 ? 
 // path entries a warp keeps (pj, G_j.hi then w_j, G_j.lo): Lmax rounded up to 32
 __host__ __device__ inline int path_capacity(int Lmax) { return Lmax <= 32 ? 32 : (Lmax + 31) / 32 * 32; }
 
-// per warp, in bytes: S0 rows [kMaxRows][dv] fp32 | U rows [kBatch][dv] fp32 |
-// k rows [kBatch][kMaxRows] (as given) | pj, G.hi / w, G.lo [cap] each
-__host__ __device__ inline uint32_t warp_smem_bytes(int dv, int tsize, int cap) {
-  return (uint32_t)kMaxRows * dv * 4 + (uint32_t)kBatch * dv * 4 +
-         (uint32_t)kBatch * kMaxRows * tsize + 3u * cap * 4;
+// per warp, in bytes: S0 rows [kMaxRows][dv] fp32 | per slot: U rows [batch][dv]
+// fp32, k rows [batch][kMaxRows] (as given) | pj, G.hi / w, G.lo [cap] each
+__host__ __device__ inline uint32_t slot_bytes(int dv, int tsize, int Lmax) {
+  return (uint32_t)batch_size(Lmax) * (dv * 4 + kMaxRows * tsize);
+}
+__host__ __device__ inline uint32_t warp_smem_bytes(int dv, int tsize, int Lmax) {
+  return (uint32_t)kMaxRows * dv * 4 + batch_slots(Lmax) * slot_bytes(dv, tsize, Lmax) +
+         3u * path_capacity(Lmax) * 4;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -55,8 +64,15 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                "l"(src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// every cp.async group of this thread but the most recent has completed
+__device__ __forceinline__ void cp_async_wait_but_last() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
 // inclusive double-float prefix sum of v across the warp's lanes
@@ -99,11 +115,14 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   const int Nmax = d.N, dk = d.dk, dv = d.dv, Hv = d.Hv, Hqk = d.Hqk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cap = path_capacity(Lmax);
-  uint8_t* ws = smem + (size_t)warp * warp_smem_bytes(dv, (int)sizeof(T), cap);
-  float* s_s = reinterpret_cast<float*>(ws);                    // [R][dv]
-  float* s_u = s_s + kMaxRows * dv;                             // [kBatch][dv]
-  T* s_k = reinterpret_cast<T*>(s_u + kBatch * dv);             // [kBatch][R]
-  int* s_pj = reinterpret_cast<int*>(s_k + kBatch * kMaxRows);  // [cap]
+  const int batch = batch_size(Lmax), nslot = batch_slots(Lmax);
+  const uint32_t sb = slot_bytes(dv, (int)sizeof(T), Lmax);
+  uint8_t* ws = smem + (size_t)warp * warp_smem_bytes(dv, (int)sizeof(T), Lmax);
+  float* s_s = reinterpret_cast<float*>(ws);  // [R][dv]
+  uint8_t* s_slots = ws + kMaxRows * dv * 4;
+  auto slot_u = [&](int sl) { return reinterpret_cast<float*>(s_slots + sl * sb); };  // [batch][dv]
+  auto slot_k = [&](int sl) { return reinterpret_cast<T*>(slot_u(sl) + batch * dv); };  // [batch][R]
+  int* s_pj = reinterpret_cast<int*>(s_slots + nslot * sb);  // [cap]
   float* s_hi = reinterpret_cast<float*>(s_pj + cap);      // [cap]: G_j.hi, then w_j
   float* s_lo = s_hi + cap;                                // [cap]: G_j.lo
 
@@ -132,19 +151,22 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   const int pj0 = lane < Lmax ? path[(size_t)b * Lmax + lane] : 0;
 
   // k (the block's R entries) and U rows of path entries j0 .. j0 + nj - 1
-  // into the warp's slots, by 16-byte copies
-  auto stage = [&](int j0, int nj) {
+  // into slot sl, by 16-byte copies (one cp.async group)
+  auto stage = [&](int j0, int nj, int sl) {
     const int uq = dv / 4, kq = R * (int)sizeof(T) / 16;
+    float* su = slot_u(sl);
+    T* sk = slot_k(sl);
     for (int q = lane; q < nj * uq; q += 32) {
       const int jj = q / uq, c = q - jj * uq;
-      cp_async16(s_u + jj * dv + 4 * c, U + (urow + s_pj[j0 + jj]) * dv + 4 * c);
+      cp_async16(su + jj * dv + 4 * c, U + (urow + s_pj[j0 + jj]) * dv + 4 * c);
     }
     for (int q = lane; q < nj * kq; q += 32) {
       const int jj = q / kq, c = q - jj * kq;
       const T* src = k + ((row + s_pj[j0 + jj]) * Hqk + hq) * dk + rb * R;
-      cp_async16(reinterpret_cast<uint8_t*>(s_k + jj * R) + 16 * c,
+      cp_async16(reinterpret_cast<uint8_t*>(sk + jj * R) + 16 * c,
                  reinterpret_cast<const uint8_t*>(src) + 16 * c);
     }
+    cp_async_commit();
   };
 
   // ---- round trip 2, 32 entries (one a lane) at a time: range check; the
@@ -154,26 +176,65 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   // prefix sums of log alpha along the path
   int bad = (L < 0 || L > N || L > Lmax);
   const int nL = bad ? 0 : L;
+  // the entries of the path's first kPre chunks come together (one a lane a
+  // chunk), then their log alpha and parent links together; chunks past those
+  // are fetched as they are reached
+  int pjr[kPre];
+  pjr[0] = pj0;
+#pragma unroll
+  for (int i = 1; i < kPre; ++i) {
+    const int e = 32 * i + lane;
+    pjr[i] = e < nL ? path[(size_t)b * Lmax + e] : 0;
+  }
+  {
+    int oor = 0;
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) oor |= (32 * i + lane < nL) && (pjr[i] < 0 || pjr[i] >= N);
+    if (__any_sync(0xffffffffu, oor)) bad = 1;
+  }
+  const int nLc = bad ? 0 : nL;  // (entries known to be in range from here on)
+  float lar[kPre];
+  int parr[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int e = 32 * i + lane;
+    lar[i] = 0.f;
+    parr[i] = -1;
+    if (e < nLc) {
+      s_pj[e] = pjr[i];
+      lar[i] = log_alpha[(row + pjr[i]) * Hv + h];
+      if (parent) parr[i] = parent[row + pjr[i]];
+    }
+  }
+  if (nLc > 0) {  // the first batch's rows start coming
+    __syncwarp();
+    stage(0, min(batch, nLc), 0);
+  }
   df carry = {0.f, 0.f};
   int last = -1;  // the previous chunk's last entry
-  for (int c0 = 0; c0 < nL; c0 += 32) {
-    const int e = c0 + lane;
-    const bool live = e < nL;
-    const int pj = c0 == 0 ? pj0 : (live ? path[(size_t)b * Lmax + e] : 0);
-    if (__any_sync(0xffffffffu, live && (pj < 0 || pj >= N))) {
-      bad = 1;
-      break;
-    }
-    if (live) s_pj[e] = pj;
-    if (c0 == 0) {
-      __syncwarp();
-      stage(0, min(kBatch, nL));
-    }
+  for (int c0 = 0; c0 < nLc; c0 += 32) {
+    const int e = c0 + lane, ci = c0 >> 5;
+    const bool live = e < nLc;
+    int pj = 0, par = -1;
     float la = 0.f;
-    int par = -1;
-    if (live) {
-      la = log_alpha[(row + pj) * Hv + h];
-      if (parent) par = parent[row + pj];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+      if (i == ci) {
+        pj = pjr[i];
+        la = lar[i];
+        par = parr[i];
+      }
+    if (ci >= kPre) {
+      pj = live ? path[(size_t)b * Lmax + e] : 0;
+      if (__any_sync(0xffffffffu, live && (pj < 0 || pj >= N))) {
+        bad = 1;
+        break;
+      }
+      if (live) {
+        s_pj[e] = pj;
+        la = log_alpha[(row + pj) * Hv + h];
+        if (parent) par = parent[row + pj];
+      }
     }
     int prev = __shfl_up_sync(0xffffffffu, pj, 1);
     if (lane == 0) prev = last;
@@ -206,15 +267,30 @@ commit_kernel(const int32_t* __restrict__ path, const int32_t* __restrict__ path
   // ---- S1 = gamma S0 + K_P^T diag(w) U_P on the block's rows, kRB rows (a
   // pass) at a time; paths past one batch of entries keep the partial sums of
   // the earlier batches in the S0 slot
-  const int nb = nL == 0 ? 1 : (nL + kBatch - 1) / kBatch;
+  const int nb = nL == 0 ? 1 : (nL + batch - 1) / batch;
   for (int bi = 0; bi < nb; ++bi) {
-    const int j0 = bi * kBatch, nj = min(kBatch, nL - j0);
-    if (bi > 0) {  // the next batch's rows
-      __syncwarp();
-      stage(j0, nj);
+    const int j0 = bi * batch, nj = min(batch, nL - j0);
+    const int sl = nslot == 2 ? (bi & 1) : 0;
+    if (nslot == 2) {
+      // two slots: batch bi + 1 is copied into the other slot (free: batch bi - 1
+      // was formed from it) while batch bi is formed
+      if (bi + 1 < nb) {
+        __syncwarp();
+        stage(j0 + batch, min(batch, nL - j0 - batch), sl ^ 1);
+        cp_async_wait_but_last();
+      } else {
+        cp_async_wait_all();
+      }
+    } else {
+      if (bi > 0) {  // one slot: the next batch's rows, here and now
+        __syncwarp();
+        stage(j0, nj, 0);
+      }
+      cp_async_wait_all();
     }
-    cp_async_wait_all();
     __syncwarp();  // every lane's copies (and weights) in place
+    const float* s_u = slot_u(sl);
+    const T* s_k = slot_k(sl);
     if (owner) {
       const bool first = bi == 0, final_ = bi == nb - 1;
       for (int r0 = 0; r0 < R; r0 += kRB) {
@@ -276,7 +352,7 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
   const long long grid = (n_blocks + kWarps - 1) / kWarps;
   if (grid > 0x7fffffffll) return cudaErrorInvalidConfiguration;
   const int tsize = a.d.dtype == GDN_TREE_BF16 ? 2 : 4;
-  const size_t smem = (size_t)kWarps * warp_smem_bytes(a.d.dv, tsize, path_capacity(a.Lmax));
+  const size_t smem = (size_t)kWarps * warp_smem_bytes(a.d.dv, tsize, a.Lmax);
   cudaError_t err;
   if (a.d.dtype == GDN_TREE_BF16) {
     err = cudaFuncSetAttribute(commit_kernel<__nv_bfloat16>,
