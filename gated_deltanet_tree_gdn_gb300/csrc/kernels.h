@@ -92,10 +92,10 @@ struct CommitVerifyArgs {
 // Normal calls use the defaults (2 s, nothing withheld); a test sets them
 // through the environment (read at every launch by wait_hooks()):
 //   GDN_TREE_TEST_WAIT_LIMIT_NS=<ns>       the bound of every wait
-//   GDN_TREE_TEST_WITHHOLD_NODE=<unit>:<node>  the tensor-core verification of unit
-//       (b * Hv + h) never arrives on that node's solve barrier, so the waits of
-//       its children and grandchildren run out (thread arrivals only: no copy or
-//       MMA is left in flight)
+//   GDN_TREE_TEST_WITHHOLD_NODE=<unit>:<node>  the tensor-core and 256-node
+//       verifications of unit (b * Hv + h) never arrive on that node's solve
+//       barrier, so the waits of its descendants run out (thread arrivals only: no
+//       copy or MMA is left in flight)
 struct WaitHooks {
   uint64_t limit_ns = 2000000000ull;
   int withhold_unit = -1, withhold_node = -1;

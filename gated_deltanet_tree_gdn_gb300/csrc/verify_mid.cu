@@ -480,7 +480,8 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     ut.w += au.w;
     *reinterpret_cast<float4*>(sU + u_at(t, lane)) = ut;
     __syncwarp();
-    if (lane == 0 && !(unit == hk.withhold_unit && t == hk.withhold_node)) sm100::mbar_arrive(&sBar[t]);
+    if (lane == 0 && !(unit == hk.withhold_unit && t == hk.withhold_node))
+      sm100::mbar_arrive(&sBar[t]);
     // o_t = seed_t + sum over the path of Y[t,s] u_s; u_t replaces the seed in U
     ao = fma4m(yself, ut, ao);
     const float o0 = seed.x + ao.x, o1 = seed.y + ao.y, o2 = seed.z + ao.z, o3 = seed.w + ao.w;

@@ -1,5 +1,5 @@
-"""The bounded on-device waits of the tensor-core kernel, made to run out on
-purpose (no fault, no trap, nothing left in flight): a short wait limit and a
+"""The bounded on-device waits of the tensor-core and 256-node kernels, made to
+run out on purpose (no fault, no trap, nothing left in flight): a short wait limit and a
 solve-barrier arrival that is withheld (test-only controls read from the
 environment).  The kernel must report GDN_TREE_STATUS_TIMEOUT for the
 sequences it could not finish, leave the other sequences correct, free its
@@ -91,3 +91,33 @@ def test_fused_iteration_reports_timeout_for_both_calls(monkeypatch):
     ok = np.arange(w.B) != b
     S1_ref = oracle.commit_workload(w)
     assert H.rel_err(S1.cpu().numpy()[ok], S1_ref[ok]) <= H.TOL_S1
+
+
+def test_mid_kernel_solve_wait_runs_out(monkeypatch):
+    """The same on the 256-node kernel: a withheld solve-barrier arrival of one
+    (sequence, head) unit makes its descendants' bounded waits run out."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    w = W.make_custom(seed=903, B=6, N=160, Hqk=2, Hv=4, dk=128, dv=128, dtype=W.BF16,
+                      tree="random", max_depth=24)
+    b, h = 4, 2
+    monkeypatch.setenv("GDN_TREE_TEST_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("GDN_TREE_TEST_WITHHOLD_NODE", f"{b * w.Hv + h}:{_withheld(w, b)}")
+    x = H.to_device(w)
+    st = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    o, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
+                     dev_status=st)
+    torch.cuda.synchronize()
+    s = st.cpu().numpy()
+    assert s[b] == gt.STATUS_TIMEOUT
+    assert (np.delete(s, b) == gt.STATUS_OK).all()
+    ok = np.arange(w.B) != b
+    o_ref, U_ref = oracle.verify_workload(w)
+    assert H.rel_err(o.float().cpu().numpy()[ok], o_ref[ok]) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U.cpu().numpy()[ok], U_ref[ok]) <= H.TOL_U
+    monkeypatch.delenv("GDN_TREE_TEST_WAIT_LIMIT_NS")
+    monkeypatch.delenv("GDN_TREE_TEST_WITHHOLD_NODE")
+    gpu = H.run_gpu(w)
+    assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
+    H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
