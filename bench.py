@@ -138,12 +138,21 @@ def verify_kernel_name(w: W.Workload) -> str:
     return "verify_generic_kernel"
 
 
+def commit_kernel_name(w: W.Workload) -> str:
+    """The commit kernel the library dispatches (mirrors the C-ABI's rule: the
+    tensor-core commit for bf16, dk = dv = 128 and paths of more than 32 entries)."""
+    if (w.dtype == W.BF16 and w.dk == 128 and w.dv == 128 and w.Lmax > 32
+            and os.environ.get("GDN_TREE_KERNEL", "auto") != "generic"):
+        return "commit_tc_kernel"
+    return "commit_kernel"
+
+
 def iteration_kernel_name(w: W.Workload) -> str:
     """The kernel one fused decoding iteration runs on (the tensor-core kernel
     with the delayed commitment fused in, where it takes the shape)."""
     if verify_kernel_name(w) == "verify_tc_kernel":
         return "verify_tc_kernel<fused commit>"
-    return "commit_kernel + " + verify_kernel_name(w)
+    return commit_kernel_name(w) + " + " + verify_kernel_name(w)
 
 
 def arithmetic_dtype(kernel: str) -> str:
@@ -724,6 +733,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                                "state_copy_us": state_copy_us,
                                "state_copy_bytes": 2 * x["S0"].numel() * 4,
                                "verify_kernel": verify_kernel_name(w),
+                               "commit_kernel": commit_kernel_name(w),
                                "verify_traffic": profiled_traffic(verify_kernel_name(w))},
         }
         line["recurrent_baseline"] = {
@@ -736,7 +746,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                               "c": 4, "w": 4, "max_depth": 24,
                               "rounds": -(-(w.N - 1) // 4)}
         line["long_trees"] = {
-            "kernel": "verify_long_kernel + commit_kernel",
+            "kernel": verify_kernel_name(wl) + " + " + commit_kernel_name(wl),
             "workload": f"B={wl.B} seqs x Hv={wl.Hv} v-heads (Hqk={wl.Hqk}), N={wl.N}-node random "
                         "trees (branching 1-4, depth<=24), accepted paths <= depth",
             "verify_us": lv_us, "commit_us": lc_us,
@@ -744,7 +754,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "verify_roofline_frac": verify_bytes(wl) / (lv_us * 1e-6) / (hbm * 1e9),
             "commit_roofline_frac": commit_bytes(wl) / (lc_us * 1e-6) / (hbm * 1e9)}
         line["config4"] = {
-            "kernel": verify_kernel_name(w4) + " + commit_kernel",
+            "kernel": verify_kernel_name(w4) + " + " + commit_kernel_name(w4),
             "workload": W.CONFIG_NAMES[4] + ": B=64 seqs x Hv=32 v-heads (Hqk=16), dk=dv=128, "
                         "bf16, N=256-node trees (256-deep chains, stars, random trees), "
                         "log alpha down to -4, beta up to 0.99",

@@ -346,7 +346,7 @@ int sm_count() {
   return n;
 }
 
-cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
+cudaError_t launch_commit_warp(const CommitArgs& a, cudaStream_t stream) {
   const long long n_blocks = (long long)a.d.B * a.d.Hv * (a.d.dk / block_rows(a.d.dk));
   if (n_blocks == 0) return cudaSuccess;
   const long long grid = (n_blocks + kWarps - 1) / kWarps;

@@ -77,6 +77,7 @@ WaitHooks wait_hooks() {
     const unsigned long long v = strtoull(e, nullptr, 10);
     if (v > 0 && v < h.limit_ns) h.limit_ns = v;
   }
+  if (const char* e = getenv("GDN_TREE_TEST_WITHHOLD_COPY")) h.withhold_copy_seq = atoi(e);
   if (const char* e = getenv("GDN_TREE_TEST_WITHHOLD_NODE")) {
     int u = -1, n = -1;
     if (sscanf(e, "%d:%d", &u, &n) == 2) {
@@ -112,6 +113,15 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
     return launch_verify_mid(a, stream);
   if (a.d.N > kMaxNHost || kernel_forced("long")) return launch_verify_long(a, stream);
   return launch_verify_generic(a, stream);
+}
+
+// paths of more than 32 entries take the tensor-core commit (the rank-L update is
+// then real work: a chain's 256-entry path is ~1 M FMAs a 32-row block); shorter
+// ones the CUDA-core kernel, whose warps hide the gathers' latency better
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream) {
+  if (!kernel_forced("generic") && a.Lmax > 32 && commit_tc_supported(a.d, a.Lmax))
+    return launch_commit_tc(a, stream);
+  return launch_commit_warp(a, stream);
 }
 
 cudaError_t launch_commit_verify(const CommitVerifyArgs& a, cudaStream_t stream) {

@@ -2,6 +2,7 @@
 // kernels of libgdntree (not installed, not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -96,9 +97,12 @@ struct CommitVerifyArgs {
 //       verifications of unit (b * Hv + h) never arrive on that node's solve
 //       barrier, so the waits of its descendants run out (thread arrivals only: no
 //       copy or MMA is left in flight)
+//   GDN_TREE_TEST_WITHHOLD_COPY=<b>        the tensor-core commit of sequence b
+//       expects its state copy but never issues it, so the wait for it runs out
 struct WaitHooks {
   uint64_t limit_ns = 2000000000ull;
   int withhold_unit = -1, withhold_node = -1;
+  int withhold_copy_seq = -1;
 };
 WaitHooks wait_hooks();
 
@@ -116,10 +120,19 @@ cudaError_t launch_verify_long(const VerifyArgs& a, cudaStream_t stream);
 bool verify_mid_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream);
 
+// 128-byte-swizzled TMA maps of fp32 states [n_states, 128, 128] as four boxes of
+// 32 columns x 128 rows each (false when the driver's encoder is unavailable)
+bool encode_state_map(CUtensorMap* map, const float* base, long long n_states);
+
 bool verify_tc_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t stream);
 
+// the commit: on the tensor cores (bf16 k, dk = dv = 128) unless the CUDA-core
+// kernels are forced, else one warp per 32-row block on CUDA cores
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t stream);
+cudaError_t launch_commit_warp(const CommitArgs& a, cudaStream_t stream);
+bool commit_tc_supported(const gdn_tree_dims& d, int32_t Lmax);
+cudaError_t launch_commit_tc(const CommitArgs& a, cudaStream_t stream);
 
 // streaming multiprocessors of the current device (cached per device; 0: no device)
 int sm_count();

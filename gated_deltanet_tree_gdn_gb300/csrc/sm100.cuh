@@ -393,6 +393,31 @@ __device__ __forceinline__ void umma_128x128x128_bmn(uint32_t d_tmem, uint32_t a
   }
 }
 
+// issue the K-steps (16 path entries each) of D (+)= A^T B for MN-major tiles of
+// `ksteps` * 16 rows: A = the path's k rows, B = its w U rows
+__device__ __forceinline__ void umma_commit_rows(uint32_t d_tmem, uint32_t a_base,
+                                                 uint32_t b_base, int ksteps, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32_amn_bmn(128, 128);
+  for (int s = 0; s < ksteps; ++s) {
+    const uint32_t off = (uint32_t)s * 2 * kMnSbo;
+    umma_bf16(d_tmem, desc_sw128_mnmajor(a_base + off, kMnLbo, kMnSbo),
+              desc_sw128_mnmajor(b_base + off, kMnLbo, kMnSbo), idesc,
+              (accumulate || s > 0) ? 1u : 0u);
+  }
+}
+
+// fp32 128-row tiles of 128 columns (a state, R / U rows) as four TMA boxes of
+// 32 columns x 128 rows with the 128-byte swizzle
+constexpr uint32_t kBoxBytes = 32 * 4 * 128;  // 16 KB
+// fp32 128 x 128 row tiles (the state, R / U) in the layout of four TMA boxes of
+// 32 columns x 128 rows with the 128-byte swizzle: row t, 4-float chunk c4
+// (0..31) sits in box c4 / 8, its 16-byte slot xor-swizzled by the row, so that
+// a row-per-thread float4 access and a half-warp reading one row's 16 chunks are
+// both bank-conflict free
+__device__ __forceinline__ uint32_t u_off(int t, int c4) {
+  return (uint32_t)((c4 >> 3) * kBoxBytes + t * 128 + (((c4 & 7) ^ (t & 7)) << 4));
+}
+
 // Arrive once on `bar` when all previously issued MMAs of this thread are done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(

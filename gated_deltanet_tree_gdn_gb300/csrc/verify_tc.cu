@@ -127,7 +127,6 @@ constexpr uint32_t OFF_P = OFF_R2;
 // region 3: the fp32 state (TMA: four boxes of 32 columns x 128 rows), S1 in
 // place until its TMA store has read it; then R / U (fp32 rows, same layout)
 constexpr uint32_t OFF_R3 = 4 * kOpBytes;
-constexpr uint32_t kBoxBytes = 32 * 4 * 128;  // 16 KB
 constexpr uint32_t OFF_PATH = OFF_R3 + kTile * kD * 4;  // uint8 [node][depth - 1] -> path node
 constexpr uint32_t OFF_SMALL = OFF_PATH + kTile * kTile;
 #ifdef GDN_TC_PROFILE
@@ -194,15 +193,6 @@ static_assert(offsetof(Small, g) % 16 == 0 && offsetof(Small, emg) % 16 == 0,
               "path log-decays are read as float4");
 static_assert(offsetof(Small, anc) % 16 == 0, "ancestor rows are read and written as uint4");
 
-// fp32 128 x 128 row tiles (the state, R / U) in the layout of four TMA boxes of
-// 32 columns x 128 rows with the 128-byte swizzle: row t, 4-float chunk c4
-// (0..31) sits in box c4 / 8, its 16-byte slot xor-swizzled by the row, so that
-// a row-per-thread float4 access and a half-warp reading one row's 16 chunks are
-// both bank-conflict free
-__device__ __forceinline__ uint32_t u_off(int t, int c4) {
-  return (uint32_t)((c4 >> 3) * kBoxBytes + t * 128 + (((c4 & 7) ^ (t & 7)) << 4));
-}
-
 // packed strictly-lower triangle of X and Y
 __device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
 
@@ -217,19 +207,6 @@ __device__ __forceinline__ float4 fma4(float a, float4 x, float4 acc) {
   const float2 lo = __ffma2_rn(aa, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
   const float2 hi = __ffma2_rn(aa, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
   return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
-
-// issue the K-steps (16 path entries each) of D (+)= A^T B for MN-major tiles of
-// `ksteps` * 16 rows: A = the path's k rows, B = its w U rows
-__device__ __forceinline__ void umma_commit_rows(uint32_t d_tmem, uint32_t a_base,
-                                                 uint32_t b_base, int ksteps, bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32_amn_bmn(128, 128);
-  for (int s = 0; s < ksteps; ++s) {
-    const uint32_t off = (uint32_t)s * 2 * kMnSbo;
-    umma_bf16(d_tmem, desc_sw128_mnmajor(a_base + off, kMnLbo, kMnSbo),
-              desc_sw128_mnmajor(b_base + off, kMnLbo, kMnSbo), idesc,
-              (accumulate || s > 0) ? 1u : 0u);
-  }
 }
 
 // 4-byte asynchronous copy global -> shared (this thread's cp.async group)
@@ -1159,6 +1136,8 @@ release:
   if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
+}  // namespace
+
 // ---- host side -------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1204,8 +1183,6 @@ bool encode_state_map(CUtensorMap* map, const float* base, long long n_states) {
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool verify_tc_supported(const gdn_tree_dims& d) {
   return d.dtype == GDN_TREE_BF16 && d.dk == kD && d.dv == kD && d.N >= 1 && d.N <= kTile &&

@@ -130,8 +130,9 @@ int gdn_tree_verify(const void *q, const void *k, const void *v,
  * links, else the sequence gets GDN_TREE_STATUS_BAD_PATH.  path_len[b] == 0
  * gives S1 = S0.  S1 may alias S0 exactly (in-place commit); any other
  * overlap is undefined.  dev_status[b] (if non-NULL) is set for every b, to
- * GDN_TREE_STATUS_OK, BAD_PATH or BAD_LAYOUT (this kernel has no on-device
- * wait, so it never reports TIMEOUT).
+ * GDN_TREE_STATUS_OK, BAD_PATH or BAD_LAYOUT, or TIMEOUT if a bounded on-device
+ * wait of the tensor-core commit (taken for bf16, dk = dv = 128 and Lmax > 32:
+ * its state copy and MMAs) ran out; S1[b, ...] is then left unwritten.
  */
 int gdn_tree_commit(const int32_t *path, const int32_t *path_len,
                     const int32_t *parent, const float *U, const void *k,

@@ -25,6 +25,11 @@ def test_byte_model_serving_workload():
                                      + L * 32 * 4 + 32 * 25 * 4)
     assert bench.verify_kernel_name(w) == "verify_tc_kernel"
     assert bench.verify_kernel_name(W.make_config(0)) == "verify_generic_kernel"
+    # the commit: CUDA cores for paths of up to 32 entries, tensor cores past them
+    assert bench.commit_kernel_name(w) == "commit_kernel"
+    w4 = W.make_config(4)
+    assert bench.commit_kernel_name(w4) == "commit_tc_kernel"
+    assert bench.verify_kernel_name(w4) == "verify_mid_kernel"
 
 
 def _rank(rank, world, port, out):

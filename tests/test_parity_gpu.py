@@ -246,3 +246,19 @@ def test_graft_on_gpu(kernel):
     torch.cuda.synchronize()
     assert H.rel_err(o_t.float().cpu().numpy(), o_g[:, L:].float().cpu().numpy()) <= 1e-2
     assert H.rel_err(U_t.cpu().numpy(), U_g[:, :, L:].cpu().numpy()) <= 1e-4
+
+
+@pytest.mark.parametrize("inplace,with_parent", [(False, True), (True, True), (False, False)])
+def test_commit_paths_past_32_entries(inplace, with_parent, kernel):
+    """Paths of up to 64 entries (Lmax > 32: the tensor-core commit for bf16,
+    d = 128; the CUDA-core commit when the generic kernels are forced) on
+    chains, stars and random trees, one sequence with an empty path (S1 = S0),
+    in place or not, with and without the parent-link check."""
+    w = W.make_custom(seed=31, B=6, N=80, Hqk=2, Hv=4, dk=128, dv=128, dtype=W.BF16,
+                      tree="mixed", max_depth=80, lmax=64)
+    w.path_len[3] = 0
+    ref = H.run_oracle(w)
+    gpu = H.run_gpu(w, inplace=inplace, with_parent=with_parent)
+    assert (gpu["status_commit"] == 0).all()
+    H.assert_parity(w, H.compare(w, gpu, ref))
+    assert np.array_equal(gpu["S1"][3], w.S0[3])

@@ -1,11 +1,11 @@
-"""The bounded on-device waits of the tensor-core and 256-node kernels, made to
-run out on purpose (no fault, no trap, nothing left in flight): a short wait limit and a
+"""The bounded on-device waits of the tensor-core verification, the 256-node
+kernel and the tensor-core commit, made to run out on purpose (no fault, no trap, nothing left in flight): a short wait limit and a
 solve-barrier arrival that is withheld (test-only controls read from the
 environment).  The kernel must report GDN_TREE_STATUS_TIMEOUT for the
 sequences it could not finish, leave the other sequences correct, free its
 resources, and leave the context usable: the next normal call on the same
-stream matches the oracle.  (The standalone commit kernel waits on nothing on
-the device, so it has no timeout to provoke.)"""
+stream matches the oracle.  The tensor-core commit's state-copy wait is made to
+run out the same way (a copy that is expected but never issued)."""
 
 import numpy as np
 import pytest
@@ -121,3 +121,37 @@ def test_mid_kernel_solve_wait_runs_out(monkeypatch):
     gpu = H.run_gpu(w)
     assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
     H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+
+
+def test_commit_state_copy_wait_runs_out(monkeypatch):
+    """The tensor-core commit (paths of more than 32 entries): one sequence's
+    state copy is expected but never issued, so its bounded wait runs out."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    w = W.make_custom(seed=905, B=8, N=96, Hqk=2, Hv=4, dk=128, dv=128, dtype=W.BF16,
+                      tree="random", max_depth=24, lmax=48)
+    x = H.to_device(w)
+    _, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"])
+    b = 2
+    monkeypatch.setenv("GDN_TREE_TEST_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("GDN_TREE_TEST_WITHHOLD_COPY", str(b))
+    st = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    S1 = torch.full_like(x["S0"], 5.0)
+    gt.commit(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["S0"], S1=S1,
+              parent=x["parent"], dev_status=st)
+    torch.cuda.synchronize()
+    s = st.cpu().numpy()
+    assert s[b] == gt.STATUS_TIMEOUT and (np.delete(s, b) == 0).all()
+    got = S1.cpu().numpy()
+    assert (got[b] == 5.0).all()  # left unwritten
+    ok = np.arange(w.B) != b
+    S1_ref = oracle.commit_workload(w)
+    assert H.rel_err(got[ok], S1_ref[ok]) <= H.TOL_S1
+    monkeypatch.delenv("GDN_TREE_TEST_WITHHOLD_COPY")
+    monkeypatch.delenv("GDN_TREE_TEST_WAIT_LIMIT_NS")
+    S1b = gt.commit(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["S0"],
+                    parent=x["parent"], dev_status=st)
+    torch.cuda.synchronize()
+    assert (st.cpu().numpy() == 0).all()
+    assert H.rel_err(S1b.cpu().numpy(), S1_ref) <= H.TOL_S1
