@@ -126,16 +126,26 @@ def kernel_source_sha() -> str:
 def verify_kernel_name(w: W.Workload) -> str:
     """The verify kernel the library dispatches for this shape (mirrors the
     C-ABI's rule: for bf16 with dk = dv = 128, the tensor-core kernel up to 128
-    nodes and the 256-node kernel up to 256)."""
+    nodes, the 256-node kernel up to 256 and the chunk pass with R on the tensor
+    cores beyond)."""
     forced = os.environ.get("GDN_TREE_KERNEL", "auto")
-    if w.dtype == W.BF16 and w.dk == 128 and w.dv == 128 and forced not in ("generic", "long"):
+    tc_shape = w.dtype == W.BF16 and w.dk == 128 and w.dv == 128
+    if tc_shape and forced not in ("generic", "long", "long_cuda"):
         if w.N <= 128 and forced != "mid":
             return "verify_tc_kernel"
         if w.N <= 256:
             return "verify_mid_kernel"
-    if w.N > 256 or forced == "long":
+    if w.N > 256 or forced in ("long", "long_cuda"):
+        if tc_shape and forced not in ("generic", "long_cuda"):
+            return "verify_long_tc_kernel"
         return "verify_long_kernel"
     return "verify_generic_kernel"
+
+
+def topw_kernel_name(N: int, c: int, w: int) -> str:
+    """The top-w kernel the library dispatches: the register-list warp kernel for
+    N c <= 512 candidate slots and w <= 4, else the general one."""
+    return "tree_topw_warp_kernel" if N * c <= 512 and w <= 4 else "tree_topw_kernel"
 
 
 def commit_kernel_name(w: W.Workload) -> str:
@@ -742,7 +752,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "tree_verify_speedup": rec_ms / statistics.mean(t_ver),
             "page": "fused tree kernel 7.1x faster than single-branch recurrent verification "
                     "at 126 tree tokens, NVIDIA B200 (DFlash-TfM, results)"}
-        line["tree_build"] = {"kernel": "tree_topw_kernel", "us": tb_us, "B": w.B, "N": w.N,
+        line["tree_build"] = {"kernel": topw_kernel_name(w.N, 4, 4), "us": tb_us, "B": w.B, "N": w.N,
                               "c": 4, "w": 4, "max_depth": 24,
                               "rounds": -(-(w.N - 1) // 4)}
         line["long_trees"] = {

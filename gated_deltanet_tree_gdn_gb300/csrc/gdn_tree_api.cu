@@ -89,16 +89,18 @@ WaitHooks wait_hooks() {
 }
 
 // GDN_TREE_KERNEL=generic forces the general CUDA-core kernel, =mid the
-// 256-node bf16 one and =long the chunked one (used by the tests to cover every
-// kernel on the same shapes); the default picks the tensor-core kernel whenever
-// it takes the shape, then the 256-node bf16 kernel, the general on-chip kernel
-// up to kMaxNHost nodes and the chunked one beyond.
+// 256-node bf16 one, =long the chunked pass (its tensor-core form where it takes
+// the shape) and =long_cuda the chunked pass on CUDA cores (used by the tests to
+// cover every kernel on the same shapes); the default picks the tensor-core
+// kernel whenever it takes the shape, then the 256-node bf16 kernel, the general
+// on-chip kernel up to kMaxNHost nodes and the chunked pass beyond.
 static bool kernel_forced(const char* name) {
   const char* e = getenv("GDN_TREE_KERNEL");
   return e && strcmp(e, name) == 0;
 }
+static bool long_forced() { return kernel_forced("long") || kernel_forced("long_cuda"); }
 static bool force_generic() {
-  return kernel_forced("generic") || kernel_forced("long") || kernel_forced("mid");
+  return kernel_forced("generic") || long_forced() || kernel_forced("mid");
 }
 
 // the tensor-core kernel takes the shape (packed rows: at least one row, for its
@@ -109,9 +111,13 @@ static bool tc_takes(const VerifyArgs& a) {
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   if (tc_takes(a)) return launch_verify_tc(a, stream);
-  if (!kernel_forced("generic") && !kernel_forced("long") && verify_mid_supported(a.d))
+  if (!kernel_forced("generic") && !long_forced() && verify_mid_supported(a.d))
     return launch_verify_mid(a, stream);
-  if (a.d.N > kMaxNHost || kernel_forced("long")) return launch_verify_long(a, stream);
+  if (a.d.N > kMaxNHost || long_forced()) {
+    if (!kernel_forced("long_cuda") && !kernel_forced("generic") && verify_long_tc_supported(a.d))
+      return launch_verify_long_tc(a, stream);
+    return launch_verify_long(a, stream);
+  }
   return launch_verify_generic(a, stream);
 }
 

@@ -93,10 +93,11 @@ struct CommitVerifyArgs {
 // Normal calls use the defaults (2 s, nothing withheld); a test sets them
 // through the environment (read at every launch by wait_hooks()):
 //   GDN_TREE_TEST_WAIT_LIMIT_NS=<ns>       the bound of every wait
-//   GDN_TREE_TEST_WITHHOLD_NODE=<unit>:<node>  the tensor-core and 256-node
-//       verifications of unit (b * Hv + h) never arrive on that node's solve
-//       barrier, so the waits of its descendants run out (thread arrivals only: no
-//       copy or MMA is left in flight)
+//   GDN_TREE_TEST_WITHHOLD_NODE=<unit>:<node>  the tensor-core, 256-node and
+//       tensor-core chunk-pass verifications of unit (b * Hv + h) never arrive on
+//       that node's solve barrier, so the waits of its descendants (in its chunk,
+//       for the chunk pass) run out (thread arrivals only: no copy or MMA is left
+//       in flight)
 //   GDN_TREE_TEST_WITHHOLD_COPY=<b>        the tensor-core commit of sequence b
 //       expects its state copy but never issues it, so the wait for it runs out
 struct WaitHooks {
@@ -116,7 +117,13 @@ cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream);
 size_t verify_long_smem_bytes(int N, int dk, int dv);
 cudaError_t launch_verify_long(const VerifyArgs& a, cudaStream_t stream);
 
-// bf16 trees of up to 256 nodes with dk = dv = 128 (CUDA cores, on chip)
+// bf16 trees of up to kMaxNLongHost nodes with dk = dv = 128: the chunk pass with
+// R and the output seeds on the tensor cores
+bool verify_long_tc_supported(const gdn_tree_dims& d);
+cudaError_t launch_verify_long_tc(const VerifyArgs& a, cudaStream_t stream);
+
+// bf16 trees of up to 256 nodes with dk = dv = 128 (R and the seeds on the tensor
+// cores, the solve on CUDA cores, on chip)
 bool verify_mid_supported(const gdn_tree_dims& d);
 cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream);
 

@@ -159,11 +159,18 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
                       int32_t* __restrict__ n_built) {
   __shared__ int s_ndepth[kWarpsPerCta][kSlots * 32];
   __shared__ float s_lp[kWarpsPerCta][kSlots * 32];
+  // the built nodes' parent, candidate index and score, written out at the end
+  __shared__ int s_par[kWarpsPerCta][kSlots * 32];  // N <= N c <= kSlots 32
+  __shared__ int s_cix[kWarpsPerCta][kSlots * 32];  // N <= N c <= kSlots 32
+  __shared__ float s_sco[kWarpsPerCta][kSlots * 32];  // N <= N c <= kSlots 32
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kWarpsPerCta + warp;
   if (b >= B) return;  // whole warps only: nothing below synchronises across warps
   int* ndepth = s_ndepth[warp];
   float* lp = s_lp[warp];  // the tree's candidate log-probabilities, by key
+  int* npar = s_par[warp];
+  int* ncix = s_cix[warp];
+  float* nsco = s_sco[warp];
   const float* lpb = cand_logp + (size_t)b * N * c;
   int32_t* par = parent + (size_t)b * N;
   int32_t* cix = cand_index ? cand_index + (size_t)b * N : nullptr;
@@ -200,9 +207,9 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
   }
   if (lane == 0) {
     ndepth[0] = 1;
-    par[0] = -1;
-    if (cix) cix[0] = -1;
-    if (sco) sco[0] = 0.f;
+    npar[0] = -1;
+    ncix[0] = -1;
+    nsco[0] = 0.f;
   }
   __syncwarp();
 
@@ -255,9 +262,9 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
       const int node = n + lane, p = node_of(key), j = (int)key - p * c;
       const float s = word_score(x);
       ndepth[node] = lane == 0 ? nd[0] : lane == 1 ? nd[1] : lane == 2 ? nd[2] : nd[3];
-      par[node] = p;
-      if (cix) cix[node] = j;
-      if (sco) sco[node] = s;
+      npar[node] = p;
+      ncix[node] = j;
+      nsco[node] = s;
     }
     // the new nodes offer their candidates: keys n c .. (n + popped) c - 1, the
     // ones of this lane's slots (one insertion each)
@@ -274,11 +281,12 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
     __syncwarp();  // the new nodes' depths are in place for the next round
     n += popped;
   }
-  // nodes that could not be built
-  for (int i = n + lane; i < N; i += 32) {
-    par[i] = -2;
-    if (cix) cix[i] = -2;
-    if (sco) sco[i] = CUDART_NAN_F;
+  // the tree out (coalesced); nodes that could not be built
+  for (int i = lane; i < N; i += 32) {
+    const bool built = i < n;
+    par[i] = built ? npar[i] : -2;
+    if (cix) cix[i] = built ? ncix[i] : -2;
+    if (sco) sco[i] = built ? nsco[i] : CUDART_NAN_F;
   }
   if (lane == 0 && n_built) n_built[b] = n;
 }

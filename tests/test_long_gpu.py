@@ -1,7 +1,8 @@
 """GPU parity of trees longer than the on-chip kernels take (N up to 1024): the
 two-level chunk pass of the verification and commit paths longer than 256
 entries, through the C ABI, against the fp64 oracle.  The chunked kernel is
-also forced onto small shapes (GDN_TREE_KERNEL=long), where its chunk
+also forced onto small shapes (GDN_TREE_KERNEL=long: its tensor-core form for
+bf16 with dk = dv = 128; =long_cuda: the CUDA-core form), where its chunk
 boundary (128 nodes) and ragged tails meet every tree family."""
 
 import numpy as np
@@ -32,15 +33,31 @@ LONG = [
 ]
 
 
-@pytest.mark.parametrize("idx", range(len(LONG)), ids=["x".join(map(str, c[:8])) for c in LONG])
-def test_long_trees_match_oracle(idx, monkeypatch):
-    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+_ORACLE = {}  # the oracle's results by case, shared by the kernels' runs
+
+
+def _long_case(idx):
     B, N, Hqk, Hv, dk, dv, dt, tree, depth = LONG[idx]
     w = W.make_custom(seed=700 + idx, B=B, N=N, Hqk=Hqk, Hv=Hv, dk=dk, dv=dv, dtype=dt,
                       tree=tree, max_depth=depth)
+    if idx not in _ORACLE:
+        _ORACLE[idx] = H.run_oracle(w)
+    return w, _ORACLE[idx]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "long_cuda"])
+@pytest.mark.parametrize("idx", range(len(LONG)), ids=["x".join(map(str, c[:8])) for c in LONG])
+def test_long_trees_match_oracle(idx, kernel, monkeypatch):
+    """The default dispatch (bf16 with dk = dv = 128: the chunk pass with R and the
+    seeds on the tensor cores) and the chunk pass on CUDA cores."""
+    if kernel == "auto":
+        monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("GDN_TREE_KERNEL", kernel)
+    w, ref = _long_case(idx)
     gpu = H.run_gpu(w)
     assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
-    H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+    H.assert_parity(w, H.compare(w, gpu, ref))
 
 
 def test_commit_path_longer_than_256():
@@ -67,9 +84,10 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("kernel", ["long", "long_cuda"])
 @pytest.mark.parametrize("idx", range(len(SMALL)), ids=["x".join(map(str, c)) for c in SMALL])
-def test_chunked_kernel_forced_on_small_shapes(idx, monkeypatch):
-    monkeypatch.setenv("GDN_TREE_KERNEL", "long")
+def test_chunked_kernel_forced_on_small_shapes(idx, kernel, monkeypatch):
+    monkeypatch.setenv("GDN_TREE_KERNEL", kernel)
     B, N, Hqk, Hv, dk, dv, dt, tree = SMALL[idx]
     w = W.make_custom(seed=760 + idx, B=B, N=N, Hqk=Hqk, Hv=Hv, dk=dk, dv=dv, dtype=dt,
                       tree=tree, max_depth=N)

@@ -1,5 +1,6 @@
 """The bounded on-device waits of the tensor-core verification, the 256-node
-kernel and the tensor-core commit, made to run out on purpose (no fault, no trap, nothing left in flight): a short wait limit and a
+kernel, the tensor-core chunk pass and the tensor-core commit, made to run out
+on purpose (no fault, no trap, nothing left in flight): a short wait limit and a
 solve-barrier arrival that is withheld (test-only controls read from the
 environment).  The kernel must report GDN_TREE_STATUS_TIMEOUT for the
 sequences it could not finish, leave the other sequences correct, free its
@@ -121,6 +122,34 @@ def test_mid_kernel_solve_wait_runs_out(monkeypatch):
     gpu = H.run_gpu(w)
     assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
     H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+
+
+def test_long_kernel_parent_wait_runs_out(monkeypatch):
+    """The chunk pass with R on the tensor cores (trees past 256 nodes): a withheld
+    arrival of a node whose child sits in the same chunk makes that child's bounded
+    wait run out."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    w = W.make_custom(seed=905, B=3, N=300, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="random", max_depth=24)
+    b, h = 1, 1
+    kids = [t for t in range(w.N) if w.parent[b, t] >= 128 * (t // 128)]
+    node = int(w.parent[b, kids[-1]])
+    monkeypatch.setenv("GDN_TREE_TEST_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("GDN_TREE_TEST_WITHHOLD_NODE", f"{b * w.Hv + h}:{node}")
+    x = H.to_device(w)
+    st = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    o, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
+                     dev_status=st)
+    torch.cuda.synchronize()
+    s = st.cpu().numpy()
+    assert s[b] == gt.STATUS_TIMEOUT
+    assert (np.delete(s, b) == gt.STATUS_OK).all()
+    ok = np.arange(w.B) != b
+    o_ref, U_ref = oracle.verify_workload(w)
+    assert H.rel_err(o.float().cpu().numpy()[ok], o_ref[ok]) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U.cpu().numpy()[ok], U_ref[ok]) <= H.TOL_U
 
 
 def test_commit_state_copy_wait_runs_out(monkeypatch):
