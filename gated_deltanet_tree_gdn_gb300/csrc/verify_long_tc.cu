@@ -10,23 +10,27 @@
 //   Y[t,s] = e^{g_t - g_s} q_t.k_s         (s on the root-to-t path, t included).
 //
 // One CTA (512 threads) per (sequence b, v-head h).  The tree's parent links are
-// checked and g and the depths come from pointer jumping (20 bytes of shared
-// memory a node, no bitsets).  S0 is split once into bf16 hi + lo (MN-major,
-// 128-byte swizzle) and stays in shared memory.  The nodes are cut in index (a
-// topological) order into chunks of 128; for each chunk
+// checked; pointer jumping gives g, the depths and, kept level by level, the
+// ancestor at every power-of-two distance (so a node's ancestor at any depth is a
+// few lookups away; 38 bytes of shared memory a node, no bitsets).  S0 is split
+// once into bf16 hi + lo (MN-major, 128-byte swizzle) and stays in shared memory.
+// The nodes are cut in index (a topological) order into chunks of 128; for each
+// chunk
 //  1. its K and Q rows land as 128-row K-major tiles (cp.async; rows past the
 //     tree zero); one thread issues K S0_hi + K S0_lo and Q S0_hi + Q S0_lo
 //     (tcgen05.mma) into 256 TMEM columns; the warps read them back by TMEM lane
 //     group, a thread per node: r_t = beta_t (v_t - gamma_t (K S0)_t) goes to the
 //     chunk's U rows in shared memory (where the tiles were), the seed
 //     gamma_t (Q S0)_t to t's row of U in global memory;
-//  2. the chunk's nodes, in depth order, take a warp each as a dataflow: a node
-//     waits (bounded, on its parent's mbarrier) until its parent is final, which
-//     makes all its ancestors final, then walks its strict ancestors parent
-//     first, four at a time: X[t,s] and Y[t,s] as warp dots of the k rows,
-//     u_t -= X[t,s] u_s and o_t += Y[t,s] u_s, with u_s from the chunk's rows in
-//     shared memory or, for an earlier chunk, from U in global memory (final
-//     since the chunk boundary's block barrier).  The node's own term closes o_t;
+//  2. the chunk's nodes, in depth order, take a warp each as a streaming
+//     dataflow.  The node's path goes root first, 32 entries at a time, an entry
+//     a lane.  X[t,s] and Y[t,s] come from warp dots of k_s with k_t and q_t (the k
+//     rows load whole, eight entries' sixteen sums reduced across the lanes
+//     together).  The terms u_t -= X[t,s] u_s and o_t += Y[t,s] u_s follow: rows
+//     of earlier chunks from U in global memory, eight at a time (final since the
+//     chunk boundary's block barrier), then rows of this chunk from shared memory,
+//     four at a time after a bounded wait on the mbarrier of the last of the four
+//     (a path's nodes complete in path order).  The node's own term closes o_t;
 //     u_t replaces the seed in U and joins the chunk's rows, and the node's
 //     barrier is arrived on.
 // The unfinished node of lowest depth order in a chunk never waits on an
@@ -45,12 +49,14 @@ constexpr int kD = 128;      // dk = dv
 constexpr int kChunk = 128;  // nodes a chunk: one M = 128 tile
 constexpr int kNodesPerThread = kMaxNLong / kThreads;
 static_assert(kMaxNLong % kThreads == 0, "pointer jumping assigns whole nodes per thread");
-constexpr int kBatch = 4;  // ancestors whose rows are loaded together
 constexpr int kTmemCols = 256;
+// ancestor tables for the distances 2^0 .. 2^10 (every distance below kMaxNLong)
+constexpr int kLiftLevels = 11;
+static_assert((1 << (kLiftLevels - 1)) >= kMaxNLong, "a distance needs at most kLiftLevels - 1 bits");
 
 struct LongTcSmem {
   // byte offsets into dynamic shared memory, from a 1024-byte aligned base
-  size_t SK, T, parent, jump, depth, g, beta, order, bar, flag, total;
+  size_t SK, T, V, lift, depth, g, beta, order, bar, flag, total;
 };
 
 __host__ __device__ inline size_t align16t(size_t x) { return (x + 15) & ~size_t(15); }
@@ -60,8 +66,8 @@ __host__ __device__ inline LongTcSmem long_tc_smem_layout(int N) {
   size_t o = 0;
   L.SK = o;     o += sizeof(float) * kD * kD;       // S0 (fp32), then its hi / lo operands
   L.T = o;      o += sizeof(float) * kChunk * kD;   // K, Q tiles; then the chunk's R / U rows
-  L.parent = o; o = align16t(o + sizeof(int) * N);
-  L.jump = o;   o = align16t(o + sizeof(int) * N);
+  L.V = o;      o += sizeof(uint16_t) * kChunk * kD;  // the chunk's v rows (bf16, swizzled)
+  L.lift = o;   o = align16t(o + sizeof(int16_t) * kLiftLevels * N);  // [level][node]
   L.depth = o;  o = align16t(o + sizeof(int) * N);
   L.g = o;      o = align16t(o + sizeof(df) * N);
   L.beta = o;   o = align16t(o + sizeof(float) * N);
@@ -70,6 +76,13 @@ __host__ __device__ inline LongTcSmem long_tc_smem_layout(int N) {
   L.flag = o;   o = align16t(o + sizeof(uint64_t) * 2);  // status flag, TMEM base; MMA barrier
   L.total = o + 1024;  // + alignment slack
   return L;
+}
+
+// byte offset of 16-byte chunk c (of 16) of row r in the staged v rows (chunks
+// XOR-swizzled by the row, so that 32 threads reading one chunk of 32 rows meet
+// two at a bank group at most)
+__device__ __forceinline__ uint32_t v_chunk(int r, int c) {
+  return (uint32_t)r * (kD * 2) + (uint32_t)((c ^ (r & 15)) << 4);
 }
 
 __device__ __forceinline__ void cp_async16t(void* dst, const void* src) {
@@ -87,9 +100,8 @@ __device__ __forceinline__ void bf16x8_to_f32t(const uint4 q, float (&v)[8]) {
   }
 }
 
-// four consecutive bf16 elements as fp32
-__device__ __forceinline__ float4 load4bf(const __nv_bfloat16* p) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+// four bf16 elements (as loaded) as fp32
+__device__ __forceinline__ float4 bf16x4_to_f32t(uint2 raw) {
   return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
 }
@@ -98,11 +110,12 @@ __device__ __forceinline__ float dot4t(float4 a, float4 b) {
   return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
 }
 
-__device__ __forceinline__ void axpy4t(float4& y, float a, float4 x) {
-  y.x = fmaf(a, x.x, y.x);
-  y.y = fmaf(a, x.y, y.y);
-  y.z = fmaf(a, x.z, y.z);
-  y.w = fmaf(a, x.w, y.w);
+// acc + a x, as two packed fp32x2 FMAs (same rounding as four fmaf)
+__device__ __forceinline__ float4 fma4t(float a, float4 x, float4 acc) {
+  const float2 aa = make_float2(a, a);
+  const float2 lo = __ffma2_rn(aa, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
+  const float2 hi = __ffma2_rn(aa, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -122,8 +135,8 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   const LongTcSmem L = long_tc_smem_layout(Nmax);
   unsigned char* sSK = smem + L.SK;
   unsigned char* sT = smem + L.T;
-  int* sPar = reinterpret_cast<int*>(smem + L.parent);
-  int* sJump = reinterpret_cast<int*>(smem + L.jump);
+  unsigned char* sV = smem + L.V;
+  int16_t* sLift = reinterpret_cast<int16_t*>(smem + L.lift);  // [0]: the parent links
   int* sDepth = reinterpret_cast<int*>(smem + L.depth);
   df* sG = reinterpret_cast<df*>(smem + L.g);
   float* sBeta = reinterpret_cast<float*>(smem + L.beta);
@@ -150,8 +163,7 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   int bad = 0;
   for (int t = tid; t < N; t += kThreads) {
     const int p = parent[row + t];
-    sPar[t] = p;
-    sJump[t] = p;
+    sLift[t] = (int16_t)p;
     sDepth[t] = 1;
     sG[t] = df{log_alpha[(row + t) * Hv + h], 0.f};
     sBeta[t] = beta[(row + t) * Hv + h];
@@ -170,17 +182,21 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   // the tree is valid: TMEM for the chunk's two accumulators
   if (warp == 0) sm100::tmem_alloc(reinterpret_cast<uint32_t*>(sFlag + 1), kTmemCols);
 
-  // ---- pointer jumping: g_t = sum of log alpha over P(t), depth_t = |P(t)| ----------
-  for (int span = 1; span < N; span <<= 1) {
+  // ---- pointer jumping: g_t = sum of log alpha over P(t), depth_t = |P(t)|; level
+  // i + 1 of the ancestor table (distance 2^(i+1)) from level i.  A level past the
+  // last one built is never read: every distance asked for is below the depth.
+  for (int i = 0; i + 1 < kLiftLevels; ++i) {
+    const int16_t* lv = sLift + (size_t)i * Nmax;
     int j[kNodesPerThread], jj[kNodesPerThread], dj[kNodesPerThread];
     df gj[kNodesPerThread];
     int live = 0;
 #pragma unroll
     for (int m = 0; m < kNodesPerThread; ++m) {
       const int t = tid + m * kThreads;
-      j[m] = t < N ? sJump[t] : -1;
+      j[m] = t < N ? lv[t] : -1;
+      jj[m] = -1;
       if (j[m] >= 0) {
-        jj[m] = sJump[j[m]];
+        jj[m] = lv[j[m]];
         dj[m] = sDepth[j[m]];
         gj[m] = sG[j[m]];
         live = 1;
@@ -190,10 +206,10 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 #pragma unroll
     for (int m = 0; m < kNodesPerThread; ++m) {
       const int t = tid + m * kThreads;
+      if (t < N) sLift[(size_t)(i + 1) * Nmax + t] = (int16_t)jj[m];
       if (j[m] >= 0) {
         sG[t] = df_add(sG[t], gj[m]);
         sDepth[t] += dj[m];
-        sJump[t] = jj[m];
       }
     }
     __syncthreads();
@@ -237,7 +253,7 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   for (int c0 = 0, ci = 0; c0 < N; c0 += kChunk, ++ci) {
     const int nc = min(kChunk, N - c0);
     const uint32_t parity = (uint32_t)(ci & 1);
-    // ---- 1. the chunk's K and Q tiles; R and the seeds on the tensor cores --------
+    // ---- 1. the chunk's K and Q tiles and v rows; R and the seeds on the tensor cores
     for (int e = tid; e < 2 * kChunk * 16; e += kThreads) {
       const int ch = e & 15, rq = e >> 4, isq = rq >> 7, r = rq & (kChunk - 1);
       unsigned char* dst = sT + isq * 32768 + sm100::sw128_chunk(r, ch);
@@ -245,6 +261,10 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         cp_async16t(dst, (isq ? q : k) + ((row + c0 + r) * Hqk + hq) * kD + 8 * ch);
       else
         *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int e = tid; e < nc * 16; e += kThreads) {
+      const int ch = e & 15, r = e >> 4;
+      cp_async16t(sV + v_chunk(r, ch), v + ((row + c0 + r) * Hv + h) * kD + 8 * ch);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     // the chunk's depth order (index order within a depth)
@@ -293,11 +313,10 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         if (!live) continue;
         const int col0 = 64 * half + 32 * c32;
         if (acc == 0) {
-          const uint4* vr = reinterpret_cast<const uint4*>(v + ((row + t) * Hv + h) * kD + col0);
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             float vv[8];
-            bf16x8_to_f32t(vr[m], vv);
+            bf16x8_to_f32t(*reinterpret_cast<const uint4*>(sV + v_chunk(tl, col0 / 8 + m)), vv);
             const int cc = col0 / 4 + 2 * m;
             *reinterpret_cast<float4*>(sT + sm100::u_off(tl, cc)) =
                 make_float4(bt * (vv[0] - gam * r[8 * m]), bt * (vv[1] - gam * r[8 * m + 1]),
@@ -318,69 +337,159 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     sm100::tc_fence_before_sync();
     __syncthreads();  // R rows and seeds in place; TMEM free for the next chunk
 
-    // ---- 2. the chunk's solve: a warp per node, depth order, parent waits ---------
+    // the next chunk's k, q and v rows start coming into L2 during this solve
+    if (c0 + kChunk < N) {
+      const int n1 = min(kChunk, N - c0 - kChunk);
+      for (int e = tid; e < 3 * n1; e += kThreads) {
+        const int which = e / n1, r = c0 + kChunk + e - which * n1;
+        const __nv_bfloat16* src = which == 2 ? v + ((row + r) * Hv + h) * kD
+                                              : (which ? q : k) + ((row + r) * Hqk + hq) * kD;
+        sm100::bulk_prefetch_l2(src, kD * 2);
+      }
+    }
+    // ---- 2. the chunk's solve: a warp per node, depth order, streaming waits ------
+    // k_t and q_t of the warp's next node, loaded one node ahead
+    auto kq_of = [&](int task, uint2& kr, uint2& qr) {
+      kr = qr = make_uint2(0u, 0u);
+      if (task < nc) {
+        const size_t tk = ((row + c0 + sOrder[task]) * Hqk + hq) * kD + c4;
+        kr = *reinterpret_cast<const uint2*>(k + tk);
+        qr = *reinterpret_cast<const uint2*>(q + tk);
+      }
+    };
+    uint2 knext, qnext;
+    kq_of(warp, knext, qnext);
     for (int task = warp; task < nc; task += kWarps) {
       const int tl = sOrder[task], t = c0 + tl;
-      const int p = sPar[t];
-      const size_t tk = ((row + t) * Hqk + hq) * kD;
-      const float4 kt = load4bf(k + tk + c4);
-      const float4 qt = load4bf(q + tk + c4);
+      const int nA = sDepth[t] - 1;  // strict ancestors
       const df gt = sG[t];
       const float bt = sBeta[t];
+      const float4 kt = bf16x4_to_f32t(knext), qt = bf16x4_to_f32t(qnext);
+      kq_of(task + kWarps, knext, qnext);
       float* urow = Ubh + (size_t)t * kD + c4;
-      float4 oc = *reinterpret_cast<const float4*>(urow);  // the seed
-      float4 u = *urow_s(tl);                               // r_t
-      if (p >= c0 && !sm100::mbar_wait(&sBar[p - c0], parity, hk.limit_ns)) timed_out = true;
-      // the strict ancestors, parent first, kBatch at a time
-      int s = p;
-      while (s >= 0) {
-        int a[kBatch];
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-          a[e] = s;
-          if (s >= 0) s = sPar[s];
+      const float4 seed = *reinterpret_cast<const float4*>(urow);
+      float4 u = *urow_s(tl);  // r_t
+      float4 au = make_float4(0.f, 0.f, 0.f, 0.f), ao = au;
+      // the path root first, 32 entries at a time: entry n is the ancestor at depth
+      // n + 1, in lane n % 32
+      for (int n0 = 0; n0 < nA; n0 += 32) {
+        const int cnt = min(32, nA - n0);
+        int a = t;
+        if (lane < cnt) {
+          for (int m = nA - n0 - lane, bit = 0; m; m >>= 1, ++bit)
+            if (m & 1) a = sLift[(size_t)bit * Nmax + a];
         }
-        float4 ka[kBatch], ua[kBatch];
-        float xk[kBatch], yq[kBatch];
+        // entries of earlier chunks: a prefix (indices fall along a path)
+        const int nE = __popc(__ballot_sync(0xffffffffu, lane < cnt && a < c0));
+        // the first eight earlier-chunk u rows start coming
+        float4 ue[8];
 #pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-          ka[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-          ua[e] = ka[e];
-          if (a[e] >= 0) {
-            ka[e] = load4bf(k + ((row + a[e]) * Hqk + hq) * kD + c4);
-            ua[e] = a[e] >= c0 ? *urow_s(a[e] - c0)
-                               : *reinterpret_cast<const float4*>(Ubh + (size_t)a[e] * kD + c4);
+        for (int jj = 0; jj < 8; ++jj) {
+          const int ss = __shfl_sync(0xffffffffu, a, jj);
+          ue[jj] = jj < nE ? *reinterpret_cast<const float4*>(Ubh + (size_t)ss * kD + c4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // X[t,a] and Y[t,a] before their factors: the dots of k_a with k_t and q_t,
+        // eight entries at a time as warp dots (a lane holds 4 of the 128 elements,
+        // the k rows load whole), the sixteen sums reduced across the lanes at once:
+        // each exchange step halves the values a lane carries, so that lane L ends
+        // with value L / 2 (entry L / 4; its k dot for L / 2 even, its q dot for odd)
+        float dkk = 0.f, dqk = 0.f;
+        for (int j0 = 0; j0 < cnt; j0 += 8) {
+          float vs[16];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int ss = __shfl_sync(0xffffffffu, a, (j0 + jj) & 31);
+            const float4 ks = j0 + jj < cnt
+                                  ? bf16x4_to_f32t(*reinterpret_cast<const uint2*>(
+                                        k + ((row + ss) * Hqk + hq) * kD + c4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            vs[2 * jj] = dot4t(kt, ks);
+            vs[2 * jj + 1] = dot4t(qt, ks);
+          }
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1) {  // 16 -> 8 -> 4 -> 2 -> 1 values a lane
+            const bool up = (lane >> 1) & w;  // this lane keeps the upper half
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float keep = up ? vs[w + i] : vs[i];
+              const float send = up ? vs[i] : vs[w + i];
+              vs[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+            }
+          }
+          vs[0] += __shfl_xor_sync(0xffffffffu, vs[0], 1);
+          // entry j0 + i: its k dot in lane 4 i, its q dot in lane 4 i + 2
+          const int i = lane - j0;
+          const float xk = __shfl_sync(0xffffffffu, vs[0], (4 * i) & 31);
+          const float yq = __shfl_sync(0xffffffffu, vs[0], (4 * i + 2) & 31);
+          if (i >= 0 && i < 8) {
+            dkk = xk;
+            dqk = yq;
           }
         }
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-          xk[e] = dot4t(kt, ka[e]);
-          yq[e] = dot4t(qt, ka[e]);
+        float xe = 0.f, ye = 0.f;
+        if (lane < cnt) {
+          const float dec = expf(df_diff(gt, sG[a]));
+          xe = bt * dec * dkk;
+          ye = dec * dqk;
         }
+        // the earlier chunks' terms (final rows, no wait), eight at a time
+        for (int j0 = 0; j0 < nE; j0 += 8) {
+          if (j0 > 0) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-          for (int e = 0; e < kBatch; ++e) {
-            xk[e] += __shfl_xor_sync(0xffffffffu, xk[e], off);
-            yq[e] += __shfl_xor_sync(0xffffffffu, yq[e], off);
+            for (int jj = 0; jj < 8; ++jj) {
+              const int ss = __shfl_sync(0xffffffffu, a, (j0 + jj) & 31);
+              ue[jj] = j0 + jj < nE ? *reinterpret_cast<const float4*>(Ubh + (size_t)ss * kD + c4)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
 #pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-          if (a[e] >= 0) {
-            const float dec = expf(df_diff(gt, sG[a[e]]));
-            axpy4t(u, -(bt * dec * xk[e]), ua[e]);
-            axpy4t(oc, dec * yq[e], ua[e]);
+          for (int jj = 0; jj < 8; ++jj) {
+            const float xx = __shfl_sync(0xffffffffu, xe, (j0 + jj) & 31);
+            const float yy = __shfl_sync(0xffffffffu, ye, (j0 + jj) & 31);
+            const bool use = j0 + jj < nE;
+            au = fma4t(use ? -xx : 0.f, ue[jj], au);
+            ao = fma4t(use ? yy : 0.f, ue[jj], ao);
+          }
+        }
+        // this chunk's terms, four entries at a time: the rows must be final first;
+        // the last of the four is the deepest, and a path's nodes complete in path
+        // order, so its being final makes all four final
+        for (int j0 = nE; j0 < cnt; j0 += 4) {
+          const int m = min(4, cnt - j0);
+          const int alast = __shfl_sync(0xffffffffu, a, j0 + m - 1);
+          if (!sm100::mbar_wait(&sBar[alast - c0], parity, hk.limit_ns)) timed_out = true;
+          float4 us[4];
+          float xj[4], yj[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int ss = __shfl_sync(0xffffffffu, a, (j0 + jj) & 31);
+            const float xx = __shfl_sync(0xffffffffu, xe, (j0 + jj) & 31);
+            const float yy = __shfl_sync(0xffffffffu, ye, (j0 + jj) & 31);
+            const bool use = jj < m;
+            xj[jj] = use ? xx : 0.f;
+            yj[jj] = use ? yy : 0.f;
+            us[jj] = *urow_s(use ? ss - c0 : tl);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            au = fma4t(-xj[jj], us[jj], au);
+            ao = fma4t(yj[jj], us[jj], ao);
           }
         }
       }
+      u.x += au.x;
+      u.y += au.y;
+      u.z += au.z;
+      u.w += au.w;
       // the node's own term Y[t,t] u_t = (q_t . k_t) u_t
       const float self = warp_sum(dot4t(qt, kt));
-      axpy4t(oc, self, u);
+      ao = fma4t(self, u, ao);
       *urow_s(tl) = u;
       *reinterpret_cast<float4*>(urow) = u;
       __nv_bfloat16* orow = o + ((row + t) * Hv + h) * kD + c4;
-      const __nv_bfloat162 p01 = __floats2bfloat162_rn(oc.x, oc.y);
-      const __nv_bfloat162 p23 = __floats2bfloat162_rn(oc.z, oc.w);
+      const __nv_bfloat162 p01 = __floats2bfloat162_rn(seed.x + ao.x, seed.y + ao.y);
+      const __nv_bfloat162 p23 = __floats2bfloat162_rn(seed.z + ao.z, seed.w + ao.w);
       *reinterpret_cast<uint2*>(orow) = make_uint2(*reinterpret_cast<const uint32_t*>(&p01),
                                                    *reinterpret_cast<const uint32_t*>(&p23));
       __syncwarp();  // every lane's part of u_t is in place before the arrival
