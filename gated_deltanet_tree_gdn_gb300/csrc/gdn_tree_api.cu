@@ -109,15 +109,24 @@ static bool tc_takes(const VerifyArgs& a) {
   return !force_generic() && verify_tc_supported(a.d) && (!a.lay.packed() || a.lay.T > 0);
 }
 
+// past 128 nodes (bf16, d = 128) the sequences whose tree is one chain go to the
+// chain kernel first; the tree kernel launched next leaves them
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   if (tc_takes(a)) return launch_verify_tc(a, stream);
-  if (!kernel_forced("generic") && !long_forced() && verify_mid_supported(a.d))
-    return launch_verify_mid(a, stream);
-  if (a.d.N > kMaxNHost || long_forced()) {
-    if (!kernel_forced("long_cuda") && !kernel_forced("generic") && verify_long_tc_supported(a.d))
-      return launch_verify_long_tc(a, stream);
-    return launch_verify_long(a, stream);
+  VerifyArgs t = a;
+  const bool forced = getenv("GDN_TREE_KERNEL") && *getenv("GDN_TREE_KERNEL") &&
+                      !kernel_forced("auto");
+  const bool mid = !kernel_forced("generic") && !long_forced() && verify_mid_supported(a.d);
+  const bool long_tc = (a.d.N > kMaxNHost || long_forced()) && !kernel_forced("long_cuda") &&
+                       !kernel_forced("generic") && verify_long_tc_supported(a.d);
+  if (!forced && (mid || long_tc) && verify_chain_supported(a.d)) {
+    const cudaError_t err = launch_verify_chain(a, stream);
+    if (err != cudaSuccess) return err;
+    t.skip_chains = true;
   }
+  if (mid) return launch_verify_mid(t, stream);
+  if (long_tc) return launch_verify_long_tc(t, stream);
+  if (a.d.N > kMaxNHost || long_forced()) return launch_verify_long(a, stream);
   return launch_verify_generic(a, stream);
 }
 

@@ -123,7 +123,8 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
                       const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
                       const float* __restrict__ beta, const int32_t* __restrict__ parent,
                       const float* __restrict__ S0, __nv_bfloat16* __restrict__ o, float* U,
-                      gdn_tree_dims d, int32_t* dev_status, SeqLayout lay, WaitHooks hk) {
+                      gdn_tree_dims d, int32_t* dev_status, SeqLayout lay, WaitHooks hk,
+                      int skip_chains) {
   // U is read back (seeds, earlier chunks' rows) after this CTA wrote it, so it is
   // neither const nor restrict: its loads must not take the read-only path.
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -160,9 +161,10 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   // ---- the tree: load, validate, seed the pointer jumping -------------------------
-  int bad = 0;
+  int bad = 0, notchain = 0;
   for (int t = tid; t < N; t += kThreads) {
     const int p = parent[row + t];
+    notchain |= p != t - 1;
     sLift[t] = (int16_t)p;
     sDepth[t] = 1;
     sG[t] = df{log_alpha[(row + t) * Hv + h], 0.f};
@@ -176,6 +178,10 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   bad = __syncthreads_or(bad);
   if (bad) {
     if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+  if (skip_chains && !__syncthreads_or(notchain)) {  // one chain: the chain kernel's
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
@@ -521,7 +527,8 @@ cudaError_t launch_verify_long_tc(const VerifyArgs& a, cudaStream_t stream) {
   verify_long_tc_kernel<<<grid, kThreads, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
       static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks());
+      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks(),
+      a.skip_chains ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -117,7 +117,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   const float* __restrict__ beta, const int32_t* __restrict__ parent,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
-                  WaitHooks hk) {
+                  WaitHooks hk, int skip_chains) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
@@ -172,11 +172,12 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   // ---- 1. the tree ------------------------------------------------------------
-  int bad = 0;
+  int bad = 0, notchain = 0;
   if (tid < N) {
     const int p = parent[row + tid];
     sPar[tid] = p;
     bad = (p < -1 || p >= tid);
+    notchain = p != tid - 1;
     sBeta[tid] = beta[(row + tid) * Hv + h];
     sLa[tid] = log_alpha[(row + tid) * Hv + h];
   }
@@ -185,6 +186,10 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   bad = __syncthreads_or(bad);
   if (bad) {
     if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+  if (skip_chains && !__syncthreads_or(notchain)) {  // one chain: the chain kernel's
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
@@ -513,7 +518,8 @@ cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream) {
   verify_mid_kernel<<<grid, kThreads, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
       static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks());
+      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks(),
+      a.skip_chains ? 1 : 0);
   return cudaGetLastError();
 }
 

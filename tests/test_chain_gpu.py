@@ -1,0 +1,77 @@
+"""GPU parity of the chain kernel (trees that are one branch, parent of t = t - 1,
+past 128 nodes, bf16 with dk = dv = 128): the chunkwise form with the state
+passed between 64-node chunks, through the C ABI, against the fp64 oracle.  Chains
+sit beside other tree families in one call too (the tree kernel launched after
+the chain kernel leaves the chains to it)."""
+
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    import gated_deltanet_tree_gdn_gb300 as gt
+    gt.build_library()
+    gt.load()
+
+
+CHAINS = [
+    # (B, N, Hqk, Hv): chunk tails of every size, one and several chunks
+    (2, 129, 1, 2),
+    (2, 200, 2, 4),
+    (1, 256, 1, 2),
+    (2, 257, 1, 2),
+    (1, 513, 1, 2),
+    (1, 1024, 1, 2),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(CHAINS)), ids=["x".join(map(str, c)) for c in CHAINS])
+def test_chains_match_oracle(idx, monkeypatch):
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    B, N, Hqk, Hv = CHAINS[idx]
+    w = W.make_custom(seed=1100 + idx, B=B, N=N, Hqk=Hqk, Hv=Hv, dk=128, dv=128,
+                      dtype=W.BF16, tree="chain", max_depth=N)
+    gpu = H.run_gpu(w)
+    assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
+    H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+
+
+def test_chain_strong_decay_and_high_beta(monkeypatch):
+    """log alpha down to -4 a node and beta = 0.99: the state's decay between chunks
+    spans e^-256, and the terms inside a chunk are large."""
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    w = W.make_custom(seed=1120, B=2, N=256, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="chain", max_depth=256, la_range=(0.01, 4.0), beta_kind="uniform")
+    w.beta[:] = np.float32(0.99)
+    gpu = H.run_gpu(w)
+    H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+    assert np.isfinite(gpu["o"]).all() and np.isfinite(gpu["U"]).all()
+
+
+@pytest.mark.parametrize("N", [256, 400])
+def test_chains_beside_other_trees(N, monkeypatch):
+    """Every tree family in one call: the chain goes to the chain kernel, the others
+    to the 256-node kernel (N = 256) or the chunk pass (N = 400)."""
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    w = W.make_custom(seed=1130 + N, B=6, N=N, Hqk=2, Hv=4, dk=128, dv=128, dtype=W.BF16,
+                      tree="mixed", max_depth=N)
+    gpu = H.run_gpu(w)
+    assert (gpu["status_verify"] == 0).all() and (gpu["status_commit"] == 0).all()
+    H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+
+
+@pytest.mark.parametrize("kernel", ["mid", "long"])
+def test_tree_kernels_still_take_chains_when_forced(kernel, monkeypatch):
+    """With a kernel forced the chain kernel stays out: the tree kernels' own
+    chain handling is covered on the same shape."""
+    monkeypatch.setenv("GDN_TREE_KERNEL", kernel)
+    w = W.make_custom(seed=1140, B=2, N=200, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                      tree="chain", max_depth=200)
+    gpu = H.run_gpu(w)
+    H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
