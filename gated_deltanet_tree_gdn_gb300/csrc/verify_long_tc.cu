@@ -154,6 +154,11 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   }
   const size_t row = (size_t)lay.row0(b, Nmax);
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
+  if (skip_chains) {  // one chain, taken by the chain kernel: leave before any copy starts
+    int notchain = 0;
+    for (int t = tid; t < N; t += kThreads) notchain |= parent[row + t] != t - 1;
+    if (!__syncthreads_or(notchain)) return;
+  }
 
   // S0 starts streaming into shared memory (fp32) at once
   const float* S0bh = S0 + ((size_t)st * Hv + h) * kD * kD;
@@ -161,10 +166,9 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   // ---- the tree: load, validate, seed the pointer jumping -------------------------
-  int bad = 0, notchain = 0;
+  int bad = 0;
   for (int t = tid; t < N; t += kThreads) {
     const int p = parent[row + t];
-    notchain |= p != t - 1;
     sLift[t] = (int16_t)p;
     sDepth[t] = 1;
     sG[t] = df{log_alpha[(row + t) * Hv + h], 0.f};
@@ -178,10 +182,6 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   bad = __syncthreads_or(bad);
   if (bad) {
     if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    return;
-  }
-  if (skip_chains && !__syncthreads_or(notchain)) {  // one chain: the chain kernel's
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }

@@ -78,10 +78,11 @@ __host__ __device__ inline MidSmem mid_smem_layout(int N) {
   return L;
 }
 
-// float offset of 4-float chunk c4 (of 32) of row t in the R / U rows (plain
-// rows: the solve's per-term address is its hottest arithmetic; the row-per-thread
-// stores of stage 2 pay the bank conflicts instead)
-__device__ __forceinline__ int u_at(int t, int c4) { return t * kD + 4 * c4; }
+// float offset of 4-float chunk c4 (of 32) of row t in the R / U rows: the chunk
+// sits at slot c4 ^ (t % 32) of its row, so that 32 threads storing one chunk of 32
+// consecutive rows (stage 2) and 32 lanes reading one row (the solve) both meet
+// no bank conflict
+__device__ __forceinline__ int u_at(int t, int c4) { return t * kD + 4 * (c4 ^ (t & 31)); }
 
 // byte offset of 16-byte chunk c (of 16) of k row r in the swizzled K tile
 __device__ __forceinline__ uint32_t k_chunk(int r, int c) {
@@ -150,12 +151,17 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   }
   const int W = (N + 31) / 32;
   const size_t row = (size_t)lay.row0(b, Nmax);
+  // one chain, taken by the chain kernel: leave before any copy starts
+  if (skip_chains && !__syncthreads_or(tid < N && parent[row + tid] != tid - 1)) return;
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
 
   // S0, K and Q start streaming into shared memory at once: S0 as it is (fp32),
   // K and Q as 128-row tiles in the tensor cores' K-major 128-byte-swizzled
   // layout (K_A, Q_A, K_B, Q_B; rows past the tree zero)
   const int ntiles = N > 128 ? 2 : 1;
+  // the v rows (read at the readout of R) start coming into L2
+  for (int r = tid; r < N; r += kThreads)
+    sm100::bulk_prefetch_l2(v + ((row + r) * Hv + h) * kD, kD * 2);
   const float* S0bh = S0 + ((size_t)st * Hv + h) * kD * kD;
   for (int i = tid; i < kD * kD / 4; i += kThreads)
     cp_async16m(sSK + 16 * i, S0bh + 4 * i);
@@ -172,12 +178,11 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   // ---- 1. the tree ------------------------------------------------------------
-  int bad = 0, notchain = 0;
+  int bad = 0;
   if (tid < N) {
     const int p = parent[row + tid];
     sPar[tid] = p;
     bad = (p < -1 || p >= tid);
-    notchain = p != tid - 1;
     sBeta[tid] = beta[(row + tid) * Hv + h];
     sLa[tid] = log_alpha[(row + tid) * Hv + h];
   }
@@ -186,10 +191,6 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   bad = __syncthreads_or(bad);
   if (bad) {
     if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_TREE);
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    return;
-  }
-  if (skip_chains && !__syncthreads_or(notchain)) {  // one chain: the chain kernel's
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
@@ -343,15 +344,21 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                                                       4 * lane)
                     : make_uint2(0u, 0u);
   };
+  // the seed of the warp's next node (parked in its U row), also one node ahead
+  auto seed_of = [&](int task) {
+    return task < N ? *reinterpret_cast<const float4*>(Ubh + (size_t)sOrder[task] * kD + 4 * lane)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
   uint2 qnext = q_of(warp);
+  float4 seednext = seed_of(warp);
   for (int task = warp; task < N; task += kWarps) {
     const int t = sOrder[task];
     const int nA = sDepth[t] - 1;  // strict ancestors
     const df gt = sG[t];
     const float bt = sBeta[t];
-    // the seed (parked in t's U row) comes while the node is worked on
     float* urow = Ubh + (size_t)t * kD + 4 * lane;
-    const float4 seed = *reinterpret_cast<const float4*>(urow);
+    const float4 seed = seednext;
+    seednext = seed_of(task + kWarps);
     // q_t into the warp's stage (fp32); the next node's q starts coming
     {
       const uint2 qq = qnext;
@@ -444,7 +451,6 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     // time as they become final: a path's nodes complete in path order, so the
     // last of the four being final makes all four final
     float4 au = make_float4(0.f, 0.f, 0.f, 0.f), ao = au;
-    const float* urow_lane = sU + 4 * lane;  // (u rows: row s at urow_lane + s kD)
     float ymine = 0.f;  // Y[t,t], in the lane that formed entry nA
 #pragma unroll
     for (int gi = 0; gi < kGroups; ++gi)
@@ -464,7 +470,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           const float xx = __shfl_sync(0xffffffffu, xn[gi], (j0 + jj) & 31);
           const float yy = __shfl_sync(0xffffffffu, yn[gi], (j0 + jj) & 31);
           const bool use = jj < m;
-          uj[jj] = urow_lane + (use ? ss : 0) * kD;
+          uj[jj] = sU + u_at(use ? ss : 0, lane);
           xj[jj] = use ? xx : 0.f;
           yj[jj] = use ? yy : 0.f;
         }
