@@ -127,20 +127,17 @@ def verify_kernel_name(w: W.Workload) -> str:
     """The verify kernel the library dispatches for this shape (mirrors the
     C-ABI's rule: for bf16 with dk = dv = 128, the tensor-core kernel up to 128
     nodes, the 256-node kernel up to 256 and the chunk pass with R on the tensor
-    cores beyond, the chain kernel ahead of the last two)."""
+    cores beyond; the last two run single-chain units in the chunkwise form)."""
     forced = os.environ.get("GDN_TREE_KERNEL", "auto")
     tc_shape = w.dtype == W.BF16 and w.dk == 128 and w.dv == 128
-    # past 128 nodes (bf16, d = 128, no kernel forced) the chain kernel runs first and
-    # takes the sequences whose tree is one chain
-    chain = "verify_chain_kernel + " if tc_shape and forced == "auto" and w.N > 128 else ""
     if tc_shape and forced not in ("generic", "long", "long_cuda"):
         if w.N <= 128 and forced != "mid":
             return "verify_tc_kernel"
         if w.N <= 256:
-            return chain + "verify_mid_kernel"
+            return "verify_mid_kernel"
     if w.N > 256 or forced in ("long", "long_cuda"):
         if tc_shape and forced not in ("generic", "long_cuda"):
-            return chain + "verify_long_tc_kernel"
+            return "verify_long_tc_kernel"
         return "verify_long_kernel"
     return "verify_generic_kernel"
 

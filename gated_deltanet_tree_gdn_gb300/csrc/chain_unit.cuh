@@ -1,7 +1,8 @@
-// verify_chain.cu -- tree verification of bf16 trees that are one chain (parent
-// of node t is t - 1: the draft is a single branch) with dk = dv = 128, up to
-// kMaxNLong nodes: the chunkwise form of the closed form, every product on the
-// tensor cores.
+// chain_unit.cuh -- the verification of one (sequence, v-head) unit whose tree is
+// one chain (parent of node t is t - 1: the draft is a single branch), bf16 with
+// dk = dv = 128, up to kMaxNLong nodes: the chunkwise form of the closed form,
+// every product on the tensor cores.  The 256-node kernel and the chunk pass run
+// it for their chain units (a CTA of 512 threads each).
 //
 // Method: "DFlash-TfM: Trees from Marginals", section 3 ("Soluzione"): with
 // g_t the log-decay summed along the root-to-t path,
@@ -17,8 +18,7 @@
 //   o_t = e^{g_t - g_{c0-1}} S_c^T q_t + sum_{c0 <= s <= t} Y[t,s] u_s,
 //   S_{c+1} = e^{g_{c1-1} - g_{c0-1}} S_c + sum_{c0 <= s < c1} e^{g_{c1-1} - g_s} k_s u_s^T.
 //
-// One CTA (128 threads) per (sequence b, v-head h); thread j owns v-column j, which
-// is TMEM lane j of the transposed products (M = dv = 128):
+// Every product is transposed so that M = dv = 128 and TMEM lane j is v-column j:
 //   P1 = S_c^T K_c^T and P2 = S_c^T Q_c^T   (S_c^T as bf16 hi + lo, two MMAs each),
 //   GK = K_c K_c^T and GQ = Q_c K_c^T        (one MMA each, rows padded to 128),
 //   O_c^T    = e P2 + U_c^T Y_c^T              (U and Y as bf16 hi + lo, three MMAs),
@@ -29,13 +29,14 @@
 // rows), then solves among its rows in registers (a thread per column), X
 // broadcast from shared memory.  S_{c+1}^T is read back, split into hi + lo and
 // becomes the next chunk's operand.
+#pragma once
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
 
 namespace gdn {
-
-namespace {
+namespace chain {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
@@ -60,7 +61,7 @@ constexpr uint32_t OFF_TREE = OFF_AUX + 2048;           // g (df) [N], beta [N]
 static_assert(2 * 128 * kC * 2 <= kXYBytes, "U^T diag(w) hi / lo fit where X and Y were");
 static_assert(OFF_YH % 1024 == 0, "the Y operand tiles start on a 1024-byte boundary");
 
-__host__ __device__ inline size_t chain_smem_bytes(int N) {
+__host__ __device__ inline size_t smem_bytes(int N) {
   return OFF_TREE + (size_t)N * (sizeof(df) + sizeof(float)) + 1024;  // + alignment slack
 }
 
@@ -102,17 +103,17 @@ __device__ __forceinline__ float bf16_bits_to_f32(unsigned short x) {
   return __uint_as_float((uint32_t)x << 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-verify_chain_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                    const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
-                    const float* __restrict__ beta, const int32_t* __restrict__ parent,
-                    const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
-                    float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
-                    WaitHooks hk) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
-  const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
-  const int h = blockIdx.x, b = blockIdx.y;
+// Whole CTA (kThreads threads): verifies unit (b, h) whose N-node tree is one chain.
+// smem: the CTA's dynamic shared memory from a 1024-byte aligned base, at least
+// smem_bytes(Nmax) long; Ubh: the unit's U rows.  Reports a timeout to dev_status.
+__device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __restrict__ q,
+                                    const __nv_bfloat16* __restrict__ k,
+                                    const __nv_bfloat16* __restrict__ v,
+                                    const float* __restrict__ log_alpha,
+                                    const float* __restrict__ beta, const float* __restrict__ S0,
+                                    __nv_bfloat16* __restrict__ o, float* __restrict__ Ubh,
+                                    int N, int Nmax, size_t row, int st, int b, int h, int Hv,
+                                    int Hqk, int32_t* dev_status, const WaitHooks& hk) {
   const int hq = h / (Hv / Hqk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // TMEM lane group (warp % 4: lanes / v-columns 32 g ..) and quarter (warp / 4)
@@ -127,20 +128,6 @@ verify_chain_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   uint64_t* sBar = reinterpret_cast<uint64_t*>(sFlag + 2);
   df* sG = reinterpret_cast<df*>(smem + OFF_TREE);
   float* sBeta = reinterpret_cast<float*>(sG + Nmax);
-
-  const int N = lay.count(b, Nmax), st = lay.state(b);
-  if (N < 0 || st < 0) {
-    if (h == 0 && tid == 0 && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_BAD_LAYOUT);
-    return;
-  }
-  if (N == 0) return;
-  const size_t row = (size_t)lay.row0(b, Nmax);
-  float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
-
-  // ---- a chain?  (any other tree is the tree kernels' work) -------------------------
-  int notchain = 0;
-  for (int t = tid; t < N; t += kThreads) notchain |= parent[row + t] != t - 1;
-  if (__syncthreads_or(notchain)) return;
 
   // ---- g by a blocked scan (kPerThread nodes a thread, df sums), beta ---------------
   {
@@ -477,24 +464,5 @@ verify_chain_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   if (tid == 0 && sFlag[0] && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
 }
 
-}  // namespace
-
-bool verify_chain_supported(const gdn_tree_dims& d) {
-  return d.dtype == GDN_TREE_BF16 && d.dk == kD && d.dv == kD && d.N >= 1 &&
-         d.N <= kMaxNLong && chain_smem_bytes(d.N) <= 227 * 1024;
-}
-
-cudaError_t launch_verify_chain(const VerifyArgs& a, cudaStream_t stream) {
-  const size_t smem = chain_smem_bytes(a.d.N);
-  const dim3 grid(a.d.Hv, a.d.B);
-  cudaError_t err = cudaFuncSetAttribute(verify_chain_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  verify_chain_kernel<<<grid, kThreads, smem, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
-      static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
-      static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks());
-  return cudaGetLastError();
-}
-
+}  // namespace chain
 }  // namespace gdn

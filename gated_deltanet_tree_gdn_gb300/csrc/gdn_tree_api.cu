@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include "../../include/gdn_tree.h"
+#include "chain_unit.cuh"
 #include "kernels.h"
 
 namespace {
@@ -109,8 +110,13 @@ static bool tc_takes(const VerifyArgs& a) {
   return !force_generic() && verify_tc_supported(a.d) && (!a.lay.packed() || a.lay.T > 0);
 }
 
-// past 128 nodes (bf16, d = 128) the sequences whose tree is one chain go to the
-// chain kernel first; the tree kernel launched next leaves them
+// past 128 nodes (bf16, d = 128) the units whose tree is one chain take the
+// chunkwise path inside the 256-node kernel or the chunk pass
+bool verify_chain_path_fits(const gdn_tree_dims& d) {
+  return d.dtype == GDN_TREE_BF16 && d.dk == 128 && d.dv == 128 && d.N >= 1 &&
+         d.N <= kMaxNLongHost && chain::smem_bytes(d.N) <= 227 * 1024;
+}
+
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   if (tc_takes(a)) return launch_verify_tc(a, stream);
   VerifyArgs t = a;
@@ -119,11 +125,7 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t stream) {
   const bool mid = !kernel_forced("generic") && !long_forced() && verify_mid_supported(a.d);
   const bool long_tc = (a.d.N > kMaxNHost || long_forced()) && !kernel_forced("long_cuda") &&
                        !kernel_forced("generic") && verify_long_tc_supported(a.d);
-  if (!forced && (mid || long_tc) && verify_chain_supported(a.d)) {
-    const cudaError_t err = launch_verify_chain(a, stream);
-    if (err != cudaSuccess) return err;
-    t.skip_chains = true;
-  }
+  t.chains = !forced && verify_chain_path_fits(a.d);
   if (mid) return launch_verify_mid(t, stream);
   if (long_tc) return launch_verify_long_tc(t, stream);
   if (a.d.N > kMaxNHost || long_forced()) return launch_verify_long(a, stream);

@@ -60,9 +60,9 @@ struct VerifyArgs {
   gdn_tree_dims d;
   int32_t* dev_status;
   SeqLayout lay = {};
-  // the chain kernel took the sequences whose tree is one chain: the tree kernels
-  // (256-node and chunk pass) leave them
-  bool skip_chains = false;
+  // the 256-node kernel and the chunk pass run the units whose tree is one chain in
+  // the chunkwise form (bf16, dk = dv = 128)
+  bool chains = false;
 };
 
 struct CommitArgs {
@@ -120,11 +120,8 @@ cudaError_t launch_verify_generic(const VerifyArgs& a, cudaStream_t stream);
 size_t verify_long_smem_bytes(int N, int dk, int dv);
 cudaError_t launch_verify_long(const VerifyArgs& a, cudaStream_t stream);
 
-// bf16 trees that are one chain (parent of t = t - 1), up to kMaxNLongHost nodes,
-// dk = dv = 128: the chunkwise form on the tensor cores (other sequences are left
-// to the tree kernels)
-bool verify_chain_supported(const gdn_tree_dims& d);
-cudaError_t launch_verify_chain(const VerifyArgs& a, cudaStream_t stream);
+// the chunkwise path for units whose tree is one chain fits beside the tree kernels
+bool verify_chain_path_fits(const gdn_tree_dims& d);
 
 // bf16 trees of up to kMaxNLongHost nodes with dk = dv = 128: the chunk pass with
 // R and the output seeds on the tensor cores

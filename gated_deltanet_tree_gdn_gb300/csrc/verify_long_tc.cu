@@ -35,6 +35,9 @@
 //     barrier is arrived on.
 // The unfinished node of lowest depth order in a chunk never waits on an
 // unfinished node, so the waits cannot cycle.
+#include <algorithm>
+
+#include "chain_unit.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -124,7 +127,7 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
                       const float* __restrict__ beta, const int32_t* __restrict__ parent,
                       const float* __restrict__ S0, __nv_bfloat16* __restrict__ o, float* U,
                       gdn_tree_dims d, int32_t* dev_status, SeqLayout lay, WaitHooks hk,
-                      int skip_chains) {
+                      int chains) {
   // U is read back (seeds, earlier chunks' rows) after this CTA wrote it, so it is
   // neither const nor restrict: its loads must not take the read-only path.
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -154,10 +157,14 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   }
   const size_t row = (size_t)lay.row0(b, Nmax);
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
-  if (skip_chains) {  // one chain, taken by the chain kernel: leave before any copy starts
+  if (chains && N > 0) {  // one chain: the chunkwise path (no copy of this path has started)
     int notchain = 0;
     for (int t = tid; t < N; t += kThreads) notchain |= parent[row + t] != t - 1;
-    if (!__syncthreads_or(notchain)) return;
+    if (!__syncthreads_or(notchain)) {
+      chain::run(smem, q, k, v, log_alpha, beta, S0, o, Ubh, N, Nmax, row, st, b, h, Hv, Hqk,
+                 dev_status, hk);
+      return;
+    }
   }
 
   // S0 starts streaming into shared memory (fp32) at once
@@ -519,7 +526,8 @@ bool verify_long_tc_supported(const gdn_tree_dims& d) {
 }
 
 cudaError_t launch_verify_long_tc(const VerifyArgs& a, cudaStream_t stream) {
-  const size_t smem = long_tc_smem_layout(a.d.N).total;
+  size_t smem = long_tc_smem_layout(a.d.N).total;
+  if (a.chains) smem = std::max(smem, chain::smem_bytes(a.d.N));
   const dim3 grid(a.d.Hv, a.d.B);
   cudaError_t err = cudaFuncSetAttribute(verify_long_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -528,7 +536,7 @@ cudaError_t launch_verify_long_tc(const VerifyArgs& a, cudaStream_t stream) {
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
       static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
       static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks(),
-      a.skip_chains ? 1 : 0);
+      a.chains ? 1 : 0);
   return cudaGetLastError();
 }
 

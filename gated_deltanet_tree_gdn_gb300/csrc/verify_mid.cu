@@ -32,6 +32,9 @@
 //     terms, not the whole ancestor sum.
 // The unfinished node of lowest depth order never waits on an unfinished node,
 // so the waits cannot cycle.
+#include <algorithm>
+
+#include "chain_unit.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -118,7 +121,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   const float* __restrict__ beta, const int32_t* __restrict__ parent,
                   const float* __restrict__ S0, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ U, gdn_tree_dims d, int32_t* dev_status, SeqLayout lay,
-                  WaitHooks hk, int skip_chains) {
+                  WaitHooks hk, int chains) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
   const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
@@ -151,9 +154,13 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   }
   const int W = (N + 31) / 32;
   const size_t row = (size_t)lay.row0(b, Nmax);
-  // one chain, taken by the chain kernel: leave before any copy starts
-  if (skip_chains && !__syncthreads_or(tid < N && parent[row + tid] != tid - 1)) return;
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
+  // one chain: the chunkwise path (no copy of this path has started)
+  if (chains && N > 0 && !__syncthreads_or(tid < N && parent[row + tid] != tid - 1)) {
+    chain::run(smem, q, k, v, log_alpha, beta, S0, o, Ubh, N, Nmax, row, st, b, h, Hv, Hqk,
+               dev_status, hk);
+    return;
+  }
 
   // S0, K and Q start streaming into shared memory at once: S0 as it is (fp32),
   // K and Q as 128-row tiles in the tensor cores' K-major 128-byte-swizzled
@@ -516,7 +523,8 @@ bool verify_mid_supported(const gdn_tree_dims& d) {
 }
 
 cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream) {
-  const size_t smem = mid_smem_layout(a.d.N).total;
+  size_t smem = mid_smem_layout(a.d.N).total;
+  if (a.chains) smem = std::max(smem, chain::smem_bytes(a.d.N));
   const dim3 grid(a.d.Hv, a.d.B);
   cudaError_t err = cudaFuncSetAttribute(verify_mid_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -525,7 +533,7 @@ cudaError_t launch_verify_mid(const VerifyArgs& a, cudaStream_t stream) {
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
       static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
       static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks(),
-      a.skip_chains ? 1 : 0);
+      a.chains ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -1,8 +1,8 @@
-"""GPU parity of the chain kernel (trees that are one branch, parent of t = t - 1,
-past 128 nodes, bf16 with dk = dv = 128): the chunkwise form with the state
-passed between 64-node chunks, through the C ABI, against the fp64 oracle.  Chains
-sit beside other tree families in one call too (the tree kernel launched after
-the chain kernel leaves the chains to it)."""
+"""GPU parity of the chunkwise path for trees that are one branch (parent of t =
+t - 1, past 128 nodes, bf16 with dk = dv = 128), which the 256-node kernel and the
+chunk pass run for such units: the state passed between 64-node chunks, through
+the C ABI, against the fp64 oracle.  Chains sit beside other tree families in one
+call too (the same launch takes both paths)."""
 
 import numpy as np
 import pytest
@@ -56,8 +56,8 @@ def test_chain_strong_decay_and_high_beta(monkeypatch):
 
 @pytest.mark.parametrize("N", [256, 400])
 def test_chains_beside_other_trees(N, monkeypatch):
-    """Every tree family in one call: the chain goes to the chain kernel, the others
-    to the 256-node kernel (N = 256) or the chunk pass (N = 400)."""
+    """Every tree family in one call: the chain takes the chunkwise path, the others
+    the 256-node kernel's (N = 256) or the chunk pass's (N = 400) tree path."""
     monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
     w = W.make_custom(seed=1130 + N, B=6, N=N, Hqk=2, Hv=4, dk=128, dv=128, dtype=W.BF16,
                       tree="mixed", max_depth=N)
@@ -68,7 +68,7 @@ def test_chains_beside_other_trees(N, monkeypatch):
 
 @pytest.mark.parametrize("kernel", ["mid", "long"])
 def test_tree_kernels_still_take_chains_when_forced(kernel, monkeypatch):
-    """With a kernel forced the chain kernel stays out: the tree kernels' own
+    """With a kernel forced the chunkwise path stays out: the tree kernels' own
     chain handling is covered on the same shape."""
     monkeypatch.setenv("GDN_TREE_KERNEL", kernel)
     w = W.make_custom(seed=1140, B=2, N=200, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
