@@ -78,6 +78,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 // block-wide barrier (the default for tree_prepare)
 struct BlockSync {
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
+  // the barrier, returning whether any thread's x is true
+  __device__ __forceinline__ bool any(bool x) const { return __syncthreads_or(x) != 0; }
 };
 
 // barrier over the first `count` threads of the block (named barrier `id`)
@@ -86,11 +88,22 @@ struct NamedSync {
   __device__ __forceinline__ void operator()() const {
     asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kCount) : "memory");
   }
+  __device__ __forceinline__ bool any(bool x) const {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)x), "n"(kId), "n"(kCount)
+        : "memory");
+    return r != 0;
+  }
 };
 
 //
 // For the tree of one sequence (parent[] already in shared memory and
-// validated), computes with pointer jumping (ceil(log2 N) rounds):
+// validated), computes with pointer jumping (ceil(log2 depth) rounds: it stops
+// once every node has reached its root):
 //   anc[t*W .. t*W+W-1] : bitset of the strict ancestors of t (W = ceil(N/32))
 //   g[t]                : double-float sum of log_alpha over the path P(t)
 // `jump` is an int scratch of N entries.  Must be called by every thread that
@@ -122,7 +135,7 @@ __device__ __forceinline__ void tree_prepare(const int* s_parent, int N, int W,
         for (int i = 0; i < kMaxN / 32; ++i) w[i] = i < W ? s_anc[j * W + i] : 0u;
       }
     }
-    sync();
+    if (!sync.any(j >= 0)) break;  // every node reached its root
     if (t < N && j >= 0) {
       s_g[t] = df_add(s_g[t], gj);
 #pragma unroll
