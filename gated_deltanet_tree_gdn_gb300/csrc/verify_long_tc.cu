@@ -127,7 +127,7 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
                       const float* __restrict__ beta, const int32_t* __restrict__ parent,
                       const float* __restrict__ S0, __nv_bfloat16* __restrict__ o, float* U,
                       gdn_tree_dims d, int32_t* dev_status, SeqLayout lay, WaitHooks hk,
-                      int chains) {
+                      int skip_chains) {
   // U is read back (seeds, earlier chunks' rows) after this CTA wrote it, so it is
   // neither const nor restrict: its loads must not take the read-only path.
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -157,14 +157,10 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   }
   const size_t row = (size_t)lay.row0(b, Nmax);
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
-  if (chains && N > 0) {  // one chain: the chunkwise path (no copy of this path has started)
+  if (skip_chains && N > 0) {  // one chain: verify_chain_kernel's (before any copy starts)
     int notchain = 0;
     for (int t = tid; t < N; t += kThreads) notchain |= parent[row + t] != t - 1;
-    if (!__syncthreads_or(notchain)) {
-      chain::run(smem, q, k, v, log_alpha, beta, S0, o, Ubh, N, Nmax, row, st, b, h, Hv, Hqk,
-                 dev_status, hk);
-      return;
-    }
+    if (!__syncthreads_or(notchain)) return;
   }
 
   // S0 starts streaming into shared memory (fp32) at once
@@ -235,7 +231,7 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     float sv[4][8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int qd = tid * 4 + j, i = qd >> 4, n8 = qd & 15;
+      const int qd = j * kThreads + tid, i = qd >> 4, n8 = qd & 15;  // a warp: two whole rows
       const float4 a = *reinterpret_cast<const float4*>(sSK + (i * kD + 8 * n8) * 4);
       const float4 c = *reinterpret_cast<const float4*>(sSK + (i * kD + 8 * n8 + 4) * 4);
       sv[j][0] = a.x; sv[j][1] = a.y; sv[j][2] = a.z; sv[j][3] = a.w;
@@ -244,7 +240,7 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int qd = tid * 4 + j, i = qd >> 4, n8 = qd & 15;
+      const int qd = j * kThreads + tid, i = qd >> 4, n8 = qd & 15;  // a warp: two whole rows
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) sm100::split2(sv[j][2 * e], sv[j][2 * e + 1], hi[e], lo[e]);
@@ -518,6 +514,29 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
   if (tid == 0 && sFlag[0] && dev_status) atomicMax(dev_status + b, GDN_TREE_STATUS_TIMEOUT);
 }
 
+// The units of trees past 256 nodes whose tree is one chain, in the chunkwise form
+// (launched ahead of the chunk pass, which then leaves them; a separate kernel, so
+// that the chunk pass keeps its own register allocation).  Other units leave at once.
+__global__ void __launch_bounds__(kThreads, 1)
+verify_chain_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                    const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
+                    const float* __restrict__ beta, const int32_t* __restrict__ parent,
+                    const float* __restrict__ S0, __nv_bfloat16* __restrict__ o, float* U,
+                    gdn_tree_dims d, int32_t* dev_status, SeqLayout lay, WaitHooks hk) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (sm100::smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int Nmax = d.N, Hv = d.Hv, Hqk = d.Hqk;
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int N = lay.count(b, Nmax), st = lay.state(b);
+  if (N <= 0 || st < 0) return;  // (a bad layout is the chunk pass's to report)
+  const size_t row = (size_t)lay.row0(b, Nmax);
+  int notchain = 0;
+  for (int t = tid; t < N; t += kThreads) notchain |= parent[row + t] != t - 1;
+  if (__syncthreads_or(notchain)) return;
+  chain::run(smem, q, k, v, log_alpha, beta, S0, o, U + lay.urow0(b, h, Hv, Nmax) * kD, N, Nmax,
+             row, st, b, h, Hv, Hqk, dev_status, hk);
+}
+
 }  // namespace
 
 bool verify_long_tc_supported(const gdn_tree_dims& d) {
@@ -526,8 +545,19 @@ bool verify_long_tc_supported(const gdn_tree_dims& d) {
 }
 
 cudaError_t launch_verify_long_tc(const VerifyArgs& a, cudaStream_t stream) {
-  size_t smem = long_tc_smem_layout(a.d.N).total;
-  if (a.chains) smem = std::max(smem, chain::smem_bytes(a.d.N));
+  const size_t smem = long_tc_smem_layout(a.d.N).total;
+  if (a.chains) {
+    const size_t csmem = chain::smem_bytes(a.d.N);
+    cudaError_t err = cudaFuncSetAttribute(verify_chain_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+    if (err != cudaSuccess) return err;
+    verify_chain_kernel<<<dim3(a.d.Hv, a.d.B), kThreads, csmem, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+        static_cast<const __nv_bfloat16*>(a.v), a.log_alpha, a.beta, a.parent, a.S0,
+        static_cast<__nv_bfloat16*>(a.o), a.U, a.d, a.dev_status, a.lay, wait_hooks());
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
   const dim3 grid(a.d.Hv, a.d.B);
   cudaError_t err = cudaFuncSetAttribute(verify_long_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -247,7 +247,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     float sv[4][8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int qd = tid * 4 + j, i = qd >> 4, n8 = qd & 15;
+      const int qd = j * kThreads + tid, i = qd >> 4, n8 = qd & 15;  // a warp: two whole rows
       const float4 a = *reinterpret_cast<const float4*>(sSK + (i * kD + 8 * n8) * 4);
       const float4 c = *reinterpret_cast<const float4*>(sSK + (i * kD + 8 * n8 + 4) * 4);
       sv[j][0] = a.x; sv[j][1] = a.y; sv[j][2] = a.z; sv[j][3] = a.w;
@@ -256,7 +256,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int qd = tid * 4 + j, i = qd >> 4, n8 = qd & 15;
+      const int qd = j * kThreads + tid, i = qd >> 4, n8 = qd & 15;  // a warp: two whole rows
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) sm100::split2(sv[j][2 * e], sv[j][2 * e + 1], hi[e], lo[e]);
