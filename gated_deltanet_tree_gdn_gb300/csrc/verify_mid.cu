@@ -290,39 +290,64 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   sm100::tc_fence_after_sync();
   {
     // warp w reads accumulator w / 4 (K S0 tile A, B; Q S0 tile A, B) for its
-    // TMEM lane group w % 4: thread = node
+    // TMEM lane group w % 4: lane = node.  The v rows come in and the seeds go out
+    // through a 4 KB staging block of the warp in the (now free) state region, so
+    // that their global accesses are whole 64 / 128-byte row segments.
     const int acc = warp >> 2, lg = warp & 3;
     if ((acc & 1) < ntiles) {  // (warp-uniform)
-      const int t = (acc & 1) * 128 + lg * 32 + lane;
+      const int t0 = (acc & 1) * 128 + lg * 32, t = t0 + lane;
       const bool live = t < N;
       const float gam = live ? expf(df_value(sG[t])) : 0.f;
       const float bt = live ? sBeta[t] : 0.f;
       const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16) + 128 * acc;
+      unsigned char* stg = sSK + warp * 4096;
 #pragma unroll 1
       for (int c32 = 0; c32 < 4; ++c32) {
+        if (acc < 2) {
+          // v[t0 + r][32 c32 ..]: lane -> row 8 i + lane / 4, 16-byte chunk lane % 4
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2), c = lane & 3;
+            if (t0 + r < N)
+              *reinterpret_cast<uint4*>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) =
+                  *reinterpret_cast<const uint4*>(v + ((row + t0 + r) * Hv + h) * kD + 32 * c32 + 8 * c);
+          }
+        }
         float r[32];
         sm100::tmem_ld_32cols(taddr + 32 * c32, r);  // warp-collective: every lane
-        if (!live) continue;
+        __syncwarp();
         if (acc < 2) {
-          const uint4* vr = reinterpret_cast<const uint4*>(v + ((row + t) * Hv + h) * kD + 32 * c32);
+          if (live) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            float vv[8];
-            bf16x8_to_f32(vr[m], vv);
-            *reinterpret_cast<float4*>(sU + u_at(t, 8 * c32 + 2 * m)) =
-                make_float4(bt * (vv[0] - gam * r[8 * m]), bt * (vv[1] - gam * r[8 * m + 1]),
-                            bt * (vv[2] - gam * r[8 * m + 2]), bt * (vv[3] - gam * r[8 * m + 3]));
-            *reinterpret_cast<float4*>(sU + u_at(t, 8 * c32 + 2 * m + 1)) =
-                make_float4(bt * (vv[4] - gam * r[8 * m + 4]), bt * (vv[5] - gam * r[8 * m + 5]),
-                            bt * (vv[6] - gam * r[8 * m + 6]), bt * (vv[7] - gam * r[8 * m + 7]));
+            for (int m = 0; m < 4; ++m) {
+              float vv[8];
+              bf16x8_to_f32(*reinterpret_cast<const uint4*>(
+                                stg + lane * 64 + ((m ^ ((lane >> 1) & 3)) << 4)), vv);
+              *reinterpret_cast<float4*>(sU + u_at(t, 8 * c32 + 2 * m)) =
+                  make_float4(bt * (vv[0] - gam * r[8 * m]), bt * (vv[1] - gam * r[8 * m + 1]),
+                              bt * (vv[2] - gam * r[8 * m + 2]), bt * (vv[3] - gam * r[8 * m + 3]));
+              *reinterpret_cast<float4*>(sU + u_at(t, 8 * c32 + 2 * m + 1)) =
+                  make_float4(bt * (vv[4] - gam * r[8 * m + 4]), bt * (vv[5] - gam * r[8 * m + 5]),
+                              bt * (vv[6] - gam * r[8 * m + 6]), bt * (vv[7] - gam * r[8 * m + 7]));
+            }
           }
         } else {
-          float4* sr = reinterpret_cast<float4*>(Ubh + (size_t)t * kD + 32 * c32);
+          // the seeds gamma_t (Q S0)_t into the staging (row = lane), then out by rows
 #pragma unroll
           for (int m = 0; m < 8; ++m)
-            sr[m] = make_float4(gam * r[4 * m], gam * r[4 * m + 1], gam * r[4 * m + 2],
-                                gam * r[4 * m + 3]);
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((m ^ (lane & 7)) << 4)) =
+                make_float4(gam * r[4 * m], gam * r[4 * m + 1], gam * r[4 * m + 2],
+                            gam * r[4 * m + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3), c = lane & 7;
+            if (t0 + rr < N)
+              *reinterpret_cast<float4*>(Ubh + (size_t)(t0 + rr) * kD + 32 * c32 + 4 * c) =
+                  *reinterpret_cast<const float4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+          }
         }
+        __syncwarp();  // the staging is read before the next 32 columns use it
       }
     }
   }
