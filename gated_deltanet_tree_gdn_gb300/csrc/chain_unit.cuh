@@ -20,7 +20,8 @@
 //
 // Every product is transposed so that M = dv = 128 and TMEM lane j is v-column j:
 //   P1 = S_c^T K_c^T and P2 = S_c^T Q_c^T   (S_c^T as bf16 hi + lo, two MMAs each),
-//   GK = K_c K_c^T and GQ = Q_c K_c^T        (one MMA each, rows padded to 128),
+//   GK = K_c K_c^T and GQ = Q_c K_c^T        (one MMA each; the A rows are K_c / Q_c
+//                                             twice, so a row sits in both lane halves),
 //   O_c^T    = e P2 + U_c^T Y_c^T              (U and Y as bf16 hi + lo, three MMAs),
 //   S_{c+1}^T = decay S_c^T + (U_c^T diag(w)) K_c  (accumulated in TMEM in fp32; the
 //                                               U operand as bf16 hi + lo).
@@ -171,9 +172,11 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
       const int r = e >> 4, ch = e & 15;
       if (r < nc) {
         const size_t src = ((row + c0 + r) * Hqk + hq) * kD + 8 * ch;
-        if (kq) {
+        if (kq) {  // rows r and r + 64: the Grams' rows land in both TMEM lane halves
           cp_async16c(smem + OFF_KT + sm100::sw128_chunk(r, ch), k + src);
           cp_async16c(smem + OFF_QT + sm100::sw128_chunk(r, ch), q + src);
+          cp_async16c(smem + OFF_KT + sm100::sw128_chunk(r + kC, ch), k + src);
+          cp_async16c(smem + OFF_QT + sm100::sw128_chunk(r + kC, ch), q + src);
         }
         if (km) cp_async16c(smem + OFF_KM + sm100::mn_chunk(r, ch), k + src);
       }
@@ -260,45 +263,44 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
     // the next chunk's K and Q tiles (these products have read the current ones)
     if (!last) load_tiles(c0 + kC, true, false);
 
-    // ---- X and Y (rows t: TMEM lanes 0..63, columns 16 qd ..), e and w -------------
-    if (lg < 2) {
-      const int t = j;  // 32 lg + lane
-      const bool live = t < nc;
-      const df gt = live ? sG[c0 + t] : df{0.f, 0.f};
-      const float bt = live ? sBeta[c0 + t] : 0.f;
-      float gk[16], gq[16];
-      sm100::tmem_ld_16cols(tl + TM_GK + 16 * qd, gk);
-      sm100::tmem_ld_16cols(tl + TM_GQ + 16 * qd, gq);
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) {
-        float x[8], y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = 16 * qd + 8 * h8 + e;
-          x[e] = 0.f;
-          y[e] = 0.f;
-          if (live && s <= t) {
-            const float dec = s == t ? 1.f : expf(df_diff(gt, sG[c0 + s]));
-            y[e] = dec * gq[8 * h8 + e];
-            if (s < t) x[e] = bt * dec * gk[8 * h8 + e];
-          }
-        }
-        float* xr = sX + t * kXStride + 16 * qd + 8 * h8;
-        *reinterpret_cast<float4*>(xr) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(xr + 4) = make_float4(x[4], x[5], x[6], x[7]);
-        // Y as the output product's B operand: row t, chunk 2 qd + h8, bf16 hi + lo
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sm100::split2(y[2 * e], y[2 * e + 1], hi[e], lo[e]);
-        const uint32_t off = sm100::sw128_chunk(t, 2 * qd + h8);
-        *reinterpret_cast<uint4*>(smem + OFF_YH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + OFF_YH + kC * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    } else if (qd == 0) {
-      const int t = j - 64;
+    // ---- e and w; X and Y: row t in TMEM lanes t and 64 + t, so that every warp
+    // takes 8 of a row's 64 columns (part qd + 4 (lg / 2)) --------------------------
+    if (tid < kC) {
+      const int t = tid;
       const bool live = t < nc;
       sE[t] = live ? expf(df_diff(sG[c0 + t], gref)) : 0.f;
       sW[t] = live ? expf(df_diff(sG[c0 + nc - 1], sG[c0 + t])) : 0.f;
+    }
+    {
+      const int t = 32 * (lg & 1) + lane, part = qd + 4 * (lg >> 1);
+      const bool live = t < nc;
+      const df gt = live ? sG[c0 + t] : df{0.f, 0.f};
+      const float bt = live ? sBeta[c0 + t] : 0.f;
+      float gk[8], gq[8];
+      sm100::tmem_ld_8cols(tl + TM_GK + 8 * part, gk);
+      sm100::tmem_ld_8cols(tl + TM_GQ + 8 * part, gq);
+      float x[8], y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int s = 8 * part + e;
+        x[e] = 0.f;
+        y[e] = 0.f;
+        if (live && s <= t) {
+          const float dec = s == t ? 1.f : expf(df_diff(gt, sG[c0 + s]));
+          y[e] = dec * gq[e];
+          if (s < t) x[e] = bt * dec * gk[e];
+        }
+      }
+      float* xr = sX + t * kXStride + 8 * part;
+      *reinterpret_cast<float4*>(xr) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(xr + 4) = make_float4(x[4], x[5], x[6], x[7]);
+      // Y as the output product's B operand: row t, chunk part, bf16 hi + lo
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm100::split2(y[2 * e], y[2 * e + 1], hi[e], lo[e]);
+      const uint32_t off = sm100::sw128_chunk(t, part);
+      *reinterpret_cast<uint4*>(smem + OFF_YH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + OFF_YH + kC * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     __syncthreads();  // X, Y, e, w in shared memory
     // ---- r_t = beta_t (v_t - e_t P1[j][t]) for rows t = 16 qd + i ------------------

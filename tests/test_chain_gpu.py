@@ -75,3 +75,33 @@ def test_tree_kernels_still_take_chains_when_forced(kernel, monkeypatch):
                       tree="chain", max_depth=200)
     gpu = H.run_gpu(w)
     H.assert_parity(w, H.compare(w, gpu, H.run_oracle(w)))
+
+
+@pytest.mark.parametrize("Ns", [[129, 200, 0, 256, 64, 5], [300, 700, 1, 0, 257]],
+                         ids=["256-node-kernel", "chunk-pass"])
+def test_ragged_chains_with_a_state_pool(Ns, monkeypatch):
+    """Ragged batches of chains (short ones too: a chain of 5 takes one partial
+    chunk) through the packed entry points, states from a pool; then the commit of
+    each accepted path into the pool."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    from tests.test_packed_gpu import Packed, check_verify
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    P = Packed(1150 + len(Ns), Ns, 1, 2, 128, 128, W.BF16, n_slots=9, tree="chain")
+    x = P.device()
+    st = torch.full((P.B,), -7, dtype=torch.int32, device="cuda")
+    o, U = gt.verify_packed(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"],
+                            x["cu"], x["pool"], state_slot=x["slot"], dev_status=st)
+    torch.cuda.synchronize()
+    check_verify(P, o.float().cpu().numpy(), U.cpu().numpy(), st.cpu().numpy())
+    pool = x["pool"]
+    cs = torch.full((P.B,), -7, dtype=torch.int32, device="cuda")
+    gt.commit_packed(x["path"], x["path_len"], U, x["k"], x["log_alpha"], x["cu"], pool,
+                     pool_out=pool, state_slot=x["slot"], parent=x["parent"], dev_status=cs)
+    torch.cuda.synchronize()
+    assert (cs.cpu().numpy() == 0).all()
+    got, ref = pool.cpu().numpy(), P.oracle_commit()
+    used = np.zeros(len(ref), bool)
+    used[P.slot] = True
+    assert H.rel_err(got[used], ref[used]) <= H.TOL_S1
+    assert np.array_equal(got[~used], P.pool[~used])
