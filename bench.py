@@ -137,7 +137,9 @@ def verify_kernel_name(w: W.Workload) -> str:
             return "verify_mid_kernel"
     if w.N > 256 or forced in ("long", "long_cuda"):
         if tc_shape and forced not in ("generic", "long_cuda"):
-            return "verify_long_tc_kernel"
+            # (past 256 nodes the units whose tree is one chain go to a kernel of their
+            # own, launched first; past 128 the 256-node kernel runs them itself)
+            return ("verify_chain_kernel + " if forced == "auto" else "") + "verify_long_tc_kernel"
         return "verify_long_kernel"
     return "verify_generic_kernel"
 

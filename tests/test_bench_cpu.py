@@ -32,7 +32,7 @@ def test_byte_model_serving_workload():
     assert bench.verify_kernel_name(w4) == "verify_mid_kernel"
     wl = W.make_custom(seed=1, B=1, N=300, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
                        tree="random", max_depth=24)
-    assert bench.verify_kernel_name(wl) == "verify_long_tc_kernel"
+    assert bench.verify_kernel_name(wl) == "verify_chain_kernel + verify_long_tc_kernel"
     wf = W.make_custom(seed=1, B=1, N=300, Hqk=1, Hv=2, dk=64, dv=64, dtype=W.F32,
                        tree="random", max_depth=24)
     assert bench.verify_kernel_name(wf) == "verify_long_kernel"
