@@ -155,8 +155,16 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int W = (N + 31) / 32;
   const size_t row = (size_t)lay.row0(b, Nmax);
   float* Ubh = U + lay.urow0(b, h, Hv, Nmax) * kD;
+  // this thread's node: parent link and gates, loaded once
+  int pt = -1;
+  float bet = 0.f, lat = 0.f;
+  if (tid < N) {
+    pt = parent[row + tid];
+    bet = beta[(row + tid) * Hv + h];
+    lat = log_alpha[(row + tid) * Hv + h];
+  }
   // one chain: the chunkwise path (no copy of this path has started)
-  if (chains && N > 0 && !__syncthreads_or(tid < N && parent[row + tid] != tid - 1)) {
+  if (chains && N > 0 && !__syncthreads_or(tid < N && pt != tid - 1)) {
     chain::run(smem, q, k, v, log_alpha, beta, S0, o, Ubh, N, Nmax, row, st, b, h, Hv, Hqk,
                dev_status, hk);
     return;
@@ -187,11 +195,10 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   // ---- 1. the tree ------------------------------------------------------------
   int bad = 0;
   if (tid < N) {
-    const int p = parent[row + tid];
-    sPar[tid] = p;
-    bad = (p < -1 || p >= tid);
-    sBeta[tid] = beta[(row + tid) * Hv + h];
-    sLa[tid] = log_alpha[(row + tid) * Hv + h];
+    sPar[tid] = pt;
+    bad = (pt < -1 || pt >= tid);
+    sBeta[tid] = bet;
+    sLa[tid] = lat;
   }
   if (tid <= kMidN) sLevel[tid] = 0;
   if (tid == 0) sFlag[0] = 0;

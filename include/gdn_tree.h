@@ -60,7 +60,10 @@
  * Limits: 1 <= N <= 1024 and Lmax <= 1024; dk, dv in {16, 32, 48, ..., 128};
  * B, Hv >= 1.  Trees of up to 256 nodes are verified on chip; longer trees go
  * through a two-level chunk pass (chunks of 128 nodes on chip, earlier chunks'
- * U rows read back from U), which is correct for every shape but slower.
+ * U rows read back from U), which is correct for every shape but slower.  For
+ * bf16 with dk = dv = 128 and N > 128, a sequence whose tree is one chain (the
+ * parent of node t is t - 1) is verified in the chunkwise form of the same
+ * closed form (the state carried between 64-node chunks), on the tensor cores.
  * B == 0 or N == 0 is a valid empty call that enqueues nothing.
  */
 #ifndef GDN_TREE_H
