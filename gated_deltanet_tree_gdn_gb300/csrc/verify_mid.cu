@@ -419,8 +419,18 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         uint32_t bits = anc[wi];
         const int c = __popc(bits);
         if (left < c) {
-          for (int r = 0; r < left; ++r) bits &= bits - 1;
-          return wi * 32 + __ffs(bits) - 1;
+          // the left-th set bit (from bit 0): halve the window by the count below
+          int pos = 0;
+#pragma unroll
+          for (int half = 16; half > 0; half >>= 1) {
+            const int below = __popc(bits & ((1u << half) - 1u));
+            if (left >= below) {
+              left -= below;
+              bits >>= half;
+              pos += half;
+            }
+          }
+          return wi * 32 + pos;
         }
         left -= c;
       }
