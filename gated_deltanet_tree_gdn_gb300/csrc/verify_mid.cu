@@ -407,6 +407,53 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
       qnext = q_of(task + kWarps);
     }
     __syncwarp();
+    if (nA <= 1) {
+      // a root or a root's child: its dots as warp dots (a lane holds elements
+      // 4 lane .. 4 lane + 3), no path table
+      auto k4 = [&](int r) {  // row r's four elements of this lane, fp32
+        const uint2 w2 = *reinterpret_cast<const uint2*>(sSK + k_chunk(r, lane >> 1) + (lane & 1) * 8);
+        return make_float4(__uint_as_float(w2.x << 16), __uint_as_float(w2.x & 0xffff0000u),
+                           __uint_as_float(w2.y << 16), __uint_as_float(w2.y & 0xffff0000u));
+      };
+      const float4 qt4 = *reinterpret_cast<const float4*>(qs + 4 * lane);
+      const float4 kt4 = k4(t);
+      float qk = qt4.x * kt4.x + qt4.y * kt4.y + qt4.z * kt4.z + qt4.w * kt4.w;
+      float xk = 0.f, yq = 0.f;
+      const int p = nA == 1 ? sPar[t] : -1;
+      if (p >= 0) {
+        const float4 kp4 = k4(p);
+        xk = kt4.x * kp4.x + kt4.y * kp4.y + kt4.z * kp4.z + kt4.w * kp4.w;
+        yq = qt4.x * kp4.x + qt4.y * kp4.y + qt4.z * kp4.z + qt4.w * kp4.w;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        qk += __shfl_xor_sync(0xffffffffu, qk, off);
+        xk += __shfl_xor_sync(0xffffffffu, xk, off);
+        yq += __shfl_xor_sync(0xffffffffu, yq, off);
+      }
+      float4 ut = *reinterpret_cast<const float4*>(sU + u_at(t, lane));  // r_t
+      float4 ao = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p >= 0) {
+        const float dec = expf(df_diff(gt, sG[p]));
+        wait_final(p);
+        const float4 up = *reinterpret_cast<const float4*>(sU + u_at(p, lane));
+        ut = fma4m(-(bt * dec * xk), up, ut);
+        ao = fma4m(dec * yq, up, ao);
+      }
+      *reinterpret_cast<float4*>(sU + u_at(t, lane)) = ut;
+      __syncwarp();
+      if (lane == 0 && !(unit == hk.withhold_unit && t == hk.withhold_node))
+        sm100::mbar_arrive(&sBar[t]);
+      ao = fma4m(qk, ut, ao);  // the node's own term (q_t . k_t) u_t
+      __nv_bfloat16* orow = o + ((row + t) * Hv + h) * kD + 4 * lane;
+      const __nv_bfloat162 p01 = __floats2bfloat162_rn(seed.x + ao.x, seed.y + ao.y);
+      const __nv_bfloat162 p23 = __floats2bfloat162_rn(seed.z + ao.z, seed.w + ao.w);
+      *reinterpret_cast<uint2*>(orow) = make_uint2(*reinterpret_cast<const uint32_t*>(&p01),
+                                                   *reinterpret_cast<const uint32_t*>(&p23));
+      *reinterpret_cast<float4*>(urow) = ut;
+      __syncwarp();  // the stage is read before the next node's q_t lands in it
+      continue;
+    }
     // X[t,s] and Y[t,s] for path entry n (strict ancestors in index order, then
     // t itself), left in lane n % 32 as the n / 32-th of sn / xn / yn
     int sn[kGroups];
