@@ -313,6 +313,16 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
         sUc[t * kD + j] = t < nc ? sBeta[c0 + t] * (vv[i] - sE[t] * p1[i]) : 0.f;
       }
     }
+    // S_c^T *= e^{g_{c1-1} - g_{c0-1}} in TMEM, ahead of the update's accumulation (the
+    // chunk's products read the operand copy, not TMEM)
+    if (!last) {
+      const float decay = expf(df_diff(sG[c0 + nc - 1], gref));
+      float sv[32];
+      sm100::tmem_ld_32cols(tl + TM_S + 32 * qd, sv);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) sv[i] *= decay;
+      sm100::tmem_st_32cols(tl + TM_S + 32 * qd, sv);
+    }
     __syncthreads();
 
     // ---- the substitution (I + X) U = R, blocked by 16 rows ------------------------
@@ -363,18 +373,29 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
       __syncthreads();
     }
 
-    // ---- O_c^T = e P2 + U_c^T Y_c^T on the tensor cores; the outputs ----------------
-    // U_c^T (bf16 hi + lo, K-major: row jc, entries 16 rq ..) goes where S_c^T's
-    // operand was (its products are done; it is rewritten after the update)
+    // ---- O_c^T = e P2 + U_c^T Y_c^T and S_{c+1}^T = decay S_c^T + (U_c^T diag(w)) K_c
+    // on the tensor cores, one round trip; the outputs -----------------------------
+    // U_c^T and U_c^T diag(w) (bf16 hi + lo, K-major: row jc, entries 16 rq ..) go
+    // where S_c^T's operand was (its products are done; it is rewritten below)
 #pragma unroll
     for (int k8 = 2 * rq; k8 < 2 * rq + 2; ++k8) {
+      float uu[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) uu[e] = sUc[(8 * k8 + e) * kD + jc];
+      const uint32_t off = sm100::sw128_chunk(jc, k8);
       uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sm100::split2(sUc[(8 * k8 + 2 * e) * kD + jc], sUc[(8 * k8 + 2 * e + 1) * kD + jc], hi[e], lo[e]);
-      const uint32_t off = sm100::sw128_chunk(jc, k8);
+      for (int e = 0; e < 4; ++e) sm100::split2(uu[2 * e], uu[2 * e + 1], hi[e], lo[e]);
       *reinterpret_cast<uint4*>(smem + OFF_ST + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(smem + OFF_ST + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      if (!last) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sm100::split2(uu[2 * e] * sW[8 * k8 + 2 * e], uu[2 * e + 1] * sW[8 * k8 + 2 * e + 1],
+                        hi[e], lo[e]);
+        *reinterpret_cast<uint4*>(smem + OFF_ST + 32768 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + OFF_ST + 49152 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
     }
     sm100::fence_proxy_async_smem();
     sm100::tc_fence_before_sync();
@@ -385,6 +406,10 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
       umma_kmajor(tmem + TM_GK, aST, aYH, kC, kC / 16, false);
       umma_kmajor(tmem + TM_GK, aST, aYL, kC, kC / 16, true);
       umma_kmajor(tmem + TM_GK, aST + 16384, aYH, kC, kC / 16, true);
+      if (!last) {
+        umma_update(tmem + TM_S, aST + 32768, aKM);
+        umma_update(tmem + TM_S, aST + 49152, aKM);
+      }
       sm100::umma_commit(sBar);
     }
     // the next chunk's v values start coming meanwhile
@@ -397,6 +422,7 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
                   : 0.f;
     }
     wait_mma();
+    if (!last) load_tiles(c0 + kC, false, true);  // the next MN-major K tile (this one is read)
     {
       // thread: column j, rows 16 qd .. 16 qd + 15
       float pc[16], dc[16];
@@ -415,43 +441,6 @@ __device__ __forceinline__ void run(unsigned char* smem, const __nv_bfloat16* __
 #pragma unroll
     for (int i = 0; i < 16; ++i) vv[i] = vn[i];
     if (last) break;
-
-    // ---- S_{c+1}^T = decay S_c^T + (U_c^T diag(w)) K_c -----------------------------
-    __syncthreads();  // X and Y are used: U^T diag(w) takes their place
-    {
-      // thread: row jc of U^T diag(w), entries 16 rq .. 16 rq + 15 (two chunks of 8)
-#pragma unroll
-      for (int k8 = 2 * rq; k8 < 2 * rq + 2; ++k8) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sm100::split2(sUc[(8 * k8 + 2 * e) * kD + jc] * sW[8 * k8 + 2 * e],
-                        sUc[(8 * k8 + 2 * e + 1) * kD + jc] * sW[8 * k8 + 2 * e + 1], hi[e], lo[e]);
-        const uint32_t off = sm100::sw128_chunk(jc, k8);
-        *reinterpret_cast<uint4*>(smem + OFF_XY + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + OFF_XY + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-    {
-      const float decay = expf(df_diff(sG[c0 + nc - 1], gref));
-      float sv[32];
-      sm100::tmem_ld_32cols(tl + TM_S + 32 * qd, sv);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) sv[i] *= decay;
-      sm100::tmem_st_32cols(tl + TM_S + 32 * qd, sv);
-    }
-    sm100::fence_proxy_async_smem();
-    sm100::tc_fence_before_sync();
-    __syncthreads();
-    sm100::tc_fence_after_sync();
-    if (tid == 0) {
-      umma_update(tmem + TM_S, aXY, aKM);
-      umma_update(tmem + TM_S, aXY + 16384, aKM);
-      sm100::umma_commit(sBar);
-    }
-    wait_mma();
-    // the next chunk's MN-major K tile (the update has read this one)
-    load_tiles(c0 + kC, false, true);
     // S_{c+1}^T -> the operand tile
     {
       float sv[32];
