@@ -35,6 +35,9 @@
 //     barrier is arrived on.
 // The unfinished node of lowest depth order in a chunk never waits on an
 // unfinished node, so the waits cannot cycle.
+//
+// Units whose tree is one chain are verified by verify_chain_kernel (this file,
+// launched first; the chunkwise form of chain_unit.cuh) and left by the chunk pass.
 #include <algorithm>
 
 #include "chain_unit.cuh"
