@@ -116,13 +116,14 @@ tree_topw_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w
 
 // Trees of up to 512 candidate slots, w <= 4: one warp per tree.  Lane l owns
 // the slots l, l + 32, ..., l + 480 (key = p * c + j): their log-probabilities,
-// and its live slots sorted best first, in registers, as 64-bit words (the
-// score's order-preserving bits, then the inverted key, so that one unsigned
-// comparison orders by score and then by lower key; 0 = empty).  A round takes
-// the warp's four best words at once -- a butterfly over the lanes merges their
-// sorted top four -- the owners drop what was taken from the front of their
-// arrays, and the new nodes' candidates are inserted by the lanes that own their
-// slots.  Same fp32 sums and tie rule as the general kernel, so the same tree.
+// and its live slots as 64-bit words (the score's order-preserving bits, then
+// 511 - key, then the depth the node would have, so that one unsigned comparison
+// orders by score and then by lower key; 0 = empty): its best four sorted in
+// registers, the rest unsorted in shared memory.  A round takes the warp's four
+// best words at once -- a butterfly over the lanes merges their sorted top four --
+// the owners drop what was taken and refill from their rest, and the new nodes'
+// candidates are inserted by the lanes that own their slots.  Same fp32 sums and
+// tie rule as the general kernel, so the same tree.
 constexpr int kSlots = 16;
 constexpr int kTop = 4;
 
@@ -134,10 +135,12 @@ __device__ __forceinline__ uint32_t order_bits(float x) {
 __device__ __forceinline__ float from_order_bits(uint32_t o) {
   return __uint_as_float(o ^ ((o >> 31) ? 0x80000000u : 0xffffffffu));
 }
-__device__ __forceinline__ uint64_t cand_word(float s, uint32_t key) {
-  return ((uint64_t)order_bits(s) << 32) | (uint64_t)(~key);
+// key < 512, depth < 1024
+__device__ __forceinline__ uint64_t cand_word(float s, uint32_t key, uint32_t depth) {
+  return ((uint64_t)order_bits(s) << 32) | (uint64_t)(((511u - key) << 10) | depth);
 }
-__device__ __forceinline__ uint32_t word_key(uint64_t x) { return ~(uint32_t)x; }
+__device__ __forceinline__ uint32_t word_key(uint64_t x) { return 511u - ((uint32_t)x >> 10); }
+__device__ __forceinline__ int word_depth(uint64_t x) { return (int)((uint32_t)x & 1023u); }
 __device__ __forceinline__ float word_score(uint64_t x) {
   return from_order_bits((uint32_t)(x >> 32));
 }
@@ -157,20 +160,14 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
                       int max_depth, int32_t* __restrict__ parent,
                       int32_t* __restrict__ cand_index, float* __restrict__ score,
                       int32_t* __restrict__ n_built) {
-  __shared__ int s_ndepth[kWarpsPerCta][kSlots * 32];
   __shared__ float s_lp[kWarpsPerCta][kSlots * 32];
-  // the built nodes' parent, candidate index and score, written out at the end
-  __shared__ int s_par[kWarpsPerCta][kSlots * 32];  // N <= N c <= kSlots 32
-  __shared__ int s_cix[kWarpsPerCta][kSlots * 32];  // N <= N c <= kSlots 32
-  __shared__ float s_sco[kWarpsPerCta][kSlots * 32];  // N <= N c <= kSlots 32
+  // each lane's live words past its best four, unsorted: slot i of lane l at [i][l]
+  __shared__ uint64_t s_bag[kWarpsPerCta][kSlots][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kWarpsPerCta + warp;
   if (b >= B) return;  // whole warps only: nothing below synchronises across warps
-  int* ndepth = s_ndepth[warp];
   float* lp = s_lp[warp];  // the tree's candidate log-probabilities, by key
-  int* npar = s_par[warp];
-  int* ncix = s_cix[warp];
-  float* nsco = s_sco[warp];
+  uint64_t (*bag)[32] = s_bag[warp];
   const float* lpb = cand_logp + (size_t)b * N * c;
   int32_t* par = parent + (size_t)b * N;
   int32_t* cix = cand_index ? cand_index + (size_t)b * N : nullptr;
@@ -181,35 +178,39 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
   const uint32_t cinv = 65536u / (uint32_t)c + 1u;
   auto node_of = [&](uint32_t key) { return (int)((key * cinv) >> 16); };
 
-  uint64_t srt[kSlots];  // this lane's live slots, best first (0 = empty)
 #pragma unroll
   for (int m = 0; m < kSlots; ++m) {
     const int k = lane + 32 * m;
     lp[k] = k < nslots ? lpb[k] : kNegInf;
-    srt[m] = 0;
   }
-  // a live candidate into the sorted array: its place is the number of larger
-  // words; the words from there on move down one (independent selects)
+  // this lane's live words: its best four sorted in registers (0 = empty), the rest
+  // in the bag, all below top[3] (so the bag is empty while top has room)
+  uint64_t top[kTop] = {0, 0, 0, 0};
+  int nb = 0;
   auto insert = [&](uint64_t x) {
-    int at = 0;
-#pragma unroll
-    for (int i = 0; i < kSlots; ++i) at += srt[i] > x;
-#pragma unroll
-    for (int i = kSlots - 1; i > 0; --i) srt[i] = i > at ? srt[i - 1] : (i == at ? x : srt[i]);
-    if (at == 0) srt[0] = x;
+    if (x > top[kTop - 1]) {
+      const uint64_t out = top[kTop - 1];
+      const int at = (top[0] > x) + (top[1] > x) + (top[2] > x);
+      top[3] = at == 3 ? x : top[2];
+      top[2] = at == 2 ? x : (at < 2 ? top[1] : top[2]);
+      top[1] = at == 1 ? x : (at < 1 ? top[0] : top[1]);
+      if (at == 0) top[0] = x;
+      if (out != 0) bag[nb++][lane] = out;
+    } else {
+      bag[nb++][lane] = x;
+    }
   };
   // the root (node 0, score 0, depth 1) offers its candidates (keys 0 .. c-1)
   if (max_depth > 1) {
     for (int k = lane; k < c; k += 32) {
       const float s = 0.f + lp[k];
-      if (s != kNegInf) insert(cand_word(s, (uint32_t)k));
+      if (s != kNegInf) insert(cand_word(s, (uint32_t)k, 2u));
     }
   }
   if (lane == 0) {
-    ndepth[0] = 1;
-    npar[0] = -1;
-    ncix[0] = -1;
-    nsco[0] = 0.f;
+    par[0] = -1;
+    if (cix) cix[0] = -1;
+    if (sco) sco[0] = 0.f;
   }
   __syncwarp();
 
@@ -217,7 +218,7 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
   while (n < N) {
     const int take = min(w, N - n);
     // the warp's four best words: every lane ends with the same sorted list
-    uint64_t t[kTop] = {srt[0], srt[1], srt[2], srt[3]};
+    uint64_t t[kTop] = {top[0], top[1], top[2], top[3]};
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       uint64_t o[kTop];
@@ -241,30 +242,55 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
       }
     }
     if (popped == 0) break;  // no live candidate (uniform across the warp)
-    // this lane's taken words are the front of its array
+    // this lane's taken words are the front of top: shift, then refill from the bag
+    // with its best words in turn
+    if (mine > 0) {
 #pragma unroll
-    for (int i = 0; i < kSlots; ++i) {
-      uint64_t x = srt[i];
+      for (int i = 0; i < kTop; ++i) {
+        uint64_t x = 0;
 #pragma unroll
-      for (int q = 1; q <= kTop; ++q)
-        if (mine == q) x = i + q < kSlots ? srt[(i + q) & (kSlots - 1)] : 0;
-      srt[i] = x;
+        for (int q = 1; q <= kTop; ++q)
+          if (mine == q && i + q < kTop) x = top[i + q];
+        top[i] = x;
+      }
+      for (int r = kTop - mine; r < kTop && nb > 0; ++r) {
+        // the bag's best: every slot loaded at once, then a pairwise maximum with its
+        // slot (empty slots count as 0)
+        uint64_t y[kSlots];
+        int yi[kSlots];
+#pragma unroll
+        for (int i = 0; i < kSlots; ++i) {
+          y[i] = i < nb ? bag[i][lane] : 0;
+          yi[i] = i;
+        }
+#pragma unroll
+        for (int span = kSlots / 2; span > 0; span >>= 1) {
+#pragma unroll
+          for (int i = 0; i < span; ++i) {
+            const bool hi = y[i + span] > y[i];
+            y[i] = hi ? y[i + span] : y[i];
+            yi[i] = hi ? yi[i + span] : yi[i];
+          }
+        }
+        bag[yi[0]][lane] = bag[nb - 1][lane];
+        --nb;
+#pragma unroll
+        for (int i = 0; i < kTop; ++i)
+          if (i == r) top[i] = y[0];
+      }
     }
-    // the new nodes n + i (i < popped): every lane has their words; their depth is
-    // their parent's + 1
+    // the new nodes n + i (i < popped): every lane has their words, depths included
     int nd[kTop];
 #pragma unroll
-    for (int i = 0; i < kTop; ++i) nd[i] = i < popped ? ndepth[node_of(word_key(t[i]))] + 1 : 0;
+    for (int i = 0; i < kTop; ++i) nd[i] = i < popped ? word_depth(t[i]) : 0;
     // lane i < popped records node n + i
     if (lane < popped) {
       const uint64_t x = lane == 0 ? t[0] : lane == 1 ? t[1] : lane == 2 ? t[2] : t[3];
       const uint32_t key = word_key(x);
       const int node = n + lane, p = node_of(key), j = (int)key - p * c;
-      const float s = word_score(x);
-      ndepth[node] = lane == 0 ? nd[0] : lane == 1 ? nd[1] : lane == 2 ? nd[2] : nd[3];
-      npar[node] = p;
-      ncix[node] = j;
-      nsco[node] = s;
+      par[node] = p;
+      if (cix) cix[node] = j;
+      if (sco) sco[node] = word_score(x);
     }
     // the new nodes offer their candidates: keys n c .. (n + popped) c - 1, the
     // ones of this lane's slots (one insertion each)
@@ -275,18 +301,17 @@ tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, 
       const int d = i == 0 ? nd[0] : i == 1 ? nd[1] : i == 2 ? nd[2] : nd[3];
       if (d < max_depth) {
         const float s = word_score(x) + lp[k];
-        if (s != kNegInf) insert(cand_word(s, (uint32_t)k));
+        if (s != kNegInf) insert(cand_word(s, (uint32_t)k, (uint32_t)d + 1u));
       }
     }
-    __syncwarp();  // the new nodes' depths are in place for the next round
+    __syncwarp();
     n += popped;
   }
-  // the tree out (coalesced); nodes that could not be built
-  for (int i = lane; i < N; i += 32) {
-    const bool built = i < n;
-    par[i] = built ? npar[i] : -2;
-    if (cix) cix[i] = built ? ncix[i] : -2;
-    if (sco) sco[i] = built ? nsco[i] : CUDART_NAN_F;
+  // nodes that could not be built
+  for (int i = n + lane; i < N; i += 32) {
+    par[i] = -2;
+    if (cix) cix[i] = -2;
+    if (sco) sco[i] = CUDART_NAN_F;
   }
   if (lane == 0 && n_built) n_built[b] = n;
 }
