@@ -105,3 +105,35 @@ def test_ragged_chains_with_a_state_pool(Ns, monkeypatch):
     used[P.slot] = True
     assert H.rel_err(got[used], ref[used]) <= H.TOL_S1
     assert np.array_equal(got[~used], P.pool[~used])
+
+
+def test_decoding_iteration_into_chains(monkeypatch):
+    """One decoding iteration (commit of the previous path, then the verification of
+    the next tree from S1) whose next trees are 200-node chains and mixed families:
+    the verification's chains take the chunkwise path."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    import oracle
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    prev = W.make_custom(seed=1160, B=3, N=128, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                         tree="random", max_depth=24)
+    nxt = W.make_custom(seed=1161, B=3, N=200, Hqk=1, Hv=2, dk=128, dv=128, dtype=W.BF16,
+                        tree="mixed", max_depth=200)
+    xp, xn = H.to_device(prev), H.to_device(nxt)
+    _, U_prev = gt.verify(xp["q"], xp["k"], xp["v"], xp["log_alpha"], xp["beta"], xp["parent"],
+                          xp["S0"])
+    cs = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    vs = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    S1, o, U = gt.commit_verify(xp["path"], xp["path_len"], U_prev, xp["k"], xp["log_alpha"],
+                                xp["S0"], xn["q"], xn["k"], xn["v"], xn["log_alpha"],
+                                xn["beta"], xn["parent"], prev_parent=xp["parent"],
+                                commit_status=cs, verify_status=vs)
+    torch.cuda.synchronize()
+    assert (cs.cpu().numpy() == 0).all() and (vs.cpu().numpy() == 0).all()
+    S1_ref = oracle.commit_workload(prev)
+    assert H.rel_err(S1.cpu().numpy(), S1_ref) <= H.TOL_S1
+    # the next tree against the oracle run from the state the GPU committed
+    o_ref, U_ref = oracle.verify(nxt.q, nxt.k, nxt.v, nxt.log_alpha, nxt.beta, nxt.parent,
+                                 S1.cpu().numpy())
+    assert H.rel_err(o.float().cpu().numpy(), o_ref) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U.cpu().numpy(), U_ref) <= H.TOL_U
