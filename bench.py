@@ -145,9 +145,9 @@ def verify_kernel_name(w: W.Workload) -> str:
 
 
 def topw_kernel_name(N: int, c: int, w: int) -> str:
-    """The top-w kernel the library dispatches: the register-list warp kernel for
-    N c <= 512 candidate slots and w <= 4, else the general one."""
-    return "tree_topw_warp_kernel" if N * c <= 512 and w <= 4 else "tree_topw_kernel"
+    """The top-w kernel the library dispatches: the sorted-list kernel for rounds of
+    at most 32 offers (w c <= 32), else the general one."""
+    return "tree_topw_list_kernel" if w * c <= 32 and N <= 256 else "tree_topw_kernel"
 
 
 def commit_kernel_name(w: W.Workload) -> str:

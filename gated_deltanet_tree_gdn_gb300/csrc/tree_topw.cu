@@ -12,9 +12,9 @@
 //   as new nodes in that order, and only then do they offer their candidates.
 //   A -inf candidate is never taken; construction stops when none is left.
 //
-// One warp per sequence.  Trees of up to 512 candidate slots with w <= 4 keep
-// them sorted in registers (tree_topw_warp_kernel); other shapes in shared
-// memory indexed by their key (slots of nodes not yet built, and taken
+// One warp per sequence.  Rounds of at most 32 offers (w * c <= 32) keep the
+// live candidates as one sorted list (tree_topw_list_kernel); other shapes in
+// shared memory indexed by their key (slots of nodes not yet built, and taken
 // candidates, hold -inf), a pop being one strided scan per lane and a warp
 // argmax over (score, key).
 #include <math_constants.h>
@@ -114,18 +114,22 @@ tree_topw_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w
   if (lane == 0 && n_built) n_built[b] = n;
 }
 
-// Trees of up to 512 candidate slots, w <= 4: one warp per tree.  Lane l owns
-// the slots l, l + 32, ..., l + 480 (key = p * c + j): their log-probabilities,
-// and its live slots as 64-bit words (the score's order-preserving bits, then
-// 511 - key, then the depth the node would have, so that one unsigned comparison
-// orders by score and then by lower key; 0 = empty): its best four sorted in
-// registers, the rest unsorted in shared memory.  A round takes the warp's four
-// best words at once -- a butterfly over the lanes merges their sorted top four --
-// the owners drop what was taken and refill from their rest, and the new nodes'
-// candidates are inserted by the lanes that own their slots.  Same fp32 sums and
-// tie rule as the general kernel, so the same tree.
-constexpr int kSlots = 16;
-constexpr int kTop = 4;
+// Rounds that offer at most 32 candidates (w * c <= 32), trees of up to 256 nodes:
+// a CTA of four warps per tree keeps its live candidates as one list in shared
+// memory, sorted best first, as 64-bit order-preserving words (the fp32 score's bits
+// made monotone in the high half; in the low half kKeyTop - key, so that one
+// unsigned comparison orders by score and then by lower key, and the depth the node
+// would have; 0 = none).  The list is cut to the N - built best: a candidate ranked at
+// or below the number of nodes still to build is never taken, since every round
+// takes only candidates ranked above it.  A round's takes are then the list's front,
+// and its offers (one word per lane, formed by every warp alike) are merged in: each
+// offer is broadcast in turn and compared with every listed word (each warp holds a
+// quarter of the list), which gives each listed word the number of offers above it
+// (it moves down by that much) and, counted over the warps, each offer the number of
+// listed words above it (its place is that plus the offers above it).  The built
+// nodes' words are kept and written out once at the end.  Same fp32 sums and tie
+// rule as the general kernel, so the same tree.
+constexpr uint32_t kKeyTop = (1u << 21) - 1u;  // keys < 2^21, depths < 2^11
 
 // fp32 -> uint32 with the same order (no NaN)
 __device__ __forceinline__ uint32_t order_bits(float x) {
@@ -135,185 +139,171 @@ __device__ __forceinline__ uint32_t order_bits(float x) {
 __device__ __forceinline__ float from_order_bits(uint32_t o) {
   return __uint_as_float(o ^ ((o >> 31) ? 0x80000000u : 0xffffffffu));
 }
-// key < 512, depth < 1024
 __device__ __forceinline__ uint64_t cand_word(float s, uint32_t key, uint32_t depth) {
-  return ((uint64_t)order_bits(s) << 32) | (uint64_t)(((511u - key) << 10) | depth);
+  return ((uint64_t)order_bits(s) << 32) | (uint64_t)(((kKeyTop - key) << 11) | depth);
 }
-__device__ __forceinline__ uint32_t word_key(uint64_t x) { return 511u - ((uint32_t)x >> 10); }
-__device__ __forceinline__ int word_depth(uint64_t x) { return (int)((uint32_t)x & 1023u); }
+__device__ __forceinline__ uint32_t word_key(uint64_t x) { return kKeyTop - ((uint32_t)x >> 11); }
+__device__ __forceinline__ int word_depth(uint64_t x) { return (int)((uint32_t)x & 2047u); }
 __device__ __forceinline__ float word_score(uint64_t x) {
   return from_order_bits((uint32_t)(x >> 32));
 }
-__device__ __forceinline__ uint64_t shfl_xor64(uint64_t x, int off) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)x, off);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(x >> 32), off);
+
+constexpr int kListOffers = 32;  // offers a round can make (w * c)
+
+__device__ __forceinline__ uint64_t shfl64(uint64_t x, int src) {
+  const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)x, src);
+  const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(x >> 32), src);
   return ((uint64_t)hi << 32) | lo;
 }
-__device__ __forceinline__ void cswap_desc(uint64_t& a, uint64_t& b) {
-  const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-  a = hi;
-  b = lo;
+
+// 4-byte global -> shared copy that the thread does not wait for (cp.async.wait_all)
+__device__ __forceinline__ void copy4_async(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
 }
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32, 1)
-tree_topw_warp_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w,
-                      int max_depth, int32_t* __restrict__ parent,
-                      int32_t* __restrict__ cand_index, float* __restrict__ score,
-                      int32_t* __restrict__ n_built) {
-  __shared__ float s_lp[kWarpsPerCta][kSlots * 32];
-  // each lane's live words past its best four, unsorted: slot i of lane l at [i][l]
-  __shared__ uint64_t s_bag[kWarpsPerCta][kSlots][32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kWarpsPerCta + warp;
-  if (b >= B) return;  // whole warps only: nothing below synchronises across warps
-  float* lp = s_lp[warp];  // the tree's candidate log-probabilities, by key
-  uint64_t (*bag)[32] = s_bag[warp];
+constexpr int kListWarps = 4;
+
+inline size_t topw_list_smem_bytes(int N, int c, int slots) {
+  return (size_t)(32 * kListWarps * (slots + 1) + N) * sizeof(uint64_t) +
+         (size_t)32 * kListWarps * sizeof(int) + (size_t)N * c * sizeof(float);
+}
+
+// kSlots: listed words per thread (the list holds up to 128 * kSlots >= N words;
+// warp v's slots are (s * 4 + v) * 32 + lane); kOffers: offers scanned per round
+// (>= w * c).
+template <int kSlots, int kOffers>
+__global__ void __launch_bounds__(32 * kListWarps)
+tree_topw_list_kernel(const float* __restrict__ cand_logp, int N, int c, int w, int max_depth,
+                      int32_t* __restrict__ parent, int32_t* __restrict__ cand_index,
+                      float* __restrict__ score, int32_t* __restrict__ n_built) {
+  constexpr int kThreads = 32 * kListWarps, kCap = kThreads * kSlots;
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* list = reinterpret_cast<uint64_t*>(smem);  // [kCap] live words, best first
+  uint64_t* sink = list + kCap;                         // [kThreads] stores of dropped words
+  uint64_t* node = sink + kThreads;                     // [N] the built nodes' words
+  int* part = reinterpret_cast<int*>(node + N);         // [4][32] per warp: listed words
+                                                        //   below offer lane
+  float* lp = reinterpret_cast<float*>(part + kThreads);  // [N * c], by key
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
   const float* lpb = cand_logp + (size_t)b * N * c;
+  const float kNegInf = -CUDART_INF_F;
+
+  // every copy in flight at once, then one wait
+  for (int k = tid; k < N * c; k += kThreads) copy4_async(lp + k, lpb + k);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (tid == 0) node[0] = cand_word(0.f, 0u, 1u);  // the root: score 0, depth 1
+  const int from = lane / c;  // the taken node whose candidate lane - from * c this lane offers
+  __syncthreads();
+
+  int n0 = 0, nt = 1, len = 0;  // the round's first node, its takes, the list's length
+  int built;
+  for (;;) {
+    const int n = n0 + nt;  // nodes built with the round's takes
+    if (n >= N) {
+      built = n;
+      break;
+    }
+    // the takes (nodes n0 .. n - 1) offer their candidates: keys n0 c .. n c - 1, one
+    // per lane (every warp forms the same words)
+    uint64_t my = 0;
+    if (lane < nt * c) {
+      const int key = n0 * c + lane;
+      const float l = lp[key];
+      const uint64_t x = node[n0 + from];
+      const int d = word_depth(x);
+      const float s = word_score(x) + l;
+      if (d < max_depth && s != kNegInf) my = cand_word(s, (uint32_t)key, (uint32_t)d + 1u);
+    }
+    // this warp's listed words (an empty slot holds the largest word, so that no offer
+    // counts as above it)
+    uint64_t m[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+      const int k = (s * kListWarps + warp) * 32 + lane;
+      m[s] = k < len ? list[k] : ~0ull;
+    }
+    // each offer y in turn, broadcast from its lane: the offers above this lane's
+    // offer, the offers above each of this thread's listed words, and this warp's
+    // listed words below y (words are distinct: the listed words above y are the rest)
+    int rank = 0, below_mine = 0, cnt[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) cnt[s] = 0;
+#pragma unroll
+    for (int j = 0; j < kOffers; ++j) {
+      const uint64_t y = shfl64(my, j);
+      rank += (int)(y > my);
+      int below = 0;
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s) {
+        const bool g = y > m[s];
+        cnt[s] += (int)g;
+        below += __popc(__ballot_sync(0xffffffffu, g));
+      }
+      if (lane == j) below_mine = below;
+    }
+    part[tid] = below_mine;
+    const int total = len + __popc(__ballot_sync(0xffffffffu, my != 0));
+    const int left = N - n;  // nodes still to build
+    const int take = min(w, left), keep = min(total, left);
+    __syncthreads();  // every read of the list is done, every warp's count is in
+    // merged place pos: the next round's takes are nodes n .. n + take - 1, the list
+    // keeps places take .. keep - 1, the rest is dropped (into this thread's sink slot)
+    auto dest = [&](int pos, bool live) {
+      return !live ? sink + tid
+                   : pos < take ? node + n + pos : pos < keep ? list + (pos - take) : sink + tid;
+    };
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+      const int k = (s * kListWarps + warp) * 32 + lane;
+      *dest(k + cnt[s], k < len) = m[s];
+    }
+    if (warp == 0) {
+      int below = 0;
+#pragma unroll
+      for (int v = 0; v < kListWarps; ++v) below += part[v * 32 + lane];
+      *dest(rank + len - below, my != 0) = my;
+    }
+    __syncthreads();
+    n0 = n;
+    nt = min(take, total);
+    len = keep > take ? keep - take : 0;
+    if (nt == 0) {  // no live candidate (uniform across the CTA)
+      built = n;
+      break;
+    }
+  }
+  // every node's record, from its word
   int32_t* par = parent + (size_t)b * N;
   int32_t* cix = cand_index ? cand_index + (size_t)b * N : nullptr;
   float* sco = score ? score + (size_t)b * N : nullptr;
-  const float kNegInf = -CUDART_INF_F;
-  const int nslots = N * c;
-  // key / c as a multiply and shift (exact for key * c < 2^16: key < 512, c <= 32)
-  const uint32_t cinv = 65536u / (uint32_t)c + 1u;
-  auto node_of = [&](uint32_t key) { return (int)((key * cinv) >> 16); };
+  for (int i = tid; i < N; i += kThreads) {
+    int p = -2, j = -2;
+    float v = CUDART_NAN_F;
+    if (i == 0) {
+      p = -1, j = -1, v = 0.f;
+    } else if (i < built) {
+      const uint64_t x = node[i];
+      const int key = (int)word_key(x);
+      p = key / c, j = key - p * c, v = word_score(x);
+    }
+    par[i] = p;
+    if (cix) cix[i] = j;
+    if (sco) sco[i] = v;
+  }
+  if (tid == 0 && n_built) n_built[b] = built;
+}
 
-#pragma unroll
-  for (int m = 0; m < kSlots; ++m) {
-    const int k = lane + 32 * m;
-    lp[k] = k < nslots ? lpb[k] : kNegInf;
-  }
-  // this lane's live words: its best four sorted in registers (0 = empty), the rest
-  // in the bag, all below top[3] (so the bag is empty while top has room)
-  uint64_t top[kTop] = {0, 0, 0, 0};
-  int nb = 0;
-  auto insert = [&](uint64_t x) {
-    if (x > top[kTop - 1]) {
-      const uint64_t out = top[kTop - 1];
-      const int at = (top[0] > x) + (top[1] > x) + (top[2] > x);
-      top[3] = at == 3 ? x : top[2];
-      top[2] = at == 2 ? x : (at < 2 ? top[1] : top[2]);
-      top[1] = at == 1 ? x : (at < 1 ? top[0] : top[1]);
-      if (at == 0) top[0] = x;
-      if (out != 0) bag[nb++][lane] = out;
-    } else {
-      bag[nb++][lane] = x;
-    }
-  };
-  // the root (node 0, score 0, depth 1) offers its candidates (keys 0 .. c-1)
-  if (max_depth > 1) {
-    for (int k = lane; k < c; k += 32) {
-      const float s = 0.f + lp[k];
-      if (s != kNegInf) insert(cand_word(s, (uint32_t)k, 2u));
-    }
-  }
-  if (lane == 0) {
-    par[0] = -1;
-    if (cix) cix[0] = -1;
-    if (sco) sco[0] = 0.f;
-  }
-  __syncwarp();
-
-  int n = 1;
-  while (n < N) {
-    const int take = min(w, N - n);
-    // the warp's four best words: every lane ends with the same sorted list
-    uint64_t t[kTop] = {top[0], top[1], top[2], top[3]};
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      uint64_t o[kTop];
-#pragma unroll
-      for (int i = 0; i < kTop; ++i) o[i] = shfl_xor64(t[i], off);
-      // top four of two sorted lists: the larger of a[i] and b[3 - i] (a bitonic
-      // sequence), then sorted
-#pragma unroll
-      for (int i = 0; i < kTop; ++i) t[i] = t[i] > o[kTop - 1 - i] ? t[i] : o[kTop - 1 - i];
-      cswap_desc(t[0], t[2]);
-      cswap_desc(t[1], t[3]);
-      cswap_desc(t[0], t[1]);
-      cswap_desc(t[2], t[3]);
-    }
-    int popped = 0, mine = 0;
-#pragma unroll
-    for (int i = 0; i < kTop; ++i) {
-      if (i < take && t[i] != 0) {
-        ++popped;
-        mine += (int)(word_key(t[i]) & 31u) == lane;
-      }
-    }
-    if (popped == 0) break;  // no live candidate (uniform across the warp)
-    // this lane's taken words are the front of top: shift, then refill from the bag
-    // with its best words in turn
-    if (mine > 0) {
-#pragma unroll
-      for (int i = 0; i < kTop; ++i) {
-        uint64_t x = 0;
-#pragma unroll
-        for (int q = 1; q <= kTop; ++q)
-          if (mine == q && i + q < kTop) x = top[i + q];
-        top[i] = x;
-      }
-      for (int r = kTop - mine; r < kTop && nb > 0; ++r) {
-        // the bag's best: every slot loaded at once, then a pairwise maximum with its
-        // slot (empty slots count as 0)
-        uint64_t y[kSlots];
-        int yi[kSlots];
-#pragma unroll
-        for (int i = 0; i < kSlots; ++i) {
-          y[i] = i < nb ? bag[i][lane] : 0;
-          yi[i] = i;
-        }
-#pragma unroll
-        for (int span = kSlots / 2; span > 0; span >>= 1) {
-#pragma unroll
-          for (int i = 0; i < span; ++i) {
-            const bool hi = y[i + span] > y[i];
-            y[i] = hi ? y[i + span] : y[i];
-            yi[i] = hi ? yi[i + span] : yi[i];
-          }
-        }
-        bag[yi[0]][lane] = bag[nb - 1][lane];
-        --nb;
-#pragma unroll
-        for (int i = 0; i < kTop; ++i)
-          if (i == r) top[i] = y[0];
-      }
-    }
-    // the new nodes n + i (i < popped): every lane has their words, depths included
-    int nd[kTop];
-#pragma unroll
-    for (int i = 0; i < kTop; ++i) nd[i] = i < popped ? word_depth(t[i]) : 0;
-    // lane i < popped records node n + i
-    if (lane < popped) {
-      const uint64_t x = lane == 0 ? t[0] : lane == 1 ? t[1] : lane == 2 ? t[2] : t[3];
-      const uint32_t key = word_key(x);
-      const int node = n + lane, p = node_of(key), j = (int)key - p * c;
-      par[node] = p;
-      if (cix) cix[node] = j;
-      if (sco) sco[node] = word_score(x);
-    }
-    // the new nodes offer their candidates: keys n c .. (n + popped) c - 1, the
-    // ones of this lane's slots (one insertion each)
-    const int k0 = n * c, k1 = (n + popped) * c;
-    for (int k = k0 + ((lane - k0) & 31); k < k1; k += 32) {
-      const int i = node_of((uint32_t)k) - n;
-      const uint64_t x = i == 0 ? t[0] : i == 1 ? t[1] : i == 2 ? t[2] : t[3];
-      const int d = i == 0 ? nd[0] : i == 1 ? nd[1] : i == 2 ? nd[2] : nd[3];
-      if (d < max_depth) {
-        const float s = word_score(x) + lp[k];
-        if (s != kNegInf) insert(cand_word(s, (uint32_t)k, (uint32_t)d + 1u));
-      }
-    }
-    __syncwarp();
-    n += popped;
-  }
-  // nodes that could not be built
-  for (int i = n + lane; i < N; i += 32) {
-    par[i] = -2;
-    if (cix) cix[i] = -2;
-    if (sco) sco[i] = CUDART_NAN_F;
-  }
-  if (lane == 0 && n_built) n_built[b] = n;
+template <int kSlots, int kOffers>
+cudaError_t launch_topw_list(const float* cand_logp, int B, int N, int c, int w, int max_depth,
+                             int32_t* parent, int32_t* cand_index, float* score, int32_t* n_built,
+                             cudaStream_t stream) {
+  tree_topw_list_kernel<kSlots, kOffers>
+      <<<B, 32 * kListWarps, topw_list_smem_bytes(N, c, kSlots), stream>>>(
+          cand_logp, N, c, w, max_depth, parent, cand_index, score, n_built);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -325,12 +315,18 @@ size_t tree_topw_smem_bytes(int N, int c) {
 cudaError_t launch_tree_topw(const float* cand_logp, int B, int N, int c, int w, int max_depth,
                              int32_t* parent, int32_t* cand_index, float* score, int32_t* n_built,
                              cudaStream_t stream) {
-  const int grid = (B + kWarpsPerCta - 1) / kWarpsPerCta;
-  if (N * c <= kSlots * 32 && w <= kTop) {
-    tree_topw_warp_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(
-        cand_logp, B, N, c, w, max_depth, parent, cand_index, score, n_built);
-    return cudaGetLastError();
+  if (w * c <= kListOffers && N <= 256) {
+    if (N <= 128)
+      return w * c <= 16 ? launch_topw_list<1, 16>(cand_logp, B, N, c, w, max_depth, parent,
+                                                   cand_index, score, n_built, stream)
+                         : launch_topw_list<1, 32>(cand_logp, B, N, c, w, max_depth, parent,
+                                                   cand_index, score, n_built, stream);
+    return w * c <= 16 ? launch_topw_list<2, 16>(cand_logp, B, N, c, w, max_depth, parent,
+                                                 cand_index, score, n_built, stream)
+                       : launch_topw_list<2, 32>(cand_logp, B, N, c, w, max_depth, parent,
+                                                 cand_index, score, n_built, stream);
   }
+  const int grid = (B + kWarpsPerCta - 1) / kWarpsPerCta;
   const size_t smem = tree_topw_smem_bytes(N, c);
   cudaError_t err = cudaFuncSetAttribute(tree_topw_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -36,8 +36,9 @@ def test_byte_model_serving_workload():
     wf = W.make_custom(seed=1, B=1, N=300, Hqk=1, Hv=2, dk=64, dv=64, dtype=W.F32,
                        tree="random", max_depth=24)
     assert bench.verify_kernel_name(wf) == "verify_long_kernel"
-    assert bench.topw_kernel_name(128, 4, 4) == "tree_topw_warp_kernel"
-    assert bench.topw_kernel_name(256, 4, 4) == "tree_topw_kernel"
+    assert bench.topw_kernel_name(128, 4, 4) == "tree_topw_list_kernel"
+    assert bench.topw_kernel_name(256, 8, 4) == "tree_topw_list_kernel"
+    assert bench.topw_kernel_name(256, 8, 8) == "tree_topw_kernel"
 
 
 def _rank(rank, world, port, out):

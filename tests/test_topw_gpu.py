@@ -52,6 +52,23 @@ def test_topw_matches_oracle(B, N, c, w, max_depth):
     check(logp, w, max_depth)
 
 
+@pytest.mark.parametrize("B,N,c,w,max_depth", [
+    (6, 128, 8, 4, 30),     # 32 offers a round, the 128-node list
+    (6, 129, 4, 4, 30),     # the 256-node list from 129 nodes
+    (4, 256, 4, 8, 40),     # 256 nodes, 32 offers
+    (4, 256, 2, 3, 300),    # deep trees, few offers
+    (3, 200, 1, 32, 300),   # one offer per take, 32 takes a round
+])
+def test_topw_list_shapes_with_positive_scores(B, N, c, w, max_depth):
+    """The sorted-list kernel at its size boundaries, with log-probabilities of both
+    signs (a new candidate can then outrank the nodes just taken) and rounded values
+    (many equal scores: creation order decides)."""
+    rng = np.random.default_rng(N * 31 + c * 7 + w)
+    logp = rng.normal(0.0, 1.0, size=(B, N, c)).astype(np.float32)
+    logp[B // 2:] = np.round(logp[B // 2:])
+    check(logp, w, max_depth)
+
+
 def test_topw_ties_infinities_and_exhaustion():
     rng = np.random.default_rng(9)
     logp = np.round(np.log(rng.uniform(0.05, 1.0, size=(6, 50, 4))), 1).astype(np.float32)
