@@ -407,36 +407,47 @@ verify_long_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         // each exchange step halves the values a lane carries, so that lane L ends
         // with value L / 2 (entry L / 4; its k dot for L / 2 even, its q dot for odd)
         float dkk = 0.f, dqk = 0.f;
-        for (int j0 = 0; j0 < cnt; j0 += 8) {
-          float vs[16];
+        for (int j0 = 0; j0 < cnt; j0 += 16) {
+          // sixteen k rows in flight at once (one round trip for paths of up to 16
+          // entries), then two groups of eight dots
+          uint2 kr[16];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
+          for (int jj = 0; jj < 16; ++jj) {
             const int ss = __shfl_sync(0xffffffffu, a, (j0 + jj) & 31);
-            const float4 ks = j0 + jj < cnt
-                                  ? bf16x4_to_f32t(*reinterpret_cast<const uint2*>(
-                                        k + ((row + ss) * Hqk + hq) * kD + c4))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            vs[2 * jj] = dot4t(kt, ks);
-            vs[2 * jj + 1] = dot4t(qt, ks);
+            kr[jj] = j0 + jj < cnt
+                         ? *reinterpret_cast<const uint2*>(k + ((row + ss) * Hqk + hq) * kD + c4)
+                         : make_uint2(0u, 0u);
           }
 #pragma unroll
-          for (int w = 8; w >= 1; w >>= 1) {  // 16 -> 8 -> 4 -> 2 -> 1 values a lane
-            const bool up = (lane >> 1) & w;  // this lane keeps the upper half
+          for (int half = 0; half < 2; ++half) {
+            const int j1 = j0 + 8 * half;
+            if (j1 >= cnt) break;  // (uniform)
+            float vs[16];
 #pragma unroll
-            for (int i = 0; i < w; ++i) {
-              const float keep = up ? vs[w + i] : vs[i];
-              const float send = up ? vs[i] : vs[w + i];
-              vs[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+            for (int jj = 0; jj < 8; ++jj) {
+              const float4 ks = bf16x4_to_f32t(kr[8 * half + jj]);
+              vs[2 * jj] = dot4t(kt, ks);
+              vs[2 * jj + 1] = dot4t(qt, ks);
             }
-          }
-          vs[0] += __shfl_xor_sync(0xffffffffu, vs[0], 1);
-          // entry j0 + i: its k dot in lane 4 i, its q dot in lane 4 i + 2
-          const int i = lane - j0;
-          const float xk = __shfl_sync(0xffffffffu, vs[0], (4 * i) & 31);
-          const float yq = __shfl_sync(0xffffffffu, vs[0], (4 * i + 2) & 31);
-          if (i >= 0 && i < 8) {
-            dkk = xk;
-            dqk = yq;
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1) {  // 16 -> 8 -> 4 -> 2 -> 1 values a lane
+              const bool up = (lane >> 1) & w;  // this lane keeps the upper half
+#pragma unroll
+              for (int i = 0; i < w; ++i) {
+                const float keep = up ? vs[w + i] : vs[i];
+                const float send = up ? vs[i] : vs[w + i];
+                vs[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+              }
+            }
+            vs[0] += __shfl_xor_sync(0xffffffffu, vs[0], 1);
+            // entry j1 + i: its k dot in lane 4 i, its q dot in lane 4 i + 2
+            const int i = lane - j1;
+            const float xk = __shfl_sync(0xffffffffu, vs[0], (4 * i) & 31);
+            const float yq = __shfl_sync(0xffffffffu, vs[0], (4 * i + 2) & 31);
+            if (i >= 0 && i < 8) {
+              dkk = xk;
+              dqk = yq;
+            }
           }
         }
         float xe = 0.f, ye = 0.f;
