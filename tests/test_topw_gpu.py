@@ -58,6 +58,7 @@ def test_topw_matches_oracle(B, N, c, w, max_depth):
     (4, 256, 4, 8, 40),     # 256 nodes, 32 offers
     (4, 256, 2, 3, 300),    # deep trees, few offers
     (3, 200, 1, 32, 300),   # one offer per take, 32 takes a round
+    (2, 256, 32, 1, 300),   # the list kernel's largest shared memory (32 K log-probabilities)
 ])
 def test_topw_list_shapes_with_positive_scores(B, N, c, w, max_depth):
     """The sorted-list kernel at its size boundaries, with log-probabilities of both
