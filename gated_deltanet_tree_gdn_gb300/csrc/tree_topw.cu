@@ -115,7 +115,7 @@ tree_topw_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w
 }
 
 // Rounds that offer at most 32 candidates (w * c <= 32), trees of up to 256 nodes:
-// a CTA of four warps per tree keeps its live candidates as one list in shared
+// a CTA of two or four warps per tree keeps its live candidates as one list in shared
 // memory, sorted best first, as 64-bit order-preserving words (the fp32 score's bits
 // made monotone in the high half; in the low half kKeyTop - key, so that one
 // unsigned comparison orders by score and then by lower key, and the depth the node
@@ -123,8 +123,8 @@ tree_topw_kernel(const float* __restrict__ cand_logp, int B, int N, int c, int w
 // or below the number of nodes still to build is never taken, since every round
 // takes only candidates ranked above it.  A round's takes are then the list's front,
 // and its offers (one word per lane, formed by every warp alike) are merged in: each
-// offer is broadcast in turn and compared with every listed word (each warp holds a
-// quarter of the list), which gives each listed word the number of offers above it
+// offer is broadcast in turn and compared with every listed word (each warp holds its
+// share of the list), which gives each listed word the number of offers above it
 // (it moves down by that much) and, counted over the warps, each offer the number of
 // listed words above it (its place is that plus the offers above it).  The built
 // nodes' words are kept and written out once at the end.  Same fp32 sums and tie
@@ -164,17 +164,15 @@ __device__ __forceinline__ void copy4_async(float* dst, const float* src) {
                : "memory");
 }
 
-constexpr int kListWarps = 4;
-
-inline size_t topw_list_smem_bytes(int N, int c, int slots) {
-  return (size_t)(32 * kListWarps * (slots + 1) + N) * sizeof(uint64_t) +
-         (size_t)32 * kListWarps * sizeof(int) + (size_t)N * c * sizeof(float);
+inline size_t topw_list_smem_bytes(int N, int c, int slots, int warps) {
+  return (size_t)(32 * warps * (slots + 1) + N) * sizeof(uint64_t) +
+         (size_t)32 * warps * sizeof(int) + (size_t)N * c * sizeof(float);
 }
 
-// kSlots: listed words per thread (the list holds up to 128 * kSlots >= N words;
-// warp v's slots are (s * 4 + v) * 32 + lane); kOffers: offers scanned per round
-// (>= w * c).
-template <int kSlots, int kOffers>
+// kSlots: listed words per thread and kListWarps: warps per tree (the list holds up
+// to 32 kListWarps kSlots >= N words; warp v's slots are (s kListWarps + v) 32 + lane);
+// kOffers: offers scanned per round (>= w * c).
+template <int kSlots, int kOffers, int kListWarps>
 __global__ void __launch_bounds__(32 * kListWarps)
 tree_topw_list_kernel(const float* __restrict__ cand_logp, int N, int c, int w, int max_depth,
                       int32_t* __restrict__ parent, int32_t* __restrict__ cand_index,
@@ -184,8 +182,8 @@ tree_topw_list_kernel(const float* __restrict__ cand_logp, int N, int c, int w, 
   uint64_t* list = reinterpret_cast<uint64_t*>(smem);  // [kCap] live words, best first
   uint64_t* sink = list + kCap;                         // [kThreads] stores of dropped words
   uint64_t* node = sink + kThreads;                     // [N] the built nodes' words
-  int* part = reinterpret_cast<int*>(node + N);         // [4][32] per warp: listed words
-                                                        //   below offer lane
+  int* part = reinterpret_cast<int*>(node + N);         // [warps][32] per warp: listed
+                                                        //   words below offer lane
   float* lp = reinterpret_cast<float*>(part + kThreads);  // [N * c], by key
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x;
   const float* lpb = cand_logp + (size_t)b * N * c;
@@ -296,13 +294,17 @@ tree_topw_list_kernel(const float* __restrict__ cand_logp, int N, int c, int w, 
   if (tid == 0 && n_built) n_built[b] = built;
 }
 
-template <int kSlots, int kOffers>
+template <int kSlots, int kListWarps>
 cudaError_t launch_topw_list(const float* cand_logp, int B, int N, int c, int w, int max_depth,
                              int32_t* parent, int32_t* cand_index, float* score, int32_t* n_built,
                              cudaStream_t stream) {
-  tree_topw_list_kernel<kSlots, kOffers>
-      <<<B, 32 * kListWarps, topw_list_smem_bytes(N, c, kSlots), stream>>>(
-          cand_logp, N, c, w, max_depth, parent, cand_index, score, n_built);
+  const size_t smem = topw_list_smem_bytes(N, c, kSlots, kListWarps);
+  if (w * c <= 16)
+    tree_topw_list_kernel<kSlots, 16, kListWarps><<<B, 32 * kListWarps, smem, stream>>>(
+        cand_logp, N, c, w, max_depth, parent, cand_index, score, n_built);
+  else
+    tree_topw_list_kernel<kSlots, 32, kListWarps><<<B, 32 * kListWarps, smem, stream>>>(
+        cand_logp, N, c, w, max_depth, parent, cand_index, score, n_built);
   return cudaGetLastError();
 }
 
@@ -316,15 +318,17 @@ cudaError_t launch_tree_topw(const float* cand_logp, int B, int N, int c, int w,
                              int32_t* parent, int32_t* cand_index, float* score, int32_t* n_built,
                              cudaStream_t stream) {
   if (w * c <= kListOffers && N <= 256) {
+    // two warps up to 64 nodes (fewer threads at each barrier), four with one listed
+    // word a thread up to 128, four with two up to 256 (measured faster than eight
+    // with one)
+    if (N <= 64)
+      return launch_topw_list<1, 2>(cand_logp, B, N, c, w, max_depth, parent, cand_index,
+                                    score, n_built, stream);
     if (N <= 128)
-      return w * c <= 16 ? launch_topw_list<1, 16>(cand_logp, B, N, c, w, max_depth, parent,
-                                                   cand_index, score, n_built, stream)
-                         : launch_topw_list<1, 32>(cand_logp, B, N, c, w, max_depth, parent,
-                                                   cand_index, score, n_built, stream);
-    return w * c <= 16 ? launch_topw_list<2, 16>(cand_logp, B, N, c, w, max_depth, parent,
-                                                 cand_index, score, n_built, stream)
-                       : launch_topw_list<2, 32>(cand_logp, B, N, c, w, max_depth, parent,
-                                                 cand_index, score, n_built, stream);
+      return launch_topw_list<1, 4>(cand_logp, B, N, c, w, max_depth, parent, cand_index,
+                                    score, n_built, stream);
+    return launch_topw_list<2, 4>(cand_logp, B, N, c, w, max_depth, parent, cand_index, score,
+                                  n_built, stream);
   }
   const int grid = (B + kWarpsPerCta - 1) / kWarpsPerCta;
   const size_t smem = tree_topw_smem_bytes(N, c);
