@@ -179,6 +179,42 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- cluster launch control (work stealing) -------------------------------------
+
+// One thread: asks the hardware scheduler to cancel a CTA of this grid that has not
+// been launched yet.  The 16-byte response lands at `resp` (16-byte aligned shared
+// memory) and completes a phase of `bar` by its byte count (this thread arms it).
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, 16);
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(smem_addr(resp)),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Decodes a landed response: true when a CTA was cancelled, its blockIdx.x in *ctaid_x
+// (the cancelled CTA never runs: its work is the caller's).
+__device__ __forceinline__ bool clc_cancelled(const void* resp, int* ctaid_x) {
+  uint32_t ok = 0, x = 0;
+  asm volatile(
+      "{\n"
+      " .reg .b128 r;\n"
+      " .reg .pred p;\n"
+      " .reg .b64 lo, hi;\n"
+      " ld.shared.v2.b64 {lo, hi}, [%2];\n"
+      " mov.b128 r, {lo, hi};\n"
+      " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      " @p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n"
+      "}"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_addr(resp))
+      : "memory");
+  *ctaid_x = (int)x;
+  return ok != 0;
+}
+
 // ---- TMEM -------------------------------------------------------------------
 
 // Whole warp: allocate ncols TMEM columns, base address written to *dst.

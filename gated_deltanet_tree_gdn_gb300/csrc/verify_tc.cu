@@ -11,9 +11,11 @@
 // substitution and applies the output stage in one pass; this kernel does the
 // same in one launch, laid out for Blackwell:
 //
-//   a persistent grid, one CTA (512 threads, 512 TMEM columns) per SM, walks the
-//   (sequence b, v-head h) units; the next unit's K, Q and state are already
-//   being copied while the current unit finishes.  Per unit:
+//   a CTA (512 threads, 512 TMEM columns) per (sequence b, v-head h) unit, one
+//   fitting an SM; a running CTA takes over the units of CTAs not launched yet
+//   (cluster launch control: it cancels them), one unit ahead, so that the SMs
+//   stay busy however uneven the units; the next unit's K, Q and state are
+//   already being copied while the current unit finishes.  Per unit:
 //   1. TMA brings K and Q of the q/k head (128-byte swizzle) and the fp32 state
 //      tile (four 32-column boxes).  Fused with the delayed commitment of the
 //      previous tree's accepted path, K_P^T diag(w) U_P is one tcgen05 MMA
@@ -173,6 +175,14 @@ struct Small {
   // phases issued on bar_kq, bar_g, bar_ks, bar_s, bar_c (for the drain)
   int n_kq, n_g, n_ks, n_s, n_c;
   int s1_pending;  // a TMA store of S1 is in flight
+  // work stealing: the unit after the current one (n_units: none) in slot it & 1 of
+  // iteration it, the response of the cluster-launch-control request in flight (it
+  // names the unit after that), its mbarrier and phase count
+  uint4 clc_resp;
+  uint64_t bar_clc;
+  int n_clc;
+  int clc_pending;
+  int next_unit[2];
   // fused delayed commitment of the previous tree's accepted path
   int cpath[kMaxN];
   int pre_path[kMaxN];  // the next unit's accepted path and its length, prefetched
@@ -195,6 +205,22 @@ static_assert(offsetof(Small, anc) % 16 == 0, "ancestor rows are read and writte
 
 // packed strictly-lower triangle of X and Y
 __device__ __forceinline__ int x_index(int t, int s) { return (t * (t - 1) >> 1) + s; }
+
+// The issuer: the unit that the work-stealing request in flight took over (the
+// cancelled CTA's blockIdx.x), or n_units when none is in flight, when the grid had no
+// CTA left to cancel, or when the response did not land within the limit (S.err is
+// then set and the request stays pending)
+__device__ __forceinline__ int clc_take(Small& S, int n_units, uint64_t limit_ns) {
+  if (!S.clc_pending) return n_units;
+  if (!mbar_wait(&S.bar_clc, (uint32_t)S.n_clc & 1u, limit_ns)) {
+    S.err = 5;
+    return n_units;
+  }
+  ++S.n_clc;
+  S.clc_pending = 0;
+  int x = 0;
+  return clc_cancelled(&S.clc_resp, &x) && x >= 0 && x < n_units ? x : n_units;
+}
 
 __device__ __forceinline__ uint32_t pack2f(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -654,15 +680,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     mbar_init(&S.bar_s, 1);
     mbar_init(&S.bar_stage, 1);
     mbar_init(&S.bar_c, 1);
+    mbar_init(&S.bar_clc, 1);
     S.err = 0;
     S.n_kq = S.n_g = S.n_ks = S.n_s = S.n_c = 0;
     S.s1_pending = 0;
     S.cbad = 0;
     S.cL = 0;
+    S.n_clc = 0;
+    S.clc_pending = 0;
+    S.next_unit[0] = S.next_unit[1] = n_units;
     mbar_fence_init();
     if (unit < n_units) {
       issue_kq(S, smem, &tmK, &tmQ, lay, unit, Hv, Hqk, Nmax);
       issue_state(S, smem, &tmS, lay, unit, Hv, Nmax);
+      // the unit after this one: a CTA of the grid not launched yet, cancelled and
+      // taken over (the response lands while the first copies do)
+      clc_try_cancel(&S.clc_resp, &S.bar_clc);
+      S.clc_pending = 1;
+      S.next_unit[0] = clc_take(S, n_units, kWaitLimitNs);
     }
   }
   if constexpr (kFused) {
@@ -681,11 +716,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t trow = tmem + trow_off;
   uint32_t stage_ph = 0;  // the issuer's count of bar_stage phases
 
-  for (uint32_t it = 0; unit < n_units; unit += gridDim.x, ++it) {
+  uint32_t it = 0;
+  for (; unit < n_units; ++it) {
     const uint32_t ph = it & 1u;
     const int b = unit / Hv, h = unit - b * Hv;
     const int hq = h / (Hv / Hqk);
-    const int next = unit + gridDim.x;
+    // the unit after this one, and (requested now, taken at the end of this unit)
+    // the one after that
+    const int next = S.next_unit[ph];
+    if (tid == kIssuer && next < n_units) {
+      clc_try_cancel(&S.clc_resp, &S.bar_clc);
+      S.clc_pending = 1;
+    }
     // this unit's nodes (an invalid sequence layout runs as an empty tree, unwritten)
     const UnitGeom geo = unit_geom(lay, b, Nmax);
     const int N = geo.n;
@@ -1096,6 +1138,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
       }
     }
+    if (tid == kIssuer) S.next_unit[ph ^ 1u] = clc_take(S, n_units, kWaitLimitNs);
     // regions 1 and 3 are free: the next unit's K, Q and state start loading
     tc_fence_before_sync();
     if (__syncthreads_or(S.err)) goto fail;
@@ -1106,6 +1149,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       issue_kq(S, smem, &tmK, &tmQ, lay, next, Hv, Hqk, Nmax);
       issue_state(S, smem, &tmS, lay, next, Hv, Nmax);
     }
+    unit = next;
   }
   goto release;
 
@@ -1114,8 +1158,14 @@ fail:
   // sequences of every unit this CTA has not reached (their outputs stay
   // unwritten), let in-flight copies, stores and MMAs drain (again bounded),
   // then free TMEM
-  if (tid == 0) {
-    for (int u = unit; u < n_units; u += gridDim.x) {
+  if (tid == kIssuer) {
+    // the units this CTA owns: the current one, the one after it, and the one the
+    // request in flight names (a slot not yet rewritten holds the current unit)
+    int own[4] = {unit, S.next_unit[it & 1u], S.next_unit[(it & 1u) ^ 1u], n_units};
+    if (S.clc_pending) own[3] = clc_take(S, n_units, kWaitLimitNs);
+    for (int i = 0; i < 4; ++i) {
+      const int u = own[i];
+      if (u < 0 || u >= n_units) continue;
       if (dev_status) atomicMax(dev_status + u / Hv, GDN_TREE_STATUS_TIMEOUT);
       if (kFused && fc.status) atomicMax(fc.status + u / Hv, GDN_TREE_STATUS_TIMEOUT);
     }
@@ -1205,13 +1255,11 @@ cudaError_t launch_tc(const VerifyArgs& a, const FusedCommit& fc, cudaStream_t s
   cudaError_t err = cudaFuncSetAttribute(verify_tc_kernel<kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (err != cudaSuccess) return err;
-  // persistent: one CTA per SM (the shared memory admits no second), each walking
-  // units blockIdx.x, blockIdx.x + gridDim.x, ...
+  // a CTA per unit; one fits an SM (the shared memory admits no second), and each
+  // running CTA takes over the units of CTAs not launched yet (work stealing), so
+  // the SMs stay busy until the units run out, however uneven the units
   const int n_units = a.d.B * a.d.Hv;
-  const int n_sm = sm_count();
-  if (n_sm <= 0) return cudaErrorInvalidDevice;
-  const int grid = n_units < n_sm ? n_units : n_sm;
-  verify_tc_kernel<kFused><<<grid, kThreads, kSmemBytes, stream>>>(
+  verify_tc_kernel<kFused><<<n_units, kThreads, kSmemBytes, stream>>>(
       tmQ, tmK, tmV, tmS, tmS1, a.S0, a.log_alpha, a.beta, a.parent,
       static_cast<const __nv_bfloat16*>(a.v), static_cast<__nv_bfloat16*>(a.o), a.U, a.d,
       a.dev_status, a.lay, fc, wait_hooks());
