@@ -184,3 +184,41 @@ def test_commit_state_copy_wait_runs_out(monkeypatch):
     torch.cuda.synchronize()
     assert (st.cpu().numpy() == 0).all()
     assert H.rel_err(S1b.cpu().numpy(), S1_ref) <= H.TOL_S1
+
+
+def test_timeout_with_units_taken_over(monkeypatch):
+    """More units than SMs (256 on 152), so running CTAs take over the units of CTAs not
+    launched yet.  A withheld solve-barrier arrival makes one unit's wait run out: its
+    CTA reports TIMEOUT for the units it owns (that unit, and at most the next one and
+    the one a request in flight took over, which may be other sequences') and leaves
+    them unwritten; every other sequence is exact and the next call is clean."""
+    import torch
+    import gated_deltanet_tree_gdn_gb300 as gt
+    monkeypatch.delenv("GDN_TREE_KERNEL", raising=False)
+    w = W.make_custom(seed=907, B=64, N=96, Hqk=2, Hv=4, dk=128, dv=128, dtype=W.BF16,
+                      tree="random", max_depth=24)
+    b, h = 37, 2
+    monkeypatch.setenv("GDN_TREE_TEST_WAIT_LIMIT_NS", LIMIT_NS)
+    monkeypatch.setenv("GDN_TREE_TEST_WITHHOLD_NODE", f"{b * w.Hv + h}:{_withheld(w, b)}")
+    x = H.to_device(w)
+    st = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    o, U = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
+                     dev_status=st)
+    torch.cuda.synchronize()
+    s = st.cpu().numpy()
+    assert s[b] == gt.STATUS_TIMEOUT
+    others = np.flatnonzero((s != gt.STATUS_OK) & (np.arange(w.B) != b))
+    assert len(others) <= 2 and (s[others] == gt.STATUS_TIMEOUT).all()
+    ok = s == gt.STATUS_OK
+    o_ref, U_ref = oracle.verify_workload(w)
+    assert H.rel_err(o.float().cpu().numpy()[ok], o_ref[ok]) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U.cpu().numpy()[ok], U_ref[ok]) <= H.TOL_U
+    monkeypatch.delenv("GDN_TREE_TEST_WAIT_LIMIT_NS")
+    monkeypatch.delenv("GDN_TREE_TEST_WITHHOLD_NODE")
+    st2 = torch.full((w.B,), -7, dtype=torch.int32, device="cuda")
+    o2, U2 = gt.verify(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["parent"], x["S0"],
+                       dev_status=st2)
+    torch.cuda.synchronize()
+    assert (st2.cpu().numpy() == gt.STATUS_OK).all()
+    assert H.rel_err(o2.float().cpu().numpy(), o_ref) <= H.TOL_O[W.BF16]
+    assert H.rel_err(U2.cpu().numpy(), U_ref) <= H.TOL_U
