@@ -10,7 +10,7 @@
 //
 // One CTA (512 threads) per (sequence b, v-head h), in four stages:
 //  1. the tree: parent links checked; strict-ancestor bitsets and g by pointer
-//     jumping; depths, and the nodes ordered by depth (the solve's task order);
+//     jumping; depths, and the nodes grouped by depth (the solve's task order);
 //  2. R and the output seeds gamma_t q_t^T S0 for every node at once, on the
 //     tensor cores: K and Q (two 128-row tiles each, 128-byte swizzled K-major)
 //     and S0 = hi + lo (bf16, MN-major) in shared memory, K S0_hi + K S0_lo and
@@ -211,7 +211,7 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   // the tree is valid: the CTA takes the SM's 512 TMEM columns (one CTA an SM)
   if (warp == 0) sm100::tmem_alloc(reinterpret_cast<uint32_t*>(sFlag + 1), 512);
   tree_prepare(sPar, N, W, sLa, sJump, sAnc, sG);
-  // depth, level sizes, then the depth order (index order within a level)
+  // depth, level sizes, then the nodes grouped by depth
   if (tid < N) {
     int dep = 1;
     for (int i = 0; i < W; ++i) dep += __popc(sAnc[tid * W + i]);
@@ -238,11 +238,17 @@ verify_mid_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     }
   }
   __syncthreads();
-  if (tid < N) {
-    const int dep = sDepth[tid];
-    int rank = 0;
-    for (int s = 0; s < tid; ++s) rank += (sDepth[s] == dep);
-    sOrder[sLevel[dep] + rank] = tid;
+  {
+    // each level's nodes claim consecutive slots from its start: one atomic per group
+    // of a warp's lanes of equal depth (any order within a level serves the solve, and
+    // no node's result depends on it)
+    const int dep = tid < N ? sDepth[tid] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, dep);
+    const int leader = __ffs(peers) - 1;
+    int base = 0;
+    if (lane == leader && dep >= 0) base = atomicAdd(&sLevel[dep], __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (dep >= 0) sOrder[base + __popc(peers & ((1u << lane) - 1u))] = tid;
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
