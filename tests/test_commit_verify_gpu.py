@@ -160,3 +160,34 @@ def test_bench_step_two_iterations_match_oracle():
         assert errs["o"] <= H.TOL_O[W.BF16], errs
         assert errs["U"] <= H.TOL_U, errs
         assert H.rel_err(U_gpu, U_ref) <= H.TOL_U + (i + 1) * H.TOL_S1
+
+
+def test_commit_verify_invalid_paths_among_many_units():
+    """More units than SMs (384 on 152, so CTAs take over the units of CTAs not launched
+    yet): sequences whose accepted path is invalid are reported by both calls and left
+    unwritten, an empty path commits S_prev, and every other sequence matches the oracle
+    in S1, o and U."""
+    prev, nxt = _pair(520, 24, 96, 96, 8, 16, 128, W.BF16)
+    prev.path_len[2] = 0                       # empty: S1 = S_prev
+    prev.path[7, :] = -1                       # not a root chain
+    prev.path[7, 0], prev.path[7, 1] = 5, 3
+    prev.path_len[7] = 2
+    prev.path_len[19] = 200                    # longer than the tree
+    g = _run(prev, nxt)
+    bad = [7, 19]
+    cs, vs = g["cs"].tolist(), g["vs"].tolist()
+    for b in range(prev.B):
+        want = 2 if b in bad else 0            # GDN_TREE_STATUS_BAD_PATH
+        assert cs[b] == want and vs[b] == want, (b, cs[b], vs[b])
+    assert np.array_equal(g["S1"][2], prev.S0[2])
+    ok = [b for b in range(prev.B) if b not in bad]
+    S1_ref = oracle.commit(prev.path[ok], prev.path_len[ok], prev.k[ok], prev.v[ok],
+                           prev.log_alpha[ok], prev.beta[ok], prev.S0[ok])
+    o_ref, _ = oracle.verify(nxt.q[ok], nxt.k[ok], nxt.v[ok], nxt.log_alpha[ok],
+                             nxt.beta[ok], nxt.parent[ok], S1_ref)
+    assert H.rel_err(g["S1"][ok], S1_ref) <= H.TOL_S1
+    assert H.rel_err(g["o"][ok], o_ref) <= H.TOL_O[W.BF16]
+    # U against the oracle run from the GPU's own S1 (the state it verified from)
+    _, U_own = oracle.verify(nxt.q[ok], nxt.k[ok], nxt.v[ok], nxt.log_alpha[ok],
+                             nxt.beta[ok], nxt.parent[ok], g["S1"][ok])
+    assert H.rel_err(g["U"][ok], U_own) <= H.TOL_U
