@@ -101,8 +101,13 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
 
 
+# The marshalling below runs on every call, ahead of a launch that can take only a few
+# microseconds (a decoding step of one sequence), so it is kept lean: pointers go to
+# ctypes as plain integers, shapes are compared as they are, and the stream is read as
+# its raw handle.
+
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _check(t: torch.Tensor, name: str, dtype=None, shape=None):
@@ -114,20 +119,36 @@ def _check(t: torch.Tensor, name: str, dtype=None, shape=None):
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+# the current stream's handle without building a Stream object (the public call is the
+# fallback where the accessor is absent)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream) -> int:
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+_dims_cache: dict = {}
 
 
 def dims_of(q: torch.Tensor, v: torch.Tensor) -> Dims:
-    B, N, Hqk, dk = q.shape
-    Hv, dv = v.shape[2], v.shape[3]
-    return Dims(B, N, Hqk, Hv, dk, dv, _dtype_code(q))
+    key = (q.shape, v.shape, q.dtype)
+    d = _dims_cache.get(key)
+    if d is None:
+        B, N, Hqk, dk = q.shape
+        Hv, dv = v.shape[2], v.shape[3]
+        d = Dims(B, N, Hqk, Hv, dk, dv, _dtype_code(q))
+        if len(_dims_cache) < 256:
+            _dims_cache[key] = d
+    return d
 
 
 def verify(q, k, v, log_alpha, beta, parent, S0, *, o=None, U=None, dev_status=None,
