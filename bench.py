@@ -594,6 +594,63 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     lv_us = 1e3 * statistics.mean(evl[i][0].elapsed_time(evl[i][1]) for i in range(1, Kl + 1))
     lc_us = 1e3 * statistics.mean(evl[i][1].elapsed_time(evl[i][2]) for i in range(1, Kl + 1))
 
+    # one decoding step of one sequence (the decode shape: 1 sequence x 32 v-heads, a
+    # 16-node tree; the state drawn at random, which changes no timing): what a serving
+    # loop waits when the GPU is idle at the call (binding, launch and kernel, read by
+    # the host after a synchronize), the host's part of it, and the device time alone
+    w1 = W.make_config(1)
+    w1.S0 = W.draw_state(np.random.Generator(np.random.PCG64(1001)), w1.B, w1.Hv, w1.dk, w1.dv)
+    x1 = {kk: torch.from_numpy(np.ascontiguousarray(getattr(w1, kk))).to(
+        device=dev, dtype=dt if kk in ("q", "k", "v") else None)
+        for kk in ("q", "k", "v", "log_alpha", "beta", "parent", "S0")}
+    o1 = torch.empty((w1.B, w1.N, w1.Hv, w1.dv), dtype=dt, device=dev)
+    U1 = torch.empty((w1.B, w1.Hv, w1.N, w1.dv), dtype=torch.float32, device=dev)
+
+    def decode_call():
+        gt.verify(x1["q"], x1["k"], x1["v"], x1["log_alpha"], x1["beta"], x1["parent"],
+                  x1["S0"], o=o1, U=U1)
+
+    for _ in range(10):
+        decode_call()
+    torch.cuda.synchronize()
+    d_host, d_done = [], []
+    for _ in range(50):
+        t0 = time.perf_counter()
+        decode_call()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        t2 = time.perf_counter()
+        d_host.append((t1 - t0) * 1e6)
+        d_done.append((t2 - t0) * 1e6)
+    d_stream = torch.cuda.Stream()
+    d_stream.wait_stream(stream)
+    with torch.cuda.stream(d_stream):
+        decode_call()
+    torch.cuda.synchronize()
+    d_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(d_graph, stream=d_stream):
+        for _ in range(20):
+            decode_call()
+    d_dev = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(d_stream):
+            e0.record(d_stream)
+            d_graph.replay()
+            e1.record(d_stream)
+        torch.cuda.synchronize()
+        d_dev.append(1e3 * e0.elapsed_time(e1) / 20)
+    del d_graph, x1, o1, U1
+    decode_step = {"workload": f"decode-B{w1.B}-Hv{w1.Hv}-N{w1.N}: B={w1.B} x Hv={w1.Hv} "
+                               f"(Hqk={w1.Hqk}), N={w1.N}-node tree, d={w1.dk}, bf16, state "
+                               "drawn at random (timing only)",
+                   "kernel": verify_kernel_name(w1),
+                   "call_to_done_us": statistics.median(d_done),
+                   "host_us": statistics.median(d_host),
+                   "device_us": statistics.median(d_dev),
+                   "timing": "median of 50 calls with the GPU idle at each call (host clock, "
+                             "synchronize included); device time from a CUDA graph of 20"}
+
     # the stress shapes: 64 sequences of 256-node trees mixing 256-deep chains,
     # stars and random trees, strong decay and beta up to 0.99 (the CUDA-core
     # on-chip kernel: the tensor-core kernel takes trees of up to 128 nodes)
@@ -771,6 +828,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             "tree_verify_speedup": rec_ms / statistics.mean(t_ver),
             "page": "fused tree kernel 7.1x faster than single-branch recurrent verification "
                     "at 126 tree tokens, NVIDIA B200 (DFlash-TfM, results)"}
+        line["decode_step"] = decode_step
         line["tree_build"] = {"kernel": topw_kernel_name(w.N, 4, 4), "us": tb_us,
                               "timing": "device time per call, 20 calls replayed from a CUDA "
                                         "graph (median of 5 replays)",
