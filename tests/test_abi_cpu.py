@@ -129,3 +129,21 @@ def test_commit_verify_refuses_U_overlapping_prev_U(lib):
     # a partial overlap
     assert _commit_verify(lib, d, 16, base + unit_bytes, base) == gt.EINVAL
     assert _commit_verify(lib, d, 16, base, base + 256) == gt.EINVAL
+
+
+def test_binding_marshalling_helpers():
+    """The binding's per-call marshalling: pointers pass as plain integers (NULL as
+    None), the dims struct matches the tensors and is reused for equal shapes, and a
+    shape or dtype mismatch is refused before any call."""
+    import torch
+    from gated_deltanet_tree_gdn_gb300 import _binding as bd
+    q = torch.zeros((2, 8, 4, 32), dtype=torch.bfloat16)
+    v = torch.zeros((2, 8, 8, 32), dtype=torch.bfloat16)
+    d = bd.dims_of(q, v)
+    assert (d.B, d.N, d.Hqk, d.Hv, d.dk, d.dv, d.dtype) == (2, 8, 4, 8, 32, 32, bd.BF16)
+    assert bd.dims_of(q.clone(), v.clone()) is d
+    d2 = bd.dims_of(q.float(), v.float())
+    assert d2 is not d and d2.dtype == bd.F32
+    assert bd._ptr(None) is None and bd._ptr(q) == q.data_ptr()
+    with pytest.raises(ValueError):  # not a CUDA tensor
+        bd._check(q, "q", torch.bfloat16, (2, 8, 4, 32))
