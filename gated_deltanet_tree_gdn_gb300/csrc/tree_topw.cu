@@ -229,9 +229,13 @@ tree_topw_list_kernel(const float* __restrict__ cand_logp, int N, int c, int w, 
     int rank = 0, below_mine = 0, cnt[kSlots];
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) cnt[s] = 0;
+    // every offer's broadcast first, so that the shuffles' latency is paid once
+    uint64_t ys[kOffers];
+#pragma unroll
+    for (int j = 0; j < kOffers; ++j) ys[j] = shfl64(my, j);
 #pragma unroll
     for (int j = 0; j < kOffers; ++j) {
-      const uint64_t y = shfl64(my, j);
+      const uint64_t y = ys[j];
       rank += (int)(y > my);
       int below = 0;
 #pragma unroll
